@@ -1,0 +1,300 @@
+/*
+ * kvd_oracle.c -- plain, slow fp64 CPU reference of the KV-cached decoder step.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product library calls, links or includes
+ * this file; only the tests, the smoke check and the CPU-baseline leg of the benchmark
+ * use it. It shares no code, header, table or constant with the CUDA library.
+ *
+ * Every function is the plain definition of the result, written loop by loop:
+ * no blocking, no fusion, no online softmax, no split. 16-bit inputs are decoded
+ * exactly to double; all arithmetic on them is double precision; comparisons of
+ * fp32 logits happen in their own precision (exactly, since comparing two floats
+ * as doubles gives the same answer).
+ *
+ * Sources (web pages, cited by title and section):
+ *  [W]  readoss.com, "Whisper のデコーダー内部：Beam Search、Logit フィルター、KV キャッシュ"
+ *  [S]  agentlenshq.com, "추측 디코딩으로 Whisper 추론 속도 2배 향상"
+ *  [N]  agentlenshq.com, "nanoVLM における KV キャッシュ実装"
+ *  [A]  aitime.ge, Whisper speculative-decoding article (single-paragraph body with the
+ *       "The quick brown sock / fox" example)
+ *
+ * Element types (argument `dtype`): 0 = IEEE binary16 stored as uint16 bits,
+ * 1 = bfloat16 stored as uint16 bits, 2 = IEEE binary64.
+ *
+ * Error results are bit masks: bit (code - 16) for code 16 = length overflow,
+ * 17 = bad parent index, 18 = draft id outside the vocabulary, 19 = NaN logit.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define KVO_ERR_LEN_OVERFLOW (1u << 0)
+#define KVO_ERR_BAD_INDEX    (1u << 1)
+#define KVO_ERR_BAD_TOKEN    (1u << 2)
+#define KVO_ERR_NAN          (1u << 3)
+
+/* ---- number formats ---------------------------------------------------------------- */
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double kvo_decode_f16(uint16_t bits)
+{
+    int sign = (bits >> 15) & 1;
+    int expo = (bits >> 10) & 0x1F;
+    int frac = bits & 0x3FF;
+    double mag;
+    if (expo == 0)
+        mag = ldexp((double)frac, -24);              /* subnormal: frac * 2^(1-15-10) */
+    else if (expo == 31)
+        mag = frac ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(1024 + frac), expo - 25); /* (1 + frac/2^10) * 2^(expo-15) */
+    return sign ? -mag : mag;
+}
+
+/* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits. */
+double kvo_decode_bf16(uint16_t bits)
+{
+    int sign = (bits >> 15) & 1;
+    int expo = (bits >> 7) & 0xFF;
+    int frac = bits & 0x7F;
+    double mag;
+    if (expo == 0)
+        mag = ldexp((double)frac, -133);             /* subnormal: frac * 2^(1-127-7) */
+    else if (expo == 255)
+        mag = frac ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(128 + frac), expo - 134); /* (1 + frac/2^7) * 2^(expo-127) */
+    return sign ? -mag : mag;
+}
+
+static size_t elem_size(int dtype) { return dtype == 2 ? 8 : 2; }
+
+static double load(int dtype, const void *base, int64_t idx)
+{
+    if (dtype == 0) return kvo_decode_f16(((const uint16_t *)base)[idx]);
+    if (dtype == 1) return kvo_decode_bf16(((const uint16_t *)base)[idx]);
+    return ((const double *)base)[idx];
+}
+
+static void copy_elem(int dtype, void *dst, int64_t di, const void *src, int64_t si)
+{
+    size_t n = elem_size(dtype);
+    memcpy((char *)dst + (size_t)di * n, (const char *)src + (size_t)si * n, n);
+}
+
+/* ---- A1: append the new tokens' K/V to the cache -----------------------------------
+ *
+ * [N] "KV キャッシュが推論を最適化する方法", steps 2-3: after the first pass only the newest
+ * token's K and V are computed, and they are added to the stored per-layer K/V whose
+ * shape is (batch, heads, seq_len_cached, head_dim). [W] "Inference 抽象と KV キャッシュ":
+ * the self-attention projections of the new token are concatenated onto the cached
+ * sequence along the sequence axis.
+ *
+ * K, V: [batch, heads, capacity, head_dim] with element strides sb, sh, st (1 over D).
+ * k_new, v_new: contiguous [batch, heads, q, head_dim].
+ * K[b,h,lens_in[b]+j,:] = k_new[b,h,j,:] for j < q; lens_out[b] = lens_in[b] + q.
+ * A row with lens_in[b] + q > capacity (or lens_in[b] < 0) is left untouched,
+ * lens_out[b] = lens_in[b], and the length-overflow bit is returned.
+ */
+unsigned kvo_kv_append(int dtype, int batch, int heads, int capacity, int head_dim, int q,
+                       void *K, void *V, int64_t sb, int64_t sh, int64_t st,
+                       const void *k_new, const void *v_new,
+                       const int32_t *lens_in, int32_t *lens_out)
+{
+    unsigned err = 0;
+    for (int b = 0; b < batch; ++b) {
+        int32_t len = lens_in[b];
+        if (len < 0 || (int64_t)len + q > capacity) {
+            err |= KVO_ERR_LEN_OVERFLOW;
+            if (lens_out) lens_out[b] = len;
+            continue;
+        }
+        for (int h = 0; h < heads; ++h)
+            for (int j = 0; j < q; ++j)
+                for (int d = 0; d < head_dim; ++d) {
+                    int64_t dst = b * sb + h * sh + (int64_t)(len + j) * st + d;
+                    int64_t src = (((int64_t)b * heads + h) * q + j) * head_dim + d;
+                    copy_elem(dtype, K, dst, k_new, src);
+                    copy_elem(dtype, V, dst, v_new, src);
+                }
+        if (lens_out) lens_out[b] = len + q;
+    }
+    return err;
+}
+
+/* ---- A2 / A3 / A5: attention of a query block over cached K/V ----------------------
+ *
+ * [N] "KV キャッシュが推論を最適化する方法", step 4: the current token's query is combined
+ * with the cached K and V to produce the output. [W] "Inference 抽象と KV キャッシュ": the
+ * attention layer sees the whole concatenated key/value sequence, the token just
+ * appended included; cross-attention K/V come from the encoder output, are computed
+ * on the first pass and then reused. [S] "추측 디코딩이란?" and [A]: the main model checks
+ * all candidate tokens in a single forward pass -- query i of a block of nq new tokens
+ * sits at absolute position len - nq + i and (causal) sees positions 0 .. len - nq + i.
+ * [N] "nanoVLM における技術的実装", item 1: grouped attention, several query heads read
+ * one K/V head.
+ *
+ * q:   contiguous [batch, n_q_heads, nq, head_dim]
+ * K,V: [kv_batch, n_kv_heads, capacity, head_dim] with strides sb, sh, st
+ * row r reads cache row r / rows_per_kv; query head hq reads KV head hq / (n_q/n_kv).
+ * len = lens ? lens[r / rows_per_kv] : fixed_len.
+ * out[r,hq,i,:] = sum_{t < limit} softmax_t(scale * q.K_t) V_t in double, where
+ * limit = len (non-causal) or len - nq + 1 + i (causal). limit <= 0 gives zeros.
+ * Two passes over the positions: max of the scores, then sum of exp(score - max),
+ * then the weighted sum of V divided by that sum.
+ */
+unsigned kvo_attention(int dtype, int batch, int n_q_heads, int nq, int head_dim,
+                       const void *q, int n_kv_heads, int capacity,
+                       const void *K, const void *V, int64_t sb, int64_t sh, int64_t st,
+                       const int32_t *lens, int fixed_len, int rows_per_kv, int causal,
+                       double scale, double *out)
+{
+    unsigned err = 0;
+    int group = n_q_heads / n_kv_heads;
+    for (int r = 0; r < batch; ++r) {
+        int bk = r / rows_per_kv;
+        int32_t len = lens ? lens[bk] : fixed_len;
+        for (int hq = 0; hq < n_q_heads; ++hq) {
+            int h = hq / group;
+            for (int i = 0; i < nq; ++i) {
+                double *o = out + (((int64_t)r * n_q_heads + hq) * nq + i) * head_dim;
+                const int64_t qoff = (((int64_t)r * n_q_heads + hq) * nq + i) * head_dim;
+                for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+                if (len < 0 || len > capacity) {
+                    err |= KVO_ERR_LEN_OVERFLOW;
+                    continue;
+                }
+                int limit = causal ? len - nq + 1 + i : len;
+                if (limit > len) limit = len;
+                if (limit <= 0) continue;
+
+                double m = -INFINITY;
+                for (int t = 0; t < limit; ++t) {
+                    double s = 0.0;
+                    for (int d = 0; d < head_dim; ++d)
+                        s += load(dtype, q, qoff + d) *
+                             load(dtype, K, bk * sb + h * sh + (int64_t)t * st + d);
+                    s *= scale;
+                    if (s > m) m = s;
+                }
+                double l = 0.0;
+                for (int t = 0; t < limit; ++t) {
+                    double s = 0.0;
+                    for (int d = 0; d < head_dim; ++d)
+                        s += load(dtype, q, qoff + d) *
+                             load(dtype, K, bk * sb + h * sh + (int64_t)t * st + d);
+                    s *= scale;
+                    double w = exp(s - m);
+                    l += w;
+                    for (int d = 0; d < head_dim; ++d)
+                        o[d] += w * load(dtype, V, bk * sb + h * sh + (int64_t)t * st + d);
+                }
+                for (int d = 0; d < head_dim; ++d) o[d] /= l;
+            }
+        }
+    }
+    return err;
+}
+
+/* ---- A6: greedy verification -- accept up to the first mismatch --------------------
+ *
+ * [W] "Inference 抽象と KV キャッシュ" (GreedyDecoder): at temperature 0 the next token is
+ * the argmax of the logits. [S] "추측 디코딩이란?" and [A]: the main model's token at each
+ * candidate position is compared with the candidate; candidates are accepted up to the
+ * first mismatch, the mismatching candidate is replaced by the main model's token and
+ * the rest are dropped. [S] "배치 크기 고려사항": in a batch, every row's candidates must
+ * match for the batch to advance together -- n_min is the per-batch minimum.
+ *
+ * logits: [batch, k+1, vocab] fp32; draft: [batch, k] int32.
+ * a_i = argmax_v logits[b,i,v]: the first (lowest) index on ties; a NaN ranks above
+ * every number and the first NaN wins; -inf is an ordinary value.
+ * n_b = first i < k with draft[b,i] != a_i (an id outside [0, vocab) never matches),
+ * or k when all k match; next_b = a_{n_b}. Outputs that are NULL are skipped.
+ */
+static int beats(float cand, float best)
+{
+    if (isnan(best)) return 0;
+    if (isnan(cand)) return 1;
+    return cand > best;
+}
+
+unsigned kvo_greedy_accept(int batch, int k, int vocab, const float *logits,
+                           const int32_t *draft, int32_t *n_accepted, int32_t *next_token,
+                           int32_t *n_min, int32_t *argmax_out)
+{
+    unsigned err = 0;
+    int32_t running_min = k;
+    int32_t *amax = (int32_t *)malloc(sizeof(int32_t) * (size_t)(k + 1));
+    if (!amax) return ~0u;
+    for (int b = 0; b < batch; ++b) {
+        for (int i = 0; i <= k; ++i) {
+            const float *row = logits + ((int64_t)b * (k + 1) + i) * vocab;
+            int32_t best = 0;
+            for (int v = 0; v < vocab; ++v) {
+                if (isnan(row[v])) err |= KVO_ERR_NAN;
+                if (v > 0 && beats(row[v], row[best])) best = v;
+            }
+            amax[i] = best;
+            if (argmax_out) argmax_out[b * (k + 1) + i] = best;
+        }
+        int32_t n = k;
+        for (int i = 0; i < k; ++i) {
+            int32_t d = draft[(int64_t)b * k + i];
+            if (d < 0 || d >= vocab) err |= KVO_ERR_BAD_TOKEN;
+        }
+        for (int i = 0; i < k; ++i) {
+            int32_t d = draft[(int64_t)b * k + i];
+            if (d < 0 || d >= vocab || d != amax[i]) {
+                n = i;
+                break;
+            }
+        }
+        if (n_accepted) n_accepted[b] = n;
+        if (next_token) next_token[b] = amax[n];
+        if (n < running_min) running_min = n;
+    }
+    if (n_min) *n_min = running_min;
+    free(amax);
+    return err;
+}
+
+/* ---- A7: beam-search cache reorder ------------------------------------------------
+ *
+ * [W] "Inference 抽象と KV キャッシュ" (BeamSearchDecoder.update and rearrange_kv_cache):
+ * after the beams are re-ranked the stored key/value tensors must be put in the new
+ * beam order; otherwise a beam would continue from another beam's cache.
+ *
+ * One layer's K or V: src, dst [rows, heads, capacity, head_dim] with strides sb, sh,
+ * st (same for both). Row r belongs to window r / beam; its parent must lie in that
+ * window's block [w*beam, (w+1)*beam), else the bad-index bit is set and the row keeps
+ * its own data. dst[r,h,t,:] = src[parent[r],h,t,:] for t < len; positions t >= len
+ * keep dst[r] = src[r]. len outside [0, capacity] sets the length bit and copies src.
+ * Written out-of-place on purpose: dst and src must not overlap.
+ */
+unsigned kvo_beam_reorder(int dtype, int rows, int beam, int heads, int capacity,
+                          int head_dim, int len, const int32_t *parent,
+                          const void *src, void *dst, int64_t sb, int64_t sh, int64_t st)
+{
+    unsigned err = 0;
+    if (len < 0 || len > capacity) {
+        err |= KVO_ERR_LEN_OVERFLOW;
+        len = 0;
+    }
+    for (int r = 0; r < rows; ++r) {
+        int w = r / beam;
+        int p = parent[r];
+        if (p < w * beam || p >= (w + 1) * beam) {
+            err |= KVO_ERR_BAD_INDEX;
+            p = r;
+        }
+        for (int h = 0; h < heads; ++h)
+            for (int t = 0; t < capacity; ++t) {
+                int from = t < len ? p : r;
+                for (int d = 0; d < head_dim; ++d)
+                    copy_elem(dtype, dst, r * sb + h * sh + (int64_t)t * st + d,
+                              src, from * sb + h * sh + (int64_t)t * st + d);
+            }
+    }
+    return err;
+}
