@@ -1,0 +1,269 @@
+/*
+ * kvdecode.h -- C ABI of the GB300 (sm_103a) KV-cached decoder-step library.
+ *
+ * The library implements the data-parallel hot path of KV-cached autoregressive
+ * decoding: appending the new tokens' K/V to a per-layer cache, single-query
+ * attention over that cache and over cross-attention K/V computed once per audio
+ * window, the k-token causal verify pass of speculative decoding, the greedy
+ * accept-to-first-mismatch step, and the beam-search cache reorder.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [W] readoss.com, "Whisper のデコーダー内部：Beam Search、Logit フィルター、KV キャッシュ"
+ *   [S] agentlenshq.com, "추측 디코딩으로 Whisper 추론 속도 2배 향상"
+ *   [N] agentlenshq.com, "nanoVLM における KV キャッシュ実装"
+ *   [A] aitime.ge, Whisper speculative-decoding article ("The quick brown sock/fox" example)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Memory: every tensor pointer is DEVICE memory owned by the caller. The library
+ *    never allocates, frees or synchronises. Calls are asynchronous on `stream`
+ *    (a cudaStream_t; NULL is the legacy default stream) and contain no host
+ *    synchronisation, so they can be captured in a CUDA graph.
+ *  - Host errors: a non-KVD_OK status is returned synchronously and nothing is
+ *    launched (null pointers, unsupported shapes, misalignment, a workspace that is
+ *    too small). KVD_ERR_CUDA reports a launch failure (cudaGetLastError).
+ *  - Device errors: conditions only visible on the device (a length past the
+ *    capacity, a parent outside its window, a draft id outside the vocabulary, a
+ *    NaN logit) are written to `*dev_err` with an atomic compare-and-swap from 0, so
+ *    the first code wins; the offending unit of work is skipped, nothing traps and
+ *    nothing spins. `dev_err` (device int32) may be NULL to ignore them. The caller
+ *    reads and clears it when it chooses.
+ *  - Layout: a per-layer cache is K, V : [batch, n_kv_heads, capacity, head_dim],
+ *    head_dim contiguous ([N] "KV キャッシュが推論を最適化する方法": the per-layer key
+ *    and value tensors are kept as (batch, heads, seq_len_cached, head_dim)). Other
+ *    strides are given in elements. head_dim must be 64. Pointers and the strides
+ *    times the element size must be multiples of 16 bytes.
+ *  - Types: KVD_F16 or KVD_BF16 for q, the cache and the outputs; arithmetic is fp32
+ *    and outputs are rounded to nearest even. greedy_accept reads fp32 logits.
+ *  - Workspace: the attention and accept calls split work across thread blocks and
+ *    merge partial results through `workspace` (device memory, at least
+ *    kvd_workspace_size() bytes, 256-byte aligned). Its first KVD_WS_COUNTER_BYTES
+ *    hold arrival counters that MUST be zero before the first call that uses the
+ *    buffer; every call returns them to zero when it completes. One workspace may be
+ *    shared by calls on one stream; calls that may run concurrently need separate
+ *    workspaces.
+ *  - Flags: KVD_FLAG_PDL launches the kernel with programmatic stream serialization
+ *    (Hopper/Blackwell programmatic dependent launch): it may start while the
+ *    previous kernel on the stream finishes and waits for it before reading any
+ *    input or writing any output. KVD_FLAG_EARLY_KV (attention only, implies PDL)
+ *    additionally lets it read the lengths and start loading cache K/V BEFORE that
+ *    wait; use it only when the previous kernel on the stream writes neither the
+ *    cache positions being attended nor `lens` (true of cross-attention K/V, which
+ *    are written once per window).
+ *  - Threading: no global mutable state except a per-device attribute cache; calls
+ *    from several host threads are safe.
+ */
+#ifndef KVDECODE_H
+#define KVDECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *kvd_stream_t; /* identical to cudaStream_t */
+
+typedef enum kvd_status {
+    KVD_OK = 0,
+    KVD_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad alignment, aliasing */
+    KVD_ERR_UNSUPPORTED = 2,  /* head_dim != 64, qlen > 16, beam > 8, ... */
+    KVD_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than kvd_workspace_size() */
+    KVD_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+    /* device-side codes, written to *dev_err */
+    KVD_ERR_LEN_OVERFLOW = 16, /* a length < 0 or > capacity (or lens + q > capacity) */
+    KVD_ERR_BAD_INDEX = 17,    /* a beam parent outside its window's block */
+    KVD_ERR_BAD_TOKEN = 18,    /* a draft id outside [0, vocab) */
+    KVD_ERR_NAN = 19,          /* a NaN among the logits */
+    KVD_ERR_TIMEOUT = 20       /* a bounded wait for a shared-memory copy gave up; the
+                                  workspace counters may be left non-zero: re-zero them */
+} kvd_status;
+
+typedef enum kvd_dtype { KVD_F16 = 0, KVD_BF16 = 1 } kvd_dtype;
+
+typedef enum kvd_op {
+    KVD_OP_DECODE_ATTN = 0,
+    KVD_OP_VERIFY_ATTN = 1,
+    KVD_OP_GREEDY_ACCEPT = 2
+} kvd_op;
+
+enum {
+    KVD_FLAG_PDL = 1u << 0,
+    KVD_FLAG_EARLY_KV = 1u << 1
+};
+
+#define KVD_WS_COUNTER_BYTES 65536
+#define KVD_HEAD_DIM 64
+#define KVD_MAX_QLEN 16
+#define KVD_MAX_BEAM 8
+#define KVD_MAX_LAYERS_PER_CALL 64
+
+/* One layer's cache: K and V share the shape and strides. */
+typedef struct kvd_cache {
+    void *k;
+    void *v;
+    int64_t stride_b;   /* elements between consecutive batch rows            */
+    int64_t stride_h;   /* elements between consecutive KV heads               */
+    int64_t stride_t;   /* elements between consecutive positions (>= 64)      */
+    int32_t batch;      /* rows of the cache (kv batch)                        */
+    int32_t n_kv_heads;
+    int32_t head_dim;   /* must be 64                                          */
+    int32_t capacity;   /* positions allocated per (row, head)                 */
+} kvd_cache;
+
+/*
+ * kvd_kv_append -- A1. Write the new tokens' K/V into the cache.
+ *
+ * [N] "KV キャッシュが推論を最適化する方法", steps 2-3 (only the newest token's K/V are
+ * computed and added to the cache); [W] "Inference 抽象と KV キャッシュ" (the
+ * self-attention projections of the new token are concatenated along the sequence
+ * axis). Here the cache is preallocated, so the append is an O(q) write, not a
+ * reallocation.
+ *
+ *   K[b, h, lens_in[b] + j, :] = k_new[b, h, j, :]  (same for V), j < q, b < batch
+ *   lens_out[b] = lens_in[b] + q                     (if lens_out != NULL)
+ *
+ * k_new, v_new : device [batch, n_kv_heads, q, 64], contiguous
+ * lens_in      : device int32 [batch], read only
+ * lens_out     : device int32 [batch] or NULL; must not alias lens_in. Every layer of
+ *                a step may pass the same lens_out: it writes the same values.
+ * Device error : lens_in[b] < 0 or lens_in[b] + q > capacity -> KVD_ERR_LEN_OVERFLOW,
+ *                row b is not written and lens_out[b] = lens_in[b].
+ */
+kvd_status kvd_kv_append(kvd_dtype dtype, const kvd_cache *cache, int32_t batch, int32_t q,
+                         const void *k_new, const void *v_new, const int32_t *lens_in,
+                         int32_t *lens_out, uint32_t flags, int32_t *dev_err,
+                         kvd_stream_t stream);
+
+/*
+ * kvd_decode_attn -- A2/A3 (+A4). One query token per row attends over the cache.
+ *
+ * [N] "KV キャッシュが推論を最適化する方法", step 4 (the current token's query meets the
+ * cached K/V); [W] "Inference 抽象と KV キャッシュ" (attention sees the full
+ * concatenated sequence, the token just appended included; cross-attention K/V are
+ * computed from the encoder output once and reused); [N] "nanoVLM における技術的実装"
+ * item 1 (grouped attention: n_q_heads / n_kv_heads query heads share a KV head).
+ *
+ *   out[r, hq, 0, :] = sum_{t < len} softmax_t(scale * q[r,hq] . K[b,h,t]) V[b,h,t]
+ *   b = r / rows_per_kv, h = hq / (n_q_heads / kv->n_kv_heads),
+ *   len = lens ? lens[b] : fixed_len
+ *
+ * q, out       : device [batch, n_q_heads, 1, 64], contiguous
+ * kv           : cache with kv->batch >= batch / rows_per_kv
+ * lens         : device int32 [batch / rows_per_kv] (e.g. lens_out of kv_append) or
+ *                NULL to use fixed_len (cross-attention: 1500 encoder frames)
+ * rows_per_kv  : rows r .. r+rows_per_kv-1 share cache row r / rows_per_kv (beam rows
+ *                of one audio window share its cross K/V); batch % rows_per_kv == 0
+ * len == 0 gives a zero output. Long caches are split across thread blocks and the
+ * partial results merged with their log-sum-exp weights (flash-decoding).
+ * Device error : len < 0 or len > capacity -> KVD_ERR_LEN_OVERFLOW, output left as is.
+ */
+kvd_status kvd_decode_attn(kvd_dtype dtype, int32_t batch, int32_t n_q_heads, const void *q,
+                           const kvd_cache *kv, const int32_t *lens, int32_t fixed_len,
+                           int32_t rows_per_kv, float scale, void *out, void *workspace,
+                           size_t workspace_bytes, uint32_t flags, int32_t *dev_err,
+                           kvd_stream_t stream);
+
+/*
+ * kvd_verify_attn -- A5. A block of qlen query tokens per row in one pass.
+ *
+ * [S] "추측 디코딩이란?" and [A]: the main model checks all candidate tokens in a single
+ * forward pass. The block's K/V are already appended (kvd_kv_append with q = qlen),
+ * so query i sits at absolute position len - qlen + i:
+ *
+ *   causal:     out[r,hq,i,:] = sum_{t <= len - qlen + i} softmax(...) V_t
+ *   non-causal: out[r,hq,i,:] = sum_{t < len} softmax(...) V_t   (cross-attention)
+ *
+ * q, out : device [batch, n_q_heads, qlen, 64], contiguous; 1 <= qlen <= 16.
+ * The Q.K^T and P.V products run on the tensor cores. Other arguments and errors as
+ * kvd_decode_attn; a causal row with len < qlen sees only its visible positions and a
+ * query with no visible position gets a zero output.
+ */
+kvd_status kvd_verify_attn(kvd_dtype dtype, int32_t batch, int32_t n_q_heads, int32_t qlen,
+                           const void *q, const kvd_cache *kv, const int32_t *lens,
+                           int32_t fixed_len, int32_t rows_per_kv, int32_t causal,
+                           float scale, void *out, void *workspace, size_t workspace_bytes,
+                           uint32_t flags, int32_t *dev_err, kvd_stream_t stream);
+
+/*
+ * kvd_greedy_accept -- A6. Greedy verification of k draft tokens.
+ *
+ * [W] "Inference 抽象と KV キャッシュ" (GreedyDecoder: argmax at temperature 0);
+ * [S] "추측 디코딩이란?" and [A] (accept candidates up to the first mismatch, replace
+ * the mismatch by the main model's token, drop the rest); [S] "배치 크기 고려사항"
+ * (in a batch all rows must match to advance together: n_min).
+ *
+ *   a_i    = argmax_v logits[b, i, v], i = 0..k (lowest index on ties; a NaN ranks
+ *            above every number and the first NaN wins; -inf is an ordinary value)
+ *   n_b    = min { i < k : draft[b, i] != a_i }, or k if all match
+ *   next_b = a_{n_b}           (the correction, or the bonus token when n_b == k)
+ *   emitted tokens: draft[b, 0..n_b-1] followed by next_b; the caller rolls its
+ *   caches back to L_before + n_b + 1 positions (a length change only).
+ *
+ * logits     : device fp32 [batch, k+1, vocab], contiguous; 1 <= k <= 16
+ * draft      : device int32 [batch, k]
+ * n_accepted, next_token : device int32 [batch]
+ * n_min      : device int32 [1] or NULL -- min_b n_b
+ * argmax     : device int32 [batch, k+1] or NULL -- every a_i
+ * Device errors: a draft id outside [0, vocab) -> KVD_ERR_BAD_TOKEN (it never
+ * matches); a NaN logit -> KVD_ERR_NAN (outputs still follow the rule above).
+ */
+kvd_status kvd_greedy_accept(const float *logits, int32_t batch, int32_t k, int32_t vocab,
+                             const int32_t *draft, int32_t *n_accepted, int32_t *next_token,
+                             int32_t *n_min, int32_t *argmax, void *workspace,
+                             size_t workspace_bytes, uint32_t flags, int32_t *dev_err,
+                             kvd_stream_t stream);
+
+/*
+ * kvd_beam_reorder_kv -- A7. Reorder the self-attention caches of all layers.
+ *
+ * [W] "Inference 抽象と KV キャッシュ" (BeamSearchDecoder.update, rearrange_kv_cache):
+ * after beams are re-ranked the key/value tensors are put in the new beam order, so
+ * that no beam continues another beam's cache.
+ *
+ *   for every layer l < n_layers, K and V, row r < rows, head h, position t < len_r:
+ *     C'[l][r, h, t, :] = C[l][parent[r], h, t, :]
+ *   len_r = lens ? lens[r] : fixed_len. Rows are grouped in windows of `beam`; a
+ *   parent must lie in its row's window [w*beam, (w+1)*beam).
+ *
+ * In place and allocation-free: each thread block reads, for one window and one
+ * tile of positions, every source row it needs before writing any row, so repeated
+ * parents (a beam with several children) and cycles are handled without scratch.
+ * Rows whose parent is themselves are not touched. Cross-attention K/V are not part
+ * of the reorder (they are shared per window).
+ *
+ * layers   : host array of n_layers caches (n_layers <= 64), each with batch >= rows
+ * parent   : device int32 [rows]; beam in 1..8; rows % beam == 0
+ * lens     : device int32 [rows] or NULL to use fixed_len
+ * Device errors: parent outside its window -> KVD_ERR_BAD_INDEX (row left as is);
+ * len_r < 0 or > capacity -> KVD_ERR_LEN_OVERFLOW (row left as is).
+ */
+kvd_status kvd_beam_reorder_kv(kvd_dtype dtype, const kvd_cache *layers, int32_t n_layers,
+                               int32_t rows, int32_t beam, const int32_t *parent,
+                               const int32_t *lens, int32_t fixed_len, uint32_t flags,
+                               int32_t *dev_err, kvd_stream_t stream);
+
+/*
+ * kvd_workspace_size -- bytes of workspace a call needs (always includes the
+ * KVD_WS_COUNTER_BYTES counter region). Arguments not used by `op` are ignored:
+ *   KVD_OP_DECODE_ATTN : batch, n_q_heads, n_kv_heads, rows_per_kv, max_len
+ *   KVD_OP_VERIFY_ATTN : the same plus qlen
+ *   KVD_OP_GREEDY_ACCEPT: batch, qlen = k, vocab
+ * max_len is an upper bound of the attended length (the capacity, or fixed_len).
+ * Returns 0 for invalid arguments.
+ */
+size_t kvd_workspace_size(kvd_op op, int32_t batch, int32_t n_q_heads, int32_t n_kv_heads,
+                          int32_t rows_per_kv, int32_t qlen, int32_t max_len, int32_t vocab);
+
+/* Human-readable name of a status code (static storage). */
+const char *kvd_status_string(kvd_status status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int32_t kvd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVDECODE_H */

@@ -1,0 +1,199 @@
+"""Python binding of ``libkvdecode.so`` -- the GB300 KV-cached decoder-step library.
+
+Argument marshalling only: every function passes ``torch.Tensor.data_ptr()`` values,
+sizes and the current CUDA stream to the C entry point of the same name declared in
+``include/kvdecode.h``; all work happens in the library's CUDA kernels. There is no
+fallback: if the library has not been built (``python -m kv_cached_decode_gb300.build``)
+or a call fails, an exception is raised.
+
+Tensors: caches are ``[batch, n_kv_heads, capacity, 64]`` fp16/bf16 CUDA tensors with
+the last axis contiguous; queries/outputs are contiguous ``[batch, n_q_heads, qlen, 64]``;
+lengths, drafts, parents and outputs of ``kvd_greedy_accept`` are int32 CUDA tensors;
+logits are contiguous fp32 ``[batch, k+1, vocab]``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvdecode.so")
+
+KVD_OK = 0
+STATUS_NAMES = {0: "KVD_OK", 1: "KVD_ERR_INVALID_ARG", 2: "KVD_ERR_UNSUPPORTED",
+                3: "KVD_ERR_WORKSPACE", 4: "KVD_ERR_CUDA", 16: "KVD_ERR_LEN_OVERFLOW",
+                17: "KVD_ERR_BAD_INDEX", 18: "KVD_ERR_BAD_TOKEN", 19: "KVD_ERR_NAN",
+                20: "KVD_ERR_TIMEOUT"}
+KVD_F16, KVD_BF16 = 0, 1
+KVD_OP_DECODE_ATTN, KVD_OP_VERIFY_ATTN, KVD_OP_GREEDY_ACCEPT = 0, 1, 2
+KVD_FLAG_PDL, KVD_FLAG_EARLY_KV = 1, 2
+KVD_WS_COUNTER_BYTES = 65536
+HEAD_DIM = 64
+
+EXPORTED = ("kvd_kv_append", "kvd_decode_attn", "kvd_verify_attn", "kvd_greedy_accept",
+            "kvd_beam_reorder_kv", "kvd_workspace_size", "kvd_status_string", "kvd_version")
+
+
+class KvdError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        super().__init__(f"{call} failed: {STATUS_NAMES.get(status, status)}")
+
+
+class Cache(ctypes.Structure):
+    """Mirror of ``kvd_cache``: one layer's K and V buffers with shared strides."""
+
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("stride_b", ctypes.c_int64), ("stride_h", ctypes.c_int64),
+                ("stride_t", ctypes.c_int64), ("batch", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("capacity", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load the CUDA library (raises if it was never built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m kv_cached_decode_gb300.build` "
+                "(there is no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        P, I32, U32, F, SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_float,
+                              ctypes.c_size_t)
+        CP = ctypes.POINTER(Cache)
+        sig = {
+            "kvd_kv_append": [I32, CP, I32, I32, P, P, P, P, U32, P, P],
+            "kvd_decode_attn": [I32, I32, I32, P, CP, P, I32, I32, F, P, P, SZ, U32, P, P],
+            "kvd_verify_attn": [I32, I32, I32, I32, P, CP, P, I32, I32, I32, F, P, P, SZ, U32,
+                                P, P],
+            "kvd_greedy_accept": [P, I32, I32, I32, P, P, P, P, P, P, SZ, U32, P, P],
+            "kvd_beam_reorder_kv": [I32, CP, I32, I32, I32, P, P, I32, U32, P, P],
+            "kvd_workspace_size": [I32, I32, I32, I32, I32, I32, I32, I32],
+            "kvd_status_string": [I32],
+            "kvd_version": [],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = I32
+        lib.kvd_workspace_size.restype = SZ
+        lib.kvd_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return KVD_F16
+    if t.dtype == torch.bfloat16:
+        return KVD_BF16
+    raise TypeError(f"expected float16 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, call: str):
+    if status != KVD_OK:
+        raise KvdError(status, call)
+
+
+def make_cache(k: torch.Tensor, v: torch.Tensor) -> Cache:
+    """Describe one layer's ``[batch, heads, capacity, 64]`` K/V tensors for the C ABI."""
+    if k.shape != v.shape or k.stride() != v.stride() or k.dtype != v.dtype:
+        raise ValueError("K and V must share shape, strides and dtype")
+    if k.dim() != 4 or k.shape[3] != HEAD_DIM or k.stride(3) != 1:
+        raise ValueError("cache must be [batch, heads, capacity, 64] with the last axis contiguous")
+    if not (k.is_cuda and v.is_cuda):
+        raise ValueError("cache tensors must be CUDA tensors")
+    B, H, cap, D = k.shape
+    return Cache(k.data_ptr(), v.data_ptr(), k.stride(0), k.stride(1), k.stride(2), B, H, D, cap)
+
+
+def kvd_version() -> int:
+    return load_library().kvd_version()
+
+
+def kvd_status_string(status: int) -> str:
+    return load_library().kvd_status_string(status).decode()
+
+
+def kvd_workspace_size(op: int, batch: int, n_q_heads: int = 1, n_kv_heads: int = 1,
+                       rows_per_kv: int = 1, qlen: int = 1, max_len: int = 0,
+                       vocab: int = 0) -> int:
+    return load_library().kvd_workspace_size(op, batch, n_q_heads, n_kv_heads, rows_per_kv,
+                                             qlen, max_len, vocab)
+
+
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zero-filled device workspace (the counter region must start at zero)."""
+    return torch.zeros(max(int(nbytes), KVD_WS_COUNTER_BYTES), dtype=torch.uint8,
+                       device=device or "cuda")
+
+
+def kvd_kv_append(cache: Cache, k_new, v_new, lens_in, lens_out=None, flags: int = 0,
+                  dev_err=None, stream=None):
+    B, H, q, D = k_new.shape
+    _check(load_library().kvd_kv_append(_dtype_code(k_new), ctypes.byref(cache), B, q, _ptr(k_new),
+                                        _ptr(v_new), _ptr(lens_in), _ptr(lens_out), flags,
+                                        _ptr(dev_err), _stream(stream)), "kvd_kv_append")
+
+
+def kvd_decode_attn(q, cache: Cache, out, workspace, lens=None, fixed_len: int = 0,
+                    rows_per_kv: int = 1, scale: float = 0.125, flags: int = 0,
+                    dev_err=None, stream=None):
+    B, Hq, ql, D = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().kvd_decode_attn(_dtype_code(q), B, Hq, _ptr(q), ctypes.byref(cache),
+                                          _ptr(lens), fixed_len, rows_per_kv, scale, _ptr(out),
+                                          _ptr(workspace), ws_bytes, flags, _ptr(dev_err),
+                                          _stream(stream)), "kvd_decode_attn")
+
+
+def kvd_verify_attn(q, cache: Cache, out, workspace, lens=None, fixed_len: int = 0,
+                    rows_per_kv: int = 1, causal: bool = True, scale: float = 0.125,
+                    flags: int = 0, dev_err=None, stream=None):
+    B, Hq, ql, D = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().kvd_verify_attn(_dtype_code(q), B, Hq, ql, _ptr(q),
+                                          ctypes.byref(cache), _ptr(lens), fixed_len,
+                                          rows_per_kv, int(bool(causal)), scale, _ptr(out),
+                                          _ptr(workspace), ws_bytes, flags, _ptr(dev_err),
+                                          _stream(stream)), "kvd_verify_attn")
+
+
+def kvd_greedy_accept(logits, draft, n_accepted, next_token, workspace, n_min=None,
+                      argmax=None, flags: int = 0, dev_err=None, stream=None):
+    B, k1, V = logits.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load_library().kvd_greedy_accept(_ptr(logits), B, k1 - 1, V, _ptr(draft),
+                                            _ptr(n_accepted), _ptr(next_token), _ptr(n_min),
+                                            _ptr(argmax), _ptr(workspace), ws_bytes, flags,
+                                            _ptr(dev_err), _stream(stream)), "kvd_greedy_accept")
+
+
+def kvd_beam_reorder_kv(caches, rows: int, beam: int, parent, lens=None, fixed_len: int = 0,
+                        dtype=torch.float16, flags: int = 0, dev_err=None, stream=None):
+    arr = (Cache * len(caches))(*caches)
+    code = KVD_F16 if dtype == torch.float16 else KVD_BF16
+    _check(load_library().kvd_beam_reorder_kv(code, arr, len(caches), rows, beam,
+                                              _ptr(parent), _ptr(lens), fixed_len, flags,
+                                              _ptr(dev_err), _stream(stream)),
+           "kvd_beam_reorder_kv")

@@ -1,0 +1,222 @@
+// greedy_accept.cu -- A6: greedy verification of k draft tokens.
+//
+// "추측 디코딩이란?" of "추측 디코딩으로 Whisper 추론 속도 2배 향상" and the aitime.ge
+// speculative-decoding article: the main model's token at every candidate position is
+// compared with the candidate; candidates are kept up to the first mismatch, the
+// mismatch is replaced by the main model's token and the rest are dropped. At
+// temperature 0 the main model's token is the argmax of its logits (GreedyDecoder in
+// "Inference 抽象と KV キャッシュ" of "Whisper のデコーダー内部"). "배치 크기 고려사항":
+// rows of a batch advance together only as far as every row matched -> n_min.
+//
+// Design: the [batch, k+1, vocab] fp32 logits (1.24 MB at k=5, vocab 51865) are read
+// once by enough thread blocks to cover the GPU. Each block reduces one segment of one
+// row to a (value, index) pair with the rule "NaN first (lowest index among NaNs), then
+// larger value, then lower index"; the last block to finish a batch row (atomic ticket)
+// reduces the segment results of its k+1 rows in index order and applies the accept
+// rule; the last batch row to finish writes the batch minimum. Integer outputs are
+// therefore exact and independent of scheduling.
+#include <algorithm>
+
+#include "kvd_common.cuh"
+#include "kvd_internal.h"
+
+namespace kvd {
+
+struct AcceptParams {
+    const float* logits;
+    const int32_t* draft;
+    int32_t* n_acc;
+    int32_t* next;
+    int32_t* n_min;
+    int32_t* amax;
+    float* ws_val;
+    int32_t* ws_idx;
+    int32_t* ws_n;
+    int32_t* cnt;  // [batch] per-row tickets, [batch] = global ticket
+    int32_t* dev_err;
+    int32_t batch, k, vocab, seg, seg_len;
+};
+
+struct Cand {
+    float v;
+    int i;  // -1 = empty
+};
+
+__device__ __forceinline__ bool beats(const Cand& a, const Cand& b) {
+    if (a.i < 0) return false;
+    if (b.i < 0) return true;
+    const bool an = isnan(a.v), bn = isnan(b.v);
+    if (an != bn) return an;
+    if (!an && a.v != b.v) return a.v > b.v;
+    return a.i < b.i;
+}
+
+__device__ __forceinline__ Cand warp_best(Cand c) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        Cand o;
+        o.v = __shfl_xor_sync(0xffffffffu, c.v, off);
+        o.i = __shfl_xor_sync(0xffffffffu, c.i, off);
+        if (beats(o, c)) c = o;
+    }
+    return c;
+}
+
+constexpr int kAcceptThreads = 256;
+
+__global__ void __launch_bounds__(kAcceptThreads) greedy_accept_kernel(const AcceptParams p) {
+    __shared__ Cand s_warp[kAcceptThreads / 32];
+    __shared__ int s_amax[KVD_MAX_QLEN + 1];
+    __shared__ int s_flag;
+    pdl_wait();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int s = blockIdx.x, row = blockIdx.y, b = blockIdx.z;
+    const int k1 = p.k + 1;
+    const float* x = p.logits + ((int64_t)b * k1 + row) * p.vocab;
+    const int lo = s * p.seg_len, hi = min(p.vocab, lo + p.seg_len);
+
+    Cand best = {0.f, -1};
+    bool saw_nan = false;
+    for (int base = lo; base < hi; base += 4 * kAcceptThreads) {
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = base + u * kAcceptThreads + tid;
+            v[u] = i < hi ? __ldcs(x + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = base + u * kAcceptThreads + tid;
+            if (i < hi) {
+                saw_nan |= isnan(v[u]);
+                const Cand c = {v[u], i};
+                if (beats(c, best)) best = c;
+            }
+        }
+    }
+    best = warp_best(best);
+    if (lane == 0) s_warp[warp] = best;
+    if (__syncthreads_or(saw_nan) && tid == 0) flag_error(p.dev_err, KVD_ERR_NAN);
+    if (warp == 0) {
+        Cand c = lane < kAcceptThreads / 32 ? s_warp[lane] : Cand{0.f, -1};
+        c = warp_best(c);
+        if (lane == 0) {
+            const int64_t slot = ((int64_t)b * k1 + row) * p.seg + s;
+            p.ws_val[slot] = c.v;
+            p.ws_idx[slot] = c.i;
+        }
+    }
+    pdl_trigger();
+
+    // ---- the last block of batch row b reduces the segments and applies the rule ----
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_flag = atomicAdd(&p.cnt[b], 1) == k1 * p.seg - 1;
+    __syncthreads();
+    if (!s_flag) return;
+    __threadfence();
+    for (int r = warp; r < k1; r += kAcceptThreads / 32) {
+        Cand c = {0.f, -1};
+        const int64_t base = ((int64_t)b * k1 + r) * p.seg;
+        for (int j = lane; j < p.seg; j += 32) {
+            const Cand o = {__ldcg(p.ws_val + base + j), __ldcg(p.ws_idx + base + j)};
+            if (beats(o, c)) c = o;
+        }
+        c = warp_best(c);
+        if (lane == 0) s_amax[r] = c.i;
+    }
+    __syncthreads();
+    if (tid != 0) return;
+    int n = p.k;
+    bool bad_token = false;
+    for (int i = 0; i < p.k; ++i) {
+        const int d = p.draft[(int64_t)b * p.k + i];
+        const bool oob = d < 0 || d >= p.vocab;
+        bad_token |= oob;
+        if (n == p.k && (oob || d != s_amax[i])) n = i;
+    }
+    if (bad_token) flag_error(p.dev_err, KVD_ERR_BAD_TOKEN);
+    p.n_acc[b] = n;
+    p.next[b] = s_amax[n];
+    if (p.amax)
+        for (int i = 0; i < k1; ++i) p.amax[(int64_t)b * k1 + i] = s_amax[i];
+    p.cnt[b] = 0;
+    if (!p.n_min) return;
+    p.ws_n[b] = n;
+    __threadfence();
+    if (atomicAdd(&p.cnt[p.batch], 1) != p.batch - 1) return;
+    __threadfence();
+    int mn = p.k;
+    for (int i = 0; i < p.batch; ++i) mn = min(mn, __ldcg(p.ws_n + i));
+    *p.n_min = mn;
+    p.cnt[p.batch] = 0;
+}
+
+namespace {
+struct AcceptPlan {
+    int seg, seg_len;
+    size_t val_off, idx_off, n_off, bytes;
+};
+AcceptPlan plan_accept(int batch, int k, int vocab, int target) {
+    AcceptPlan P;
+    const int rows = batch * (k + 1);
+    const int max_seg = std::max(1, (vocab + 2047) / 2048);
+    const int want = std::max(1, (target + rows - 1) / rows);
+    int seg = std::min(max_seg, want);
+    P.seg_len = ((vocab + seg - 1) / seg + 31) / 32 * 32;
+    P.seg = (vocab + P.seg_len - 1) / P.seg_len;
+    const size_t slots = (size_t)rows * P.seg;
+    P.val_off = KVD_WS_COUNTER_BYTES;
+    P.idx_off = P.val_off + (slots * 4 + 255) / 256 * 256;
+    P.n_off = P.idx_off + (slots * 4 + 255) / 256 * 256;
+    P.bytes = P.n_off + ((size_t)batch * 4 + 255) / 256 * 256;
+    return P;
+}
+}  // namespace
+
+size_t accept_workspace_bytes(int batch, int k, int vocab, int target) {
+    return plan_accept(batch, k, vocab, target).bytes;
+}
+
+}  // namespace kvd
+
+using namespace kvd;
+
+extern "C" kvd_status kvd_greedy_accept(const float* logits, int32_t batch, int32_t k,
+                                        int32_t vocab, const int32_t* draft,
+                                        int32_t* n_accepted, int32_t* next_token,
+                                        int32_t* n_min, int32_t* argmax, void* workspace,
+                                        size_t workspace_bytes, uint32_t flags,
+                                        int32_t* dev_err, kvd_stream_t stream) {
+    if (batch < 0 || vocab <= 0) return KVD_ERR_INVALID_ARG;
+    if (k < 1 || k > KVD_MAX_QLEN) return KVD_ERR_UNSUPPORTED;
+    if (batch == 0) return KVD_OK;
+    if (!logits || !draft || !n_accepted || !next_token) return KVD_ERR_INVALID_ARG;
+    if ((size_t)(batch + 1) * sizeof(int32_t) > KVD_WS_COUNTER_BYTES || batch > 65535)
+        return KVD_ERR_UNSUPPORTED;
+    const int nsm = sm_count();
+    if (nsm <= 0) return KVD_ERR_CUDA;
+    const AcceptPlan P = plan_accept(batch, k, vocab, 4 * nsm);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) || workspace_bytes < P.bytes)
+        return KVD_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    AcceptParams p;
+    p.logits = logits;
+    p.draft = draft;
+    p.n_acc = n_accepted;
+    p.next = next_token;
+    p.n_min = n_min;
+    p.amax = argmax;
+    p.ws_val = reinterpret_cast<float*>(ws + P.val_off);
+    p.ws_idx = reinterpret_cast<int32_t*>(ws + P.idx_off);
+    p.ws_n = reinterpret_cast<int32_t*>(ws + P.n_off);
+    p.cnt = reinterpret_cast<int32_t*>(ws);
+    p.dev_err = dev_err;
+    p.batch = batch;
+    p.k = k;
+    p.vocab = vocab;
+    p.seg = P.seg;
+    p.seg_len = P.seg_len;
+    return launch(greedy_accept_kernel, dim3(P.seg, k + 1, batch), dim3(kAcceptThreads), 0,
+                  reinterpret_cast<cudaStream_t>(stream), (flags & KVD_FLAG_PDL) != 0, p);
+}

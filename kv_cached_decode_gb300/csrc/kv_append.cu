@@ -1,0 +1,89 @@
+// kv_append.cu -- A1: write the new tokens' K/V into the preallocated cache.
+//
+// "KV キャッシュが推論を最適化する方法" (steps 2-3) of "nanoVLM における KV キャッシュ実装":
+// only the newest token's K/V are computed and added to the stored cache; "Inference 抽象
+// と KV キャッシュ" of "Whisper のデコーダー内部": they are concatenated along the sequence
+// axis. With a preallocated [batch, heads, capacity, 64] cache this is an O(q) write of
+// 16-byte chunks; nothing already cached moves.
+#include "kvd_common.cuh"
+#include "kvd_internal.h"
+
+namespace kvd {
+
+struct AppendParams {
+    uint8_t* k;
+    uint8_t* v;
+    int64_t sb, sh, st;  // bytes
+    const uint8_t* k_new;
+    const uint8_t* v_new;
+    const int32_t* lens_in;
+    int32_t* lens_out;
+    int32_t* dev_err;
+    int32_t capacity, heads, q;
+    int64_t chunks;  // 16-byte chunks per tensor: batch * heads * q * 8
+};
+
+__global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
+    pdl_wait();
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx < 2 * p.chunks) {
+        const bool is_v = idx >= p.chunks;
+        const int64_t rem = is_v ? idx - p.chunks : idx;
+        const int c = (int)(rem & 7);
+        const int64_t row = rem >> 3;  // (b, h, j)
+        const int j = (int)(row % p.q);
+        const int64_t bh = row / p.q;
+        const int h = (int)(bh % p.heads);
+        const int b = (int)(bh / p.heads);
+        const int len = p.lens_in[b];
+        const bool first = !is_v && h == 0 && j == 0 && c == 0;
+        if (len < 0 || (int64_t)len + p.q > p.capacity) {
+            if (first) {
+                flag_error(p.dev_err, KVD_ERR_LEN_OVERFLOW);
+                if (p.lens_out) p.lens_out[b] = len;
+            }
+        } else {
+            const uint4 val = *reinterpret_cast<const uint4*>((is_v ? p.v_new : p.k_new) + rem * 16);
+            uint8_t* dst = (is_v ? p.v : p.k) + b * p.sb + h * p.sh + (int64_t)(len + j) * p.st + c * 16;
+            *reinterpret_cast<uint4*>(dst) = val;
+            if (first && p.lens_out) p.lens_out[b] = len + p.q;
+        }
+    }
+    pdl_trigger();
+}
+
+}  // namespace kvd
+
+using namespace kvd;
+
+extern "C" kvd_status kvd_kv_append(kvd_dtype dtype, const kvd_cache* cache, int32_t batch,
+                                    int32_t q, const void* k_new, const void* v_new,
+                                    const int32_t* lens_in, int32_t* lens_out, uint32_t flags,
+                                    int32_t* dev_err, kvd_stream_t stream) {
+    if (dtype != KVD_F16 && dtype != KVD_BF16) return KVD_ERR_INVALID_ARG;
+    if (kvd_status s = validate_cache(cache)) return s;
+    if (batch < 0 || q < 0 || batch > cache->batch) return KVD_ERR_INVALID_ARG;
+    if (batch == 0 || q == 0) return KVD_OK;
+    if (!k_new || !v_new || !lens_in || !aligned16(k_new) || !aligned16(v_new))
+        return KVD_ERR_INVALID_ARG;
+    if (lens_out && lens_out == lens_in) return KVD_ERR_INVALID_ARG;
+    AppendParams p;
+    p.k = static_cast<uint8_t*>(cache->k);
+    p.v = static_cast<uint8_t*>(cache->v);
+    p.sb = cache->stride_b * 2;
+    p.sh = cache->stride_h * 2;
+    p.st = cache->stride_t * 2;
+    p.k_new = static_cast<const uint8_t*>(k_new);
+    p.v_new = static_cast<const uint8_t*>(v_new);
+    p.lens_in = lens_in;
+    p.lens_out = lens_out;
+    p.dev_err = dev_err;
+    p.capacity = cache->capacity;
+    p.heads = cache->n_kv_heads;
+    p.q = q;
+    p.chunks = (int64_t)batch * cache->n_kv_heads * q * 8;
+    const int64_t blocks = (2 * p.chunks + 255) / 256;
+    if (blocks > 0x7fffffff) return KVD_ERR_UNSUPPORTED;
+    return launch(kv_append_kernel, dim3((unsigned)blocks), dim3(256), 0,
+                  reinterpret_cast<cudaStream_t>(stream), (flags & KVD_FLAG_PDL) != 0, p);
+}

@@ -1,0 +1,89 @@
+// kvd_internal.h -- host-side helpers shared by the launchers (not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kvdecode.h"
+
+namespace kvd {
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// 4-D TMA descriptor over one layer's K or V cache: dims (64, capacity, heads, batch),
+// box (64 dims, min(64, capacity) positions, 1, 1), 128-byte swizzle, zero fill out of
+// range.
+kvd_status encode_cache_map(CUtensorMap* map, kvd_dtype dtype, void* base, const kvd_cache* c);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kvd_status validate_cache(const kvd_cache* c);
+
+// Launch with an optional programmatic-dependent-launch attribute; maps errors.
+// Launch with an optional programmatic-dependent-launch attribute and an optional
+// cluster shape (cluster_x CTAs along x); maps errors.
+template <typename Kernel, typename... Args>
+kvd_status launch_ex(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     bool pdl, unsigned cluster_x, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    return e == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
+}
+
+template <typename Kernel, typename... Args>
+kvd_status launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                  bool pdl, Args... args) {
+    return launch_ex(kernel, grid, block, smem, stream, pdl, 1u, args...);
+}
+
+
+// ---- attention work plan ------------------------------------------------------------
+// The query vectors of one (cache row, KV head) -- rows_per_kv rows x group query
+// heads x qlen tokens -- are processed together so every K/V tile is read once for
+// all of them; they are cut into `nsub` blocks of at most `mmax`. The attended range
+// is cut into `splits` chunks of `tiles_per_split` 64-position tiles so that about
+// `target_ctas` thread blocks exist; partial results are merged through the workspace.
+// Splits of one unit that fit in one thread-block cluster merge through distributed
+// shared memory (no workspace); more splits merge through the workspace.
+struct AttnPlan {
+    int bkv, group, M, msub, nsub, units, tiles_total, splits, tiles_per_split, stages;
+    bool cluster;
+    size_t part_offset, ml_offset, ws_bytes;
+};
+
+constexpr int kMaxStages = 4;
+constexpr int kMaxSplits = 128;        // splits per unit (merge scratch is sized for this)
+constexpr int kMaxClusterSplits = 16;  // largest cluster used for a merge
+constexpr int kWsTargetBound = 4096;   // upper bound of target_ctas used for sizing
+
+// max_cluster: largest usable cluster (1 = never merge through a cluster).
+AttnPlan plan_attention(int batch, int n_q_heads, int n_kv_heads, int rows_per_kv, int qlen,
+                        int len_bound, int mmax, int target_ctas, int max_cluster);
+
+// Workspace bytes of greedy_accept for a given target block count (greedy_accept.cu).
+size_t accept_workspace_bytes(int batch, int k, int vocab, int target_ctas);
+
+}  // namespace kvd

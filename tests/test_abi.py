@@ -1,0 +1,125 @@
+"""The C ABI library builds for sm_103a, loads, and exports every declared entry point.
+
+CPU only: nothing here launches a kernel. Host-side argument checks that fail before
+any CUDA call are exercised with fake (aligned, never dereferenced) pointers.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvdecode.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from kv_cached_decode_gb300 import build, load_library
+
+    build.build()
+    return load_library()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"\b(kvd_[a-z_0-9]+)\s*\(", text))
+
+
+def test_header_declares_the_entry_points():
+    want = {"kvd_kv_append", "kvd_decode_attn", "kvd_verify_attn", "kvd_greedy_accept",
+            "kvd_beam_reorder_kv", "kvd_workspace_size", "kvd_status_string", "kvd_version"}
+    assert want <= _declared()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in sorted(_declared()):
+        assert hasattr(lib, name), name
+
+
+def test_exports_are_plain_c_symbols(lib):
+    out = os.popen(f"nm -D --defined-only {lib._name}").read()
+    for name in _declared():
+        assert re.search(rf"\bT {name}$", out, flags=re.M), name
+
+
+def test_status_strings_and_version(lib):
+    from kv_cached_decode_gb300 import STATUS_NAMES, kvd_status_string, kvd_version
+
+    for code, name in STATUS_NAMES.items():
+        assert kvd_status_string(code).startswith(name)
+    assert kvd_status_string(99) == "unknown kvd_status"
+    assert kvd_version() >= 100
+
+
+def test_workspace_sizes_cover_the_counter_region(lib):
+    from kv_cached_decode_gb300 import (KVD_OP_DECODE_ATTN, KVD_OP_GREEDY_ACCEPT,
+                                        KVD_OP_VERIFY_ATTN, KVD_WS_COUNTER_BYTES,
+                                        kvd_workspace_size)
+
+    a = kvd_workspace_size(KVD_OP_DECODE_ATTN, 1, 20, 20, 1, 1, 1500)
+    b = kvd_workspace_size(KVD_OP_VERIFY_ATTN, 1, 20, 20, 1, 5, 448)
+    c = kvd_workspace_size(KVD_OP_GREEDY_ACCEPT, 1, qlen=5, vocab=51865)
+    assert min(a, b, c) >= KVD_WS_COUNTER_BYTES
+    assert a > KVD_WS_COUNTER_BYTES  # the 1500-frame cross attention is split
+    # invalid arguments give 0
+    assert kvd_workspace_size(KVD_OP_DECODE_ATTN, 1, 20, 3) == 0
+    assert kvd_workspace_size(KVD_OP_VERIFY_ATTN, 1, 20, 20, 1, 17, 448) == 0
+    assert kvd_workspace_size(KVD_OP_GREEDY_ACCEPT, 1, qlen=0, vocab=10) == 0
+
+
+def _fake_cache(**kw):
+    from kv_cached_decode_gb300 import Cache
+
+    c = dict(k=0x10000, v=0x20000, stride_b=20 * 448 * 64, stride_h=448 * 64, stride_t=64,
+             batch=1, n_kv_heads=20, head_dim=64, capacity=448)
+    c.update(kw)
+    return Cache(**c)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=128), 2),
+    (dict(k=0), 1),
+    (dict(k=0x10008), 1),         # not 16-byte aligned
+    (dict(stride_t=60), 1),
+    (dict(stride_h=448 * 64 + 4), 1),
+    (dict(capacity=0), 1),
+])
+def test_host_rejects_bad_caches_before_touching_the_gpu(lib, kw, status):
+    c = _fake_cache(**kw)
+    q = ctypes.c_void_p(0x30000)
+    r = lib.kvd_decode_attn(0, 1, 20, q, ctypes.byref(c), None, 10, 1, 0.125, q, None, 0, 0,
+                            None, None)
+    assert r == status
+
+
+def test_host_rejects_bad_shapes(lib):
+    c = _fake_cache()
+    q = ctypes.c_void_p(0x30000)
+    # query heads not a multiple of KV heads
+    assert lib.kvd_decode_attn(0, 1, 30, q, ctypes.byref(c), None, 10, 1, 0.125, q, None, 0, 0,
+                               None, None) == 1
+    # batch not a multiple of rows_per_kv
+    assert lib.kvd_decode_attn(0, 3, 20, q, ctypes.byref(c), None, 10, 2, 0.125, q, None, 0, 0,
+                               None, None) == 1
+    # fixed length past the capacity
+    assert lib.kvd_decode_attn(0, 1, 20, q, ctypes.byref(c), None, 449, 1, 0.125, q, None, 0,
+                               0, None, None) == 1
+    # verify block longer than 16
+    assert lib.kvd_verify_attn(0, 1, 20, 17, q, ctypes.byref(c), None, 10, 1, 1, 0.125, q,
+                               None, 0, 0, None, None) == 2
+    # append: lens_out aliasing lens_in
+    lens = ctypes.c_void_p(0x40000)
+    assert lib.kvd_kv_append(0, ctypes.byref(c), 1, 1, q, q, lens, lens, 0, None, None) == 1
+    # beam larger than 8, rows not a multiple of beam
+    arr = (type(c) * 1)(c)
+    assert lib.kvd_beam_reorder_kv(0, arr, 1, 9, 9, lens, None, 4, 0, None, None) == 2
+    assert lib.kvd_beam_reorder_kv(0, arr, 1, 7, 5, lens, None, 4, 0, None, None) == 1
+    # accept: k out of range
+    assert lib.kvd_greedy_accept(q, 1, 0, 100, q, q, q, None, None, q, 1 << 20, 0, None,
+                                 None) == 2
+    # empty batches are a no-op
+    assert lib.kvd_decode_attn(0, 0, 20, None, ctypes.byref(c), None, 0, 1, 0.125, None, None,
+                               0, 0, None, None) == 0
