@@ -166,6 +166,38 @@ kvd_status kvd_decode_attn(kvd_dtype dtype, int32_t batch, int32_t n_q_heads, co
                            kvd_stream_t stream);
 
 /*
+ * kvd_decode_attn_noalloc -- kvd_decode_attn for callers that cannot allocate.
+ *
+ * The pages have no counterpart: this is a library convenience. Some callers cannot
+ * hand the library a workspace: a plugin or custom-op interface that passes an op
+ * only its input and output pointers, a server that reserves its whole memory budget
+ * at start-up and may not allocate in the decode loop, or a host that must not take
+ * the allocator's locks or device-wide synchronisation at that point. For them this
+ * entry point takes the same arguments as kvd_decode_attn minus the workspace, and
+ * does the same computation with the same kernel, merging split partial results in a
+ * fixed scratch buffer of KVD_NOALLOC_SCRATCH_BYTES compiled into the library (every
+ * GPU that loads the library holds it until the process exits). It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ *  - Set-up: the first call on each device looks up the scratch address there
+ *    (cudaGetSymbolAddress, with that device current). Make that first call before
+ *    any stream capture.
+ *  - Every call first clears the scratch's arrival counters on `stream` (a 64 KiB
+ *    memset of the library's own buffer; nothing else), then launches the kernel.
+ *  - All calls on a device share the one buffer: calls that can overlap on the GPU
+ *    (different streams, or graphs replayed concurrently) race and give wrong results.
+ *    Serialise them on one stream.
+ *  - Shapes whose split merge needs more than the buffer holds return
+ *    KVD_ERR_WORKSPACE and launch no kernel; use kvd_decode_attn with a workspace.
+ */
+#define KVD_NOALLOC_SCRATCH_BYTES (512u * 1024u)
+kvd_status kvd_decode_attn_noalloc(kvd_dtype dtype, int32_t batch, int32_t n_q_heads,
+                                   const void *q, const kvd_cache *kv, const int32_t *lens,
+                                   int32_t fixed_len, int32_t rows_per_kv, float scale,
+                                   void *out, uint32_t flags, int32_t *dev_err,
+                                   kvd_stream_t stream);
+
+/*
  * kvd_verify_attn -- A5. A block of qlen query tokens per row in one pass.
  *
  * [S] "추측 디코딩이란?" and [A]: the main model checks all candidate tokens in a single

@@ -35,7 +35,8 @@ KVD_WS_COUNTER_BYTES = 65536
 HEAD_DIM = 64
 
 EXPORTED = ("kvd_kv_append", "kvd_decode_attn", "kvd_verify_attn", "kvd_greedy_accept",
-            "kvd_beam_reorder_kv", "kvd_workspace_size", "kvd_status_string", "kvd_version")
+            "kvd_beam_reorder_kv", "kvd_workspace_size", "kvd_status_string", "kvd_version",
+            "kvd_decode_attn_noalloc")
 
 
 class KvdError(RuntimeError):
@@ -75,6 +76,7 @@ def load_library(path: str = LIB_PATH):
         sig = {
             "kvd_kv_append": [I32, CP, I32, I32, P, P, P, P, U32, P, P],
             "kvd_decode_attn": [I32, I32, I32, P, CP, P, I32, I32, F, P, P, SZ, U32, P, P],
+            "kvd_decode_attn_noalloc": [I32, I32, I32, P, CP, P, I32, I32, F, P, U32, P, P],
             "kvd_verify_attn": [I32, I32, I32, I32, P, CP, P, I32, I32, I32, F, P, P, SZ, U32,
                                 P, P],
             "kvd_greedy_accept": [P, I32, I32, I32, P, P, P, P, P, P, SZ, U32, P, P],
@@ -165,6 +167,18 @@ def kvd_decode_attn(q, cache: Cache, out, workspace, lens=None, fixed_len: int =
                                           _ptr(lens), fixed_len, rows_per_kv, scale, _ptr(out),
                                           _ptr(workspace), ws_bytes, flags, _ptr(dev_err),
                                           _stream(stream)), "kvd_decode_attn")
+
+
+def kvd_decode_attn_noalloc(q, cache: Cache, out, lens=None, fixed_len: int = 0,
+                            rows_per_kv: int = 1, scale: float = 0.125, flags: int = 0,
+                            dev_err=None, stream=None):
+    """kvd_decode_attn without a workspace: the library's built-in scratch is used."""
+    B, Hq, ql, D = q.shape
+    _check(load_library().kvd_decode_attn_noalloc(_dtype_code(q), B, Hq, _ptr(q),
+                                                  ctypes.byref(cache), _ptr(lens), fixed_len,
+                                                  rows_per_kv, scale, _ptr(out), flags,
+                                                  _ptr(dev_err), _stream(stream)),
+           "kvd_decode_attn_noalloc")
 
 
 def kvd_verify_attn(q, cache: Cache, out, workspace, lens=None, fixed_len: int = 0,

@@ -815,3 +815,46 @@ extern "C" kvd_status kvd_verify_attn(kvd_dtype dtype, int32_t batch, int32_t n_
                           rows_per_kv, causal, scale, out, workspace, workspace_bytes, flags,
                           dev_err, reinterpret_cast<cudaStream_t>(stream));
 }
+
+// ---------------------------------------------------------------- no-allocation entry
+// kvd_decode_attn_noalloc: the decode kernel with its split-merge scratch in a buffer
+// compiled into the library, for callers that cannot allocate a workspace (see
+// kvdecode.h). Host code must never pass `g_noalloc_scratch` itself to a kernel: on the
+// host that name is only a stand-in for the device symbol. The device address is looked
+// up once per device with cudaGetSymbolAddress while that device is current.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[KVD_NOALLOC_SCRATCH_BYTES];
+
+namespace kvd {
+namespace {
+std::once_flag g_noalloc_once[kMaxDev];
+void* g_noalloc_ptr[kMaxDev];
+cudaError_t g_noalloc_err[kMaxDev];
+
+kvd_status noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return KVD_ERR_CUDA;
+    std::call_once(g_noalloc_once[dev], [dev] {
+        g_noalloc_err[dev] = cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_noalloc_scratch);
+    });
+    if (g_noalloc_err[dev] != cudaSuccess || !g_noalloc_ptr[dev]) return KVD_ERR_CUDA;
+    *out = g_noalloc_ptr[dev];
+    return KVD_OK;
+}
+}  // namespace
+}  // namespace kvd
+
+extern "C" kvd_status kvd_decode_attn_noalloc(kvd_dtype dtype, int32_t batch, int32_t n_q_heads,
+                                              const void* q, const kvd_cache* kv,
+                                              const int32_t* lens, int32_t fixed_len,
+                                              int32_t rows_per_kv, float scale, void* out,
+                                              uint32_t flags, int32_t* dev_err,
+                                              kvd_stream_t stream) {
+    void* scratch = nullptr;
+    if (kvd_status s = kvd::noalloc_scratch(&scratch)) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // The buffer keeps whatever the previous call left; its arrival counters must start
+    // at zero, so clear them (a call that stopped early could have left them non-zero).
+    if (cudaMemsetAsync(scratch, 0, KVD_WS_COUNTER_BYTES, st) != cudaSuccess) return KVD_ERR_CUDA;
+    return kvd::attention(false, dtype, batch, n_q_heads, 1, q, kv, lens, fixed_len, rows_per_kv,
+                          0, scale, out, scratch, KVD_NOALLOC_SCRATCH_BYTES, flags, dev_err, st);
+}
