@@ -74,7 +74,7 @@ class WhisperStep:
     """Device state and launches of the timed step (see the module docstring)."""
 
     def __init__(self, device, L_decode=447, L_verify=443, k=5, seed_salt=0, flags=0,
-                 cross_flags=None):
+                 cross_flags=None, fused=True):
         import torch
 
         import kv_cached_decode_gb300 as kvd
@@ -87,6 +87,8 @@ class WhisperStep:
         # Cross K/V are written once per audio window, never by the kernel before a
         # cross-attention call, so those calls may stage K/V before the dependency wait.
         self.cross_flags = flags if cross_flags is None else cross_flags
+        # fused: the new tokens' K/V are appended inside the self-attention call
+        self.fused = fused
         self.scale = w["scale"]
         dev = device
         H, cap, F, NL = self.H, self.cap, self.F, self.NL
@@ -198,29 +200,43 @@ class WhisperStep:
     def run_decode(self, layers=None, parts=("append", "self", "cross")):
         kvd, f = self.kvd, self.flags
         for l in range(self.NL) if layers is None else layers:
-            if "append" in parts:
-                kvd.kvd_kv_append(self.c_dec_self[l], self.kn1[l], self.vn1[l], self.dec_lens_in,
-                                  self.dec_lens, flags=f, dev_err=self.err)
-            if "self" in parts:
-                kvd.kvd_decode_attn(self.q_self[l], self.c_dec_self[l], self.o_self[l], self.ws,
-                                    lens=self.dec_lens, scale=self.scale, flags=f,
-                                    dev_err=self.err)
+            if self.fused:
+                if "self" in parts:
+                    kvd.kvd_decode_attn(self.q_self[l], self.c_dec_self[l], self.o_self[l],
+                                        self.ws, lens=self.dec_lens_in, scale=self.scale,
+                                        flags=self.cross_flags, dev_err=self.err,
+                                        append=(self.kn1[l], self.vn1[l], self.dec_lens))
+            else:
+                if "append" in parts:
+                    kvd.kvd_kv_append(self.c_dec_self[l], self.kn1[l], self.vn1[l],
+                                      self.dec_lens_in, self.dec_lens, flags=f, dev_err=self.err)
+                if "self" in parts:
+                    kvd.kvd_decode_attn(self.q_self[l], self.c_dec_self[l], self.o_self[l],
+                                        self.ws, lens=self.dec_lens, scale=self.scale, flags=f,
+                                        dev_err=self.err)
             if "cross" in parts:
                 kvd.kvd_decode_attn(self.q_cross[l], self.c_dec_cross[l], self.o_cross[l],
                                     self.ws, fixed_len=self.F, scale=self.scale,
-                                    flags=self.cross_flags,
-                                    dev_err=self.err)
+                                    flags=self.cross_flags, dev_err=self.err)
 
     def run_verify(self, layers=None, parts=("append", "self", "cross", "accept")):
         kvd, f = self.kvd, self.flags
         for l in range(self.NL) if layers is None else layers:
-            if "append" in parts:
-                kvd.kvd_kv_append(self.c_ver_self[l], self.kn5[l], self.vn5[l], self.ver_lens_in,
-                                  self.ver_lens, flags=f, dev_err=self.err)
-            if "self" in parts:
-                kvd.kvd_verify_attn(self.qv_self[l], self.c_ver_self[l], self.ov_self[l], self.ws,
-                                    lens=self.ver_lens, causal=True, scale=self.scale, flags=f,
-                                    dev_err=self.err)
+            if self.fused:
+                if "self" in parts:
+                    kvd.kvd_verify_attn(self.qv_self[l], self.c_ver_self[l], self.ov_self[l],
+                                        self.ws, lens=self.ver_lens_in, causal=True,
+                                        scale=self.scale, flags=self.cross_flags,
+                                        dev_err=self.err,
+                                        append=(self.kn5[l], self.vn5[l], self.ver_lens))
+            else:
+                if "append" in parts:
+                    kvd.kvd_kv_append(self.c_ver_self[l], self.kn5[l], self.vn5[l],
+                                      self.ver_lens_in, self.ver_lens, flags=f, dev_err=self.err)
+                if "self" in parts:
+                    kvd.kvd_verify_attn(self.qv_self[l], self.c_ver_self[l], self.ov_self[l],
+                                        self.ws, lens=self.ver_lens, causal=True,
+                                        scale=self.scale, flags=f, dev_err=self.err)
             if "cross" in parts:
                 kvd.kvd_verify_attn(self.qv_cross[l], self.c_ver_cross[l], self.ov_cross[l],
                                     self.ws, fixed_len=self.F, causal=False, scale=self.scale,
@@ -233,7 +249,7 @@ class WhisperStep:
         self.run_decode()
         self.run_verify()
 
-    launches_per_step = property(lambda self: 6 * self.NL + 1)
+    launches_per_step = property(lambda self: (4 if self.fused else 6) * self.NL + 1)
 
     # -- algorithmic bytes --------------------------------------------------------------
     def bytes_decode(self):
@@ -417,9 +433,14 @@ def run_ours(args):
     kbuild.build()
     import kv_cached_decode_gb300 as kvd
 
-    flags = kvd.KVD_FLAG_PDL if (args.pdl or args.early_kv) else 0
-    cross_flags = flags | (kvd.KVD_FLAG_EARLY_KV if args.early_kv else 0)
-    step = WhisperStep(dev, flags=flags, cross_flags=cross_flags)
+    fused = args.mode == "fused"
+    if fused:  # the default: fused append, PDL everywhere, early K/V staging
+        flags = kvd.KVD_FLAG_PDL
+        cross_flags = kvd.KVD_FLAG_PDL | kvd.KVD_FLAG_EARLY_KV
+    else:
+        flags = kvd.KVD_FLAG_PDL if (args.pdl or args.early_kv) else 0
+        cross_flags = flags | (kvd.KVD_FLAG_EARLY_KV if args.early_kv else 0)
+    step = WhisperStep(dev, flags=flags, cross_flags=cross_flags, fused=fused)
     stream = torch.cuda.Stream(device=dev)
     g = capture(torch, step.run, stream)
 
@@ -499,12 +520,19 @@ def run_ours(args):
     cross_bytes = attn_bytes(1, H, H, F, 1)
     t_cross = kern_time("decode_attn_cross_1500", lambda: step.run_decode(parts=("cross",)),
                         step.NL, cross_bytes)
-    kern_time("decode_attn_self_448", lambda: step.run_decode(parts=("self",)), step.NL,
-              attn_bytes(1, H, H, L, 1))
-    kern_time("kv_append_q1", lambda: step.run_decode(parts=("append",)), step.NL,
-              append_bytes(1, H, 1))
-    kern_time("verify_attn_self_448_q5", lambda: step.run_verify(parts=("self",)), step.NL,
-              attn_bytes(1, H, H, step.Lv + step.k, step.k))
+    if fused:
+        kern_time("decode_attn_self_448_fused_append", lambda: step.run_decode(parts=("self",)),
+                  step.NL, attn_bytes(1, H, H, L, 1) + append_bytes(1, H, 1))
+        kern_time("verify_attn_self_448_q5_fused_append",
+                  lambda: step.run_verify(parts=("self",)), step.NL,
+                  attn_bytes(1, H, H, step.Lv + step.k, step.k) + append_bytes(1, H, step.k))
+    else:
+        kern_time("decode_attn_self_448", lambda: step.run_decode(parts=("self",)), step.NL,
+                  attn_bytes(1, H, H, L, 1))
+        kern_time("kv_append_q1", lambda: step.run_decode(parts=("append",)), step.NL,
+                  append_bytes(1, H, 1))
+        kern_time("verify_attn_self_448_q5", lambda: step.run_verify(parts=("self",)), step.NL,
+                  attn_bytes(1, H, H, step.Lv + step.k, step.k))
     kern_time("verify_attn_cross_1500_q5", lambda: step.run_verify(parts=("cross",)), step.NL,
               attn_bytes(1, H, H, F, step.k))
     kern_time("greedy_accept_6x51865", lambda: step.run_verify(layers=[], parts=("accept",)), 1,
@@ -535,7 +563,9 @@ def run_ours(args):
                    "bytes_per_step": bytes_step,
                    "l2": "inputs larger than L2: 640 MB of distinct K/V per step",
                    "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}",
-                   "flags": ("pdl+early-kv(cross)" if args.early_kv else
+                   "mode": args.mode,
+                   "flags": ("pdl, early K/V staging in every attention call" if fused else
+                             "pdl+early-kv(cross)" if args.early_kv else
                              "pdl" if args.pdl else "none")},
         "pct_of_8tbs": round(100 * value / NOMINAL_HBM_GBS / world, 2),
         "decode_attn_gbs": round(bytes_dec / (ms_dec * 1e-3) / 1e9, 2),
@@ -557,16 +587,148 @@ def run_ours(args):
     return 0
 
 
+def run_sweep(args):
+    """Decode-attention sweep (batch x length x heads) and the beam-search step.
+
+    Timing only (parity of these shapes is in the tests). Caches are slices of one
+    pool of seeded normals (torch Philox on the device) holding at least twice the L2,
+    and consecutive launches use distinct slices, so no launch finds its K/V in L2.
+    Prints one JSON line per point.
+    """
+    import torch
+
+    from kv_cached_decode_gb300 import build as kbuild
+
+    kbuild.build()
+    import kv_cached_decode_gb300 as kvd
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    peak, peak_kind = measured_hbm_peak()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20240)
+    flags = kvd.KVD_FLAG_PDL if (args.pdl or args.early_kv) else 0
+    if args.early_kv:
+        flags |= kvd.KVD_FLAG_EARLY_KV
+    w = WORKLOADS["decode_sweep"]
+    for (Hq, Hkv) in w["heads"]:
+        for B in w["batches"]:
+            for L in w["lens"]:
+                half = B * Hkv * L * D          # elements of K (or V)
+                slice_elems = 2 * half
+                pool_elems = max(2 * l2 // 2, slice_elems)
+                n = max(1, min(256, pool_elems // slice_elems))
+                pool = torch.empty(n * slice_elems, dtype=torch.float16, device=dev)
+                pool.normal_(0.0, 0.125, generator=gen)
+                caches = []
+                for i in range(n):
+                    base = pool[i * slice_elems:(i + 1) * slice_elems]
+                    k = base[:half].view(B, Hkv, L, D)
+                    v = base[half:].view(B, Hkv, L, D)
+                    caches.append(kvd.make_cache(k, v))
+                q = torch.empty(B, Hq, 1, D, dtype=torch.float16, device=dev).normal_(
+                    0.0, 0.125, generator=gen)
+                out = torch.empty_like(q)
+                lens = torch.full((B,), L, dtype=torch.int32, device=dev)
+                ws = kvd.new_workspace(kvd.kvd_workspace_size(kvd.KVD_OP_DECODE_ATTN, B, Hq, Hkv,
+                                                              1, 1, L), device=dev)
+
+                def fn():
+                    for c in caches:
+                        kvd.kvd_decode_attn(q, c, out, ws, lens=lens, flags=flags)
+
+                g = capture(torch, fn, stream)
+                reps = max(3, int(2e-3 / max(1e-9, n * 2e-6)))
+                t = time_graph(torch, g, stream, reps) / n  # ms per launch
+                nbytes = attn_bytes(B, Hq, Hkv, L, 1)
+                gbs = nbytes / (t * 1e-3) / 1e9
+                print(json.dumps({"sweep": "decode_attn", "batch": B, "len": L, "heads": f"{Hq}/{Hkv}",
+                                  "us": round(t * 1e3, 3), "bytes": nbytes, "gbs": round(gbs, 1),
+                                  "pct_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 1),
+                                  f"pct_{peak_kind}": round(100 * gbs / peak, 1),
+                                  "distinct_slices": n, "flags": flags}), flush=True)
+                del pool, caches, g
+                torch.cuda.empty_cache()
+    run_beam_step(torch, kvd, dev, stream, peak, flags)
+    return 0
+
+
+def run_beam_step(torch, kvd, dev, stream, peak, flags):
+    """Beam search step: 8 windows x beam 5 = 40 rows, 32 layers, 20 heads, fp16,
+    capacity 448: beam_reorder_kv over all layers, then per layer append, self decode
+    over len+1 positions and cross decode over 1500 frames shared per window."""
+    w = WORKLOADS["beam_step"]
+    W, beam, NL, H, cap, F = w["windows"], w["beam"], w["n_layers"], w["n_q_heads"], w["capacity"], w["cross_len"]
+    R = W * beam
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5050)
+    f16 = torch.float16
+    selfs = [(torch.empty(R, H, cap, D, dtype=f16, device=dev).normal_(0, 0.125, generator=gen),
+              torch.empty(R, H, cap, D, dtype=f16, device=dev).normal_(0, 0.125, generator=gen))
+             for _ in range(NL)]
+    cross = [(torch.empty(W, H, F, D, dtype=f16, device=dev).normal_(0, 0.125, generator=gen),
+              torch.empty(W, H, F, D, dtype=f16, device=dev).normal_(0, 0.125, generator=gen))
+             for _ in range(NL)]
+    c_self = [kvd.make_cache(*kv) for kv in selfs]
+    c_cross = [kvd.make_cache(*kv) for kv in cross]
+    parent_np = gen_parents(make_rng(seed_for("beam_step")), W, beam)
+    parent = torch.from_numpy(parent_np).to(dev)
+    q = torch.empty(R, H, 1, D, dtype=f16, device=dev).normal_(0, 0.125, generator=gen)
+    kn = torch.empty(R, H, 1, D, dtype=f16, device=dev).normal_(0, 0.125, generator=gen)
+    out = torch.empty_like(q)
+    ws = kvd.new_workspace(kvd.kvd_workspace_size(kvd.KVD_OP_DECODE_ATTN, R, H, H, beam, 1, F),
+                           device=dev)
+    moved = int(np.sum(parent_np != np.arange(R)))
+    for L in w["lens"]:
+        lens_in = torch.full((R,), L, dtype=torch.int32, device=dev)
+        lens = torch.full((R,), L + 1, dtype=torch.int32, device=dev)
+
+        def reorder():
+            kvd.kvd_beam_reorder_kv(c_self, R, beam, parent, lens=lens_in, flags=flags)
+
+        def step():
+            reorder()
+            for l in range(NL):
+                kvd.kvd_kv_append(c_self[l], kn, kn, lens_in, lens, flags=flags)
+                kvd.kvd_decode_attn(q, c_self[l], out, ws, lens=lens, flags=flags)
+                kvd.kvd_decode_attn(q, c_cross[l], out, ws, fixed_len=F, rows_per_kv=beam,
+                                    flags=flags)
+
+        t_re = time_graph(torch, capture(torch, reorder, stream), stream, 50)
+        t_step = time_graph(torch, capture(torch, step, stream), stream, 50)
+        # reorder: distinct sources read + moved rows written, per layer, K and V
+        srcs = sum(len({int(parent_np[r]) for r in range(wi * beam, (wi + 1) * beam)
+                        if parent_np[r] != r}) for wi in range(W))
+        row = H * L * D * 2
+        re_bytes = NL * 2 * (srcs + moved) * row
+        step_bytes = re_bytes + NL * (append_bytes(R, H, 1) + attn_bytes(R, H, H, L + 1, 1)
+                                      + attn_bytes(R, H, H, F, 1, windows=W))
+        print(json.dumps({"sweep": "beam_step", "rows": R, "len": L,
+                          "reorder_us": round(t_re * 1e3, 2),
+                          "reorder_gbs": round(re_bytes / (t_re * 1e-3) / 1e9, 1),
+                          "step_us": round(t_step * 1e3, 2),
+                          "step_gbs": round(step_bytes / (t_step * 1e-3) / 1e9, 1),
+                          "tokens_per_s": round(R / (t_step * 1e-3), 1),
+                          "moved_rows": moved, "source_rows": srcs}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--mode", choices=["fused", "separate"], default="fused",
+                    help="fused: append inside the self-attention call with PDL and early K/V "
+                         "staging (default); separate: kv_append then attention")
     ap.add_argument("--pdl", action="store_true", help="launch with programmatic dependent launch")
     ap.add_argument("--early-kv", action="store_true",
                     help="PDL, and cross-attention calls stage K/V before the dependency wait")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="decode-attention batch x length sweep and the beam step (JSON lines)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu DRAM bytes per launch of the dominant kernel, if measured")
@@ -575,6 +737,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 

@@ -43,13 +43,16 @@
  *    shared by calls on one stream; calls that may run concurrently need separate
  *    workspaces.
  *  - Flags: KVD_FLAG_PDL launches the kernel with programmatic stream serialization
- *    (Hopper/Blackwell programmatic dependent launch): it may start while the
- *    previous kernel on the stream finishes and waits for it before reading any
- *    input or writing any output. KVD_FLAG_EARLY_KV (attention only, implies PDL)
- *    additionally lets it read the lengths and start loading cache K/V BEFORE that
- *    wait; use it only when the previous kernel on the stream writes neither the
- *    cache positions being attended nor `lens` (true of cross-attention K/V, which
- *    are written once per window).
+ *    (programmatic dependent launch): it may start while the previous kernel on the
+ *    stream is still running, waits for that kernel to finish before reading any
+ *    input or writing any output, and lets the next kernel start once its own first
+ *    copies are issued. KVD_FLAG_EARLY_KV (attention only; implies KVD_FLAG_PDL) also
+ *    reads `lens` and starts copying cached K/V BEFORE that wait. Use it only when no
+ *    kernel that can still be running writes those cache positions or `lens`: cross
+ *    K/V written once per audio window qualify, and so does a self cache whose new
+ *    tokens come through the fused append (they are never read from the cache in the
+ *    call that appends them). q, the new tokens, outputs and the workspace are always
+ *    accessed after the wait.
  *  - Threading: no global mutable state except a per-device attribute cache; calls
  *    from several host threads are safe.
  */
@@ -98,6 +101,13 @@ enum {
 #define KVD_MAX_QLEN 16
 #define KVD_MAX_BEAM 8
 #define KVD_MAX_LAYERS_PER_CALL 64
+
+/* The new tokens' K/V for a fused append inside an attention call. */
+typedef struct kvd_new_tokens {
+    const void *k_new;  /* device [kv_batch, n_kv_heads, qlen, 64], contiguous */
+    const void *v_new;  /* same shape                                         */
+    int32_t *lens_out;  /* device [kv_batch] or NULL: receives lens + qlen     */
+} kvd_new_tokens;
 
 /* One layer's cache: K and V share the shape and strides. */
 typedef struct kvd_cache {
@@ -153,17 +163,25 @@ kvd_status kvd_kv_append(kvd_dtype dtype, const kvd_cache *cache, int32_t batch,
  * kv           : cache with kv->batch >= batch / rows_per_kv
  * lens         : device int32 [batch / rows_per_kv] (e.g. lens_out of kv_append) or
  *                NULL to use fixed_len (cross-attention: 1500 encoder frames)
+ * append       : NULL, or the new token's K/V ([kv_batch, n_kv_heads, 1, 64]) to append
+ *                in the same launch: they are written at position lens[b] and attention
+ *                runs over lens[b] + 1 positions (lens = the length BEFORE the append,
+ *                required); lens_out, if given, receives lens + 1. This equals
+ *                kvd_kv_append followed by kvd_decode_attn, without the extra launch.
  * rows_per_kv  : rows r .. r+rows_per_kv-1 share cache row r / rows_per_kv (beam rows
  *                of one audio window share its cross K/V); batch % rows_per_kv == 0
  * len == 0 gives a zero output. Long caches are split across thread blocks and the
- * partial results merged with their log-sum-exp weights (flash-decoding).
- * Device error : len < 0 or len > capacity -> KVD_ERR_LEN_OVERFLOW, output left as is.
+ * partial results merged with their log-sum-exp weights (flash-decoding). One query
+ * vector per KV head runs on CUDA cores; two or more (grouped-query heads, beam rows
+ * sharing a window) form a small GEMM and run on the tensor cores.
+ * Device error : len < 0 or len (+1 when appending) > capacity -> KVD_ERR_LEN_OVERFLOW,
+ *                output and cache left as is.
  */
 kvd_status kvd_decode_attn(kvd_dtype dtype, int32_t batch, int32_t n_q_heads, const void *q,
                            const kvd_cache *kv, const int32_t *lens, int32_t fixed_len,
-                           int32_t rows_per_kv, float scale, void *out, void *workspace,
-                           size_t workspace_bytes, uint32_t flags, int32_t *dev_err,
-                           kvd_stream_t stream);
+                           const kvd_new_tokens *append, int32_t rows_per_kv, float scale,
+                           void *out, void *workspace, size_t workspace_bytes, uint32_t flags,
+                           int32_t *dev_err, kvd_stream_t stream);
 
 /*
  * kvd_decode_attn_noalloc -- kvd_decode_attn for callers that cannot allocate.
@@ -193,9 +211,9 @@ kvd_status kvd_decode_attn(kvd_dtype dtype, int32_t batch, int32_t n_q_heads, co
 #define KVD_NOALLOC_SCRATCH_BYTES (512u * 1024u)
 kvd_status kvd_decode_attn_noalloc(kvd_dtype dtype, int32_t batch, int32_t n_q_heads,
                                    const void *q, const kvd_cache *kv, const int32_t *lens,
-                                   int32_t fixed_len, int32_t rows_per_kv, float scale,
-                                   void *out, uint32_t flags, int32_t *dev_err,
-                                   kvd_stream_t stream);
+                                   int32_t fixed_len, const kvd_new_tokens *append,
+                                   int32_t rows_per_kv, float scale, void *out, uint32_t flags,
+                                   int32_t *dev_err, kvd_stream_t stream);
 
 /*
  * kvd_verify_attn -- A5. A block of qlen query tokens per row in one pass.
@@ -208,15 +226,19 @@ kvd_status kvd_decode_attn_noalloc(kvd_dtype dtype, int32_t batch, int32_t n_q_h
  *   non-causal: out[r,hq,i,:] = sum_{t < len} softmax(...) V_t   (cross-attention)
  *
  * q, out : device [batch, n_q_heads, qlen, 64], contiguous; 1 <= qlen <= 16.
+ * append  : NULL, or the block's K/V ([kv_batch, n_kv_heads, qlen, 64]) appended in the
+ *           same launch at positions lens[b] .. lens[b]+qlen-1 (lens = the length
+ *           before the append); attention then runs as if kvd_kv_append had run first.
  * The Q.K^T and P.V products run on the tensor cores. Other arguments and errors as
  * kvd_decode_attn; a causal row with len < qlen sees only its visible positions and a
  * query with no visible position gets a zero output.
  */
 kvd_status kvd_verify_attn(kvd_dtype dtype, int32_t batch, int32_t n_q_heads, int32_t qlen,
                            const void *q, const kvd_cache *kv, const int32_t *lens,
-                           int32_t fixed_len, int32_t rows_per_kv, int32_t causal,
-                           float scale, void *out, void *workspace, size_t workspace_bytes,
-                           uint32_t flags, int32_t *dev_err, kvd_stream_t stream);
+                           int32_t fixed_len, const kvd_new_tokens *append,
+                           int32_t rows_per_kv, int32_t causal, float scale, void *out,
+                           void *workspace, size_t workspace_bytes, uint32_t flags,
+                           int32_t *dev_err, kvd_stream_t stream);
 
 /*
  * kvd_greedy_accept -- A6. Greedy verification of k draft tokens.

@@ -55,6 +55,13 @@ class Cache(ctypes.Structure):
                 ("capacity", ctypes.c_int32)]
 
 
+class NewTokens(ctypes.Structure):
+    """Mirror of ``kvd_new_tokens``: new K/V appended inside an attention call."""
+
+    _fields_ = [("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+                ("lens_out", ctypes.c_void_p)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -73,12 +80,13 @@ def load_library(path: str = LIB_PATH):
         P, I32, U32, F, SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_float,
                               ctypes.c_size_t)
         CP = ctypes.POINTER(Cache)
+        NP = ctypes.POINTER(NewTokens)
         sig = {
             "kvd_kv_append": [I32, CP, I32, I32, P, P, P, P, U32, P, P],
-            "kvd_decode_attn": [I32, I32, I32, P, CP, P, I32, I32, F, P, P, SZ, U32, P, P],
-            "kvd_decode_attn_noalloc": [I32, I32, I32, P, CP, P, I32, I32, F, P, U32, P, P],
-            "kvd_verify_attn": [I32, I32, I32, I32, P, CP, P, I32, I32, I32, F, P, P, SZ, U32,
-                                P, P],
+            "kvd_decode_attn": [I32, I32, I32, P, CP, P, I32, NP, I32, F, P, P, SZ, U32, P, P],
+            "kvd_decode_attn_noalloc": [I32, I32, I32, P, CP, P, I32, NP, I32, F, P, U32, P, P],
+            "kvd_verify_attn": [I32, I32, I32, I32, P, CP, P, I32, NP, I32, I32, F, P, P, SZ,
+                                U32, P, P],
             "kvd_greedy_accept": [P, I32, I32, I32, P, P, P, P, P, P, SZ, U32, P, P],
             "kvd_beam_reorder_kv": [I32, CP, I32, I32, I32, P, P, I32, U32, P, P],
             "kvd_workspace_size": [I32, I32, I32, I32, I32, I32, I32, I32],
@@ -110,6 +118,15 @@ def _ptr(t):
 def _stream(stream):
     s = torch.cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _append_arg(append):
+    """``append`` is None or ``(k_new, v_new, lens_out_or_None)`` device tensors."""
+    if append is None:
+        return None
+    k_new, v_new, lens_out = append
+    return ctypes.byref(NewTokens(k_new.data_ptr(), v_new.data_ptr(),
+                                  None if lens_out is None else lens_out.data_ptr()))
 
 
 def _check(status: int, call: str):
@@ -160,35 +177,38 @@ def kvd_kv_append(cache: Cache, k_new, v_new, lens_in, lens_out=None, flags: int
 
 def kvd_decode_attn(q, cache: Cache, out, workspace, lens=None, fixed_len: int = 0,
                     rows_per_kv: int = 1, scale: float = 0.125, flags: int = 0,
-                    dev_err=None, stream=None):
+                    dev_err=None, stream=None, append=None):
     B, Hq, ql, D = q.shape
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load_library().kvd_decode_attn(_dtype_code(q), B, Hq, _ptr(q), ctypes.byref(cache),
-                                          _ptr(lens), fixed_len, rows_per_kv, scale, _ptr(out),
-                                          _ptr(workspace), ws_bytes, flags, _ptr(dev_err),
-                                          _stream(stream)), "kvd_decode_attn")
+                                          _ptr(lens), fixed_len, _append_arg(append),
+                                          rows_per_kv, scale, _ptr(out), _ptr(workspace),
+                                          ws_bytes, flags, _ptr(dev_err), _stream(stream)),
+           "kvd_decode_attn")
 
 
 def kvd_decode_attn_noalloc(q, cache: Cache, out, lens=None, fixed_len: int = 0,
                             rows_per_kv: int = 1, scale: float = 0.125, flags: int = 0,
-                            dev_err=None, stream=None):
+                            dev_err=None, stream=None, append=None):
     """kvd_decode_attn without a workspace: the library's built-in scratch is used."""
     B, Hq, ql, D = q.shape
     _check(load_library().kvd_decode_attn_noalloc(_dtype_code(q), B, Hq, _ptr(q),
                                                   ctypes.byref(cache), _ptr(lens), fixed_len,
-                                                  rows_per_kv, scale, _ptr(out), flags,
-                                                  _ptr(dev_err), _stream(stream)),
+                                                  _append_arg(append), rows_per_kv, scale,
+                                                  _ptr(out), flags, _ptr(dev_err),
+                                                  _stream(stream)),
            "kvd_decode_attn_noalloc")
 
 
 def kvd_verify_attn(q, cache: Cache, out, workspace, lens=None, fixed_len: int = 0,
                     rows_per_kv: int = 1, causal: bool = True, scale: float = 0.125,
-                    flags: int = 0, dev_err=None, stream=None):
+                    flags: int = 0, dev_err=None, stream=None, append=None):
     B, Hq, ql, D = q.shape
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load_library().kvd_verify_attn(_dtype_code(q), B, Hq, ql, _ptr(q),
                                           ctypes.byref(cache), _ptr(lens), fixed_len,
-                                          rows_per_kv, int(bool(causal)), scale, _ptr(out),
+                                          _append_arg(append), rows_per_kv, int(bool(causal)),
+                                          scale, _ptr(out),
                                           _ptr(workspace), ws_bytes, flags, _ptr(dev_err),
                                           _stream(stream)), "kvd_verify_attn")
 

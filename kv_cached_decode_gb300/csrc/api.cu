@@ -76,16 +76,19 @@ AttnPlan plan_attention(int batch, int n_q_heads, int n_kv_heads, int rows_per_k
     P.msub = (P.M + P.nsub - 1) / P.nsub;
     P.units = P.bkv * n_kv_heads * P.nsub;
     P.tiles_total = (std::max(len_bound, 0) + 63) / 64;
+    // Work is handed out in rounds of two 64-position tiles (the eight warps of a block
+    // work on two tiles at once).
+    const int rounds = (P.tiles_total + 1) / 2;
     const int want = std::max(1, (target_ctas + P.units - 1) / P.units);
-    int s = std::max(1, std::min({P.tiles_total, want, kMaxSplits}));
+    int s = std::max(1, std::min({rounds, want, kMaxSplits}));
     // Fewer, cluster-sized splits are preferred while they still give about one block
-    // per SM (target_ctas is ~4 blocks per SM): their merge stays on chip.
-    if (s > max_cluster && max_cluster > 1 && (int64_t)P.units * max_cluster * 4 >= target_ctas)
+    // per SM (target_ctas is ~2 blocks per SM): their merge stays on chip.
+    if (s > max_cluster && max_cluster > 1 && (int64_t)P.units * max_cluster * 2 >= target_ctas)
         s = max_cluster;
-    P.tiles_per_split = std::max(1, (P.tiles_total + s - 1) / s);
+    P.tiles_per_split = 2 * std::max(1, (rounds + s - 1) / s);
     P.splits = P.tiles_total > 0 ? (P.tiles_total + P.tiles_per_split - 1) / P.tiles_per_split : 1;
     P.cluster = P.splits > 1 && P.splits <= max_cluster;
-    P.stages = std::min(kMaxStages, P.tiles_per_split);
+    P.stages = P.tiles_per_split >= 4 ? 4 : 2;
     P.part_offset = KVD_WS_COUNTER_BYTES;
     const size_t slots = (size_t)P.units * P.splits * P.msub;
     P.ml_offset = align_up(P.part_offset + slots * 64 * sizeof(float), 256);
@@ -108,7 +111,9 @@ extern "C" size_t kvd_workspace_size(kvd_op op, int32_t batch, int32_t n_q_heads
             n_q_heads % n_kv_heads || batch % rows_per_kv || q < 1 || q > KVD_MAX_QLEN ||
             max_len < 0)
             return 0;
-        const int mmax = op == KVD_OP_DECODE_ATTN ? 8 : 16;
+        // one query vector per KV head runs alone; two or more go in blocks of 16
+        const int64_t M = (int64_t)rows_per_kv * (n_q_heads / n_kv_heads) * q;
+        const int mmax = M >= 2 ? kMmaQueryBlock : 1;
         // Sized for the workspace path (no cluster), which covers every launch plan.
         AttnPlan P = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, q, max_len, mmax,
                                     kWsTargetBound, 1);

@@ -1,37 +1,56 @@
-// attention.cu -- decode attention (A2/A3), verify-block attention (A5) and the split
-// merge (A4) for sm_103a.
+// attention.cu -- decode attention (A2/A3), verify-block attention (A5), the split
+// merge (A4) and the optional fused append of the new tokens (A1) for sm_103a.
 //
-// What is computed ("KV キャッシュが推論を最適化する方法" step 4 of "nanoVLM における KV
+// What is computed ("KV キャッシュが推論を最適化する方法" steps 2-4 of "nanoVLM における KV
 // キャッシュ実装"; "Inference 抽象と KV キャッシュ" of "Whisper のデコーダー内部"; "추측
 // 디코딩이란?" of "추측 디코딩으로 Whisper 추론 속도 2배 향상"):
 //   out[r,hq,i,:] = sum_{t < limit_i} softmax_t(scale * q[r,hq,i] . K[b,h,t]) V[b,h,t]
 // with b = r / rows_per_kv, h = hq / group, limit_i = len (decode, cross) or
-// len - qlen + 1 + i (causal verify block whose K/V are already appended).
+// len - qlen + 1 + i (causal verify block whose K/V are appended).
 //
 // How (GB300 design):
 //  * One thread block handles one (cache row b, KV head h, chunk of positions) and ALL
 //    query vectors that read that KV head -- rows_per_kv beam rows x group query heads x
-//    qlen tokens -- so every K/V byte is fetched from HBM once per step.
+//    qlen tokens -- so every K/V byte is fetched from HBM once per call.
 //  * K/V tiles of 64 positions x 64 dims (8 KiB each) are staged into shared memory by
-//    TMA (cp.async.bulk.tensor, 128-byte swizzle) through a ring of up to 4 stages whose
+//    TMA (cp.async.bulk.tensor, 128-byte swizzle) through a ring of 2 or 4 stages whose
 //    full-barriers are mbarriers with transaction counts; one thread issues the copies.
-//  * Decode (one query token): CUDA cores. Eight lanes share a cache position, each
-//    holding 16 bytes (8 dims) of K and V; dot products are finished with three xor
-//    shuffles and folded into an online softmax in the exp2 domain.
-//  * Verify (a block of up to 16 query vectors): tensor cores. S = Q.K^T and O = P.V
-//    run as mma.sync m16n8k16 (fp16/bf16 in, fp32 accumulate) with operands read from
-//    the swizzled tiles by ldmatrix (K) and ldmatrix.trans (V).
-//  * Long ranges are split over thread blocks; each writes its partial (max, sum, o)
-//    to the workspace and the last block to arrive (atomic ticket) merges the splits in
-//    fixed order with log-sum-exp weights, so results do not depend on timing.
+//    Eight warps work on two tiles at a time, each warp on its own 16-position slab, so
+//    a warp waits only for its own tile and no block barrier is needed except before a
+//    stage is refilled.
+//  * One query vector per KV head (plain multi-head decode) runs on CUDA cores: eight
+//    lanes share a cache position, each holding 16 bytes (8 dims) of K and V; the dot
+//    product finishes with three xor shuffles and feeds an online softmax in exp2 form.
+//  * Two to sixteen query vectors per KV head (grouped-query heads, beam rows sharing a
+//    window, a verify block) form a small GEMM and run on the tensor cores: S = Q.K^T
+//    and O = P.V as mma.sync m16n8k16 (fp16/bf16 in, fp32 accumulate), operands read
+//    from the swizzled tiles by ldmatrix (K) and ldmatrix.trans (V).
+//  * Fused append: when the new tokens' K/V are passed, the warp whose slab holds their
+//    positions writes them into the cache and into its staged tile, so attention sees
+//    them without a separate launch.
+//  * Long ranges are split over thread blocks. Splits of one unit that fit in a cluster
+//    (<= 16 CTAs) store their (max, sum, o) partials straight into the shared memory of
+//    the cluster's first CTA (st.shared::cluster) and arrive on its mbarrier; that CTA
+//    merges them locally while the others exit. More splits go through the workspace
+//    and the last block to arrive (atomic ticket) merges them. Merges run in fixed
+//    split order, so results are repeatable.
+//  * Programmatic dependent launch: every block lets the next kernel on the stream
+//    start as soon as its own copies are issued; with KVD_FLAG_EARLY_KV it also issues
+//    those copies before waiting for the previous kernel.
 #include <algorithm>
 #include <atomic>
+#include <climits>
 #include <mutex>
 
 #include "kvd_common.cuh"
 #include "kvd_internal.h"
 
 namespace kvd {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kSlot = kHeadDim + 4;   // floats per merge slot: o[64], max, sum, 2 pad
+constexpr int kSlotQuads = kSlot / 4;  // 17 float4 per slot
 
 struct AttnParams {
     const void* q;
@@ -52,7 +71,15 @@ struct AttnParams {
     int32_t stages;
     int32_t box_rows;
     int32_t early;
-    int32_t cluster;  // 1: the splits of a unit form one thread-block cluster
+    int32_t cluster;   // 1: the splits of a unit form one thread-block cluster
+    int32_t append;    // 1: k_new/v_new are written at positions lens[b] .. lens[b]+qlen-1
+    const uint8_t* k_new;
+    const uint8_t* v_new;
+    int32_t* lens_out;
+    uint8_t* kc;       // cache bases and byte strides, for the appended rows
+    uint8_t* vc;
+    int64_t sb, sh, st;
+    int32_t n_kv_heads;
     float scale_log2;
     float* ws_part;
     float2* ws_ml;
@@ -60,23 +87,30 @@ struct AttnParams {
     int32_t* dev_err;
 };
 
-// Shared memory: [stages x (K tile, V tile)] [stage barriers] [warp partials]
-// [block partial, read by the other CTAs of the cluster] [flag]
+// Shared memory: [stages x (K tile, V tile); after the tile loop the same bytes hold the
+// warp partials] [stage barriers, merge barrier] [split partials of the cluster, used in
+// its first CTA] [flag]. The last 4 KiB of the stage area are scratch for the
+// workspace merge.
 struct SmemLayout {
-    uint32_t bar_off, red_off, fin_off, misc_off, total;
+    uint32_t bar_off, red_off, mrg_off, misc_off, total;
 };
-__host__ __device__ inline SmemLayout smem_layout(int stages, int rmax) {
+__host__ __device__ inline SmemLayout smem_layout(int stages, int rmax, int merge_slots) {
     SmemLayout L;
-    L.bar_off = stages * 2 * kTileBytes;
-    L.red_off = (L.bar_off + stages * 8 + 15) & ~15u;
-    L.fin_off = L.red_off + 4 * rmax * (kHeadDim + 2) * 4;
-    L.misc_off = L.fin_off + rmax * (kHeadDim + 2) * 4;
+    const uint32_t tiles = stages * 2 * kTileBytes;
+    const uint32_t red = kWarps * rmax * (kHeadDim + 2) * 4;
+    L.red_off = 0;
+    L.bar_off = ((tiles > red ? tiles : red) + 1023) & ~1023u;
+    L.mrg_off = (L.bar_off + (stages + 1) * 8 + 15) & ~15u;
+    L.misc_off = L.mrg_off + merge_slots * kSlot * 4;
     L.total = L.misc_off + 16 + 1024;  // + slack to align the base to 1024 B
     return L;
 }
+__host__ __device__ inline int merge_slots(int cluster, int splits, int msub) {
+    return cluster ? splits * msub : 0;
+}
 
 struct CtaCtx {
-    int bk, h, sub, s, m0, mcount, len, t_begin, t_end, n_tiles, unit;
+    int bk, h, sub, s, m0, mcount, len, new0, t_begin, t_end, n_tiles, unit;
     bool bad;
 };
 
@@ -89,11 +123,13 @@ __device__ __forceinline__ void setup_ctx(const AttnParams& p, CtaCtx& c) {
     c.h = blockIdx.y / p.nsub;
     c.sub = blockIdx.y % p.nsub;
     c.bk = blockIdx.z;
-    c.unit = (c.bk * (gridDim.y / p.nsub) + c.h) * p.nsub + c.sub;
+    c.unit = (c.bk * p.n_kv_heads + c.h) * p.nsub + c.sub;
     c.m0 = c.sub * p.msub;
     c.mcount = min(p.msub, p.M - c.m0);
-    c.len = p.lens ? p.lens[c.bk] : p.fixed_len;
-    c.bad = c.len < 0 || c.len > p.capacity;
+    const int len0 = p.lens ? p.lens[c.bk] : p.fixed_len;
+    c.len = p.append ? len0 + p.qlen : len0;
+    c.new0 = p.append ? len0 : INT_MAX;
+    c.bad = len0 < 0 || c.len > p.capacity;
     c.t_begin = c.s * p.tiles_per_split * kTile;
     c.t_end = c.bad ? c.t_begin : min(c.len, c.t_begin + p.tiles_per_split * kTile);
     c.n_tiles = c.t_end > c.t_begin ? (c.t_end - c.t_begin + kTile - 1) / kTile : 0;
@@ -106,6 +142,12 @@ __device__ __forceinline__ int64_t qrow(const AttnParams& p, int bk, int h, int 
     const int r = bk * p.rows_per_kv + t2 / p.group;
     const int hq = h * p.group + t2 % p.group;
     return ((int64_t)(r * p.n_q_heads + hq) * p.qlen + i) * kHeadDim;
+}
+
+// Threads of a non-first CTA that store a piece of its partial into the first CTA (each
+// arrives once on the first CTA's merge barrier).
+__device__ __forceinline__ int merge_senders(int mcount) {
+    return min(kSlotQuads * mcount, kThreads);
 }
 
 __device__ __forceinline__ void issue_tile(const CUtensorMap* tmk, const CUtensorMap* tmv,
@@ -125,48 +167,248 @@ __device__ __forceinline__ void store_out(const AttnParams& p, const CtaCtx& c, 
     *o = Half16<T>::from_f(v);
 }
 
-// Combine the four warps' partial states, then
+// Shared prologue. Reads the length, initialises the stage barriers (and, in the first
+// CTA of a cluster, the merge barrier), issues the first copies, lets the next kernel
+// start, and waits for the previous one (before all of this unless the call was made
+// with KVD_FLAG_EARLY_KV). Returns false if the length is out of range: flagged,
+// nothing written.
+__device__ __forceinline__ bool prologue(const AttnParams& p, CtaCtx& c, uint8_t* smem,
+                                         uint64_t* bars, const CUtensorMap* tmk,
+                                         const CUtensorMap* tmv) {
+    const int tid = threadIdx.x;
+    if (!p.early) pdl_wait();
+    setup_ctx(p, c);
+    if (c.bad) {
+        if (p.early) pdl_wait();
+        if (tid == 0 && c.s == 0 && c.h == 0 && c.sub == 0) {
+            flag_error(p.dev_err, KVD_ERR_LEN_OVERFLOW);
+            if (p.append && p.lens_out) p.lens_out[c.bk] = p.lens[c.bk];
+        }
+        return false;
+    }
+    if (tid == 0) {
+        for (int j = 0; j < p.stages; ++j) mbar_init(smem_u32(&bars[j]), 1);
+        if (p.cluster && c.s == 0)
+            mbar_init(smem_u32(&bars[p.stages]), (p.splits - 1) * merge_senders(c.mcount));
+        fence_barrier_init();
+        prefetch_tensormap(tmk);
+        prefetch_tensormap(tmv);
+        const uint32_t tx = 2u * p.box_rows * kRowBytes;
+        const int first = min(p.stages, c.n_tiles);
+        for (int j = 0; j < first; ++j)
+            issue_tile(tmk, tmv, smem, bars, j, c.t_begin + j * kTile, c.h, c.bk, tx);
+    }
+    if (p.early && tid < c.mcount)  // bring the query rows into L2 while waiting
+        prefetch_l2(static_cast<const uint8_t*>(p.q) + qrow(p, c.bk, c.h, c.m0 + tid) * 2);
+    __syncthreads();
+    if (p.cluster) cluster_arrive();  // publishes the first CTA's merge barrier
+    pdl_trigger();
+    if (p.early) pdl_wait();
+    if (p.append && p.lens_out && tid == 0 && c.s == 0 && c.h == 0 && c.sub == 0)
+        p.lens_out[c.bk] = c.len;
+    return true;
+}
+
+// Fused append, per warp: the rows of this warp's 16-position slab that hold new tokens
+// come from k_new/v_new, not from the copy (which saw the cache before the append).
+// They are written into the staged tile (the warp reads only its own slab) and, by the
+// first query sub-block, into the cache.
+__device__ __forceinline__ void inject_slab(const AttnParams& p, const CtaCtx& c, uint8_t* sK,
+                                            uint8_t* sV, int tile0, int slab0) {
+    const int r0 = max(tile0 + slab0, c.new0), r1 = min(tile0 + slab0 + 16, c.len);
+    if (r0 >= r1) return;
+    const int lane = threadIdx.x & 31;
+    const int n = (r1 - r0) * 8;
+    for (int x = lane; x < 2 * n; x += 32) {
+        const bool is_v = x >= n;
+        const int y = is_v ? x - n : x;
+        const int t = r0 + (y >> 3), ch = y & 7;
+        const int j = t - c.new0;
+        const int64_t src =
+            (((int64_t)c.bk * p.n_kv_heads + c.h) * p.qlen + j) * kRowBytes + ch * 16;
+        const uint4 val = *reinterpret_cast<const uint4*>((is_v ? p.v_new : p.k_new) + src);
+        *reinterpret_cast<uint4*>((is_v ? sV : sK) + swz(t - tile0, ch)) = val;
+        if (c.sub == 0)
+            *reinterpret_cast<uint4*>((is_v ? p.vc : p.kc) + c.bk * p.sb + c.h * p.sh +
+                                      (int64_t)t * p.st + ch * 16) = val;
+    }
+    fence_proxy_async();  // the stage is refilled by TMA later
+    __syncwarp();
+}
+
+// After a timed-out wait: wait (bounded) for the latest copy issued into every stage, so
+// that none is still writing shared memory when the block exits; then keep the cluster's
+// merge consistent -- a non-first CTA still arrives (without data) on the first CTA's
+// barrier, and the first CTA waits for the others, which may still be writing into its
+// shared memory, before it exits.
+__device__ void abort_after_timeout(const AttnParams& p, const CtaCtx& c, uint64_t* bars,
+                                    int issued) {
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        flag_error(p.dev_err, KVD_ERR_TIMEOUT);
+        for (int j = max(0, issued - p.stages); j < issued; ++j)
+            mbar_wait_bounded(smem_u32(&bars[j % p.stages]), (j / p.stages) & 1);
+    }
+    __syncthreads();
+    if (p.cluster) {
+        cluster_wait();
+        if (c.s != 0) {
+            if (tid < merge_senders(c.mcount))
+                mbar_arrive_remote(map_shared(smem_u32(&bars[p.stages]), 0));
+        } else if (tid == 0) {
+            mbar_wait_bounded_cluster(smem_u32(&bars[p.stages]), 0);
+        }
+    }
+}
+
+// The tile loop shared by both kernels. Tiles are taken two at a time (a round); warp w
+// works on tile 2r + w/4, positions (w%4)*16 .. +15, through slab(sK, sV, tile0, slab0).
+// Returns false after a timeout (already handled: the caller just returns).
+template <typename Slab>
+__device__ __forceinline__ bool run_tiles(const AttnParams& p, const CtaCtx& c, uint8_t* smem,
+                                          uint64_t* bars, const CUtensorMap* tmk,
+                                          const CUtensorMap* tmv, Slab&& slab) {
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int half = warp >> 2, slab0 = (warp & 3) * 16;
+    const uint32_t tx = 2u * p.box_rows * kRowBytes;
+    bool all_ok = true;
+    int issued = min(p.stages, c.n_tiles);
+    const int rounds = (c.n_tiles + 1) / 2;
+    for (int r = 0; r < rounds; ++r) {
+        const int j = 2 * r + half;
+        if (j < c.n_tiles) {
+            const int st = j % p.stages;
+            // after a failed wait this thread does not wait again; the block aborts at the
+            // next block barrier
+            const bool ok = all_ok && mbar_wait_bounded(smem_u32(&bars[st]), (j / p.stages) & 1);
+            all_ok = ok;
+            if (ok) {
+                uint8_t* sK = smem + st * 2 * kTileBytes;
+                uint8_t* sV = sK + kTileBytes;
+                const int tile0 = c.t_begin + j * kTile;
+                if (p.append) inject_slab(p, c, sK, sV, tile0, slab0);
+                slab(sK, sV, tile0, slab0);
+            }
+        }
+        if (2 * r + p.stages < c.n_tiles) {  // this round's stages are refilled
+            if (__syncthreads_or(!all_ok)) {
+                abort_after_timeout(p, c, bars, issued);
+                return false;
+            }
+            if (tid == 0) {
+                fence_proxy_async();
+                for (int k = 0; k < 2 && 2 * r + p.stages + k < c.n_tiles; ++k) {
+                    const int jn = 2 * r + p.stages + k;
+                    issue_tile(tmk, tmv, smem, bars, jn % p.stages, c.t_begin + jn * kTile, c.h,
+                               c.bk, tx);
+                }
+            }
+            issued = min(c.n_tiles, issued + 2);
+        }
+    }
+    if (__syncthreads_or(!all_ok)) {
+        abort_after_timeout(p, c, bars, issued);
+        return false;
+    }
+    return true;
+}
+
+// Combine the eight warps' partial states, then
 //  * one split: write the output;
-//  * splits forming a cluster: publish the block's (max, sum, o) in shared memory and
-//    merge through distributed shared memory, the work spread over the cluster's CTAs;
+//  * splits forming a cluster: store the block's (max, sum, o) into the first CTA's merge
+//    slots (one float4 per thread, then one arrive per thread on its barrier); the first
+//    CTA waits for all of them and merges locally;
 //  * more splits than a cluster holds: publish to the workspace; the last block to
 //    arrive (atomic ticket) merges all splits, loading them in parallel.
 // Merges run over the splits in index order, so results do not depend on timing.
-// red: o [4][RMAX][64], m [4][RMAX], l [4][RMAX]; fin: o [RMAX][64], m [RMAX], l [RMAX].
+// red: o [8][RMAX][64], m [8][RMAX], l [8][RMAX]; mrg: [splits][msub][kSlot].
 template <typename T, int RMAX>
-__device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, float* fin,
-                           int* misc, uint8_t* stage_mem) {
+__device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, float* mrg,
+                           uint64_t* merge_bar, int* misc, uint8_t* scratch4k) {
     const float* red_o = red;
-    const float* red_m = red + 4 * RMAX * kHeadDim;
-    const float* red_l = red_m + 4 * RMAX;
-    float* fin_o = fin;
-    float* fin_m = fin + RMAX * kHeadDim;
-    float* fin_l = fin_m + RMAX;
+    const float* red_m = red + kWarps * RMAX * kHeadDim;
+    const float* red_l = red_m + kWarps * RMAX;
     const int tid = threadIdx.x;
     const int S = p.splits;
     const size_t base = (size_t)c.unit * S * p.msub;
+
+    if (S > 1 && p.cluster) {
+        cluster_wait();  // the first CTA's merge barrier is initialised
+        const bool leader = c.s == 0;
+        const uint32_t dst = leader ? 0u : map_shared(smem_u32(mrg), 0);
+        bool sent = false;
+        for (int it = tid; it < kSlotQuads * c.mcount; it += blockDim.x) {
+            const int m = it / kSlotQuads, k = it % kSlotQuads;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * RMAX + m]);
+            const float ref = mx == -INFINITY ? 0.f : mx;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float a = exp2f(red_m[w * RMAX + m] - ref);
+                if (k < kHeadDim / 4) {
+                    const float4 o = *reinterpret_cast<const float4*>(
+                        red_o + (w * RMAX + m) * kHeadDim + 4 * k);
+                    v.x = fmaf(o.x, a, v.x);
+                    v.y = fmaf(o.y, a, v.y);
+                    v.z = fmaf(o.z, a, v.z);
+                    v.w = fmaf(o.w, a, v.w);
+                } else {
+                    v.y = fmaf(red_l[w * RMAX + m], a, v.y);
+                }
+            }
+            if (k == kHeadDim / 4) v.x = mx;
+            const int slot = (c.s * p.msub + m) * kSlot + 4 * k;
+            if (leader)
+                *reinterpret_cast<float4*>(mrg + slot) = v;
+            else
+                st_dsmem4(dst + slot * 4, v);
+            sent = true;
+        }
+        if (!leader) {
+            if (sent) mbar_arrive_remote(map_shared(smem_u32(merge_bar), 0));
+            return;
+        }
+        const bool ok = mbar_wait_bounded_cluster(smem_u32(merge_bar), 0);
+        __syncthreads();  // the first CTA's own slots were written by other threads
+        if (!ok) {
+            if (tid == 0) flag_error(p.dev_err, KVD_ERR_TIMEOUT);
+            return;
+        }
+        for (int idx = tid; idx < c.mcount * kHeadDim; idx += blockDim.x) {
+            const int m = idx >> 6, d = idx & 63;
+            float mx = -INFINITY;
+            for (int r = 0; r < S; ++r) mx = fmaxf(mx, mrg[(r * p.msub + m) * kSlot + kHeadDim]);
+            const float ref = mx == -INFINITY ? 0.f : mx;
+            float l = 0.f, o = 0.f;
+            for (int r = 0; r < S; ++r) {
+                const float* sl = mrg + (r * p.msub + m) * kSlot;
+                const float a = exp2f(sl[kHeadDim] - ref);
+                l = fmaf(sl[kHeadDim + 1], a, l);
+                o = fmaf(sl[d], a, o);
+            }
+            store_out<T>(p, c, m, d, l > 0.f ? o / l : 0.f);
+        }
+        return;
+    }
+
     const size_t slot0 = base + (size_t)c.s * p.msub;
     for (int idx = tid; idx < c.mcount * kHeadDim; idx += blockDim.x) {
         const int m = idx >> 6, d = idx & 63;
         float mx = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) mx = fmaxf(mx, red_m[w * RMAX + m]);
+        for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * RMAX + m]);
         const float ref = mx == -INFINITY ? 0.f : mx;
         float l = 0.f, o = 0.f;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
+        for (int w = 0; w < kWarps; ++w) {
             const float a = exp2f(red_m[w * RMAX + m] - ref);
             l = fmaf(red_l[w * RMAX + m], a, l);
             o = fmaf(red_o[(w * RMAX + m) * kHeadDim + d], a, o);
         }
         if (S == 1) {
             store_out<T>(p, c, m, d, l > 0.f ? o / l : 0.f);
-        } else if (p.cluster) {
-            fin_o[m * kHeadDim + d] = o;
-            if (d == 0) {
-                fin_m[m] = mx;
-                fin_l[m] = l;
-            }
         } else {
             p.ws_part[(slot0 + m) * kHeadDim + d] = o;
             if (d == 0) p.ws_ml[slot0 + m] = make_float2(mx, l);
@@ -174,41 +416,13 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
     }
     if (S == 1) return;
 
-    if (p.cluster) {
-        cluster_sync();  // every split's partial is now visible cluster-wide
-        const uint32_t fo = smem_u32(fin_o), fm = smem_u32(fin_m), fl = smem_u32(fin_l);
-        for (int it = c.s * blockDim.x + tid; it < c.mcount * kHeadDim; it += S * blockDim.x) {
-            const int m = it >> 6, d = it & 63;
-            float ms[kMaxClusterSplits];
-            float mx = -INFINITY;
-#pragma unroll
-            for (int r = 0; r < kMaxClusterSplits; ++r) {
-                ms[r] = r < S ? ld_dsmem(map_shared(fm + m * 4, r)) : -INFINITY;
-                mx = fmaxf(mx, ms[r]);
-            }
-            const float ref = mx == -INFINITY ? 0.f : mx;
-            float l = 0.f, o = 0.f;
-#pragma unroll
-            for (int r = 0; r < kMaxClusterSplits; ++r) {
-                if (r < S) {
-                    const float a = exp2f(ms[r] - ref);
-                    l = fmaf(ld_dsmem(map_shared(fl + m * 4, r)), a, l);
-                    o = fmaf(ld_dsmem(map_shared(fo + (m * kHeadDim + d) * 4, r)), a, o);
-                }
-            }
-            store_out<T>(p, c, m, d, l > 0.f ? o / l : 0.f);
-        }
-        cluster_sync();  // no CTA leaves while another may still read its shared memory
-        return;
-    }
-
     __threadfence();
     __syncthreads();
     if (tid == 0) misc[0] = (atomicAdd(&p.ws_cnt[c.unit], 1) == S - 1) ? 1 : 0;
     __syncthreads();
     if (!misc[0]) return;
     __threadfence();
-    // (a) all (max, sum) pairs at once -> normalised weights in shared memory
+    // (a) all (max, sum) pairs at once -> normalised weights in shared memory.
     // 2 * S * mcount <= 2 * kMaxSplits * RMAX floats fit in the warp-partial area; each
     // query's thread then overwrites its pairs' first field with the normalised weight.
     float2* ml = reinterpret_cast<float2*>(red);
@@ -231,9 +445,9 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
     //     of a thread independent; split groups are combined in a fixed order.
     const int nq4 = c.mcount * (kHeadDim / 4);
     const int groups = max(1, (int)blockDim.x / nq4);
-    // groups * nq4 <= max(blockDim.x, nq4) float4s (at most 4 KiB) go to the stage
-    // buffers, whose copies have all completed.
-    float4* tmp = reinterpret_cast<float4*>(stage_mem);
+    // groups * nq4 <= max(blockDim.x, nq4) float4s (at most 4 KiB), at the end of the
+    // stage area, clear of the weights above
+    float4* tmp = reinterpret_cast<float4*>(scratch4k);
     for (int item = tid; item < nq4 * groups; item += blockDim.x) {
         const int q4 = item % nq4, g = item / nq4;
         const int m = q4 / (kHeadDim / 4), d4 = q4 % (kHeadDim / 4);
@@ -269,67 +483,18 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
     if (tid == 0) p.ws_cnt[c.unit] = 0;
 }
 
-// After a timeout the block still has to meet its cluster peers at both merge barriers.
-__device__ __forceinline__ void abort_block(const AttnParams& p) {
-    if (p.cluster && p.splits > 1) {
-        cluster_sync();
-        cluster_sync();
-    }
-}
-
-// Shared prologue: barrier init, first copies, PDL wait. Returns false if the block
-// has nothing to do (a bad length: flagged, nothing written).
-__device__ __forceinline__ bool prologue(const AttnParams& p, CtaCtx& c, uint8_t* smem,
-                                         uint64_t* bars, const CUtensorMap* tmk,
-                                         const CUtensorMap* tmv) {
-    const int tid = threadIdx.x;
-    if (!p.early) pdl_wait();
-    setup_ctx(p, c);
-    if (c.bad) {
-        if (p.early) pdl_wait();
-        if (tid == 0 && c.s == 0 && c.h == 0 && c.sub == 0)
-            flag_error(p.dev_err, KVD_ERR_LEN_OVERFLOW);
-        return false;
-    }
-    if (tid == 0) {
-        for (int j = 0; j < p.stages; ++j) mbar_init(smem_u32(&bars[j]), 1);
-        fence_barrier_init();
-        prefetch_tensormap(tmk);
-        prefetch_tensormap(tmv);
-    }
-    __syncthreads();
-    if (tid == 0) {
-        const uint32_t tx = 2u * p.box_rows * kRowBytes;
-        const int first = min(p.stages, c.n_tiles);
-        for (int j = 0; j < first; ++j)
-            issue_tile(tmk, tmv, smem, bars, j, c.t_begin + j * kTile, c.h, c.bk, tx);
-    }
-    if (p.early) pdl_wait();
-    return true;
-}
-
-// Wait (bounded) for the copies of stages whose tiles were issued but never consumed,
-// so that no copy is still writing shared memory when the block exits after a timeout.
-__device__ void drain_after_timeout(const AttnParams& p, const CtaCtx& c, uint64_t* bars,
-                                    int next_tile) {
-    if (threadIdx.x != 0) return;
-    flag_error(p.dev_err, KVD_ERR_TIMEOUT);
-    const int last = min(c.n_tiles, next_tile + p.stages);
-    for (int j = next_tile; j < last; ++j)
-        mbar_wait_bounded(smem_u32(&bars[j % p.stages]), (j / p.stages) & 1);
-}
-
-// ---------------------------------------------------------------- decode (SIMT) ----
-template <typename T, int MS>
-__global__ void __launch_bounds__(128)
+// ------------------------------------------------- one query vector per KV head (SIMT) --
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
+    constexpr int RM = 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
-    const SmemLayout L = smem_layout(p.stages, MS);
+    const SmemLayout L = smem_layout(p.stages, RM, merge_slots(p.cluster, p.splits, p.msub));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
     float* red = reinterpret_cast<float*>(smem + L.red_off);
-    float* fin = reinterpret_cast<float*>(smem + L.fin_off);
+    float* mrg = reinterpret_cast<float*>(smem + L.mrg_off);
     int* misc = reinterpret_cast<int*>(smem + L.misc_off);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int grp = lane >> 3, c8 = lane & 7;
@@ -337,146 +502,101 @@ __global__ void __launch_bounds__(128)
     CtaCtx c;
     if (!prologue(p, c, smem, bars, &tmk, &tmv)) return;
 
-    float qf[MS][8];
-#pragma unroll
-    for (int m = 0; m < MS; ++m) {
-        if (m < c.mcount) {
-            const uint4 u = *reinterpret_cast<const uint4*>(
-                static_cast<const T*>(p.q) + qrow(p, c.bk, c.h, c.m0 + m) + c8 * 8);
-            unpack8<T>(u, qf[m]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) qf[m][e] = 0.f;
-        }
+    float qf[8];
+    {
+        const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
+                                                        qrow(p, c.bk, c.h, c.m0) + c8 * 8);
+        unpack8<T>(u, qf);
     }
-    float mrun[MS], lrun[MS], acc[MS][8];
+    float mrun = -INFINITY, lrun = 0.f, acc[8];
 #pragma unroll
-    for (int m = 0; m < MS; ++m) {
-        mrun[m] = -INFINITY;
-        lrun[m] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[m][e] = 0.f;
-    }
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 
-    const uint32_t tx = 2u * p.box_rows * kRowBytes;
-    for (int j = 0; j < c.n_tiles; ++j) {
-        const int st = j % p.stages;
-        const bool ok = mbar_wait_bounded(smem_u32(&bars[st]), (j / p.stages) & 1);
-        if (ok) {
-            const uint8_t* sK = smem + st * 2 * kTileBytes;
-            const uint8_t* sV = sK + kTileBytes;
-            const int tile0 = c.t_begin + j * kTile;
-            float sc[4][MS];
+    auto slab = [&](const uint8_t* sK, const uint8_t* sV, int tile0, int slab0) {
+        float sc[4];
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int row = warp * 16 + grp * 4 + jj;
-                const bool valid = tile0 + row < c.t_end;
-                const uint4 kr = *reinterpret_cast<const uint4*>(sK + swz(row, c8));
-                float kf[8];
-                unpack8<T>(kr, kf);
+        for (int jj = 0; jj < 4; ++jj) {
+            const int row = slab0 + grp * 4 + jj;
+            const bool valid = tile0 + row < c.t_end;
+            const uint4 kr = *reinterpret_cast<const uint4*>(sK + swz(row, c8));
+            float kf[8];
+            unpack8<T>(kr, kf);
+            float d = 0.f;
 #pragma unroll
-                for (int m = 0; m < MS; ++m) {
-                    float d = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) d = fmaf(qf[m][e], kf[e], d);
-                    d += __shfl_xor_sync(0xffffffffu, d, 1);
-                    d += __shfl_xor_sync(0xffffffffu, d, 2);
-                    d += __shfl_xor_sync(0xffffffffu, d, 4);
-                    sc[jj][m] = valid ? d * p.scale_log2 : -INFINITY;
-                }
-            }
-#pragma unroll
-            for (int m = 0; m < MS; ++m) {
-                const float mt = fmaxf(fmaxf(sc[0][m], sc[1][m]), fmaxf(sc[2][m], sc[3][m]));
-                const float mn = fmaxf(mrun[m], mt);
-                const float ref = mn == -INFINITY ? 0.f : mn;
-                const float alpha = exp2f(mrun[m] - ref);
-                float ls = 0.f;
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    sc[jj][m] = exp2f(sc[jj][m] - ref);
-                    ls += sc[jj][m];
-                }
-                lrun[m] = fmaf(lrun[m], alpha, ls);
-                mrun[m] = mn;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[m][e] *= alpha;
-            }
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int row = warp * 16 + grp * 4 + jj;
-                const bool valid = tile0 + row < c.t_end;
-                const uint4 vr = *reinterpret_cast<const uint4*>(sV + swz(row, c8));
-                float vf[8];
-                unpack8<T>(vr, vf);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) vf[e] = valid ? vf[e] : 0.f;
-#pragma unroll
-                for (int m = 0; m < MS; ++m)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[m][e] = fmaf(sc[jj][m], vf[e], acc[m][e]);
-            }
+            for (int e = 0; e < 8; ++e) d = fmaf(qf[e], kf[e], d);
+            d += __shfl_xor_sync(0xffffffffu, d, 1);
+            d += __shfl_xor_sync(0xffffffffu, d, 2);
+            d += __shfl_xor_sync(0xffffffffu, d, 4);
+            sc[jj] = valid ? d * p.scale_log2 : -INFINITY;
         }
-        if (__syncthreads_or(!ok)) {
-            drain_after_timeout(p, c, bars, j);
-            abort_block(p);
-            return;
+        const float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        const float mn = fmaxf(mrun, mt);
+        const float ref = mn == -INFINITY ? 0.f : mn;
+        const float alpha = exp2f(mrun - ref);
+        float ls = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            sc[jj] = exp2f(sc[jj] - ref);
+            ls += sc[jj];
         }
-        if (tid == 0 && j + p.stages < c.n_tiles) {
-            fence_proxy_async();
-            issue_tile(&tmk, &tmv, smem, bars, st, c.t_begin + (j + p.stages) * kTile, c.h,
-                       c.bk, tx);
+        lrun = fmaf(lrun, alpha, ls);
+        mrun = mn;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] *= alpha;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int row = slab0 + grp * 4 + jj;
+            const bool valid = tile0 + row < c.t_end;
+            const uint4 vr = *reinterpret_cast<const uint4*>(sV + swz(row, c8));
+            float vf[8];
+            unpack8<T>(vr, vf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(sc[jj], valid ? vf[e] : 0.f, acc[e]);
         }
-    }
-    pdl_trigger();
+    };
+    if (!run_tiles(p, c, smem, bars, &tmk, &tmv, slab)) return;
 
     // Merge the four 8-lane groups of each warp (they saw different positions).
 #pragma unroll
     for (int off = 8; off <= 16; off <<= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, mrun, off);
+        const float lo = __shfl_xor_sync(0xffffffffu, lrun, off);
+        const float mn = fmaxf(mrun, mo);
+        const float ref = mn == -INFINITY ? 0.f : mn;
+        const float a = exp2f(mrun - ref), b = exp2f(mo - ref);
+        lrun = lrun * a + lo * b;
 #pragma unroll
-        for (int m = 0; m < MS; ++m) {
-            const float mo = __shfl_xor_sync(0xffffffffu, mrun[m], off);
-            const float lo = __shfl_xor_sync(0xffffffffu, lrun[m], off);
-            const float mn = fmaxf(mrun[m], mo);
-            const float ref = mn == -INFINITY ? 0.f : mn;
-            const float a = exp2f(mrun[m] - ref), b = exp2f(mo - ref);
-            lrun[m] = lrun[m] * a + lo * b;
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                acc[m][e] = acc[m][e] * a + __shfl_xor_sync(0xffffffffu, acc[m][e], off) * b;
-            mrun[m] = mn;
-        }
+        for (int e = 0; e < 8; ++e)
+            acc[e] = acc[e] * a + __shfl_xor_sync(0xffffffffu, acc[e], off) * b;
+        mrun = mn;
     }
     if (grp == 0) {
         float* red_o = red;
-        float* red_m = red + 4 * MS * kHeadDim;
-        float* red_l = red_m + 4 * MS;
+        float* red_m = red + kWarps * RM * kHeadDim;
+        float* red_l = red_m + kWarps * RM;
 #pragma unroll
-        for (int m = 0; m < MS; ++m) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) red_o[(warp * MS + m) * kHeadDim + c8 * 8 + e] = acc[m][e];
-            if (c8 == 0) {
-                red_m[warp * MS + m] = mrun[m];
-                red_l[warp * MS + m] = lrun[m];
-            }
+        for (int e = 0; e < 8; ++e) red_o[warp * kHeadDim + c8 * 8 + e] = acc[e];
+        if (c8 == 0) {
+            red_m[warp] = mrun;
+            red_l[warp] = lrun;
         }
     }
     __syncthreads();
-    finish_cta<T, MS>(p, c, red, fin, misc, smem);
+    finish_cta<T, RM>(p, c, red, mrg, &bars[p.stages], misc, smem + L.bar_off - 4096);
 }
 
-// ---------------------------------------------------------------- verify (MMA) -----
+// ------------------------------------ 2..16 query vectors per KV head (tensor cores) ----
 template <typename T>
-__global__ void __launch_bounds__(128)
-    verify_attn_kernel(const __grid_constant__ CUtensorMap tmk,
-                       const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
+__global__ void __launch_bounds__(kThreads)
+    block_attn_kernel(const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
     constexpr int RM = 16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
-    const SmemLayout L = smem_layout(p.stages, RM);
+    const SmemLayout L = smem_layout(p.stages, RM, merge_slots(p.cluster, p.splits, p.msub));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
     float* red = reinterpret_cast<float*>(smem + L.red_off);
-    float* fin = reinterpret_cast<float*>(smem + L.fin_off);
+    float* mrg = reinterpret_cast<float*>(smem + L.mrg_off);
     int* misc = reinterpret_cast<int*>(smem + L.misc_off);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int qr = lane >> 2, qc = (lane & 3) * 2;  // fragment row / column pair
@@ -513,96 +633,79 @@ __global__ void __launch_bounds__(128)
         for (int e = 0; e < 4; ++e) oacc[n][e] = 0.f;
     float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
 
-    const uint32_t tx = 2u * p.box_rows * kRowBytes;
-    for (int j = 0; j < c.n_tiles; ++j) {
-        const int st = j % p.stages;
-        const bool ok = mbar_wait_bounded(smem_u32(&bars[st]), (j / p.stages) & 1);
-        const int tile0 = c.t_begin + j * kTile;
-        const int nvalid = min(16, max(0, c.t_end - tile0 - warp * 16));
-        if (ok && nvalid > 0) {
-            uint8_t* sK = smem + st * 2 * kTileBytes;
-            uint8_t* sV = sK + kTileBytes;
-            if (nvalid < 16) {
-                // Rows past the end hold stale or fill data; P is 0 there but 0 * NaN
-                // would still poison the product, so clear them before P.V.
-                for (int x = lane; x < (16 - nvalid) * 8; x += 32) {
-                    const int row = warp * 16 + nvalid + (x >> 3);
-                    *reinterpret_cast<uint4*>(sV + swz(row, x & 7)) = make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async();
-                __syncwarp();
+    auto slab = [&](uint8_t* sK, uint8_t* sV, int tile0, int slab0) {
+        const int nvalid = min(16, max(0, c.t_end - tile0 - slab0));
+        if (nvalid == 0) return;
+        if (nvalid < 16) {
+            // Rows past the end hold stale or fill data; P is 0 there but 0 * NaN would
+            // still poison the product, so clear them before P.V.
+            for (int x = lane; x < (16 - nvalid) * 8; x += 32) {
+                const int row = slab0 + nvalid + (x >> 3);
+                *reinterpret_cast<uint4*>(sV + swz(row, x & 7)) = make_uint4(0, 0, 0, 0);
             }
-            const uint32_t kb = smem_u32(sK), vb = smem_u32(sV);
-            float sacc[2][4];
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sacc[n][e] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const int krow = warp * 16 + (jm >> 1) * 8 + rr;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kb + swz(krow, kk * 2 + (jm & 1)), b0, b1, b2, b3);
-                Mma<T>::run(sacc[0], qa[kk], b0, b1);
-                Mma<T>::run(sacc[1], qa[kk], b2, b3);
-            }
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int key = tile0 + warp * 16 + n * 8 + qc + (e & 1);
-                    const int lim = e < 2 ? limA : limB;
-                    sacc[n][e] = key < lim ? sacc[n][e] * p.scale_log2 : -INFINITY;
-                }
-            float tA = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
-            float tB = fmaxf(fmaxf(sacc[0][2], sacc[0][3]), fmaxf(sacc[1][2], sacc[1][3]));
-            tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 1));
-            tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 2));
-            tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 1));
-            tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 2));
-            const float nA = fmaxf(mA, tA), nB = fmaxf(mB, tB);
-            const float refA = nA == -INFINITY ? 0.f : nA, refB = nB == -INFINITY ? 0.f : nB;
-            const float aA = exp2f(mA - refA), aB = exp2f(mB - refB);
-            mA = nA;
-            mB = nB;
-            uint32_t pa[4];
-            pa[0] = Half16<T>::from_f2(exp2f(sacc[0][0] - refA), exp2f(sacc[0][1] - refA));
-            pa[1] = Half16<T>::from_f2(exp2f(sacc[0][2] - refB), exp2f(sacc[0][3] - refB));
-            pa[2] = Half16<T>::from_f2(exp2f(sacc[1][0] - refA), exp2f(sacc[1][1] - refA));
-            pa[3] = Half16<T>::from_f2(exp2f(sacc[1][2] - refB), exp2f(sacc[1][3] - refB));
-            // The normaliser sums the rounded weights that actually multiply V.
-            const float2 r0 = Half16<T>::to_f2(pa[0]), r1 = Half16<T>::to_f2(pa[1]);
-            const float2 r2 = Half16<T>::to_f2(pa[2]), r3 = Half16<T>::to_f2(pa[3]);
-            lA = fmaf(lA, aA, (r0.x + r0.y) + (r2.x + r2.y));
-            lB = fmaf(lB, aB, (r1.x + r1.y) + (r3.x + r3.y));
-#pragma unroll
-            for (int n = 0; n < 8; ++n) {
-                oacc[n][0] *= aA;
-                oacc[n][1] *= aA;
-                oacc[n][2] *= aB;
-                oacc[n][3] *= aB;
-            }
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                const int vrow = warp * 16 + (jm & 1) * 8 + rr;
-                uint32_t v0, v1, v2, v3;
-                ldsm_x4_t(vb + swz(vrow, 2 * np + (jm >> 1)), v0, v1, v2, v3);
-                Mma<T>::run(oacc[2 * np], pa, v0, v1);
-                Mma<T>::run(oacc[2 * np + 1], pa, v2, v3);
-            }
-        }
-        if (__syncthreads_or(!ok)) {
-            drain_after_timeout(p, c, bars, j);
-            abort_block(p);
-            return;
-        }
-        if (tid == 0 && j + p.stages < c.n_tiles) {
             fence_proxy_async();
-            issue_tile(&tmk, &tmv, smem, bars, st, c.t_begin + (j + p.stages) * kTile, c.h,
-                       c.bk, tx);
+            __syncwarp();
         }
-    }
-    pdl_trigger();
+        const uint32_t kb = smem_u32(sK), vb = smem_u32(sV);
+        float sacc[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[n][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const int krow = slab0 + (jm >> 1) * 8 + rr;
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kb + swz(krow, kk * 2 + (jm & 1)), b0, b1, b2, b3);
+            Mma<T>::run(sacc[0], qa[kk], b0, b1);
+            Mma<T>::run(sacc[1], qa[kk], b2, b3);
+        }
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int key = tile0 + slab0 + n * 8 + qc + (e & 1);
+                const int lim = e < 2 ? limA : limB;
+                sacc[n][e] = key < lim ? sacc[n][e] * p.scale_log2 : -INFINITY;
+            }
+        float tA = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
+        float tB = fmaxf(fmaxf(sacc[0][2], sacc[0][3]), fmaxf(sacc[1][2], sacc[1][3]));
+        tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 1));
+        tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 2));
+        tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 1));
+        tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 2));
+        const float nA = fmaxf(mA, tA), nB = fmaxf(mB, tB);
+        const float refA = nA == -INFINITY ? 0.f : nA, refB = nB == -INFINITY ? 0.f : nB;
+        const float aA = exp2f(mA - refA), aB = exp2f(mB - refB);
+        mA = nA;
+        mB = nB;
+        uint32_t pa[4];
+        pa[0] = Half16<T>::from_f2(exp2f(sacc[0][0] - refA), exp2f(sacc[0][1] - refA));
+        pa[1] = Half16<T>::from_f2(exp2f(sacc[0][2] - refB), exp2f(sacc[0][3] - refB));
+        pa[2] = Half16<T>::from_f2(exp2f(sacc[1][0] - refA), exp2f(sacc[1][1] - refA));
+        pa[3] = Half16<T>::from_f2(exp2f(sacc[1][2] - refB), exp2f(sacc[1][3] - refB));
+        // The normaliser sums the rounded weights that actually multiply V.
+        const float2 r0 = Half16<T>::to_f2(pa[0]), r1 = Half16<T>::to_f2(pa[1]);
+        const float2 r2 = Half16<T>::to_f2(pa[2]), r3 = Half16<T>::to_f2(pa[3]);
+        lA = fmaf(lA, aA, (r0.x + r0.y) + (r2.x + r2.y));
+        lB = fmaf(lB, aB, (r1.x + r1.y) + (r3.x + r3.y));
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+            oacc[n][0] *= aA;
+            oacc[n][1] *= aA;
+            oacc[n][2] *= aB;
+            oacc[n][3] *= aB;
+        }
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+            const int vrow = slab0 + (jm & 1) * 8 + rr;
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4_t(vb + swz(vrow, 2 * np + (jm >> 1)), v0, v1, v2, v3);
+            Mma<T>::run(oacc[2 * np], pa, v0, v1);
+            Mma<T>::run(oacc[2 * np + 1], pa, v2, v3);
+        }
+    };
+    if (!run_tiles(p, c, smem, bars, &tmk, &tmv, slab)) return;
 
     lA += __shfl_xor_sync(0xffffffffu, lA, 1);
     lA += __shfl_xor_sync(0xffffffffu, lA, 2);
@@ -610,8 +713,8 @@ __global__ void __launch_bounds__(128)
     lB += __shfl_xor_sync(0xffffffffu, lB, 2);
     {
         float* red_o = red;
-        float* red_m = red + 4 * RM * kHeadDim;
-        float* red_l = red_m + 4 * RM;
+        float* red_m = red + kWarps * RM * kHeadDim;
+        float* red_l = red_m + kWarps * RM;
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
             float* oa = red_o + (warp * RM + qr) * kHeadDim + n * 8 + qc;
@@ -629,14 +732,12 @@ __global__ void __launch_bounds__(128)
         }
     }
     __syncthreads();
-    finish_cta<T, RM>(p, c, red, fin, misc, smem);
+    finish_cta<T, RM>(p, c, red, mrg, &bars[p.stages], misc, smem + L.bar_off - 4096);
 }
 
 // ---------------------------------------------------------------- host side --------
 namespace {
 
-constexpr int kDecodeMmax = 8;
-constexpr int kVerifyMmax = 16;
 constexpr int kMaxDev = 64;
 
 // Once per kernel and device: allow more than 48 KiB of dynamic shared memory and
@@ -661,66 +762,31 @@ int prepare_kernel(size_t smem_bytes) {
     return result[dev];
 }
 
-template <typename T, int MS>
-int prepare_decode_ms() {
-    return prepare_kernel<decode_attn_kernel<T, MS>>(smem_layout(kMaxStages, MS).total);
+template <typename T>
+int prepare(bool mma) {
+    return mma ? prepare_kernel<block_attn_kernel<T>>(
+                     smem_layout(kMaxStages, 16, kMaxClusterSplits * kMmaQueryBlock).total)
+               : prepare_kernel<decode_attn_kernel<T>>(
+                     smem_layout(kMaxStages, 1, kMaxClusterSplits).total);
 }
+
 
 template <typename T>
-int prepare_decode(int ms) {
-    switch (ms) {
-    case 1: return prepare_decode_ms<T, 1>();
-    case 2: return prepare_decode_ms<T, 2>();
-    case 3: return prepare_decode_ms<T, 3>();
-    case 4: return prepare_decode_ms<T, 4>();
-    case 5: return prepare_decode_ms<T, 5>();
-    case 6: return prepare_decode_ms<T, 6>();
-    case 7: return prepare_decode_ms<T, 7>();
-    case 8: return prepare_decode_ms<T, 8>();
-    }
-    return 0;
-}
-
-template <typename T>
-int prepare_verify() {
-    return prepare_kernel<verify_attn_kernel<T>>(smem_layout(kMaxStages, 16).total);
-}
-
-template <typename T, int MS>
-kvd_status launch_decode_ms(dim3 grid, cudaStream_t st, bool pdl, unsigned cl,
-                            const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p) {
-    return launch_ex(decode_attn_kernel<T, MS>, grid, dim3(128), smem_layout(p.stages, MS).total,
-                     st, pdl, cl, mk, mv, p);
-}
-
-template <typename T>
-kvd_status launch_decode(int ms, dim3 grid, cudaStream_t st, bool pdl, unsigned cl,
-                         const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p) {
-    switch (ms) {
-    case 1: return launch_decode_ms<T, 1>(grid, st, pdl, cl, mk, mv, p);
-    case 2: return launch_decode_ms<T, 2>(grid, st, pdl, cl, mk, mv, p);
-    case 3: return launch_decode_ms<T, 3>(grid, st, pdl, cl, mk, mv, p);
-    case 4: return launch_decode_ms<T, 4>(grid, st, pdl, cl, mk, mv, p);
-    case 5: return launch_decode_ms<T, 5>(grid, st, pdl, cl, mk, mv, p);
-    case 6: return launch_decode_ms<T, 6>(grid, st, pdl, cl, mk, mv, p);
-    case 7: return launch_decode_ms<T, 7>(grid, st, pdl, cl, mk, mv, p);
-    case 8: return launch_decode_ms<T, 8>(grid, st, pdl, cl, mk, mv, p);
-    }
-    return KVD_ERR_UNSUPPORTED;
-}
-
-template <typename T>
-kvd_status launch_verify(dim3 grid, cudaStream_t st, bool pdl, unsigned cl,
-                         const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p) {
-    return launch_ex(verify_attn_kernel<T>, grid, dim3(128), smem_layout(p.stages, 16).total, st,
-                     pdl, cl, mk, mv, p);
+kvd_status launch_attn(bool mma, dim3 grid, cudaStream_t st, bool pdl, unsigned cl,
+                       const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p) {
+    const int slots = merge_slots(p.cluster, p.splits, p.msub);
+    if (mma)
+        return launch_ex(block_attn_kernel<T>, grid, dim3(kThreads),
+                         smem_layout(p.stages, 16, slots).total, st, pdl, cl, mk, mv, p);
+    return launch_ex(decode_attn_kernel<T>, grid, dim3(kThreads),
+                     smem_layout(p.stages, 1, slots).total, st, pdl, cl, mk, mv, p);
 }
 
 kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_heads,
                      int32_t qlen, const void* q, const kvd_cache* kv, const int32_t* lens,
-                     int32_t fixed_len, int32_t rows_per_kv, int32_t causal, float scale,
-                     void* out, void* ws, size_t ws_bytes, uint32_t flags, int32_t* dev_err,
-                     cudaStream_t stream) {
+                     int32_t fixed_len, const kvd_new_tokens* app, int32_t rows_per_kv,
+                     int32_t causal, float scale, void* out, void* ws, size_t ws_bytes,
+                     uint32_t flags, int32_t* dev_err, cudaStream_t stream) {
     if (dtype != KVD_F16 && dtype != KVD_BF16) return KVD_ERR_INVALID_ARG;
     if (kvd_status s = validate_cache(kv)) return s;
     if (batch < 0 || n_q_heads <= 0 || rows_per_kv <= 0) return KVD_ERR_INVALID_ARG;
@@ -730,21 +796,23 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
     if (!q || !out || !aligned16(q) || !aligned16(out)) return KVD_ERR_INVALID_ARG;
     if (batch / rows_per_kv > kv->batch || batch / rows_per_kv > 65535) return KVD_ERR_INVALID_ARG;
     if (!lens && (fixed_len < 0 || fixed_len > kv->capacity)) return KVD_ERR_INVALID_ARG;
+    if (app) {
+        if (!lens || !app->k_new || !app->v_new || !aligned16(app->k_new) ||
+            !aligned16(app->v_new) || app->lens_out == lens)
+            return KVD_ERR_INVALID_ARG;
+    }
     if (!(scale == scale)) return KVD_ERR_INVALID_ARG;
     const int nsm = sm_count();
     if (nsm <= 0) return KVD_ERR_CUDA;
     const int len_bound = lens ? kv->capacity : fixed_len;
     const bool bf = dtype == KVD_BF16;
-    const int mmax = verify ? kVerifyMmax : kDecodeMmax;
-    // the query block size per thread block depends only on the shape
-    const AttnPlan P0 = plan_attention(batch, n_q_heads, kv->n_kv_heads, rows_per_kv, qlen,
-                                       len_bound, mmax, 4 * nsm, 1);
-    const int max_cluster = verify ? (bf ? prepare_verify<__nv_bfloat16>() : prepare_verify<__half>())
-                                   : (bf ? prepare_decode<__nv_bfloat16>(P0.msub)
-                                         : prepare_decode<__half>(P0.msub));
+    const int group = n_q_heads / kv->n_kv_heads;
+    const bool mma = verify || (int64_t)rows_per_kv * group * qlen >= 2;
+    const int mmax = mma ? kMmaQueryBlock : 1;
+    const int max_cluster = bf ? prepare<__nv_bfloat16>(mma) : prepare<__half>(mma);
     if (max_cluster <= 0) return KVD_ERR_CUDA;
     const AttnPlan P = plan_attention(batch, n_q_heads, kv->n_kv_heads, rows_per_kv, qlen,
-                                      len_bound, mmax, 4 * nsm, max_cluster);
+                                      len_bound, mmax, 2 * nsm, max_cluster);
     if ((int64_t)kv->n_kv_heads * P.nsub > 65535) return KVD_ERR_UNSUPPORTED;
     if (P.splits > 1 && !P.cluster) {
         if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < P.ws_bytes)
@@ -775,6 +843,16 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
     p.box_rows = std::min(64, kv->capacity);
     p.early = (flags & KVD_FLAG_EARLY_KV) ? 1 : 0;
     p.cluster = P.cluster ? 1 : 0;
+    p.append = app ? 1 : 0;
+    p.k_new = app ? static_cast<const uint8_t*>(app->k_new) : nullptr;
+    p.v_new = app ? static_cast<const uint8_t*>(app->v_new) : nullptr;
+    p.lens_out = app ? app->lens_out : nullptr;
+    p.kc = static_cast<uint8_t*>(kv->k);
+    p.vc = static_cast<uint8_t*>(kv->v);
+    p.sb = kv->stride_b * 2;
+    p.sh = kv->stride_h * 2;
+    p.st = kv->stride_t * 2;
+    p.n_kv_heads = kv->n_kv_heads;
     p.scale_log2 = scale * kLog2e;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     p.ws_cnt = reinterpret_cast<int32_t*>(wsb);
@@ -785,11 +863,8 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
     const bool pdl = (flags & (KVD_FLAG_PDL | KVD_FLAG_EARLY_KV)) != 0;
     const dim3 grid(P.splits, kv->n_kv_heads * P.nsub, P.bkv);
     const unsigned cl = P.cluster ? (unsigned)P.splits : 1u;
-    if (verify)
-        return bf ? launch_verify<__nv_bfloat16>(grid, stream, pdl, cl, mk, mv, p)
-                  : launch_verify<__half>(grid, stream, pdl, cl, mk, mv, p);
-    return bf ? launch_decode<__nv_bfloat16>(P.msub, grid, stream, pdl, cl, mk, mv, p)
-              : launch_decode<__half>(P.msub, grid, stream, pdl, cl, mk, mv, p);
+    return bf ? launch_attn<__nv_bfloat16>(mma, grid, stream, pdl, cl, mk, mv, p)
+              : launch_attn<__half>(mma, grid, stream, pdl, cl, mk, mv, p);
 }
 
 }  // namespace
@@ -797,27 +872,29 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
 
 extern "C" kvd_status kvd_decode_attn(kvd_dtype dtype, int32_t batch, int32_t n_q_heads,
                                       const void* q, const kvd_cache* kv, const int32_t* lens,
-                                      int32_t fixed_len, int32_t rows_per_kv, float scale,
-                                      void* out, void* workspace, size_t workspace_bytes,
-                                      uint32_t flags, int32_t* dev_err, kvd_stream_t stream) {
-    return kvd::attention(false, dtype, batch, n_q_heads, 1, q, kv, lens, fixed_len, rows_per_kv,
-                          0, scale, out, workspace, workspace_bytes, flags, dev_err,
+                                      int32_t fixed_len, const kvd_new_tokens* append,
+                                      int32_t rows_per_kv, float scale, void* out,
+                                      void* workspace, size_t workspace_bytes, uint32_t flags,
+                                      int32_t* dev_err, kvd_stream_t stream) {
+    return kvd::attention(false, dtype, batch, n_q_heads, 1, q, kv, lens, fixed_len, append,
+                          rows_per_kv, 0, scale, out, workspace, workspace_bytes, flags, dev_err,
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" kvd_status kvd_verify_attn(kvd_dtype dtype, int32_t batch, int32_t n_q_heads,
                                       int32_t qlen, const void* q, const kvd_cache* kv,
                                       const int32_t* lens, int32_t fixed_len,
-                                      int32_t rows_per_kv, int32_t causal, float scale,
-                                      void* out, void* workspace, size_t workspace_bytes,
-                                      uint32_t flags, int32_t* dev_err, kvd_stream_t stream) {
-    return kvd::attention(true, dtype, batch, n_q_heads, qlen, q, kv, lens, fixed_len,
+                                      const kvd_new_tokens* append, int32_t rows_per_kv,
+                                      int32_t causal, float scale, void* out, void* workspace,
+                                      size_t workspace_bytes, uint32_t flags, int32_t* dev_err,
+                                      kvd_stream_t stream) {
+    return kvd::attention(true, dtype, batch, n_q_heads, qlen, q, kv, lens, fixed_len, append,
                           rows_per_kv, causal, scale, out, workspace, workspace_bytes, flags,
                           dev_err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------- no-allocation entry
-// kvd_decode_attn_noalloc: the decode kernel with its split-merge scratch in a buffer
+// kvd_decode_attn_noalloc: the decode kernels with their split-merge scratch in a buffer
 // compiled into the library, for callers that cannot allocate a workspace (see
 // kvdecode.h). Host code must never pass `g_noalloc_scratch` itself to a kernel: on the
 // host that name is only a stand-in for the device symbol. The device address is looked
@@ -846,15 +923,16 @@ kvd_status noalloc_scratch(void** out) {
 extern "C" kvd_status kvd_decode_attn_noalloc(kvd_dtype dtype, int32_t batch, int32_t n_q_heads,
                                               const void* q, const kvd_cache* kv,
                                               const int32_t* lens, int32_t fixed_len,
-                                              int32_t rows_per_kv, float scale, void* out,
-                                              uint32_t flags, int32_t* dev_err,
-                                              kvd_stream_t stream) {
+                                              const kvd_new_tokens* append, int32_t rows_per_kv,
+                                              float scale, void* out, uint32_t flags,
+                                              int32_t* dev_err, kvd_stream_t stream) {
     void* scratch = nullptr;
     if (kvd_status s = kvd::noalloc_scratch(&scratch)) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // The buffer keeps whatever the previous call left; its arrival counters must start
     // at zero, so clear them (a call that stopped early could have left them non-zero).
     if (cudaMemsetAsync(scratch, 0, KVD_WS_COUNTER_BYTES, st) != cudaSuccess) return KVD_ERR_CUDA;
-    return kvd::attention(false, dtype, batch, n_q_heads, 1, q, kv, lens, fixed_len, rows_per_kv,
-                          0, scale, out, scratch, KVD_NOALLOC_SCRATCH_BYTES, flags, dev_err, st);
+    return kvd::attention(false, dtype, batch, n_q_heads, 1, q, kv, lens, fixed_len, append,
+                          rows_per_kv, 0, scale, out, scratch, KVD_NOALLOC_SCRATCH_BYTES, flags,
+                          dev_err, st);
 }

@@ -75,6 +75,7 @@ struct AttnPlan {
 };
 
 constexpr int kMaxStages = 4;
+constexpr int kMmaQueryBlock = 16;     // query vectors per block on the tensor-core path
 constexpr int kMaxSplits = 128;        // splits per unit (merge scratch is sized for this)
 constexpr int kMaxClusterSplits = 16;  // largest cluster used for a merge
 constexpr int kWsTargetBound = 4096;   // upper bound of target_ctas used for sizing

@@ -90,8 +90,8 @@ def _fake_cache(**kw):
 def test_host_rejects_bad_caches_before_touching_the_gpu(lib, kw, status):
     c = _fake_cache(**kw)
     q = ctypes.c_void_p(0x30000)
-    r = lib.kvd_decode_attn(0, 1, 20, q, ctypes.byref(c), None, 10, 1, 0.125, q, None, 0, 0,
-                            None, None)
+    r = lib.kvd_decode_attn(0, 1, 20, q, ctypes.byref(c), None, 10, None, 1, 0.125, q, None,
+                            0, 0, None, None)
     assert r == status
 
 
@@ -99,17 +99,17 @@ def test_host_rejects_bad_shapes(lib):
     c = _fake_cache()
     q = ctypes.c_void_p(0x30000)
     # query heads not a multiple of KV heads
-    assert lib.kvd_decode_attn(0, 1, 30, q, ctypes.byref(c), None, 10, 1, 0.125, q, None, 0, 0,
-                               None, None) == 1
+    assert lib.kvd_decode_attn(0, 1, 30, q, ctypes.byref(c), None, 10, None, 1, 0.125, q, None,
+                               0, 0, None, None) == 1
     # batch not a multiple of rows_per_kv
-    assert lib.kvd_decode_attn(0, 3, 20, q, ctypes.byref(c), None, 10, 2, 0.125, q, None, 0, 0,
-                               None, None) == 1
+    assert lib.kvd_decode_attn(0, 3, 20, q, ctypes.byref(c), None, 10, None, 2, 0.125, q, None,
+                               0, 0, None, None) == 1
     # fixed length past the capacity
-    assert lib.kvd_decode_attn(0, 1, 20, q, ctypes.byref(c), None, 449, 1, 0.125, q, None, 0,
-                               0, None, None) == 1
+    assert lib.kvd_decode_attn(0, 1, 20, q, ctypes.byref(c), None, 449, None, 1, 0.125, q,
+                               None, 0, 0, None, None) == 1
     # verify block longer than 16
-    assert lib.kvd_verify_attn(0, 1, 20, 17, q, ctypes.byref(c), None, 10, 1, 1, 0.125, q,
-                               None, 0, 0, None, None) == 2
+    assert lib.kvd_verify_attn(0, 1, 20, 17, q, ctypes.byref(c), None, 10, None, 1, 1, 0.125,
+                               q, None, 0, 0, None, None) == 2
     # append: lens_out aliasing lens_in
     lens = ctypes.c_void_p(0x40000)
     assert lib.kvd_kv_append(0, ctypes.byref(c), 1, 1, q, q, lens, lens, 0, None, None) == 1
@@ -120,6 +120,15 @@ def test_host_rejects_bad_shapes(lib):
     # accept: k out of range
     assert lib.kvd_greedy_accept(q, 1, 0, 100, q, q, q, None, None, q, 1 << 20, 0, None,
                                  None) == 2
+    # fused append without lengths, or with lens_out aliasing lens
+    from kv_cached_decode_gb300 import NewTokens
+
+    app = NewTokens(0x50000, 0x60000, None)
+    assert lib.kvd_decode_attn(0, 1, 20, q, ctypes.byref(c), None, 10, ctypes.byref(app), 1,
+                               0.125, q, None, 0, 0, None, None) == 1
+    app_alias = NewTokens(0x50000, 0x60000, 0x40000)
+    assert lib.kvd_decode_attn(0, 1, 20, q, ctypes.byref(c), lens, 10, ctypes.byref(app_alias),
+                               1, 0.125, q, None, 0, 0, None, None) == 1
     # empty batches are a no-op
-    assert lib.kvd_decode_attn(0, 0, 20, None, ctypes.byref(c), None, 0, 1, 0.125, None, None,
-                               0, 0, None, None) == 0
+    assert lib.kvd_decode_attn(0, 0, 20, None, ctypes.byref(c), None, 0, None, 1, 0.125, None,
+                               None, 0, 0, None, None) == 0

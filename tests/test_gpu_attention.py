@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from gpu_util import (assert_attn_close, dev16, dev_i32, host16, new_err, require_gpu)
-from workloads import gen_cache, gen_lens_uniform, gen_queries, make_rng
+from workloads import gen_cache, gen_lens_uniform, gen_new_kv, gen_queries, make_rng
 
 pytestmark = pytest.mark.gpu
 
@@ -259,3 +259,131 @@ def test_verify_workspace_merge_sixteen_queries():
     got, want = run_attention("bf16", 1, 16, 1, 2048, lens=np.array([2048], np.int32), qlen=1,
                               causal=True, verify=True, seed=131)
     assert_attn_close(got, want, "bf16", "verify M=16 workspace merge")
+
+
+# ----------------------------------------------------------------- fused append ---------
+
+def run_fused(dtype, B, Hq, Hkv, cap, lens_in, qlen, *, verify, seed, flags=0):
+    """Attention with the new tokens appended in the same launch, against the oracle's
+    kv_append followed by attention over the appended cache."""
+    kvd = _kvd()
+    rng = make_rng(seed)
+    lens_in = np.asarray(lens_in, np.int32)
+    K, V = gen_cache(rng, B, Hkv, cap, D, dtype, 0.125, lens=lens_in)
+    kn, vn = gen_new_kv(rng, B, Hkv, qlen, D, dtype, 0.125)
+    q = gen_queries(rng, B, Hq, qlen, D, dtype, 0.125)
+    Kd, Vd = dev16(K, dtype), dev16(V, dtype)
+    Kw, Vw = K.copy(), V.copy()
+    lens_out_w, err = oracle.kv_append(Kw, Vw, kn, vn, lens_in, dtype)
+    want, _ = oracle.attention(q, Kw, Vw, dtype, lens=lens_out_w, causal=verify)
+    qd = dev16(q, dtype)
+    out = torch.empty_like(qd)
+    lens_out = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    op = kvd.KVD_OP_VERIFY_ATTN if verify else kvd.KVD_OP_DECODE_ATTN
+    ws = kvd.new_workspace(kvd.kvd_workspace_size(op, B, Hq, Hkv, 1, qlen, cap))
+    e = new_err()
+    app = (dev16(kn, dtype), dev16(vn, dtype), lens_out)
+    if verify:
+        kvd.kvd_verify_attn(qd, kvd.make_cache(Kd, Vd), out, ws, lens=dev_i32(lens_in),
+                            causal=True, flags=flags, dev_err=e, append=app)
+    else:
+        kvd.kvd_decode_attn(qd, kvd.make_cache(Kd, Vd), out, ws, lens=dev_i32(lens_in),
+                            flags=flags, dev_err=e, append=app)
+    torch.cuda.synchronize()
+    return host16(out), want, host16(Kd), host16(Vd), Kw, Vw, lens_out.cpu().numpy(), \
+        lens_out_w, e.item(), err
+
+
+@pytest.mark.parametrize("flags", [0, 3])  # plain, and PDL + early K/V
+def test_decode_fused_append_whisper_self(flags):
+    got, want, Kg, Vg, Kw, Vw, lo, low, e, err = run_fused(
+        "f16", 1, 20, 20, 448, [447], 1, verify=False, seed=140, flags=flags)
+    assert e == 0 and not err
+    assert np.array_equal(Kg, Kw) and np.array_equal(Vg, Vw)
+    assert np.array_equal(lo, low)
+    assert_attn_close(got, want, "f16", "fused decode")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_decode_fused_append_ragged_tile_edges(dtype):
+    lens = [0, 63, 64, 127, 128, 300, 511, 1]
+    got, want, Kg, Vg, Kw, Vw, lo, low, e, err = run_fused(
+        dtype, 8, 4, 4, 512, lens, 1, verify=False, seed=141)
+    assert e == 0 and not err
+    assert np.array_equal(Kg, Kw) and np.array_equal(Vg, Vw) and np.array_equal(lo, low)
+    assert_attn_close(got, want, dtype, "fused decode ragged")
+
+
+def test_decode_fused_append_gqa_tensor_cores():
+    rng = make_rng(142)
+    lens = gen_lens_uniform(rng, 16, 256, 2048)
+    got, want, Kg, Vg, Kw, Vw, lo, low, e, err = run_fused(
+        "bf16", 16, 9, 3, 2112, lens, 1, verify=False, seed=143, flags=3)
+    assert e == 0 and np.array_equal(Kg, Kw) and np.array_equal(lo, low)
+    assert_attn_close(got, want, "bf16", "fused gqa")
+
+
+@pytest.mark.parametrize("L", [0, 59, 60, 62, 443])
+@pytest.mark.parametrize("flags", [0, 3])
+def test_verify_fused_append_block(L, flags):
+    # L = 62: the five new rows straddle the boundary between two 64-position tiles
+    got, want, Kg, Vg, Kw, Vw, lo, low, e, err = run_fused(
+        "f16", 1, 20, 20, 448, [L], 5, verify=True, seed=150 + L, flags=flags)
+    assert e == 0 and not err
+    assert np.array_equal(Kg, Kw) and np.array_equal(Vg, Vw) and np.array_equal(lo, low)
+    assert_attn_close(got, want, "f16", f"fused verify L={L}")
+
+
+def test_fused_append_overflow_leaves_row_untouched():
+    got, want, Kg, Vg, Kw, Vw, lo, low, e, err = run_fused(
+        "f16", 2, 2, 2, 64, [62, 10], 3, verify=True, seed=160)
+    assert e == 16 and err == {16}
+    assert np.array_equal(Kg, Kw) and np.array_equal(lo, low)  # row 0 untouched, len kept
+
+
+def test_pdl_chain_on_one_stream():
+    """append -> self decode -> cross decode -> fused verify, all with PDL (cross and
+    verify with early K/V): every kernel must see its predecessor's writes."""
+    kvd = _kvd()
+    rng = make_rng(170)
+    H, cap, F = 8, 256, 1500
+    lens = np.array([200, 77], np.int32)
+    K, V = gen_cache(rng, 2, H, cap, D, "f16", 0.125, lens=lens)
+    Kx, Vx = gen_cache(rng, 2, H, F, D, "f16", 0.125)
+    kn, vn = gen_new_kv(rng, 2, H, 1, D, "f16", 0.125)
+    kb, vb = gen_new_kv(rng, 2, H, 5, D, "f16", 0.125)
+    q1 = gen_queries(rng, 2, H, 1, D, "f16", 0.125)
+    q5 = gen_queries(rng, 2, H, 5, D, "f16", 0.125)
+    # oracle: append 1, decode self, decode cross, append 5, causal verify
+    Kw, Vw = K.copy(), V.copy()
+    l1, _ = oracle.kv_append(Kw, Vw, kn, vn, lens, "f16")
+    w_self, _ = oracle.attention(q1, Kw, Vw, "f16", lens=l1)
+    w_cross, _ = oracle.attention(q1, Kx, Vx, "f16", fixed_len=F)
+    l2, _ = oracle.kv_append(Kw, Vw, kb, vb, l1, "f16")
+    w_ver, _ = oracle.attention(q5, Kw, Vw, "f16", lens=l2, causal=True)
+    # GPU
+    Kd, Vd = dev16(K, "f16"), dev16(V, "f16")
+    cache, xcache = kvd.make_cache(Kd, Vd), kvd.make_cache(dev16(Kx, "f16"), dev16(Vx, "f16"))
+    l1d = torch.zeros(2, dtype=torch.int32, device="cuda")
+    l2d = torch.zeros(2, dtype=torch.int32, device="cuda")
+    q1d, q5d = dev16(q1, "f16"), dev16(q5, "f16")
+    o_self, o_cross = torch.empty_like(q1d), torch.empty_like(q1d)
+    o_ver = torch.empty_like(q5d)
+    ws = kvd.new_workspace(kvd.kvd_workspace_size(kvd.KVD_OP_VERIFY_ATTN, 2, H, H, 1, 5, F))
+    e = new_err()
+    P, EK = kvd.KVD_FLAG_PDL, kvd.KVD_FLAG_PDL | kvd.KVD_FLAG_EARLY_KV
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        kvd.kvd_kv_append(cache, dev16(kn, "f16"), dev16(vn, "f16"), dev_i32(lens), l1d,
+                          flags=P, dev_err=e)
+        kvd.kvd_decode_attn(q1d, cache, o_self, ws, lens=l1d, flags=P, dev_err=e)
+        kvd.kvd_decode_attn(q1d, xcache, o_cross, ws, fixed_len=F, flags=EK, dev_err=e)
+        kvd.kvd_verify_attn(q5d, cache, o_ver, ws, lens=l1d, causal=True, flags=P, dev_err=e,
+                            append=(dev16(kb, "f16"), dev16(vb, "f16"), l2d))
+    torch.cuda.synchronize()
+    assert e.item() == 0
+    assert np.array_equal(l2d.cpu().numpy(), l2)
+    assert np.array_equal(host16(Kd), Kw) and np.array_equal(host16(Vd), Vw)
+    assert_attn_close(host16(o_self), w_self, "f16", "chain self")
+    assert_attn_close(host16(o_cross), w_cross, "f16", "chain cross")
+    assert_attn_close(host16(o_ver), w_ver, "f16", "chain verify")
