@@ -29,9 +29,9 @@
 //    positions writes them into the cache and into its staged tile, so attention sees
 //    them without a separate launch.
 //  * Long ranges are split over thread blocks. Splits of one unit that fit in a cluster
-//    (<= 16 CTAs) store their (max, sum, o) partials straight into the shared memory of
-//    the cluster's first CTA (st.shared::cluster) and arrive on its mbarrier; that CTA
-//    merges them locally while the others exit. More splits go through the workspace
+//    (<= 16 CTAs) send their (max, sum, o) partials straight into the shared memory of
+//    the cluster's first CTA with asynchronous stores (st.async) that count their bytes
+//    on its mbarrier; that CTA merges them locally while the others exit. More splits go through the workspace
 //    and the last block to arrive (atomic ticket) merges them. Merges run in fixed
 //    split order, so results are repeatable.
 //  * Programmatic dependent launch: every block lets the next kernel on the stream
@@ -144,10 +144,9 @@ __device__ __forceinline__ int64_t qrow(const AttnParams& p, int bk, int h, int 
     return ((int64_t)(r * p.n_q_heads + hq) * p.qlen + i) * kHeadDim;
 }
 
-// Threads of a non-first CTA that store a piece of its partial into the first CTA (each
-// arrives once on the first CTA's merge barrier).
-__device__ __forceinline__ int merge_senders(int mcount) {
-    return min(kSlotQuads * mcount, kThreads);
+// Bytes every non-first CTA of a cluster sends into the first CTA's merge slots.
+__device__ __forceinline__ uint32_t merge_bytes_per_cta(int mcount) {
+    return (uint32_t)(kSlotQuads * mcount * 16);
 }
 
 __device__ __forceinline__ void issue_tile(const CUtensorMap* tmk, const CUtensorMap* tmv,
@@ -188,9 +187,11 @@ __device__ __forceinline__ bool prologue(const AttnParams& p, CtaCtx& c, uint8_t
     }
     if (tid == 0) {
         for (int j = 0; j < p.stages; ++j) mbar_init(smem_u32(&bars[j]), 1);
-        if (p.cluster && c.s == 0)
-            mbar_init(smem_u32(&bars[p.stages]), (p.splits - 1) * merge_senders(c.mcount));
+        if (p.cluster && c.s == 0) mbar_init(smem_u32(&bars[p.stages]), 1);
         fence_barrier_init();
+        if (p.cluster && c.s == 0)  // the one arrival; the others' bytes complete the phase
+            mbar_expect_tx(smem_u32(&bars[p.stages]),
+                           (p.splits - 1) * merge_bytes_per_cta(c.mcount));
         prefetch_tensormap(tmk);
         prefetch_tensormap(tmv);
         const uint32_t tx = 2u * p.box_rows * kRowBytes;
@@ -238,11 +239,11 @@ __device__ __forceinline__ void inject_slab(const AttnParams& p, const CtaCtx& c
 
 // After a timed-out wait: wait (bounded) for the latest copy issued into every stage, so
 // that none is still writing shared memory when the block exits; then keep the cluster's
-// merge consistent -- a non-first CTA still arrives (without data) on the first CTA's
-// barrier, and the first CTA waits for the others, which may still be writing into its
+// merge consistent -- a non-first CTA still sends its (meaningless) bytes so the first
+// CTA's barrier completes, and the first CTA waits for them, since they land in its
 // shared memory, before it exits.
 __device__ void abort_after_timeout(const AttnParams& p, const CtaCtx& c, uint64_t* bars,
-                                    int issued) {
+                                    float* mrg, int issued) {
     const int tid = threadIdx.x;
     if (tid == 0) {
         flag_error(p.dev_err, KVD_ERR_TIMEOUT);
@@ -253,8 +254,11 @@ __device__ void abort_after_timeout(const AttnParams& p, const CtaCtx& c, uint64
     if (p.cluster) {
         cluster_wait();
         if (c.s != 0) {
-            if (tid < merge_senders(c.mcount))
-                mbar_arrive_remote(map_shared(smem_u32(&bars[p.stages]), 0));
+            const uint32_t dst = map_shared(smem_u32(mrg), 0);
+            const uint32_t rbar = map_shared(smem_u32(&bars[p.stages]), 0);
+            for (int it = tid; it < kSlotQuads * c.mcount; it += blockDim.x)
+                st_async_v4(dst + ((c.s * p.msub) * kSlot + 4 * it) * 4,
+                            make_float4(0.f, 0.f, 0.f, 0.f), rbar);
         } else if (tid == 0) {
             mbar_wait_bounded_cluster(smem_u32(&bars[p.stages]), 0);
         }
@@ -266,7 +270,7 @@ __device__ void abort_after_timeout(const AttnParams& p, const CtaCtx& c, uint64
 // Returns false after a timeout (already handled: the caller just returns).
 template <typename Slab>
 __device__ __forceinline__ bool run_tiles(const AttnParams& p, const CtaCtx& c, uint8_t* smem,
-                                          uint64_t* bars, const CUtensorMap* tmk,
+                                          uint64_t* bars, float* mrg, const CUtensorMap* tmk,
                                           const CUtensorMap* tmv, Slab&& slab) {
     const int tid = threadIdx.x, warp = tid >> 5;
     const int half = warp >> 2, slab0 = (warp & 3) * 16;
@@ -292,7 +296,7 @@ __device__ __forceinline__ bool run_tiles(const AttnParams& p, const CtaCtx& c, 
         }
         if (2 * r + p.stages < c.n_tiles) {  // this round's stages are refilled
             if (__syncthreads_or(!all_ok)) {
-                abort_after_timeout(p, c, bars, issued);
+                abort_after_timeout(p, c, bars, mrg, issued);
                 return false;
             }
             if (tid == 0) {
@@ -307,7 +311,7 @@ __device__ __forceinline__ bool run_tiles(const AttnParams& p, const CtaCtx& c, 
         }
     }
     if (__syncthreads_or(!all_ok)) {
-        abort_after_timeout(p, c, bars, issued);
+        abort_after_timeout(p, c, bars, mrg, issued);
         return false;
     }
     return true;
@@ -336,7 +340,7 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
         cluster_wait();  // the first CTA's merge barrier is initialised
         const bool leader = c.s == 0;
         const uint32_t dst = leader ? 0u : map_shared(smem_u32(mrg), 0);
-        bool sent = false;
+        const uint32_t rbar = leader ? 0u : map_shared(smem_u32(merge_bar), 0);
         for (int it = tid; it < kSlotQuads * c.mcount; it += blockDim.x) {
             const int m = it / kSlotQuads, k = it % kSlotQuads;
             float mx = -INFINITY;
@@ -363,13 +367,9 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
             if (leader)
                 *reinterpret_cast<float4*>(mrg + slot) = v;
             else
-                st_dsmem4(dst + slot * 4, v);
-            sent = true;
+                st_async_v4(dst + slot * 4, v, rbar);
         }
-        if (!leader) {
-            if (sent) mbar_arrive_remote(map_shared(smem_u32(merge_bar), 0));
-            return;
-        }
+        if (!leader) return;
         const bool ok = mbar_wait_bounded_cluster(smem_u32(merge_bar), 0);
         __syncthreads();  // the first CTA's own slots were written by other threads
         if (!ok) {
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(kThreads)
             for (int e = 0; e < 8; ++e) acc[e] = fmaf(sc[jj], valid ? vf[e] : 0.f, acc[e]);
         }
     };
-    if (!run_tiles(p, c, smem, bars, &tmk, &tmv, slab)) return;
+    if (!run_tiles(p, c, smem, bars, mrg, &tmk, &tmv, slab)) return;
 
     // Merge the four 8-lane groups of each warp (they saw different positions).
 #pragma unroll
@@ -705,7 +705,7 @@ __global__ void __launch_bounds__(kThreads)
             Mma<T>::run(oacc[2 * np + 1], pa, v2, v3);
         }
     };
-    if (!run_tiles(p, c, smem, bars, &tmk, &tmv, slab)) return;
+    if (!run_tiles(p, c, smem, bars, mrg, &tmk, &tmv, slab)) return;
 
     lA += __shfl_xor_sync(0xffffffffu, lA, 1);
     lA += __shfl_xor_sync(0xffffffffu, lA, 2);

@@ -185,6 +185,15 @@ __device__ __forceinline__ void st_dsmem4(uint32_t addr, float4 v) {
                  "f"(v.y), "f"(v.z), "f"(v.w)
                  : "memory");
 }
+// Asynchronous 16-byte store into another CTA's shared memory; completion is counted
+// in bytes on that CTA's mbarrier (complete_tx), so no fence or arrive is needed.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+        "[%5];" ::"r"(remote_addr),
+        "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+        : "memory");
+}
 // Split cluster barrier: arrive (release) early, wait (acquire) later.
 __device__ __forceinline__ void cluster_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
