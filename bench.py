@@ -405,6 +405,23 @@ def oracle_sample(seconds=10.0, layers_max=32):
 
 
 # ------------------------------------------------------------------------------ main --
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over all ranks (x itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(bytes_per_step: int, ms_per_step_max: float, world: int) -> float:
+    """Whole-job GB/s of `world` independent replicas timed by the slowest rank."""
+    return world * bytes_per_step / (ms_per_step_max * 1e-3) / 1e9
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
@@ -498,11 +515,7 @@ def run_ours(args):
     barrier()
     t1h = time.time()
     clocks = sampler.stop(t0h, t1h)
-    ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
     assert int(step.err.item()) == 0, f"device error {int(step.err.item())}"
 
     # e2e through the public API with host buffers --------------------------------------
@@ -518,18 +531,15 @@ def run_ours(args):
             step.h_out.copy_(step.d_out, non_blocking=True)
         e3.record(stream)
     torch.cuda.synchronize()
-    ms_e2e = e2.elapsed_time(e3) / args.steps
+    ms_e2e = max_over_ranks(e2.elapsed_time(e3) / args.steps, dev)
     if world > 1:
-        t = torch.tensor([ms_e2e], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_e2e = float(t.item())
         torch.distributed.destroy_process_group()
     if rank != 0:
         return 0
 
     bytes_step = step.bytes_step()
-    value = world * bytes_step / (ms * 1e-3) / 1e9
-    value_e2e = world * bytes_step / (ms_e2e * 1e-3) / 1e9
+    value = replica_throughput(bytes_step, ms, world)
+    value_e2e = replica_throughput(bytes_step, ms_e2e, world)
 
     # per-part and per-kernel timings (rank 0 only, outside the timed region) ----------
     reps = 200
@@ -574,6 +584,8 @@ def run_ours(args):
     achieved = vcross_bytes / (t_vcross * 1e-3) / 1e9
     traffic = args.traffic if args.traffic is not None else profiled_traffic()
 
+    vs_name = "verify_attn_self_448_q5_fused_append" if fused else "verify_attn_self_448_q5"
+    ds_name = "decode_attn_self_448_fused_append" if fused else "decode_attn_self_448"
     bytes_dec, bytes_ver = step.bytes_decode(), step.bytes_verify()
     e_n = sum(0.75 ** i for i in range(1, step.k + 1))
     verified = (e_n + 1) * 1 / (ms_ver * 1e-3 / step.NL)
@@ -605,6 +617,11 @@ def run_ours(args):
         "decode_attn_gbs": round(bytes_dec / (ms_dec * 1e-3) / 1e9, 2),
         "verify_round_gbs": round(bytes_ver / (ms_ver * 1e-3) / 1e9, 2),
         "verify_over_decode_time": round(ms_ver / ms_dec, 3),
+        # per layer, attention only (self + cross), k=5 verify block vs one-token decode
+        "verify_over_decode_per_layer": round(
+            (kern[vs_name]["us_per_launch"] + kern["verify_attn_cross_1500_q5"]["us_per_launch"])
+            / (kern[ds_name]["us_per_launch"] + kern["decode_attn_cross_1500"]["us_per_launch"]),
+            3),
         "verified_tokens_per_s_per_layer_step": round(verified, 1),
         "roofline": {"bound": "hbm",
                      "kernel": "block_attn_kernel: causal-free verify of 5 tokens over the "

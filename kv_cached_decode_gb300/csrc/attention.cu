@@ -485,7 +485,7 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
 
 // ------------------------------------------------- one query vector per KV head (SIMT) --
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: 4 blocks per SM
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
     constexpr int RM = 1;
