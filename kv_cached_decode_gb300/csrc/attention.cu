@@ -202,7 +202,7 @@ __device__ __forceinline__ bool prologue(const AttnParams& p, CtaCtx& c, uint8_t
     if (p.early && tid < c.mcount)  // bring the query rows into L2 while waiting
         prefetch_l2(static_cast<const uint8_t*>(p.q) + qrow(p, c.bk, c.h, c.m0 + tid) * 2);
     __syncthreads();
-    if (p.cluster) cluster_arrive();  // publishes the first CTA's merge barrier
+    if (p.cluster) cluster_arrive_relaxed();  // the first CTA's merge barrier is ready
     pdl_trigger();
     if (p.early) pdl_wait();
     if (p.append && p.lens_out && tid == 0 && c.s == 0 && c.h == 0 && c.sub == 0)

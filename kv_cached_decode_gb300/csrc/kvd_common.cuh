@@ -194,9 +194,10 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint
         "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
         : "memory");
 }
-// Split cluster barrier: arrive (release) early, wait (acquire) later.
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+// Split cluster barrier: arrive early, wait (acquire) later. The arrive is relaxed: what
+// it publishes (mbarrier initialisation) is ordered by fence.mbarrier_init.release.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
