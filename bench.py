@@ -38,8 +38,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from workloads import (WORKLOADS, gen_accept_inputs, gen_cache, gen_new_kv, gen_parents,  # noqa: E402
-                       gen_queries, make_rng, seed_for)
+from workloads import (WORKLOADS, gen_accept_inputs, gen_cache, gen_lens_uniform,  # noqa: E402
+                       gen_new_kv, gen_parents, gen_queries, make_rng, seed_for)
 
 METRIC = "decode-attn KV-read GB/s & % of 8 TB/s HBM; verified tokens/s per layer-step"
 NOMINAL_HBM_GBS = 8000.0
@@ -705,6 +705,9 @@ def run_sweep(args):
                 del pool, caches, g
                 torch.cuda.empty_cache()
     run_beam_step(torch, kvd, dev, stream, peak, flags)
+    run_gqa_lm_step(torch, kvd, dev, stream, peak, flags)
+    run_tiny_layer(torch, kvd, dev, stream, flags)
+    run_verify_ratio(torch, kvd, dev, stream, flags)
     return 0
 
 
@@ -767,6 +770,100 @@ def run_beam_step(torch, kvd, dev, stream, peak, flags):
                           "moved_rows": moved, "source_rows": srcs}), flush=True)
 
 
+def run_gqa_lm_step(torch, kvd, dev, stream, peak, flags):
+    """GQA decoder-LM step: 30 layers, 16 rows, 9 query heads on 3 KV heads, bf16,
+    ragged lengths uniform in [256, 2048]; per layer one fused call appends each row's
+    new token and attends over its len + 1 positions."""
+    w = WORKLOADS["gqa_lm_step"]
+    NL, B, Hq, Hkv, cap = w["n_layers"], w["batch"], w["n_q_heads"], w["n_kv_heads"], w["capacity"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3030)
+    bf = torch.bfloat16
+    caches = []
+    for _ in range(NL):
+        k = torch.empty(B, Hkv, cap, D, dtype=bf, device=dev).normal_(0, w["qkv_std"], generator=gen)
+        v = torch.empty(B, Hkv, cap, D, dtype=bf, device=dev).normal_(0, w["qkv_std"], generator=gen)
+        caches.append(kvd.make_cache(k, v))
+    lens_np = gen_lens_uniform(make_rng(seed_for("gqa_lm_step")), B, w["len_lo"], w["len_hi"])
+    lens_in = torch.from_numpy(lens_np).to(dev)
+    lens_out = torch.zeros_like(lens_in)
+    q = torch.empty(NL, B, Hq, 1, D, dtype=bf, device=dev).normal_(0, w["qkv_std"], generator=gen)
+    kn = torch.empty(NL, 2, B, Hkv, 1, D, dtype=bf, device=dev).normal_(0, w["qkv_std"], generator=gen)
+    out = torch.empty_like(q)
+    ws = kvd.new_workspace(kvd.kvd_workspace_size(kvd.KVD_OP_DECODE_ATTN, B, Hq, Hkv, 1, 1, cap),
+                           device=dev)
+
+    def step():
+        for l in range(NL):
+            kvd.kvd_decode_attn(q[l], caches[l], out[l], ws, lens=lens_in, scale=w["scale"],
+                                flags=flags, append=(kn[l, 0], kn[l, 1], lens_out))
+
+    t = time_graph(torch, capture(torch, step, stream), stream, 100)
+    kv_bytes = 2 * Hkv * int(np.sum(lens_np.astype(np.int64) + 1)) * D * 2
+    step_bytes = NL * (kv_bytes + 2 * B * Hq * D * 2 + append_bytes(B, Hkv, 1))
+    gbs = step_bytes / (t * 1e-3) / 1e9
+    print(json.dumps({"sweep": "gqa_lm_step", "layers": NL, "batch": B, "heads": f"{Hq}/{Hkv}",
+                      "mean_len": round(float(lens_np.mean()), 1), "step_us": round(t * 1e3, 2),
+                      "us_per_layer": round(t * 1e3 / NL, 3), "gbs": round(gbs, 1),
+                      "pct_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 1),
+                      "pct_peak": round(100 * gbs / peak, 1),
+                      "tokens_per_s": round(B / (t * 1e-3), 1)}), flush=True)
+
+
+def run_tiny_layer(torch, kvd, dev, stream, flags):
+    """Tiny single layer: 6 heads, 32 cached positions + 1 appended (fused), then cross
+    attention over 1500 frames."""
+    w = WORKLOADS["tiny_layer"]
+    H, cap, F = w["n_q_heads"], w["capacity"], w["cross_len"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1010)
+    f16 = torch.float16
+    k, v = (torch.empty(1, H, cap, D, dtype=f16, device=dev).normal_(0, 0.125, generator=gen)
+            for _ in range(2))
+    kx, vx = (torch.empty(1, H, F, D, dtype=f16, device=dev).normal_(0, 0.125, generator=gen)
+              for _ in range(2))
+    c_self, c_cross = kvd.make_cache(k, v), kvd.make_cache(kx, vx)
+    q = torch.empty(2, 1, H, 1, D, dtype=f16, device=dev).normal_(0, 0.125, generator=gen)
+    kn = torch.empty(2, 1, H, 1, D, dtype=f16, device=dev).normal_(0, 0.125, generator=gen)
+    out = torch.empty_like(q)
+    lens_in = torch.tensor([w["cached"]], dtype=torch.int32, device=dev)
+    lens_out = torch.zeros_like(lens_in)
+    ws = kvd.new_workspace(kvd.kvd_workspace_size(kvd.KVD_OP_DECODE_ATTN, 1, H, H, 1, 1, F),
+                           device=dev)
+
+    def layer():
+        kvd.kvd_decode_attn(q[0], c_self, out[0], ws, lens=lens_in, scale=w["scale"], flags=flags,
+                            append=(kn[0], kn[1], lens_out))
+        kvd.kvd_decode_attn(q[1], c_cross, out[1], ws, fixed_len=F, scale=w["scale"], flags=flags)
+
+    t = time_graph(torch, capture(torch, layer, stream), stream, 500)
+    nbytes = append_bytes(1, H, 1) + attn_bytes(1, H, H, cap, 1) + attn_bytes(1, H, H, F, 1)
+    print(json.dumps({"sweep": "tiny_layer", "us": round(t * 1e3, 3), "bytes": nbytes,
+                      "gbs": round(nbytes / (t * 1e-3) / 1e9, 1), "l2_resident": True}),
+          flush=True)
+
+
+def run_verify_ratio(torch, kvd, dev, stream, flags):
+    """Verify (k = 5) against single-token decode over the same Whisper-shaped caches,
+    32 layers each, across cached lengths: self (fused append) and cross attention."""
+    st = WhisperStep(dev, flags=flags)
+    for L in (0, 64, 128, 256, 443):
+        st.dec_lens_in.fill_(L)
+        st.ver_lens_in.fill_(L)
+        t = {}
+        # self + cross interleaved per layer (320 MB of distinct K/V per graph),
+        # and self alone (73 MB of self caches: L2-resident between replays)
+        for name, fn in (("decode", lambda: st.run_decode(parts=("self", "cross"))),
+                         ("verify", lambda: st.run_verify(parts=("self", "cross"))),
+                         ("decode_self", lambda: st.run_decode(parts=("self",))),
+                         ("verify_self", lambda: st.run_verify(parts=("self",)))):
+            t[name] = time_graph(torch, capture(torch, fn, stream), stream, 100) * 1e3 / st.NL
+        print(json.dumps({"sweep": "verify_ratio", "len": L, "k": st.k,
+                          **{f"{k}_us_per_layer": round(v, 3) for k, v in t.items()},
+                          "self_ratio": round(t["verify_self"] / t["decode_self"], 3),
+                          "layer_ratio": round(t["verify"] / t["decode"], 3)}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -781,7 +878,8 @@ def main(argv=None):
                     help="PDL, and cross-attention calls stage K/V before the dependency wait")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
-                    help="decode-attention batch x length sweep and the beam step (JSON lines)")
+                    help="decode-attention batch x length sweep, the beam step, the GQA-LM "
+                         "step, the tiny layer and the verify/decode ratio (JSON lines)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu DRAM bytes per launch of the dominant kernel, if measured")

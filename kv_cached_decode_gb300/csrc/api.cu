@@ -67,7 +67,7 @@ kvd_status validate_cache(const kvd_cache* c) {
 }
 
 AttnPlan plan_attention(int batch, int n_q_heads, int n_kv_heads, int rows_per_kv, int qlen,
-                        int len_bound, int mmax, int target_ctas, int max_cluster) {
+                        int len_bound, int mmax, int s, int max_cluster) {
     AttnPlan P = {};
     P.bkv = batch / rows_per_kv;
     P.group = n_q_heads / n_kv_heads;
@@ -78,14 +78,9 @@ AttnPlan plan_attention(int batch, int n_q_heads, int n_kv_heads, int rows_per_k
     P.tiles_total = (std::max(len_bound, 0) + 63) / 64;
     // Work is handed out in rounds of two 64-position tiles (the eight warps of a block
     // work on two tiles at once).
-    const int rounds = (P.tiles_total + 1) / 2;
-    const int want = std::max(1, (target_ctas + P.units - 1) / P.units);
-    int s = std::max(1, std::min({rounds, want, kMaxSplits}));
-    // Fewer, cluster-sized splits are preferred while they still give about one block
-    // per SM (target_ctas is ~2 blocks per SM): their merge stays on chip.
-    if (s > max_cluster && max_cluster > 1 && (int64_t)P.units * max_cluster * 2 >= target_ctas)
-        s = max_cluster;
-    P.tiles_per_split = 2 * std::max(1, (rounds + s - 1) / s);
+    P.rounds = (P.tiles_total + 1) / 2;
+    s = std::max(1, std::min({s, P.rounds, kMaxSplits}));
+    P.tiles_per_split = 2 * std::max(1, (P.rounds + s - 1) / s);
     P.splits = P.tiles_total > 0 ? (P.tiles_total + P.tiles_per_split - 1) / P.tiles_per_split : 1;
     P.cluster = P.splits > 1 && P.splits <= max_cluster;
     P.stages = P.tiles_per_split >= 4 ? 4 : 2;
@@ -94,6 +89,14 @@ AttnPlan plan_attention(int batch, int n_q_heads, int n_kv_heads, int rows_per_k
     P.ml_offset = align_up(P.part_offset + slots * 64 * sizeof(float), 256);
     P.ws_bytes = (P.splits > 1 && !P.cluster) ? P.ml_offset + slots * 2 * sizeof(float) : 0;
     return P;
+}
+
+bool workspace_merge_pays(int units, int rounds) {
+    if (units > kWsMaxUnits || rounds <= kMaxClusterSplits) return false;
+    const int tps_cluster = 2 * ((rounds + kMaxClusterSplits - 1) / kMaxClusterSplits);
+    const int s = std::min(rounds, kMaxSplits);
+    const int tps_ws = 2 * ((rounds + s - 1) / s);
+    return tps_cluster - tps_ws > kWsMergeTiles;
 }
 
 }  // namespace kvd
@@ -114,9 +117,12 @@ extern "C" size_t kvd_workspace_size(kvd_op op, int32_t batch, int32_t n_q_heads
         // one query vector per KV head runs alone; two or more go in blocks of 16
         const int64_t M = (int64_t)rows_per_kv * (n_q_heads / n_kv_heads) * q;
         const int mmax = M >= 2 ? kMmaQueryBlock : 1;
-        // Sized for the workspace path (no cluster), which covers every launch plan.
-        AttnPlan P = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, q, max_len, mmax,
-                                    kWsTargetBound, 1);
+        const AttnPlan P1 = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, q, max_len,
+                                           mmax, 1, 1);
+        if (!workspace_merge_pays(P1.units, P1.rounds)) return KVD_WS_COUNTER_BYTES;
+        // The most splits a launch can use bounds every workspace plan.
+        const AttnPlan P = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, q, max_len,
+                                          mmax, kMaxSplits, 1);
         return std::max<size_t>(P.ws_bytes, KVD_WS_COUNTER_BYTES);
     }
     case KVD_OP_GREEDY_ACCEPT: {

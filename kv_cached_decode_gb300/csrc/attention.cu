@@ -31,7 +31,10 @@
 //  * Long ranges are split over thread blocks. Splits of one unit that fit in a cluster
 //    (<= 16 CTAs) send their (max, sum, o) partials straight into the shared memory of
 //    the cluster's first CTA with asynchronous stores (st.async) that count their bytes
-//    on its mbarrier; that CTA merges them locally while the others exit. More splits go through the workspace
+//    on its mbarrier; that CTA merges them locally while the others exit. The split
+//    count is the largest whose clusters are all resident at once (occupancy
+//    calculator), so a launch never runs a second, partial wave. Only a handful of
+//    units over a long range split further: those partials go through the workspace
 //    and the last block to arrive (atomic ticket) merges them. Merges run in fixed
 //    split order, so results are repeatable.
 //  * Programmatic dependent launch: every block lets the next kernel on the stream
@@ -41,6 +44,7 @@
 #include <atomic>
 #include <climits>
 #include <mutex>
+#include <unordered_map>
 
 #include "kvd_common.cuh"
 #include "kvd_internal.h"
@@ -770,6 +774,11 @@ int prepare(bool mma) {
                      smem_layout(kMaxStages, 1, kMaxClusterSplits).total);
 }
 
+template <typename T>
+const void* kernel_of(bool mma) {
+    return mma ? reinterpret_cast<const void*>(block_attn_kernel<T>)
+               : reinterpret_cast<const void*>(decode_attn_kernel<T>);
+}
 
 template <typename T>
 kvd_status launch_attn(bool mma, dim3 grid, cudaStream_t st, bool pdl, unsigned cl,
@@ -780,6 +789,82 @@ kvd_status launch_attn(bool mma, dim3 grid, cudaStream_t st, bool pdl, unsigned 
                          smem_layout(p.stages, 16, slots).total, st, pdl, cl, mk, mv, p);
     return launch_ex(decode_attn_kernel<T>, grid, dim3(kThreads),
                      smem_layout(p.stages, 1, slots).total, st, pdl, cl, mk, mv, p);
+}
+
+size_t plan_smem(const AttnPlan& P, bool mma) {
+    return smem_layout(P.stages, mma ? 16 : 1, merge_slots(P.cluster, P.splits, P.msub)).total;
+}
+
+// How many thread blocks (cluster == 1, whole GPU) or clusters of `cluster` blocks can
+// be resident at once, from the CUDA occupancy calculator; cached per device, kernel,
+// shared-memory size and cluster size. 0 if the query fails.
+int resident(const void* kern, int kid, size_t smem, int cluster, int nsm) {
+    static std::mutex mu;
+    static std::unordered_map<uint64_t, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const uint64_t key = ((uint64_t)dev << 48) | ((uint64_t)kid << 40) |
+                         ((uint64_t)cluster << 32) | (uint64_t)smem;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    int n = 0;
+    if (cluster <= 1) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem) != cudaSuccess)
+            n = 0;
+        n *= nsm;
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cluster, 1, 1);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute a[1];
+        a[0].id = cudaLaunchAttributeClusterDimension;
+        a[0].val.clusterDim.x = cluster;
+        a[0].val.clusterDim.y = 1;
+        a[0].val.clusterDim.z = 1;
+        cfg.attrs = a;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    std::lock_guard<std::mutex> g(mu);
+    cache[key] = n;
+    return n;
+}
+
+// Split choice. Blocks of one launch should all be resident at once: a second, partial
+// wave costs as much as the first. So, for few long units, take the most splits whose
+// clusters (one per unit) are all resident together; fall back to one block per unit
+// when none fits (many units fill the GPU by themselves). Only for a handful of units
+// over a long range, where even 16-block clusters leave each block streaming many
+// tiles, split further and merge through the workspace.
+AttnPlan choose_plan(const void* kern, int kid, bool mma, int nsm, int batch, int n_q_heads,
+                     int n_kv_heads, int rows_per_kv, int qlen, int len_bound, int max_cluster) {
+    const int mmax = mma ? kMmaQueryBlock : 1;
+    const AttnPlan P1 = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, qlen, len_bound,
+                                       mmax, 1, max_cluster);
+    if (P1.rounds <= 1) return P1;
+    if (workspace_merge_pays(P1.units, P1.rounds)) {
+        AttnPlan W = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, qlen, len_bound,
+                                    mmax, kMaxSplits, 1);
+        const int blocks = resident(kern, kid, plan_smem(W, mma), 1, nsm);
+        return plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, qlen, len_bound, mmax,
+                              std::max(1, blocks / P1.units), max_cluster);
+    }
+    int last = 0;
+    for (int s = std::min(P1.rounds, max_cluster); s >= 2; --s) {
+        const AttnPlan P = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, qlen,
+                                          len_bound, mmax, s, max_cluster);
+        if (P.splits == last) continue;
+        last = P.splits;
+        if (P.splits < 2) break;
+        if (P.cluster && resident(kern, kid, plan_smem(P, mma), P.splits, nsm) >= P.units)
+            return P;
+    }
+    return P1;
 }
 
 kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_heads,
@@ -808,11 +893,12 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
     const bool bf = dtype == KVD_BF16;
     const int group = n_q_heads / kv->n_kv_heads;
     const bool mma = verify || (int64_t)rows_per_kv * group * qlen >= 2;
-    const int mmax = mma ? kMmaQueryBlock : 1;
     const int max_cluster = bf ? prepare<__nv_bfloat16>(mma) : prepare<__half>(mma);
     if (max_cluster <= 0) return KVD_ERR_CUDA;
-    const AttnPlan P = plan_attention(batch, n_q_heads, kv->n_kv_heads, rows_per_kv, qlen,
-                                      len_bound, mmax, 2 * nsm, max_cluster);
+    const int kid = (mma ? 2 : 0) | (bf ? 1 : 0);
+    const void* kern = bf ? kernel_of<__nv_bfloat16>(mma) : kernel_of<__half>(mma);
+    const AttnPlan P = choose_plan(kern, kid, mma, nsm, batch, n_q_heads, kv->n_kv_heads,
+                                   rows_per_kv, qlen, len_bound, max_cluster);
     if ((int64_t)kv->n_kv_heads * P.nsub > 65535) return KVD_ERR_UNSUPPORTED;
     if (P.splits > 1 && !P.cluster) {
         if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < P.ws_bytes)

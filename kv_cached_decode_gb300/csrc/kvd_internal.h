@@ -63,13 +63,13 @@ kvd_status launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 // ---- attention work plan ------------------------------------------------------------
 // The query vectors of one (cache row, KV head) -- rows_per_kv rows x group query
 // heads x qlen tokens -- are processed together so every K/V tile is read once for
-// all of them; they are cut into `nsub` blocks of at most `mmax`. The attended range
-// is cut into `splits` chunks of `tiles_per_split` 64-position tiles so that about
-// `target_ctas` thread blocks exist; partial results are merged through the workspace.
-// Splits of one unit that fit in one thread-block cluster merge through distributed
-// shared memory (no workspace); more splits merge through the workspace.
+// all of them; they are cut into `nsub` blocks of at most `mmax`. A (row, KV head,
+// block) triple is a "unit". The attended range of a unit is cut into `splits` chunks
+// of `tiles_per_split` 64-position tiles, one thread block each. Splits of one unit
+// that fit in one thread-block cluster merge through distributed shared memory (no
+// workspace); more splits merge through the workspace.
 struct AttnPlan {
-    int bkv, group, M, msub, nsub, units, tiles_total, splits, tiles_per_split, stages;
+    int bkv, group, M, msub, nsub, units, tiles_total, rounds, splits, tiles_per_split, stages;
     bool cluster;
     size_t part_offset, ml_offset, ws_bytes;
 };
@@ -78,13 +78,27 @@ constexpr int kMaxStages = 4;
 constexpr int kMmaQueryBlock = 16;     // query vectors per block on the tensor-core path
 constexpr int kMaxSplits = 128;        // splits per unit (merge scratch is sized for this)
 constexpr int kMaxClusterSplits = 16;  // largest cluster used for a merge
-constexpr int kWsTargetBound = 4096;   // upper bound of target_ctas used for sizing
+// A workspace merge (more splits than a cluster holds) is only considered for at most
+// this many units: more units already fill the GPU with cluster-sized splits.
+constexpr int kWsMaxUnits = 8;
+// What the workspace merge costs (a global ticket, partials written and read back by
+// the last block), in 64-position tiles of per-block streaming time.
+constexpr int kWsMergeTiles = 12;
 
+// The plan for a requested split count `s` (clamped to [1, min(rounds, kMaxSplits)];
+// work is handed out in rounds of two tiles, so several s give the same plan).
 // max_cluster: largest usable cluster (1 = never merge through a cluster).
 AttnPlan plan_attention(int batch, int n_q_heads, int n_kv_heads, int rows_per_kv, int qlen,
-                        int len_bound, int mmax, int target_ctas, int max_cluster);
+                        int len_bound, int mmax, int s, int max_cluster);
 
-// Workspace bytes of greedy_accept for a given target block count (greedy_accept.cu).
+// Whether splitting a unit beyond one cluster (merging through the workspace) can pay
+// off: the tiles a block streams must drop by more than the merge costs. Depends only
+// on the shape, so workspace sizing and the launcher agree.
+bool workspace_merge_pays(int units, int rounds);
+
+// Workspace bytes of greedy_accept for a given target block count (greedy_accept.cu);
+// sized with kWsTargetBound, an upper bound of the block count any launch targets.
+constexpr int kWsTargetBound = 4096;
 size_t accept_workspace_bytes(int batch, int k, int vocab, int target_ctas);
 
 }  // namespace kvd

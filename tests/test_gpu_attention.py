@@ -181,16 +181,16 @@ def test_strided_cache_view():
 
 
 def test_workspace_too_small_is_rejected():
-    """Two (row, head) units over 4096 positions merge through the workspace."""
+    """Two (row, head) units over 32768 positions merge through the workspace."""
     kvd = _kvd()
-    K = torch.zeros(1, 2, 4096, D, dtype=torch.float16, device="cuda")
+    K = torch.zeros(1, 2, 32768, D, dtype=torch.float16, device="cuda")
     q = torch.zeros(1, 2, 1, D, dtype=torch.float16, device="cuda")
     ws = torch.zeros(1024, dtype=torch.uint8, device="cuda")
     with pytest.raises(kvd.KvdError) as ei:
-        kvd.kvd_decode_attn(q, kvd.make_cache(K, K), q.clone(), ws, fixed_len=4096)
+        kvd.kvd_decode_attn(q, kvd.make_cache(K, K), q.clone(), ws, fixed_len=32768)
     assert ei.value.status == 3
     with pytest.raises(kvd.KvdError):
-        kvd.kvd_decode_attn(q, kvd.make_cache(K, K), q.clone(), None, fixed_len=4096)
+        kvd.kvd_decode_attn(q, kvd.make_cache(K, K), q.clone(), None, fixed_len=32768)
 
 
 # ------------------------------------------------------------------------- verify -------
@@ -247,16 +247,17 @@ def test_verify_single_token_equals_decode():
     assert_attn_close(b, want, "f16", "decode")
 
 
-# Few (row, head) units over a long range: more splits than a cluster holds, so the
-# partials are merged through the workspace by the last block to arrive.
+# Few (row, head) units over a long range: 16-block clusters would leave each block
+# 16 rounds of tiles, so the range is cut into 128 splits whose partials are merged
+# through the workspace by the last block to arrive.
 def test_decode_workspace_merge_long_cache():
-    got, want = run_attention("f16", 1, 2, 2, 4096, lens=np.array([4000], np.int32), seed=130)
-    assert_attn_close(got, want, "f16", "decode 2 units x 63 splits")
+    got, want = run_attention("f16", 1, 2, 2, 32768, lens=np.array([32000], np.int32), seed=130)
+    assert_attn_close(got, want, "f16", "decode 2 units x 125 splits")
 
 
 def test_verify_workspace_merge_sixteen_queries():
-    # 16 query heads on one KV head, qlen 1: 16 query vectors per block, 32 splits
-    got, want = run_attention("bf16", 1, 16, 1, 2048, lens=np.array([2048], np.int32), qlen=1,
+    # 16 query heads on one KV head, qlen 1: 16 query vectors per block, 128 splits
+    got, want = run_attention("bf16", 1, 16, 1, 32768, lens=np.array([32768], np.int32), qlen=1,
                               causal=True, verify=True, seed=131)
     assert_attn_close(got, want, "bf16", "verify M=16 workspace merge")
 

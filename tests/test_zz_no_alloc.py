@@ -30,8 +30,8 @@ def _gpu():
 
 # (dtype, batch, q heads, kv heads, capacity, lengths or None, fixed length)
 CASES = [
-    # two (row, head) units over 4096 positions: 64 splits merged in the scratch buffer
-    ("f16", 1, 2, 2, 4096, [4000], 0),
+    # two (row, head) units over 32768 positions: 125 splits merged in the scratch buffer
+    ("f16", 1, 2, 2, 32768, [32000], 0),
     # ragged GQA rows: merged inside thread-block clusters, scratch counters unused
     ("bf16", 4, 9, 3, 700, [700, 1, 333, 64], 0),
     # cross attention over 1500 frames with beam rows sharing each window's K/V
@@ -82,13 +82,13 @@ def test_noalloc_matches_workspace_entry_point_twice(case):
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     import kv_cached_decode_gb300 as kvd
 
-    # 4 KV heads x 8 query heads each over 8192 positions merge through 128 splits of
-    # 8 query vectors: about 1 MiB of partials, more than the built-in 512 KiB.
-    K = torch.zeros(1, 4, 8192, D, dtype=torch.float16, device="cuda")
+    # 2 KV heads x 16 query heads each over 32768 positions merge through 128 splits of
+    # 16 query vectors: about 1 MiB of partials, more than the built-in 512 KiB.
+    K = torch.zeros(1, 2, 32768, D, dtype=torch.float16, device="cuda")
     q = torch.zeros(1, 32, 1, D, dtype=torch.float16, device="cuda")
     out = torch.full_like(q, 5.0)
     with pytest.raises(kvd.KvdError) as ei:
-        kvd.kvd_decode_attn_noalloc(q, kvd.make_cache(K, K), out, fixed_len=8192)
+        kvd.kvd_decode_attn_noalloc(q, kvd.make_cache(K, K), out, fixed_len=32768)
     assert ei.value.status == 3  # KVD_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.all(out == 5.0)
