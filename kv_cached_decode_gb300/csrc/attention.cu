@@ -55,6 +55,10 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kSlot = kHeadDim + 4;   // floats per merge slot: o[64], max, sum, 2 pad
 constexpr int kSlotQuads = kSlot / 4;  // 17 float4 per slot
+// Row stride (floats) of the warp partials o[warp][row][.]: with 16 rows per warp the
+// fragment layout writes 8 rows at once, and a stride of 72 (8 banks apart) keeps
+// those float2 stores free of bank conflicts.
+__host__ __device__ constexpr int red_stride(int rmax) { return rmax > 1 ? kHeadDim + 8 : kHeadDim; }
 
 struct AttnParams {
     const void* q;
@@ -101,7 +105,7 @@ struct SmemLayout {
 __host__ __device__ inline SmemLayout smem_layout(int stages, int rmax, int merge_slots) {
     SmemLayout L;
     const uint32_t tiles = stages * 2 * kTileBytes;
-    const uint32_t red = kWarps * rmax * (kHeadDim + 2) * 4;
+    const uint32_t red = kWarps * rmax * (red_stride(rmax) + 2) * 4;
     L.red_off = 0;
     L.bar_off = ((tiles > red ? tiles : red) + 1023) & ~1023u;
     L.mrg_off = (L.bar_off + (stages + 1) * 8 + 15) & ~15u;
@@ -329,12 +333,13 @@ __device__ __forceinline__ bool run_tiles(const AttnParams& p, const CtaCtx& c, 
 //  * more splits than a cluster holds: publish to the workspace; the last block to
 //    arrive (atomic ticket) merges all splits, loading them in parallel.
 // Merges run over the splits in index order, so results do not depend on timing.
-// red: o [8][RMAX][64], m [8][RMAX], l [8][RMAX]; mrg: [splits][msub][kSlot].
+// red: o [8][RMAX][red_stride], m [8][RMAX], l [8][RMAX]; mrg: [splits][msub][kSlot].
 template <typename T, int RMAX>
 __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, float* mrg,
                            uint64_t* merge_bar, int* misc, uint8_t* scratch4k) {
+    constexpr int RS = red_stride(RMAX);
     const float* red_o = red;
-    const float* red_m = red + kWarps * RMAX * kHeadDim;
+    const float* red_m = red + kWarps * RMAX * RS;
     const float* red_l = red_m + kWarps * RMAX;
     const int tid = threadIdx.x;
     const int S = p.splits;
@@ -357,7 +362,7 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
                 const float a = exp2f(red_m[w * RMAX + m] - ref);
                 if (k < kHeadDim / 4) {
                     const float4 o = *reinterpret_cast<const float4*>(
-                        red_o + (w * RMAX + m) * kHeadDim + 4 * k);
+                        red_o + (w * RMAX + m) * RS + 4 * k);
                     v.x = fmaf(o.x, a, v.x);
                     v.y = fmaf(o.y, a, v.y);
                     v.z = fmaf(o.z, a, v.z);
@@ -380,19 +385,33 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
             if (tid == 0) flag_error(p.dev_err, KVD_ERR_TIMEOUT);
             return;
         }
+        // (a) one warp per query vector, one lane per split (S <= 16): the split's
+        //     normalised weight replaces its max in the slot.
+        const int lane = tid & 31;
+        for (int m = tid >> 5; m < c.mcount; m += kWarps) {
+            float* sl = mrg + (lane * p.msub + m) * kSlot;
+            const float ms = lane < S ? sl[kHeadDim] : -INFINITY;
+            float mx = ms;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            const float ref = mx == -INFINITY ? 0.f : mx;
+            const float a = lane < S ? exp2f(ms - ref) : 0.f;
+            float l = lane < S ? sl[kHeadDim + 1] * a : 0.f;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+            if (lane < S) sl[kHeadDim] = l > 0.f ? a / l : 0.f;
+        }
+        __syncthreads();
+        // (b) weighted sum over the splits, in split order
         for (int idx = tid; idx < c.mcount * kHeadDim; idx += blockDim.x) {
             const int m = idx >> 6, d = idx & 63;
-            float mx = -INFINITY;
-            for (int r = 0; r < S; ++r) mx = fmaxf(mx, mrg[(r * p.msub + m) * kSlot + kHeadDim]);
-            const float ref = mx == -INFINITY ? 0.f : mx;
-            float l = 0.f, o = 0.f;
+            float o = 0.f;
+#pragma unroll 4
             for (int r = 0; r < S; ++r) {
                 const float* sl = mrg + (r * p.msub + m) * kSlot;
-                const float a = exp2f(sl[kHeadDim] - ref);
-                l = fmaf(sl[kHeadDim + 1], a, l);
-                o = fmaf(sl[d], a, o);
+                o = fmaf(sl[d], sl[kHeadDim], o);
             }
-            store_out<T>(p, c, m, d, l > 0.f ? o / l : 0.f);
+            store_out<T>(p, c, m, d, o);
         }
         return;
     }
@@ -409,7 +428,7 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
         for (int w = 0; w < kWarps; ++w) {
             const float a = exp2f(red_m[w * RMAX + m] - ref);
             l = fmaf(red_l[w * RMAX + m], a, l);
-            o = fmaf(red_o[(w * RMAX + m) * kHeadDim + d], a, o);
+            o = fmaf(red_o[(w * RMAX + m) * RS + d], a, o);
         }
         if (S == 1) {
             store_out<T>(p, c, m, d, l > 0.f ? o / l : 0.f);
@@ -576,10 +595,10 @@ __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: 4 blocks per
     }
     if (grp == 0) {
         float* red_o = red;
-        float* red_m = red + kWarps * RM * kHeadDim;
+        float* red_m = red + kWarps * RM * red_stride(RM);
         float* red_l = red_m + kWarps * RM;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) red_o[warp * kHeadDim + c8 * 8 + e] = acc[e];
+        for (int e = 0; e < 8; ++e) red_o[warp * red_stride(RM) + c8 * 8 + e] = acc[e];
         if (c8 == 0) {
             red_m[warp] = mrun;
             red_l[warp] = lrun;
@@ -716,17 +735,19 @@ __global__ void __launch_bounds__(kThreads)
     lB += __shfl_xor_sync(0xffffffffu, lB, 1);
     lB += __shfl_xor_sync(0xffffffffu, lB, 2);
     {
+        constexpr int RS = red_stride(RM);
         float* red_o = red;
-        float* red_m = red + kWarps * RM * kHeadDim;
+        float* red_m = red + kWarps * RM * RS;
         float* red_l = red_m + kWarps * RM;
+        // only the rows that hold query vectors are read back
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
-            float* oa = red_o + (warp * RM + qr) * kHeadDim + n * 8 + qc;
-            float* ob = red_o + (warp * RM + qr + 8) * kHeadDim + n * 8 + qc;
-            oa[0] = oacc[n][0];
-            oa[1] = oacc[n][1];
-            ob[0] = oacc[n][2];
-            ob[1] = oacc[n][3];
+            if (rowA)
+                *reinterpret_cast<float2*>(red_o + (warp * RM + qr) * RS + n * 8 + qc) =
+                    make_float2(oacc[n][0], oacc[n][1]);
+            if (rowB)
+                *reinterpret_cast<float2*>(red_o + (warp * RM + qr + 8) * RS + n * 8 + qc) =
+                    make_float2(oacc[n][2], oacc[n][3]);
         }
         if ((lane & 3) == 0) {
             red_m[warp * RM + qr] = mA;
