@@ -97,10 +97,10 @@ struct AttnParams {
 
 // Shared memory: [stages x (K tile, V tile); after the tile loop the same bytes hold the
 // warp partials] [stage barriers, merge barrier] [split partials of the cluster, used in
-// its first CTA] [flag]. The last 4 KiB of the stage area are scratch for the
-// workspace merge.
+// its first CTA] [flag] [q/out row offsets]. The last 4 KiB of the stage area are scratch
+// for the workspace merge.
 struct SmemLayout {
-    uint32_t bar_off, red_off, mrg_off, misc_off, total;
+    uint32_t bar_off, red_off, mrg_off, misc_off, qoff_off, total;
 };
 __host__ __device__ inline SmemLayout smem_layout(int stages, int rmax, int merge_slots) {
     SmemLayout L;
@@ -110,7 +110,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int rmax, int merg
     L.bar_off = ((tiles > red ? tiles : red) + 1023) & ~1023u;
     L.mrg_off = (L.bar_off + (stages + 1) * 8 + 15) & ~15u;
     L.misc_off = L.mrg_off + merge_slots * kSlot * 4;
-    L.total = L.misc_off + 16 + 1024;  // + slack to align the base to 1024 B
+    L.qoff_off = L.misc_off + 16;  // element offsets of the block's query rows in q / out
+    L.total = L.qoff_off + kMmaQueryBlock * 8 + 1024;  // + slack to align the base to 1024 B
     return L;
 }
 __host__ __device__ inline int merge_slots(int cluster, int splits, int msub) {
@@ -167,10 +168,12 @@ __device__ __forceinline__ void issue_tile(const CUtensorMap* tmk, const CUtenso
     tma_load_4d(dk + kTileBytes, tmv, bar, 0, pos, h, bk);
 }
 
+// qoff[m]: element offset of the block's query vector m in q and out (computed once in
+// the prologue: the index arithmetic has runtime divisions).
 template <typename T>
-__device__ __forceinline__ void store_out(const AttnParams& p, const CtaCtx& c, int m, int d,
+__device__ __forceinline__ void store_out(const AttnParams& p, const int64_t* qoff, int m, int d,
                                           float v) {
-    T* o = static_cast<T*>(p.out) + qrow(p, c.bk, c.h, c.m0 + m) + d;
+    T* o = static_cast<T*>(p.out) + qoff[m] + d;
     *o = Half16<T>::from_f(v);
 }
 
@@ -180,7 +183,7 @@ __device__ __forceinline__ void store_out(const AttnParams& p, const CtaCtx& c, 
 // with KVD_FLAG_EARLY_KV). Returns false if the length is out of range: flagged,
 // nothing written.
 __device__ __forceinline__ bool prologue(const AttnParams& p, CtaCtx& c, uint8_t* smem,
-                                         uint64_t* bars, const CUtensorMap* tmk,
+                                         uint64_t* bars, int64_t* qoff, const CUtensorMap* tmk,
                                          const CUtensorMap* tmv) {
     const int tid = threadIdx.x;
     if (!p.early) pdl_wait();
@@ -207,8 +210,14 @@ __device__ __forceinline__ bool prologue(const AttnParams& p, CtaCtx& c, uint8_t
         for (int j = 0; j < first; ++j)
             issue_tile(tmk, tmv, smem, bars, j, c.t_begin + j * kTile, c.h, c.bk, tx);
     }
-    if (p.early && tid < c.mcount)  // bring the query rows into L2 while waiting
-        prefetch_l2(static_cast<const uint8_t*>(p.q) + qrow(p, c.bk, c.h, c.m0 + tid) * 2);
+    // the last warp, clear of thread 0's copies
+    const int qi = tid - (kThreads - kMmaQueryBlock);
+    if (qi >= 0 && qi < c.mcount) {
+        const int64_t off = qrow(p, c.bk, c.h, c.m0 + qi);
+        qoff[qi] = off;
+        if (p.early)  // bring the query rows into L2 while waiting
+            prefetch_l2(static_cast<const uint8_t*>(p.q) + off * 2);
+    }
     __syncthreads();
     if (p.cluster) cluster_arrive_relaxed();  // the first CTA's merge barrier is ready
     pdl_trigger();
@@ -336,7 +345,8 @@ __device__ __forceinline__ bool run_tiles(const AttnParams& p, const CtaCtx& c, 
 // red: o [8][RMAX][red_stride], m [8][RMAX], l [8][RMAX]; mrg: [splits][msub][kSlot].
 template <typename T, int RMAX>
 __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, float* mrg,
-                           uint64_t* merge_bar, int* misc, uint8_t* scratch4k) {
+                           uint64_t* merge_bar, int* misc, const int64_t* qoff,
+                           uint8_t* scratch4k) {
     constexpr int RS = red_stride(RMAX);
     const float* red_o = red;
     const float* red_m = red + kWarps * RMAX * RS;
@@ -379,39 +389,46 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
                 st_async_v4(dst + slot * 4, v, rbar);
         }
         if (!leader) return;
-        const bool ok = mbar_wait_bounded_cluster(smem_u32(merge_bar), 0);
-        __syncthreads();  // the first CTA's own slots were written by other threads
-        if (!ok) {
+        // One warp waits for the other CTAs' bytes; the block barrier then orders those
+        // bytes, and the slots this CTA's own threads wrote, before every thread's reads.
+        const bool ok = tid >= 32 || mbar_wait_bounded_cluster(smem_u32(merge_bar), 0);
+        if (__syncthreads_or(!ok)) {
             if (tid == 0) flag_error(p.dev_err, KVD_ERR_TIMEOUT);
             return;
         }
-        // (a) one warp per query vector, one lane per split (S <= 16): the split's
-        //     normalised weight replaces its max in the slot.
-        const int lane = tid & 31;
-        for (int m = tid >> 5; m < c.mcount; m += kWarps) {
-            float* sl = mrg + (lane * p.msub + m) * kSlot;
-            const float ms = lane < S ? sl[kHeadDim] : -INFINITY;
-            float mx = ms;
+        // One thread per (query vector, 4 dims): all S <= 16 slots are loaded at once
+        // (fully unrolled), then summed in split order.
+        for (int it = tid; it < c.mcount * (kHeadDim / 4); it += blockDim.x) {
+            const int m = it >> 4, q4 = it & 15;
+            const float* sl0 = mrg + m * kSlot;
+            const int stride = p.msub * kSlot;
+            float ms[kMaxClusterSplits];
+            float mx = -INFINITY;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float ref = mx == -INFINITY ? 0.f : mx;
-            const float a = lane < S ? exp2f(ms - ref) : 0.f;
-            float l = lane < S ? sl[kHeadDim + 1] * a : 0.f;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-            if (lane < S) sl[kHeadDim] = l > 0.f ? a / l : 0.f;
-        }
-        __syncthreads();
-        // (b) weighted sum over the splits, in split order
-        for (int idx = tid; idx < c.mcount * kHeadDim; idx += blockDim.x) {
-            const int m = idx >> 6, d = idx & 63;
-            float o = 0.f;
-#pragma unroll 4
-            for (int r = 0; r < S; ++r) {
-                const float* sl = mrg + (r * p.msub + m) * kSlot;
-                o = fmaf(sl[d], sl[kHeadDim], o);
+            for (int r = 0; r < kMaxClusterSplits; ++r) {
+                ms[r] = r < S ? sl0[r * stride + kHeadDim] : -INFINITY;
+                mx = fmaxf(mx, ms[r]);
             }
-            store_out<T>(p, c, m, d, o);
+            const float ref = mx == -INFINITY ? 0.f : mx;
+            float l = 0.f;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int r = 0; r < kMaxClusterSplits; ++r) {
+                if (r < S) {
+                    const float a = exp2f(ms[r] - ref);
+                    const float4 v = *reinterpret_cast<const float4*>(sl0 + r * stride + 4 * q4);
+                    l = fmaf(sl0[r * stride + kHeadDim + 1], a, l);
+                    o.x = fmaf(v.x, a, o.x);
+                    o.y = fmaf(v.y, a, o.y);
+                    o.z = fmaf(v.z, a, o.z);
+                    o.w = fmaf(v.w, a, o.w);
+                }
+            }
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint2 packed;
+            packed.x = Half16<T>::from_f2(o.x * inv, o.y * inv);
+            packed.y = Half16<T>::from_f2(o.z * inv, o.w * inv);
+            *reinterpret_cast<uint2*>(static_cast<T*>(p.out) + qoff[m] + 4 * q4) = packed;
         }
         return;
     }
@@ -431,7 +448,7 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
             o = fmaf(red_o[(w * RMAX + m) * RS + d], a, o);
         }
         if (S == 1) {
-            store_out<T>(p, c, m, d, l > 0.f ? o / l : 0.f);
+            store_out<T>(p, qoff, m, d, l > 0.f ? o / l : 0.f);
         } else {
             p.ws_part[(slot0 + m) * kHeadDim + d] = o;
             if (d == 0) p.ws_ml[slot0 + m] = make_float2(mx, l);
@@ -498,10 +515,10 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
             acc.w += v.w;
         }
         const int m = q4 / (kHeadDim / 4), d = (q4 % (kHeadDim / 4)) * 4;
-        store_out<T>(p, c, m, d + 0, acc.x);
-        store_out<T>(p, c, m, d + 1, acc.y);
-        store_out<T>(p, c, m, d + 2, acc.z);
-        store_out<T>(p, c, m, d + 3, acc.w);
+        uint2 packed;
+        packed.x = Half16<T>::from_f2(acc.x, acc.y);
+        packed.y = Half16<T>::from_f2(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(static_cast<T*>(p.out) + qoff[m] + d) = packed;
     }
     if (tid == 0) p.ws_cnt[c.unit] = 0;
 }
@@ -519,16 +536,17 @@ __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: 4 blocks per
     float* red = reinterpret_cast<float*>(smem + L.red_off);
     float* mrg = reinterpret_cast<float*>(smem + L.mrg_off);
     int* misc = reinterpret_cast<int*>(smem + L.misc_off);
+    int64_t* qoff = reinterpret_cast<int64_t*>(smem + L.qoff_off);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int grp = lane >> 3, c8 = lane & 7;
 
     CtaCtx c;
-    if (!prologue(p, c, smem, bars, &tmk, &tmv)) return;
+    if (!prologue(p, c, smem, bars, qoff, &tmk, &tmv)) return;
 
     float qf[8];
     {
-        const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
-                                                        qrow(p, c.bk, c.h, c.m0) + c8 * 8);
+        const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + qoff[0] +
+                                                        c8 * 8);
         unpack8<T>(u, qf);
     }
     float mrun = -INFINITY, lrun = 0.f, acc[8];
@@ -605,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: 4 blocks per
         }
     }
     __syncthreads();
-    finish_cta<T, RM>(p, c, red, mrg, &bars[p.stages], misc, smem + L.bar_off - 4096);
+    finish_cta<T, RM>(p, c, red, mrg, &bars[p.stages], misc, qoff, smem + L.bar_off - 4096);
 }
 
 // ------------------------------------ 2..16 query vectors per KV head (tensor cores) ----
@@ -621,19 +639,20 @@ __global__ void __launch_bounds__(kThreads)
     float* red = reinterpret_cast<float*>(smem + L.red_off);
     float* mrg = reinterpret_cast<float*>(smem + L.mrg_off);
     int* misc = reinterpret_cast<int*>(smem + L.misc_off);
+    int64_t* qoff = reinterpret_cast<int64_t*>(smem + L.qoff_off);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int qr = lane >> 2, qc = (lane & 3) * 2;  // fragment row / column pair
     const int jm = lane >> 3, rr = lane & 7;         // ldmatrix matrix / row
 
     CtaCtx c;
-    if (!prologue(p, c, smem, bars, &tmk, &tmv)) return;
+    if (!prologue(p, c, smem, bars, qoff, &tmk, &tmv)) return;
 
     // Q as m16n8k16 A fragments for the four 16-dim k-steps (rows >= mcount are 0).
     uint32_t qa[4][4];
     const T* qbase = static_cast<const T*>(p.q);
     const bool rowA = qr < c.mcount, rowB = qr + 8 < c.mcount;
-    const int64_t offA = rowA ? qrow(p, c.bk, c.h, c.m0 + qr) : 0;
-    const int64_t offB = rowB ? qrow(p, c.bk, c.h, c.m0 + qr + 8) : 0;
+    const int64_t offA = rowA ? qoff[qr] : 0;
+    const int64_t offB = rowB ? qoff[qr + 8] : 0;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
         const int d0 = kk * 16 + qc;
@@ -757,7 +776,7 @@ __global__ void __launch_bounds__(kThreads)
         }
     }
     __syncthreads();
-    finish_cta<T, RM>(p, c, red, mrg, &bars[p.stages], misc, smem + L.bar_off - 4096);
+    finish_cta<T, RM>(p, c, red, mrg, &bars[p.stages], misc, qoff, smem + L.bar_off - 4096);
 }
 
 // ---------------------------------------------------------------- host side --------

@@ -118,19 +118,24 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // As mbar_wait_bounded, for a barrier that other CTAs of the cluster arrive on: the
 // acquire covers their writes to this CTA's shared memory.
 __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait_cluster(bar, parity)) {
-        if (global_ns() - t0 > kWaitNs) return false;
+    // the clock is read every 64 polls only: polling threads then stay cheap
+    unsigned long long t0 = 0;
+    for (unsigned n = 1; !mbar_try_wait_cluster(bar, parity); ++n) {
+        if (n % 64 == 0) {
+            if (t0 == 0) t0 = global_ns();
+            else if (global_ns() - t0 > kWaitNs) return false;
+        }
     }
     return true;
 }
-// Wait for phase `parity` of the barrier; false if it did not complete within 1 s.
+// Wait for phase `parity` of the barrier; false if it did not complete within about 1 s.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitNs) return false;
+    unsigned long long t0 = 0;
+    for (unsigned n = 1; !mbar_try_wait(bar, parity); ++n) {
+        if (n % 64 == 0) {
+            if (t0 == 0) t0 = global_ns();
+            else if (global_ns() - t0 > kWaitNs) return false;
+        }
     }
     return true;
 }
