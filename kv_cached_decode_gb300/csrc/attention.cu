@@ -396,32 +396,39 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
             if (tid == 0) flag_error(p.dev_err, KVD_ERR_TIMEOUT);
             return;
         }
-        // One thread per (query vector, 4 dims): all S <= 16 slots are loaded at once
-        // (fully unrolled), then summed in split order.
+        // One thread per (query vector, 4 dims). Loads are unconditional (a split past S
+        // re-reads the last slot and gets weight 0) and go in batches of four, so they
+        // overlap; the sums run in split order.
         for (int it = tid; it < c.mcount * (kHeadDim / 4); it += blockDim.x) {
             const int m = it >> 4, q4 = it & 15;
             const float* sl0 = mrg + m * kSlot;
             const int stride = p.msub * kSlot;
-            float ms[kMaxClusterSplits];
             float mx = -INFINITY;
 #pragma unroll
-            for (int r = 0; r < kMaxClusterSplits; ++r) {
-                ms[r] = r < S ? sl0[r * stride + kHeadDim] : -INFINITY;
-                mx = fmaxf(mx, ms[r]);
-            }
+            for (int r = 0; r < kMaxClusterSplits; ++r)
+                mx = fmaxf(mx, sl0[min(r, S - 1) * stride + kHeadDim]);
             const float ref = mx == -INFINITY ? 0.f : mx;
             float l = 0.f;
             float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+            for (int r0 = 0; r0 < S; r0 += 4) {
+                float4 v[4];
+                float mv[4], lv[4];
 #pragma unroll
-            for (int r = 0; r < kMaxClusterSplits; ++r) {
-                if (r < S) {
-                    const float a = exp2f(ms[r] - ref);
-                    const float4 v = *reinterpret_cast<const float4*>(sl0 + r * stride + 4 * q4);
-                    l = fmaf(sl0[r * stride + kHeadDim + 1], a, l);
-                    o.x = fmaf(v.x, a, o.x);
-                    o.y = fmaf(v.y, a, o.y);
-                    o.z = fmaf(v.z, a, o.z);
-                    o.w = fmaf(v.w, a, o.w);
+                for (int j = 0; j < 4; ++j) {
+                    const float* sl = sl0 + min(r0 + j, S - 1) * stride;
+                    v[j] = *reinterpret_cast<const float4*>(sl + 4 * q4);
+                    mv[j] = sl[kHeadDim];
+                    lv[j] = sl[kHeadDim + 1];
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float a = r0 + j < S ? exp2f(mv[j] - ref) : 0.f;
+                    l = fmaf(lv[j], a, l);
+                    o.x = fmaf(v[j].x, a, o.x);
+                    o.y = fmaf(v[j].y, a, o.y);
+                    o.z = fmaf(v[j].z, a, o.z);
+                    o.w = fmaf(v[j].w, a, o.w);
                 }
             }
             const float inv = l > 0.f ? 1.f / l : 0.f;
