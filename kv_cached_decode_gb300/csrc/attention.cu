@@ -360,28 +360,40 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
         const bool leader = c.s == 0;
         const uint32_t dst = leader ? 0u : map_shared(smem_u32(mrg), 0);
         const uint32_t rbar = leader ? 0u : map_shared(smem_u32(merge_bar), 0);
+        // One thread per float4 of a slot: 16 of o, then (max, sum). Loads are
+        // unconditional (the (max, sum) thread reads an o quad it ignores) and go in
+        // batches of four warps.
         for (int it = tid; it < kSlotQuads * c.mcount; it += blockDim.x) {
             const int m = it / kSlotQuads, k = it % kSlotQuads;
+            const int kk = min(k, kHeadDim / 4 - 1);
             float mx = -INFINITY;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * RMAX + m]);
             const float ref = mx == -INFINITY ? 0.f : mx;
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            float l = 0.f;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float a = exp2f(red_m[w * RMAX + m] - ref);
-                if (k < kHeadDim / 4) {
-                    const float4 o = *reinterpret_cast<const float4*>(
-                        red_o + (w * RMAX + m) * RS + 4 * k);
-                    v.x = fmaf(o.x, a, v.x);
-                    v.y = fmaf(o.y, a, v.y);
-                    v.z = fmaf(o.z, a, v.z);
-                    v.w = fmaf(o.w, a, v.w);
-                } else {
-                    v.y = fmaf(red_l[w * RMAX + m], a, v.y);
+            for (int w0 = 0; w0 < kWarps; w0 += 4) {
+                float4 o[4];
+                float mw[4], lw[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int w = w0 + j;
+                    o[j] = *reinterpret_cast<const float4*>(red_o + (w * RMAX + m) * RS + 4 * kk);
+                    mw[j] = red_m[w * RMAX + m];
+                    lw[j] = red_l[w * RMAX + m];
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float a = exp2f(mw[j] - ref);
+                    l = fmaf(lw[j], a, l);
+                    v.x = fmaf(o[j].x, a, v.x);
+                    v.y = fmaf(o[j].y, a, v.y);
+                    v.z = fmaf(o[j].z, a, v.z);
+                    v.w = fmaf(o[j].w, a, v.w);
                 }
             }
-            if (k == kHeadDim / 4) v.x = mx;
+            if (k == kHeadDim / 4) v = make_float4(mx, l, 0.f, 0.f);
             const int slot = (c.s * p.msub + m) * kSlot + 4 * k;
             if (leader)
                 *reinterpret_cast<float4*>(mrg + slot) = v;
