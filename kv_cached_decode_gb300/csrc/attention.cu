@@ -218,6 +218,16 @@ __device__ __forceinline__ bool prologue(const AttnParams& p, CtaCtx& c, uint8_t
         if (p.early)  // bring the query rows into L2 while waiting
             prefetch_l2(static_cast<const uint8_t*>(p.q) + off * 2);
     }
+    // Blocks that inject appended rows bring those rows of k_new / v_new into L2 too
+    // (one 128-byte line per row and tensor).
+    if (p.early && p.append && c.new0 < c.t_end && c.len > c.t_begin) {
+        const int ai = tid - (kThreads - 2 * kMmaQueryBlock);
+        if (ai >= 0 && ai < 2 * p.qlen) {
+            const int j = ai >> 1;
+            const int64_t row = ((int64_t)c.bk * p.n_kv_heads + c.h) * p.qlen + j;
+            prefetch_l2((ai & 1 ? p.v_new : p.k_new) + row * kRowBytes);
+        }
+    }
     __syncthreads();
     if (p.cluster) cluster_arrive_relaxed();  // the first CTA's merge barrier is ready
     pdl_trigger();
