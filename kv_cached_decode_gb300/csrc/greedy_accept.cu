@@ -63,29 +63,35 @@ __device__ __forceinline__ Cand warp_best(Cand c) {
 }
 
 constexpr int kAcceptThreads = 256;
+constexpr int kAcceptLoads = 8;  // per thread and pass: a 2048-logit segment in one pass
 
 __global__ void __launch_bounds__(kAcceptThreads) greedy_accept_kernel(const AcceptParams p) {
     __shared__ Cand s_warp[kAcceptThreads / 32];
     __shared__ int s_amax[KVD_MAX_QLEN + 1];
     __shared__ int s_flag;
+    __shared__ int s_draft[KVD_MAX_QLEN];
     pdl_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int s = blockIdx.x, row = blockIdx.y, b = blockIdx.z;
     const int k1 = p.k + 1;
+    // The block that finishes last applies the rule; every block fetches the drafts now,
+    // so that block does not wait for them at the end.
+    if (warp == kAcceptThreads / 32 - 1 && lane < p.k)
+        s_draft[lane] = p.draft[(int64_t)b * p.k + lane];
     const float* x = p.logits + ((int64_t)b * k1 + row) * p.vocab;
     const int lo = s * p.seg_len, hi = min(p.vocab, lo + p.seg_len);
 
     Cand best = {0.f, -1};
     bool saw_nan = false;
-    for (int base = lo; base < hi; base += 4 * kAcceptThreads) {
-        float v[4];
+    // All loads of a pass are unconditional (clamped into the segment) and issued before
+    // the first compare, so a segment streams in one memory round trip.
+    for (int base = lo; base < hi; base += kAcceptLoads * kAcceptThreads) {
+        float v[kAcceptLoads];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = base + u * kAcceptThreads + tid;
-            v[u] = i < hi ? __ldcs(x + i) : 0.f;
-        }
+        for (int u = 0; u < kAcceptLoads; ++u)
+            v[u] = __ldcs(x + min(base + u * kAcceptThreads + tid, hi - 1));
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kAcceptLoads; ++u) {
             const int i = base + u * kAcceptThreads + tid;
             if (i < hi) {
                 saw_nan |= isnan(v[u]);
@@ -130,7 +136,7 @@ __global__ void __launch_bounds__(kAcceptThreads) greedy_accept_kernel(const Acc
     int n = p.k;
     bool bad_token = false;
     for (int i = 0; i < p.k; ++i) {
-        const int d = p.draft[(int64_t)b * p.k + i];
+        const int d = s_draft[i];
         const bool oob = d < 0 || d >= p.vocab;
         bad_token |= oob;
         if (n == p.k && (oob || d != s_amax[i])) n = i;
