@@ -623,8 +623,8 @@ def run_ours(args):
             3),
         "verified_tokens_per_s_per_layer_step": round(verified, 1),
         "roofline": {"bound": "hbm",
-                     "kernel": "decode_attn_kernel: one query vector per head over the "
-                               "1500-frame cross K/V (32 launches per step)",
+                     "kernel": "decode over the 1500-frame cross K/V, one query vector "
+                               "per head (block_attn_kernel; 32 launches per step)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "bytes_per_launch": cross_bytes, "traffic": traffic},
