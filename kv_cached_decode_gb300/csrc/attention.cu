@@ -100,9 +100,11 @@ struct AttnParams {
 // its first CTA] [flag] [q/out row offsets]. The last 4 KiB of the stage area are scratch
 // for the workspace merge.
 struct SmemLayout {
-    uint32_t bar_off, red_off, mrg_off, misc_off, qoff_off, total;
+    uint32_t bar_off, red_off, mrg_off, misc_off, qoff_off, app_off, total;
 };
-__host__ __device__ inline SmemLayout smem_layout(int stages, int rmax, int merge_slots) {
+// app_rows: appended rows staged for the fused append (qlen, or 0 without append).
+__host__ __device__ inline SmemLayout smem_layout(int stages, int rmax, int merge_slots,
+                                                  int app_rows) {
     SmemLayout L;
     const uint32_t tiles = stages * 2 * kTileBytes;
     const uint32_t red = kWarps * rmax * (red_stride(rmax) + 2) * 4;
@@ -111,7 +113,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int rmax, int merg
     L.mrg_off = (L.bar_off + (stages + 1) * 8 + 15) & ~15u;
     L.misc_off = L.mrg_off + merge_slots * kSlot * 4;
     L.qoff_off = L.misc_off + 16;  // element offsets of the block's query rows in q / out
-    L.total = L.qoff_off + kMmaQueryBlock * 8 + 1024;  // + slack to align the base to 1024 B
+    L.app_off = L.qoff_off + kMmaQueryBlock * 8;  // appended rows: K [app_rows][128 B], V
+    L.total = L.app_off + app_rows * 2 * kRowBytes + 1024;  // + slack to align the base
     return L;
 }
 __host__ __device__ inline int merge_slots(int cluster, int splits, int msub) {
@@ -239,22 +242,46 @@ __device__ __forceinline__ bool prologue(const AttnParams& p, CtaCtx& c, uint8_t
 
 // Fused append, per warp: the rows of this warp's 16-position slab that hold new tokens
 // come from k_new/v_new, not from the copy (which saw the cache before the append).
-// They are written into the staged tile (the warp reads only its own slab) and, by the
-// first query sub-block, into the cache.
-__device__ __forceinline__ void inject_slab(const AttnParams& p, const CtaCtx& c, uint8_t* sK,
-                                            uint8_t* sV, int tile0, int slab0) {
-    const int r0 = max(tile0 + slab0, c.new0), r1 = min(tile0 + slab0 + 16, c.len);
-    if (r0 >= r1) return;
+// The warp stages those rows into shared memory with cp.async right after the dependency
+// wait (stage_appended), so their load latency overlaps the rest of the prologue; here
+// it copies them into its staged tile (the warp reads only its own slab) and, by the
+// first query sub-block, into the cache. app: K rows [qlen][128 B], then V rows.
+__device__ __forceinline__ void for_appended_chunks(const AttnParams& p, const CtaCtx& c,
+                                                    int tile0, int slab0, int& r0, int& n2) {
+    r0 = max(tile0 + slab0, c.new0);
+    const int r1 = min(tile0 + slab0 + 16, c.len);
+    n2 = r0 < r1 ? 2 * (r1 - r0) * 8 : 0;  // 16-byte chunks of K and V
+}
+__device__ __forceinline__ void stage_appended(const AttnParams& p, const CtaCtx& c,
+                                               uint8_t* app, int tile0, int slab0) {
+    int r0, n2;
+    for_appended_chunks(p, c, tile0, slab0, r0, n2);
     const int lane = threadIdx.x & 31;
-    const int n = (r1 - r0) * 8;
-    for (int x = lane; x < 2 * n; x += 32) {
-        const bool is_v = x >= n;
-        const int y = is_v ? x - n : x;
-        const int t = r0 + (y >> 3), ch = y & 7;
-        const int j = t - c.new0;
+    for (int x = lane; x < n2; x += 32) {
+        const bool is_v = x >= n2 / 2;
+        const int y = is_v ? x - n2 / 2 : x;
+        const int j = r0 + (y >> 3) - c.new0, ch = y & 7;
         const int64_t src =
             (((int64_t)c.bk * p.n_kv_heads + c.h) * p.qlen + j) * kRowBytes + ch * 16;
-        const uint4 val = *reinterpret_cast<const uint4*>((is_v ? p.v_new : p.k_new) + src);
+        cp_async16(smem_u32(app + (is_v ? p.qlen * kRowBytes : 0) + j * kRowBytes + ch * 16),
+                   (is_v ? p.v_new : p.k_new) + src);
+    }
+}
+__device__ __forceinline__ void inject_slab(const AttnParams& p, const CtaCtx& c, uint8_t* sK,
+                                            uint8_t* sV, const uint8_t* app, int tile0,
+                                            int slab0) {
+    int r0, n2;
+    for_appended_chunks(p, c, tile0, slab0, r0, n2);
+    if (n2 == 0) return;
+    cp_async_wait_all();
+    __syncwarp();
+    const int lane = threadIdx.x & 31;
+    for (int x = lane; x < n2; x += 32) {
+        const bool is_v = x >= n2 / 2;
+        const int y = is_v ? x - n2 / 2 : x;
+        const int t = r0 + (y >> 3), ch = y & 7;
+        const uint4 val = *reinterpret_cast<const uint4*>(
+            app + (is_v ? p.qlen * kRowBytes : 0) + (t - c.new0) * kRowBytes + ch * 16);
         *reinterpret_cast<uint4*>((is_v ? sV : sK) + swz(t - tile0, ch)) = val;
         if (c.sub == 0)
             *reinterpret_cast<uint4*>((is_v ? p.vc : p.kc) + c.bk * p.sb + c.h * p.sh +
@@ -297,14 +324,21 @@ __device__ void abort_after_timeout(const AttnParams& p, const CtaCtx& c, uint64
 // Returns false after a timeout (already handled: the caller just returns).
 template <typename Slab>
 __device__ __forceinline__ bool run_tiles(const AttnParams& p, const CtaCtx& c, uint8_t* smem,
-                                          uint64_t* bars, float* mrg, const CUtensorMap* tmk,
-                                          const CUtensorMap* tmv, Slab&& slab) {
+                                          uint64_t* bars, float* mrg, uint8_t* app,
+                                          const CUtensorMap* tmk, const CUtensorMap* tmv,
+                                          Slab&& slab) {
     const int tid = threadIdx.x, warp = tid >> 5;
     const int half = warp >> 2, slab0 = (warp & 3) * 16;
     const uint32_t tx = 2u * p.box_rows * kRowBytes;
     bool all_ok = true;
     int issued = min(p.stages, c.n_tiles);
     const int rounds = (c.n_tiles + 1) / 2;
+    if (p.append && c.new0 < c.t_end) {
+        for (int r = 0; r < rounds; ++r)
+            if (2 * r + half < c.n_tiles)
+                stage_appended(p, c, app, c.t_begin + (2 * r + half) * kTile, slab0);
+        cp_async_commit();
+    }
     for (int r = 0; r < rounds; ++r) {
         const int j = 2 * r + half;
         if (j < c.n_tiles) {
@@ -317,7 +351,7 @@ __device__ __forceinline__ bool run_tiles(const AttnParams& p, const CtaCtx& c, 
                 uint8_t* sK = smem + st * 2 * kTileBytes;
                 uint8_t* sV = sK + kTileBytes;
                 const int tile0 = c.t_begin + j * kTile;
-                if (p.append) inject_slab(p, c, sK, sV, tile0, slab0);
+                if (p.append) inject_slab(p, c, sK, sV, app, tile0, slab0);
                 slab(sK, sV, tile0, slab0);
             }
         }
@@ -560,7 +594,8 @@ __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: 4 blocks per
     constexpr int RM = 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
-    const SmemLayout L = smem_layout(p.stages, RM, merge_slots(p.cluster, p.splits, p.msub));
+    const SmemLayout L = smem_layout(p.stages, RM, merge_slots(p.cluster, p.splits, p.msub),
+                                     p.append ? p.qlen : 0);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
     float* red = reinterpret_cast<float*>(smem + L.red_off);
     float* mrg = reinterpret_cast<float*>(smem + L.mrg_off);
@@ -624,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: 4 blocks per
             for (int e = 0; e < 8; ++e) acc[e] = fmaf(sc[jj], valid ? vf[e] : 0.f, acc[e]);
         }
     };
-    if (!run_tiles(p, c, smem, bars, mrg, &tmk, &tmv, slab)) return;
+    if (!run_tiles(p, c, smem, bars, mrg, smem + L.app_off, &tmk, &tmv, slab)) return;
 
     // Merge the four 8-lane groups of each warp (they saw different positions).
 #pragma unroll
@@ -663,7 +698,8 @@ __global__ void __launch_bounds__(kThreads)
     constexpr int RM = 16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
-    const SmemLayout L = smem_layout(p.stages, RM, merge_slots(p.cluster, p.splits, p.msub));
+    const SmemLayout L = smem_layout(p.stages, RM, merge_slots(p.cluster, p.splits, p.msub),
+                                     p.append ? p.qlen : 0);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
     float* red = reinterpret_cast<float*>(smem + L.red_off);
     float* mrg = reinterpret_cast<float*>(smem + L.mrg_off);
@@ -776,7 +812,7 @@ __global__ void __launch_bounds__(kThreads)
             Mma<T>::run(oacc[2 * np + 1], pa, v2, v3);
         }
     };
-    if (!run_tiles(p, c, smem, bars, mrg, &tmk, &tmv, slab)) return;
+    if (!run_tiles(p, c, smem, bars, mrg, smem + L.app_off, &tmk, &tmv, slab)) return;
 
     lA += __shfl_xor_sync(0xffffffffu, lA, 1);
     lA += __shfl_xor_sync(0xffffffffu, lA, 2);
@@ -838,9 +874,10 @@ int prepare_kernel(size_t smem_bytes) {
 template <typename T>
 int prepare(bool mma) {
     return mma ? prepare_kernel<block_attn_kernel<T>>(
-                     smem_layout(kMaxStages, 16, kMaxClusterSplits * kMmaQueryBlock).total)
+                     smem_layout(kMaxStages, 16, kMaxClusterSplits * kMmaQueryBlock,
+                                 KVD_MAX_QLEN).total)
                : prepare_kernel<decode_attn_kernel<T>>(
-                     smem_layout(kMaxStages, 1, kMaxClusterSplits).total);
+                     smem_layout(kMaxStages, 1, kMaxClusterSplits, KVD_MAX_QLEN).total);
 }
 
 template <typename T>
@@ -855,13 +892,17 @@ kvd_status launch_attn(bool mma, dim3 grid, cudaStream_t st, bool pdl, unsigned 
     const int slots = merge_slots(p.cluster, p.splits, p.msub);
     if (mma)
         return launch_ex(block_attn_kernel<T>, grid, dim3(kThreads),
-                         smem_layout(p.stages, 16, slots).total, st, pdl, cl, mk, mv, p);
+                         smem_layout(p.stages, 16, slots, p.append ? p.qlen : 0).total, st,
+                         pdl, cl, mk, mv, p);
     return launch_ex(decode_attn_kernel<T>, grid, dim3(kThreads),
-                     smem_layout(p.stages, 1, slots).total, st, pdl, cl, mk, mv, p);
+                     smem_layout(p.stages, 1, slots, p.append ? p.qlen : 0).total, st, pdl, cl,
+                     mk, mv, p);
 }
 
-size_t plan_smem(const AttnPlan& P, bool mma) {
-    return smem_layout(P.stages, mma ? 16 : 1, merge_slots(P.cluster, P.splits, P.msub)).total;
+size_t plan_smem(const AttnPlan& P, bool mma, int app_rows) {
+    return smem_layout(P.stages, mma ? 16 : 1, merge_slots(P.cluster, P.splits, P.msub),
+                       app_rows)
+        .total;
 }
 
 // How many thread blocks (cluster == 1, whole GPU) or clusters of `cluster` blocks can
@@ -911,7 +952,8 @@ int resident(const void* kern, int kid, size_t smem, int cluster, int nsm) {
 // over a long range, where even 16-block clusters leave each block streaming many
 // tiles, split further and merge through the workspace.
 AttnPlan choose_plan(const void* kern, int kid, bool mma, int nsm, int batch, int n_q_heads,
-                     int n_kv_heads, int rows_per_kv, int qlen, int len_bound, int max_cluster) {
+                     int n_kv_heads, int rows_per_kv, int qlen, int len_bound, int max_cluster,
+                     int app_rows) {
     const int mmax = mma ? kMmaQueryBlock : 1;
     const AttnPlan P1 = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, qlen, len_bound,
                                        mmax, 1, max_cluster);
@@ -919,7 +961,7 @@ AttnPlan choose_plan(const void* kern, int kid, bool mma, int nsm, int batch, in
     if (workspace_merge_pays(P1.units, P1.rounds)) {
         AttnPlan W = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, qlen, len_bound,
                                     mmax, kMaxSplits, 1);
-        const int blocks = resident(kern, kid, plan_smem(W, mma), 1, nsm);
+        const int blocks = resident(kern, kid, plan_smem(W, mma, app_rows), 1, nsm);
         return plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, qlen, len_bound, mmax,
                               std::max(1, blocks / P1.units), max_cluster);
     }
@@ -930,7 +972,7 @@ AttnPlan choose_plan(const void* kern, int kid, bool mma, int nsm, int batch, in
         if (P.splits == last) continue;
         last = P.splits;
         if (P.splits < 2) break;
-        if (P.cluster && resident(kern, kid, plan_smem(P, mma), P.splits, nsm) >= P.units)
+        if (P.cluster && resident(kern, kid, plan_smem(P, mma, app_rows), P.splits, nsm) >= P.units)
             return P;
     }
     return P1;
@@ -966,8 +1008,9 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
     if (max_cluster <= 0) return KVD_ERR_CUDA;
     int kid = (mma ? 2 : 0) | (bf ? 1 : 0);
     const void* kern = bf ? kernel_of<__nv_bfloat16>(mma) : kernel_of<__half>(mma);
+    const int app_rows = app ? qlen : 0;
     AttnPlan P = choose_plan(kern, kid, mma, nsm, batch, n_q_heads, kv->n_kv_heads,
-                             rows_per_kv, qlen, len_bound, max_cluster);
+                             rows_per_kv, qlen, len_bound, max_cluster, app_rows);
     if (!mma && P.tiles_per_split <= 2) {
         // Each block has a single round of tiles: then the time is the chain after the
         // dependency wait, and the tensor-core kernel's per-tile chain (ldmatrix + mma,
@@ -980,10 +1023,11 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
         const void* kern2 = bf ? kernel_of<__nv_bfloat16>(true) : kernel_of<__half>(true);
         if (mc2 > 0) {
             const AttnPlan P2 = choose_plan(kern2, kid2, true, nsm, batch, n_q_heads,
-                                            kv->n_kv_heads, rows_per_kv, qlen, len_bound, mc2);
+                                            kv->n_kv_heads, rows_per_kv, qlen, len_bound, mc2,
+                                            app_rows);
             const bool fits =
                 P2.cluster || (P2.splits == 1 && (int64_t)P2.units <=
-                                   resident(kern2, kid2, plan_smem(P2, true), 1, nsm));
+                                   resident(kern2, kid2, plan_smem(P2, true, app_rows), 1, nsm));
             if (fits && P2.tiles_per_split <= 2) {
                 mma = true;
                 P = P2;
