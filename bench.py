@@ -714,8 +714,9 @@ def run_sweep(args):
 
 def run_beam_step(torch, kvd, dev, stream, peak, flags):
     """Beam search step: 8 windows x beam 5 = 40 rows, 32 layers, 20 heads, fp16,
-    capacity 448: beam_reorder_kv over all layers, then per layer append, self decode
-    over len+1 positions and cross decode over 1500 frames shared per window."""
+    capacity 448: beam_reorder_kv over all layers, then per layer self decode over
+    len+1 positions with the new token appended in the same call, and cross decode over
+    1500 frames shared per window."""
     w = WORKLOADS["beam_step"]
     W, beam, NL, H, cap, F = w["windows"], w["beam"], w["n_layers"], w["n_q_heads"], w["capacity"], w["cross_len"]
     R = W * beam
@@ -745,11 +746,15 @@ def run_beam_step(torch, kvd, dev, stream, peak, flags):
         def reorder():
             kvd.kvd_beam_reorder_kv(c_self, R, beam, parent, lens=lens_in, flags=flags)
 
+        # The reorder rewrites the self caches, so the self calls must not stage K/V
+        # before their dependency wait: PDL only. Cross K/V are never rewritten.
+        self_flags = flags & kvd.KVD_FLAG_PDL
+
         def step():
             reorder()
             for l in range(NL):
-                kvd.kvd_kv_append(c_self[l], kn, kn, lens_in, lens, flags=flags)
-                kvd.kvd_decode_attn(q, c_self[l], out, ws, lens=lens, flags=flags)
+                kvd.kvd_decode_attn(q, c_self[l], out, ws, lens=lens_in, flags=self_flags,
+                                    append=(kn, kn, lens))
                 kvd.kvd_decode_attn(q, c_cross[l], out, ws, fixed_len=F, rows_per_kv=beam,
                                     flags=flags)
 
