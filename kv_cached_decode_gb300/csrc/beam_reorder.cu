@@ -14,6 +14,7 @@
 // children or parents form cycles. Rows that keep their own cache are never touched;
 // a source is read once however many children it has.
 #include <algorithm>
+#include <mutex>
 
 #include "kvd_common.cuh"
 #include "kvd_internal.h"
@@ -39,46 +40,63 @@ struct BeamParams {
 constexpr int kBeamThreads = 256;
 constexpr int kChunksPerTile = kTile * 8;  // 64 positions x 8 chunks of 16 bytes
 
-__global__ void __launch_bounds__(kBeamThreads)
-    beam_reorder_kernel(const __grid_constant__ BeamParams p) {
-    pdl_wait();
-    int64_t item = blockIdx.x;
-    const int pt = (int)(item % p.pos_tiles);
-    item /= p.pos_tiles;
-    const int h = (int)(item % p.heads);
-    item /= p.heads;
-    const int w = (int)(item % p.windows);
-    item /= p.windows;
-    const int is_v = (int)(item & 1);
-    const int l = (int)(item >> 1);
-    const BeamLayer& L = p.layer[l];
-    const bool reporter = pt == 0 && h == 0 && is_v == 0 && l == 0 && threadIdx.x == 0;
-
-    // Parents and lengths of this window's rows.
+// One block's share: (layer, K or V, window, head, 64-position tile), decoded from the
+// block index, and the window's parents. moved: rows that take another row's cache;
+// needed: rows that are read as parents; len_max: longest moved row. Bad parents and
+// lengths are flagged (once per launch) and leave their row untouched.
+struct BeamItem {
+    int pt, h, w, is_v, l, row0, len_max;
+    unsigned moved, needed;
     int par[KVD_MAX_BEAM], len[KVD_MAX_BEAM];
-    unsigned moved = 0, needed = 0;
-    int len_max = 0;
-    const int row0 = w * p.beam;
+};
+
+__device__ __forceinline__ void beam_item(const BeamParams& p, BeamItem& it) {
+    int64_t item = blockIdx.x;
+    it.pt = (int)(item % p.pos_tiles);
+    item /= p.pos_tiles;
+    it.h = (int)(item % p.heads);
+    item /= p.heads;
+    it.w = (int)(item % p.windows);
+    item /= p.windows;
+    it.is_v = (int)(item & 1);
+    it.l = (int)(item >> 1);
+    const BeamLayer& L = p.layer[it.l];
+    const bool reporter = it.pt == 0 && it.h == 0 && it.is_v == 0 && it.l == 0 && threadIdx.x == 0;
+    it.moved = it.needed = 0;
+    it.len_max = 0;
+    it.row0 = it.w * p.beam;
 #pragma unroll
     for (int j = 0; j < KVD_MAX_BEAM; ++j) {
-        par[j] = j;
-        len[j] = 0;
+        it.par[j] = j;
+        it.len[j] = 0;
         if (j < p.beam) {
-            const int pr = p.parent[row0 + j] - row0;
-            const int ln = p.lens ? p.lens[row0 + j] : p.fixed_len;
+            const int pr = p.parent[it.row0 + j] - it.row0;
+            const int ln = p.lens ? p.lens[it.row0 + j] : p.fixed_len;
             const bool ok_p = pr >= 0 && pr < p.beam;
             const bool ok_l = ln >= 0 && ln <= L.capacity;
             if (!ok_p && reporter) flag_error(p.dev_err, KVD_ERR_BAD_INDEX);
             if (!ok_l && reporter) flag_error(p.dev_err, KVD_ERR_LEN_OVERFLOW);
             if (ok_p && ok_l && pr != j) {
-                par[j] = pr;
-                len[j] = ln;
-                moved |= 1u << j;
-                needed |= 1u << pr;
-                len_max = max(len_max, ln);
+                it.par[j] = pr;
+                it.len[j] = ln;
+                it.moved |= 1u << j;
+                it.needed |= 1u << pr;
+                it.len_max = max(it.len_max, ln);
             }
         }
     }
+}
+
+__global__ void __launch_bounds__(kBeamThreads)
+    beam_reorder_kernel(const __grid_constant__ BeamParams p) {
+    pdl_wait();
+    BeamItem it;
+    beam_item(p, it);
+    const BeamLayer& L = p.layer[it.l];
+    const int pt = it.pt, h = it.h, is_v = it.is_v, row0 = it.row0, len_max = it.len_max;
+    const unsigned moved = it.moved, needed = it.needed;
+    const int* par = it.par;
+    const int* len = it.len;
     const int t0 = pt * kTile;
     if (moved && t0 < len_max) {
         uint8_t* base = (is_v ? L.v : L.k) + h * L.sh;
@@ -106,9 +124,75 @@ __global__ void __launch_bounds__(kBeamThreads)
     pdl_trigger();
 }
 
+// ---- bulk-copy path, for caches whose positions are contiguous 128-byte rows ----------
+// The block's (window, head, tile) region of every row is then one contiguous span, so
+// a single thread moves it with bulk asynchronous copies: every needed parent span is
+// copied into shared memory (completing on one mbarrier), and once all have arrived each
+// moving row's span is copied back out from its parent's copy. Loads finish before any
+// store, as in the per-thread path, so the reorder stays in place; each block keeps up to
+// beam x 8 KiB in flight.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_and_wait() {
+    asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+constexpr int kBulkThreads = 32;
+constexpr int kBulkSmem = KVD_MAX_BEAM * kTileBytes + 16;  // parent spans, mbarrier
+
+__global__ void __launch_bounds__(kBulkThreads)
+    beam_reorder_bulk_kernel(const __grid_constant__ BeamParams p) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    pdl_wait();
+    BeamItem it;
+    beam_item(p, it);
+    const int t0 = it.pt * kTile;
+    if (threadIdx.x == 0 && it.moved && t0 < it.len_max) {
+        const BeamLayer& L = p.layer[it.l];
+        uint8_t* base = (it.is_v ? L.v : L.k) + it.h * L.sh + (int64_t)t0 * kRowBytes;
+        const uint32_t bar = smem_u32(sm + KVD_MAX_BEAM * kTileBytes);
+        mbar_init(bar, 1);
+        fence_barrier_init();
+        const uint32_t bytes = (uint32_t)(min(it.len_max, t0 + kTile) - t0) * kRowBytes;
+        mbar_expect_tx(bar, bytes * __popc(it.needed));
+        for (int j = 0; j < p.beam; ++j)
+            if (it.needed >> j & 1)
+                bulk_load(smem_u32(sm + j * kTileBytes), base + (it.row0 + j) * L.sb, bytes, bar);
+        if (mbar_wait_bounded(bar, 0)) {
+            fence_proxy_async();
+            for (int j = 0; j < p.beam; ++j) {
+                const int rows = min(it.len[j], t0 + kTile) - t0;
+                if ((it.moved >> j & 1) && rows > 0)
+                    bulk_store(base + (it.row0 + j) * L.sb, smem_u32(sm + it.par[j] * kTileBytes),
+                               (uint32_t)rows * kRowBytes);
+            }
+            bulk_commit_and_wait();  // shared memory is read, and the rows are written
+        } else {
+            flag_error(p.dev_err, KVD_ERR_TIMEOUT);
+            mbar_wait_bounded(bar, 0);  // let copies still in flight land before exit
+        }
+    }
+    pdl_trigger();
+}
+
 }  // namespace kvd
 
 using namespace kvd;
+
+namespace {
+constexpr int kMaxDev = 64;
+}
 
 extern "C" kvd_status kvd_beam_reorder_kv(kvd_dtype dtype, const kvd_cache* layers,
                                           int32_t n_layers, int32_t rows, int32_t beam,
@@ -123,6 +207,7 @@ extern "C" kvd_status kvd_beam_reorder_kv(kvd_dtype dtype, const kvd_cache* laye
     if (!layers || !parent) return KVD_ERR_INVALID_ARG;
     BeamParams p;
     int cap_max = 0;
+    bool rows_contiguous = true;  // every layer's positions are adjacent 128-byte rows
     for (int l = 0; l < n_layers; ++l) {
         const kvd_cache* c = &layers[l];
         if (kvd_status s = validate_cache(c)) return s;
@@ -133,6 +218,7 @@ extern "C" kvd_status kvd_beam_reorder_kv(kvd_dtype dtype, const kvd_cache* laye
         p.layer[l].sh = c->stride_h * 2;
         p.layer[l].st = c->stride_t * 2;
         p.layer[l].capacity = c->capacity;
+        rows_contiguous = rows_contiguous && c->stride_t == KVD_HEAD_DIM;
         p.layer[l].pad = 0;
         cap_max = std::max(cap_max, c->capacity);
     }
@@ -149,6 +235,23 @@ extern "C" kvd_status kvd_beam_reorder_kv(kvd_dtype dtype, const kvd_cache* laye
     p.fixed_len = fixed_len;
     const int64_t blocks = (int64_t)n_layers * 2 * p.windows * p.heads * p.pos_tiles;
     if (blocks > 0x7fffffff) return KVD_ERR_UNSUPPORTED;
-    return launch(beam_reorder_kernel, dim3((unsigned)blocks), dim3(kBeamThreads), 0,
-                  reinterpret_cast<cudaStream_t>(stream), (flags & KVD_FLAG_PDL) != 0, p);
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const bool pdl = (flags & KVD_FLAG_PDL) != 0;
+    if (rows_contiguous) {
+        static std::once_flag once[kMaxDev];
+        static bool ok[kMaxDev];
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return KVD_ERR_CUDA;
+        std::call_once(once[dev], [dev] {
+            ok[dev] = cudaFuncSetAttribute(beam_reorder_bulk_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kBulkSmem) == cudaSuccess;
+            cudaGetLastError();
+        });
+        if (!ok[dev]) return KVD_ERR_CUDA;
+        return launch(beam_reorder_bulk_kernel, dim3((unsigned)blocks), dim3(kBulkThreads),
+                      kBulkSmem, st, pdl, p);
+    }
+    return launch(beam_reorder_kernel, dim3((unsigned)blocks), dim3(kBeamThreads), 0, st, pdl,
+                  p);
 }

@@ -219,3 +219,29 @@ def test_beam_cycle_in_place():
     assert e == 0
     assert np.array_equal(got[0][0], layer[0][parent])
     assert np.array_equal(got[0][1], layer[1][parent])
+
+
+def test_beam_padded_rows_take_the_per_thread_path():
+    """Positions padded to 72 elements (144-byte rows) are not contiguous 128-byte rows,
+    so the reorder runs its per-thread path instead of bulk copies; same result."""
+    kvd = _kvd()
+    rng = make_rng(740)
+    layer = gen_cache(rng, 10, 3, 200, D, "f16", 1.0)
+    parent = np.array([1, 1, 0, 4, 2, 9, 5, 5, 7, 6], np.int32)
+    lens = np.array([200, 7, 64, 129, 1, 0, 63, 65, 200, 128], np.int32)
+    devs = []
+    for kv in range(2):
+        big = torch.zeros(10, 3, 200, 72, dtype=torch.float16, device="cuda")
+        big[..., :D] = dev16(layer[kv], "f16")
+        devs.append(big[..., :D])
+    cache = kvd.make_cache(devs[0], devs[1])
+    assert cache.stride_t == 72
+    e = new_err()
+    kvd.kvd_beam_reorder_kv([cache], 10, 5, dev_i32(parent), lens=dev_i32(lens), dev_err=e)
+    torch.cuda.synchronize()
+    assert e.item() == 0
+    for kv in range(2):
+        want = layer[kv].copy()
+        for r in range(10):
+            want[r, :, : lens[r]] = layer[kv][parent[r], :, : lens[r]]
+        assert np.array_equal(host16(devs[kv].contiguous()), want)
