@@ -50,10 +50,11 @@ struct BeamItem {
     int par[KVD_MAX_BEAM], len[KVD_MAX_BEAM];
 };
 
-__device__ __forceinline__ void beam_item(const BeamParams& p, BeamItem& it) {
+// tiles: position tiles per block index (1 when a block walks all tiles itself).
+__device__ __forceinline__ void beam_item(const BeamParams& p, int tiles, BeamItem& it) {
     int64_t item = blockIdx.x;
-    it.pt = (int)(item % p.pos_tiles);
-    item /= p.pos_tiles;
+    it.pt = (int)(item % tiles);
+    item /= tiles;
     it.h = (int)(item % p.heads);
     item /= p.heads;
     it.w = (int)(item % p.windows);
@@ -91,7 +92,7 @@ __global__ void __launch_bounds__(kBeamThreads)
     beam_reorder_kernel(const __grid_constant__ BeamParams p) {
     pdl_wait();
     BeamItem it;
-    beam_item(p, it);
+    beam_item(p, p.pos_tiles, it);
     const BeamLayer& L = p.layer[it.l];
     const int pt = it.pt, h = it.h, is_v = it.is_v, row0 = it.row0, len_max = it.len_max;
     const unsigned moved = it.moved, needed = it.needed;
@@ -125,12 +126,13 @@ __global__ void __launch_bounds__(kBeamThreads)
 }
 
 // ---- bulk-copy path, for caches whose positions are contiguous 128-byte rows ----------
-// The block's (window, head, tile) region of every row is then one contiguous span, so
-// a single thread moves it with bulk asynchronous copies: every needed parent span is
-// copied into shared memory (completing on one mbarrier), and once all have arrived each
-// moving row's span is copied back out from its parent's copy. Loads finish before any
-// store, as in the per-thread path, so the reorder stays in place; each block keeps up to
-// beam x 8 KiB in flight.
+// The (window, head) region of every row is then one contiguous span per 64-position
+// tile, so a single thread moves it with bulk asynchronous copies. A block owns (layer,
+// K or V, window, head) and walks the tiles up to the longest moving row: every needed
+// parent span of a tile is copied into shared memory (completing on one mbarrier), and
+// once all have arrived each moving row's span is copied back out from its parent's
+// copy. Loads of a tile finish before any of its stores, as in the per-thread path, so
+// the reorder stays in place; tiles of one block touch disjoint rows' spans.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {
     asm volatile(
@@ -144,8 +146,16 @@ __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t byt
                  "r"(src), "r"(bytes)
                  : "memory");
 }
-__device__ __forceinline__ void bulk_commit_and_wait() {
-    asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the stores have read shared memory (it may be refilled)
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// the stores are complete
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 constexpr int kBulkThreads = 32;
@@ -156,32 +166,38 @@ __global__ void __launch_bounds__(kBulkThreads)
     extern __shared__ __align__(128) uint8_t sm[];
     pdl_wait();
     BeamItem it;
-    beam_item(p, it);
-    const int t0 = it.pt * kTile;
-    if (threadIdx.x == 0 && it.moved && t0 < it.len_max) {
+    beam_item(p, 1, it);
+    if (threadIdx.x == 0 && it.moved) {
         const BeamLayer& L = p.layer[it.l];
-        uint8_t* base = (it.is_v ? L.v : L.k) + it.h * L.sh + (int64_t)t0 * kRowBytes;
+        uint8_t* head = (it.is_v ? L.v : L.k) + it.h * L.sh;
         const uint32_t bar = smem_u32(sm + KVD_MAX_BEAM * kTileBytes);
         mbar_init(bar, 1);
         fence_barrier_init();
-        const uint32_t bytes = (uint32_t)(min(it.len_max, t0 + kTile) - t0) * kRowBytes;
-        mbar_expect_tx(bar, bytes * __popc(it.needed));
-        for (int j = 0; j < p.beam; ++j)
-            if (it.needed >> j & 1)
-                bulk_load(smem_u32(sm + j * kTileBytes), base + (it.row0 + j) * L.sb, bytes, bar);
-        if (mbar_wait_bounded(bar, 0)) {
+        const int n_needed = __popc(it.needed);
+        for (int t0 = 0, phase = 0; t0 < it.len_max; t0 += kTile, phase ^= 1) {
+            uint8_t* base = head + (int64_t)t0 * kRowBytes;
+            const uint32_t bytes = (uint32_t)(min(it.len_max, t0 + kTile) - t0) * kRowBytes;
+            mbar_expect_tx(bar, bytes * n_needed);
+            for (int j = 0; j < p.beam; ++j)
+                if (it.needed >> j & 1)
+                    bulk_load(smem_u32(sm + j * kTileBytes), base + (it.row0 + j) * L.sb,
+                              bytes, bar);
+            if (!mbar_wait_bounded(bar, phase)) {
+                flag_error(p.dev_err, KVD_ERR_TIMEOUT);
+                mbar_wait_bounded(bar, phase);  // let copies in flight land before exit
+                break;
+            }
             fence_proxy_async();
             for (int j = 0; j < p.beam; ++j) {
                 const int rows = min(it.len[j], t0 + kTile) - t0;
                 if ((it.moved >> j & 1) && rows > 0)
-                    bulk_store(base + (it.row0 + j) * L.sb, smem_u32(sm + it.par[j] * kTileBytes),
-                               (uint32_t)rows * kRowBytes);
+                    bulk_store(base + (it.row0 + j) * L.sb,
+                               smem_u32(sm + it.par[j] * kTileBytes), (uint32_t)rows * kRowBytes);
             }
-            bulk_commit_and_wait();  // shared memory is read, and the rows are written
-        } else {
-            flag_error(p.dev_err, KVD_ERR_TIMEOUT);
-            mbar_wait_bounded(bar, 0);  // let copies still in flight land before exit
+            bulk_commit();
+            bulk_wait_read();  // before the next tile refills shared memory
         }
+        bulk_wait_all();
     }
     pdl_trigger();
 }
@@ -249,8 +265,8 @@ extern "C" kvd_status kvd_beam_reorder_kv(kvd_dtype dtype, const kvd_cache* laye
             cudaGetLastError();
         });
         if (!ok[dev]) return KVD_ERR_CUDA;
-        return launch(beam_reorder_bulk_kernel, dim3((unsigned)blocks), dim3(kBulkThreads),
-                      kBulkSmem, st, pdl, p);
+        return launch(beam_reorder_bulk_kernel, dim3((unsigned)(blocks / p.pos_tiles)),
+                      dim3(kBulkThreads), kBulkSmem, st, pdl, p);
     }
     return launch(beam_reorder_kernel, dim3((unsigned)blocks), dim3(kBeamThreads), 0, st, pdl,
                   p);
