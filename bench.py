@@ -785,10 +785,11 @@ def run_gqa_lm_step(torch, kvd, dev, stream, peak, flags):
     gen = torch.Generator(device=dev)
     gen.manual_seed(3030)
     bf = torch.bfloat16
-    caches = []
+    kv_tensors, caches = [], []  # the caches hold raw pointers: keep the tensors alive
     for _ in range(NL):
         k = torch.empty(B, Hkv, cap, D, dtype=bf, device=dev).normal_(0, w["qkv_std"], generator=gen)
         v = torch.empty(B, Hkv, cap, D, dtype=bf, device=dev).normal_(0, w["qkv_std"], generator=gen)
+        kv_tensors.append((k, v))
         caches.append(kvd.make_cache(k, v))
     lens_np = gen_lens_uniform(make_rng(seed_for("gqa_lm_step")), B, w["len_lo"], w["len_hi"])
     lens_in = torch.from_numpy(lens_np).to(dev)

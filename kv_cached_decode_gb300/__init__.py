@@ -143,7 +143,9 @@ def make_cache(k: torch.Tensor, v: torch.Tensor) -> Cache:
     if not (k.is_cuda and v.is_cuda):
         raise ValueError("cache tensors must be CUDA tensors")
     B, H, cap, D = k.shape
-    return Cache(k.data_ptr(), v.data_ptr(), k.stride(0), k.stride(1), k.stride(2), B, H, D, cap)
+    c = Cache(k.data_ptr(), v.data_ptr(), k.stride(0), k.stride(1), k.stride(2), B, H, D, cap)
+    c._tensors = (k, v)  # the struct holds raw pointers: keep the tensors alive with it
+    return c
 
 
 def kvd_version() -> int:

@@ -193,6 +193,24 @@ def test_workspace_too_small_is_rejected():
         kvd.kvd_decode_attn(q, kvd.make_cache(K, K), q.clone(), None, fixed_len=32768)
 
 
+# One query vector per KV head runs on the CUDA-core kernel when blocks stream several
+# rounds of tiles (long caches); short caches go to the tensor-core kernel. These shapes
+# keep the CUDA-core kernel's cluster merge, single-split store and fused append covered.
+def test_decode_cuda_core_cluster_merge():
+    # 80 (row, head) units over 2048 positions: clusters of 5 splits of 8 tiles
+    lens = np.array([2048, 1900, 1, 1000], np.int32)
+    got, want = run_attention("f16", 4, 20, 20, 2048, lens=lens, seed=170)
+    assert_attn_close(got, want, "f16", "CUDA-core decode, cluster merge")
+
+
+def test_decode_cuda_core_single_split():
+    # 512 units fill the GPU by themselves: one block per unit, 8 tiles each
+    rng = make_rng(171)
+    lens = gen_lens_uniform(rng, 64, 1, 512)
+    got, want = run_attention("bf16", 64, 8, 8, 512, lens=lens, seed=172)
+    assert_attn_close(got, want, "bf16", "CUDA-core decode, one split")
+
+
 # ------------------------------------------------------------------------- verify -------
 
 @pytest.mark.parametrize("qlen", [5, 6])
@@ -333,6 +351,15 @@ def test_verify_fused_append_block(L, flags):
     assert e == 0 and not err
     assert np.array_equal(Kg, Kw) and np.array_equal(Vg, Vw) and np.array_equal(lo, low)
     assert_attn_close(got, want, "f16", f"fused verify L={L}")
+
+
+@pytest.mark.parametrize("flags", [0, 3])
+def test_decode_fused_append_cuda_core_path(flags):
+    got, want, Kg, Vg, Kw, Vw, lo, low, e, err = run_fused(
+        "bf16", 4, 20, 20, 2048, [2047, 1000, 63, 0], 1, verify=False, seed=144, flags=flags)
+    assert e == 0 and not err
+    assert np.array_equal(Kg, Kw) and np.array_equal(Vg, Vw) and np.array_equal(lo, low)
+    assert_attn_close(got, want, "bf16", "fused decode, CUDA cores")
 
 
 def test_fused_append_overflow_leaves_row_untouched():
