@@ -18,7 +18,8 @@ inputs larger than L2, no flush needed.
 writes, logits) divided by the measured step time, in GB/s. ``e2e`` is the same metric
 through the public API with host buffers: each step copies its inputs (queries, new
 K/V, logits, drafts) from pinned host memory, replays the graph and copies every
-output back. ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+output back; two buffer slots and two copy streams overlap a step's copies with the
+neighbouring steps' compute. ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
 same workload. Multi-GPU runs are independent replicas (one per rank, weak scaling).
 """
 
@@ -168,51 +169,15 @@ class WhisperStep:
         hv[: halves.nbytes] = halves.view(np.uint8)
         hv[halves.nbytes: halves.nbytes + logits.nbytes] = logits.view(np.uint8).ravel()
         hv[halves.nbytes + logits.nbytes:] = draft.view(np.uint8).ravel()
-        self.d_in = self.h_in.to(dev)
-        hal = self.d_in[: halves.nbytes].view(f16)
-        self.logits = self.d_in[halves.nbytes: halves.nbytes + logits.nbytes].view(torch.float32).view(1, k + 1, self.V)
-        self.draft = self.d_in[halves.nbytes + logits.nbytes:].view(torch.int32).view(1, k)
-        self.q_self, self.q_cross, self.kn1, self.vn1 = [], [], [], []
-        self.qv_self, self.qv_cross, self.kn5, self.vn5 = [], [], [], []
-        off = 0
-
-        def take(n, shape):
-            nonlocal off
-            t = hal[off: off + n].view(*shape)
-            off += n
-            return t
-
-        for layer in range(NL):
-            self.q_self.append(take(qd, (1, H, 1, D)))
-            self.q_cross.append(take(qd, (1, H, 1, D)))
-            self.kn1.append(take(qd, (1, H, 1, D)))
-            self.vn1.append(take(qd, (1, H, 1, D)))
-            self.qv_self.append(take(qv, (1, H, k, D)))
-            self.qv_cross.append(take(qv, (1, H, k, D)))
-            self.kn5.append(take(qv, (1, H, k, D)))
-            self.vn5.append(take(qv, (1, H, k, D)))
         self.in_bytes = nbytes_in
-
-        # outputs packed in one buffer ---------------------------------------------------
-        out_halves = NL * (2 * qd + 2 * qv)
-        self.d_out = torch.zeros(out_halves * 2 + 16, dtype=torch.uint8, device=dev)
-        oh = self.d_out[: out_halves * 2].view(f16)
-        off2 = 0
-
-        def otake(n, shape):
-            nonlocal off2
-            t = oh[off2: off2 + n].view(*shape)
-            off2 += n
-            return t
-
-        self.o_self = [otake(qd, (1, H, 1, D)) for _ in range(NL)]
-        self.o_cross = [otake(qd, (1, H, 1, D)) for _ in range(NL)]
-        self.ov_self = [otake(qv, (1, H, k, D)) for _ in range(NL)]
-        self.ov_cross = [otake(qv, (1, H, k, D)) for _ in range(NL)]
-        tail = self.d_out[out_halves * 2:].view(torch.int32)
-        self.n_acc, self.next_tok = tail[0:1], tail[1:2]
-        self.h_out = torch.empty_like(self.d_out, device="cpu").pin_memory()
-        self.out_bytes = self.d_out.numel()
+        self.n_halves, self.n_logit_bytes = halves.nbytes, logits.nbytes
+        # Two device buffer sets ("slots") for the inputs and outputs, so that the e2e
+        # leg can copy step i+1's inputs and step i-1's outputs while step i computes.
+        self._slots = [self._make_slot(dev) for _ in range(2)]
+        self.h_out = [torch.empty_like(sl["d_out"], device="cpu").pin_memory()
+                      for sl in self._slots]
+        self.out_bytes = self._slots[0]["d_out"].numel()
+        self.use_slot(0)
 
         i32 = dict(dtype=torch.int32, device=dev)
         self.dec_lens_in = torch.tensor([L_decode], **i32)
@@ -225,6 +190,50 @@ class WhisperStep:
         self.ws = kvd.new_workspace(ws, device=dev)
         self.ws_acc = kvd.new_workspace(kvd.kvd_workspace_size(
             kvd.KVD_OP_GREEDY_ACCEPT, 1, qlen=k, vocab=self.V), device=dev)
+
+    def _make_slot(self, dev):
+        """One device copy of the packed inputs and the packed outputs, with the views
+        the launches take (per layer: q, new K/V, outputs; logits, drafts, accept)."""
+        import torch
+
+        NL, H, k = self.NL, self.H, self.k
+        f16 = torch.float16
+        qd, qv = H * D, H * k * D
+        sl = {"d_in": self.h_in.to(dev)}
+        d_in = sl["d_in"]
+        hal = d_in[: self.n_halves].view(f16)
+        sl["logits"] = d_in[self.n_halves: self.n_halves + self.n_logit_bytes].view(
+            torch.float32).view(1, k + 1, self.V)
+        sl["draft"] = d_in[self.n_halves + self.n_logit_bytes:].view(torch.int32).view(1, k)
+        names = ("q_self", "q_cross", "kn1", "vn1", "qv_self", "qv_cross", "kn5", "vn5")
+        for n in names:
+            sl[n] = []
+        off = 0
+        for _ in range(NL):
+            for n, size, shape in (("q_self", qd, (1, H, 1, D)), ("q_cross", qd, (1, H, 1, D)),
+                                   ("kn1", qd, (1, H, 1, D)), ("vn1", qd, (1, H, 1, D)),
+                                   ("qv_self", qv, (1, H, k, D)), ("qv_cross", qv, (1, H, k, D)),
+                                   ("kn5", qv, (1, H, k, D)), ("vn5", qv, (1, H, k, D))):
+                sl[n].append(hal[off: off + size].view(*shape))
+                off += size
+        out_halves = NL * (2 * qd + 2 * qv)
+        sl["d_out"] = torch.zeros(out_halves * 2 + 16, dtype=torch.uint8, device=dev)
+        oh = sl["d_out"][: out_halves * 2].view(f16)
+        off = 0
+        for n, size, shape in (("o_self", qd, (1, H, 1, D)), ("o_cross", qd, (1, H, 1, D)),
+                               ("ov_self", qv, (1, H, k, D)), ("ov_cross", qv, (1, H, k, D))):
+            sl[n] = []
+            for _ in range(NL):
+                sl[n].append(oh[off: off + size].view(*shape))
+                off += size
+        tail = sl["d_out"][out_halves * 2:].view(torch.int32)
+        sl["n_acc"], sl["next_tok"] = tail[0:1], tail[1:2]
+        return sl
+
+    def use_slot(self, i):
+        """Point the launches at buffer slot i (graphs captured afterwards use it)."""
+        for n, v in self._slots[i].items():
+            setattr(self, n, v)
 
     # -- launches -----------------------------------------------------------------------
     def run_decode(self, layers=None, parts=("append", "self", "cross")):
@@ -489,6 +498,10 @@ def run_ours(args):
         cross_flags = flags | (kvd.KVD_FLAG_EARLY_KV if args.early_kv else 0)
     step = WhisperStep(dev, flags=flags, cross_flags=cross_flags, fused=fused)
     stream = torch.cuda.Stream(device=dev)
+    # one graph per buffer slot (the e2e leg alternates them); slot 0 is the default
+    step.use_slot(1)
+    g_slot1 = capture(torch, step.run, stream)
+    step.use_slot(0)
     g = capture(torch, step.run, stream)
 
     def barrier():
@@ -519,17 +532,43 @@ def run_ours(args):
     assert int(step.err.item()) == 0, f"device error {int(step.err.item())}"
 
     # e2e through the public API with host buffers --------------------------------------
+    # Every step copies its inputs from pinned host memory and all its outputs back.
+    # Two buffer slots and two copy streams pipeline it: step i+1's inputs go up and
+    # step i-1's outputs come down while step i computes.
     barrier()
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        e2 = torch.cuda.Event(enable_timing=True)
-        e3 = torch.cuda.Event(enable_timing=True)
-        e2.record(stream)
-        for _ in range(args.steps):
-            step.d_in.copy_(step.h_in, non_blocking=True)
-            g.replay()
-            step.h_out.copy_(step.d_out, non_blocking=True)
-        e3.record(stream)
+    graphs = [g, g_slot1]
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    h2d_done = [ev() for _ in range(2)]
+    comp_done = [ev() for _ in range(2)]
+    d2h_done = [ev() for _ in range(2)]
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    up.wait_event(e2)
+    down.wait_event(e2)
+    for i in range(args.steps):
+        b = i % 2
+        slot = step._slots[b]
+        with torch.cuda.stream(up):
+            if i >= 2:
+                up.wait_event(comp_done[b])  # step i-2 has read this slot's inputs
+            slot["d_in"].copy_(step.h_in, non_blocking=True)
+            h2d_done[b].record(up)
+        stream.wait_event(h2d_done[b])
+        if i >= 2:
+            stream.wait_event(d2h_done[b])  # step i-2's outputs have left this slot
+        with torch.cuda.stream(stream):
+            graphs[b].replay()
+        comp_done[b].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(comp_done[b])
+            step.h_out[b].copy_(slot["d_out"], non_blocking=True)
+            d2h_done[b].record(down)
+    for b in range(2):
+        stream.wait_event(d2h_done[b])
+    e3.record(stream)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(e2.elapsed_time(e3) / args.steps, dev)
     if world > 1:
