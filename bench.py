@@ -614,8 +614,13 @@ def run_ours(args):
                   attn_bytes(1, H, H, step.Lv + step.k, step.k))
     t_vcross = kern_time("verify_attn_cross_1500_q5", lambda: step.run_verify(parts=("cross",)),
                          step.NL, attn_bytes(1, H, H, F, step.k))
-    kern_time("greedy_accept_6x51865", lambda: step.run_verify(layers=[], parts=("accept",)), 1,
-              accept_bytes(1, step.k, step.V))
+    # 32 back-to-back accepts on the step's logits (1.24 MB, L2-resident after the
+    # first): a one-launch graph would mostly time the graph launch itself
+    def accepts():
+        for _ in range(step.NL):
+            step.run_verify(layers=[], parts=("accept",))
+
+    kern_time("greedy_accept_6x51865_l2", accepts, step.NL, accept_bytes(1, step.k, step.V))
     peak, peak_kind = measured_hbm_peak()
     # The dominant launch type (largest share of the ncu launch list, and of the timed
     # graph) is the 5-token verify over the 1500-frame cross K/V; the one-query decode
@@ -858,7 +863,8 @@ def run_gqa_lm_step(torch, kvd, dev, stream, peak, flags):
 
 def run_tiny_layer(torch, kvd, dev, stream, flags):
     """Tiny single layer: 6 heads, 32 cached positions + 1 appended (fused), then cross
-    attention over 1500 frames."""
+    attention over 1500 frames; time per layer over a graph of 32 repetitions (the
+    same buffers, so L2-resident)."""
     w = WORKLOADS["tiny_layer"]
     H, cap, F = w["n_q_heads"], w["capacity"], w["cross_len"]
     gen = torch.Generator(device=dev)
@@ -877,12 +883,14 @@ def run_tiny_layer(torch, kvd, dev, stream, flags):
     ws = kvd.new_workspace(kvd.kvd_workspace_size(kvd.KVD_OP_DECODE_ATTN, 1, H, H, 1, 1, F),
                            device=dev)
 
-    def layer():
-        kvd.kvd_decode_attn(q[0], c_self, out[0], ws, lens=lens_in, scale=w["scale"], flags=flags,
-                            append=(kn[0], kn[1], lens_out))
-        kvd.kvd_decode_attn(q[1], c_cross, out[1], ws, fixed_len=F, scale=w["scale"], flags=flags)
+    def layers():  # 32 repetitions of the layer: a 2-launch graph would mostly time its launch
+        for _ in range(32):
+            kvd.kvd_decode_attn(q[0], c_self, out[0], ws, lens=lens_in, scale=w["scale"],
+                                flags=flags, append=(kn[0], kn[1], lens_out))
+            kvd.kvd_decode_attn(q[1], c_cross, out[1], ws, fixed_len=F, scale=w["scale"],
+                                flags=flags)
 
-    t = time_graph(torch, capture(torch, layer, stream), stream, 500)
+    t = time_graph(torch, capture(torch, layers, stream), stream, 100) / 32
     nbytes = append_bytes(1, H, 1) + attn_bytes(1, H, H, cap, 1) + attn_bytes(1, H, H, F, 1)
     print(json.dumps({"sweep": "tiny_layer", "us": round(t * 1e3, 3), "bytes": nbytes,
                       "gbs": round(nbytes / (t * 1e-3) / 1e9, 1), "l2_resident": True}),
