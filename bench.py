@@ -518,17 +518,22 @@ def run_ours(args):
     barrier()
     torch.cuda.synchronize()
     t0h = time.time()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one event between consecutive steps as well, for the per-step distribution
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    e0, e1 = evs[0], evs[-1]
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for _ in range(args.steps):
+        for i in range(args.steps):
             g.replay()
-        e1.record(stream)
+            evs[i + 1].record(stream)
     torch.cuda.synchronize()
     barrier()
     t1h = time.time()
     clocks = sampler.stop(t0h, t1h)
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    per_step = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
+    pct = [round(per_step[min(len(per_step) - 1, int(f * len(per_step)))], 4)
+           for f in (0.1, 0.5, 0.9)]
     assert int(step.err.item()) == 0, f"device error {int(step.err.item())}"
 
     # e2e through the public API with host buffers --------------------------------------
@@ -645,6 +650,7 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "ms_per_step_p10_p50_p90": pct,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded PCG64 N(0,1/64) fp16 K/V/Q; fp32 N(0,4) logits)",
         "config": {"workload": "whisper-large-v2 decoder step (32 layers, self 447->448, cross "
@@ -898,10 +904,18 @@ def run_tiny_layer(torch, kvd, dev, stream, flags):
 
 
 def run_verify_ratio(torch, kvd, dev, stream, flags):
-    """Verify (k = 5) against single-token decode over the same Whisper-shaped caches,
-    32 layers each, across cached lengths: self (fused append) and cross attention."""
-    st = WhisperStep(dev, flags=flags)
-    for L in (0, 64, 128, 256, 443):
+    """Verify (k = 5, and k = 6) against single-token decode over the same Whisper-shaped
+    caches, 32 layers each, across cached lengths: self (fused append) and cross
+    attention."""
+    for k, lens in ((5, (0, 64, 128, 256, 443)), (6, (0, 256, 442))):
+        st = WhisperStep(dev, flags=flags, k=k, L_verify=448 - k)
+        verify_ratio_lines(torch, st, stream, lens)
+        del st
+        torch.cuda.empty_cache()
+
+
+def verify_ratio_lines(torch, st, stream, lens):
+    for L in lens:
         st.dec_lens_in.fill_(L)
         st.ver_lens_in.fill_(L)
         t = {}
