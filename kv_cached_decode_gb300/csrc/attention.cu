@@ -691,8 +691,11 @@ __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: 4 blocks per
 }
 
 // ------------------------------------ 2..16 query vectors per KV head (tensor cores) ----
-template <typename T>
-__global__ void __launch_bounds__(kThreads)
+// MINB: blocks per SM the register budget is cut for. 2 (no cut) is the default; 3 gives
+// more resident blocks, hence more splits, when a launch is limited by residency, at the
+// price of a few spilled registers.
+template <typename T, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
     block_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
     constexpr int RM = 16;
@@ -871,32 +874,47 @@ int prepare_kernel(size_t smem_bytes) {
     return result[dev];
 }
 
+// Kernel variants: the CUDA-core kernel, and the tensor-core kernel built for 2 or 3
+// resident blocks per SM.
+enum Variant { kSimt = 1, kMma = 2, kMma3 = 3 };
+
 template <typename T>
-int prepare(bool mma) {
-    return mma ? prepare_kernel<block_attn_kernel<T>>(
-                     smem_layout(kMaxStages, 16, kMaxClusterSplits * kMmaQueryBlock,
-                                 KVD_MAX_QLEN).total)
-               : prepare_kernel<decode_attn_kernel<T>>(
-                     smem_layout(kMaxStages, 1, kMaxClusterSplits, KVD_MAX_QLEN).total);
+int prepare(int var) {
+    const uint32_t mma_smem =
+        smem_layout(kMaxStages, 16, kMaxClusterSplits * kMmaQueryBlock, KVD_MAX_QLEN).total;
+    switch (var) {
+    case kMma: return prepare_kernel<block_attn_kernel<T, 2>>(mma_smem);
+    case kMma3: return prepare_kernel<block_attn_kernel<T, 3>>(mma_smem);
+    default:
+        return prepare_kernel<decode_attn_kernel<T>>(
+            smem_layout(kMaxStages, 1, kMaxClusterSplits, KVD_MAX_QLEN).total);
+    }
 }
 
 template <typename T>
-const void* kernel_of(bool mma) {
-    return mma ? reinterpret_cast<const void*>(block_attn_kernel<T>)
-               : reinterpret_cast<const void*>(decode_attn_kernel<T>);
+const void* kernel_of(int var) {
+    switch (var) {
+    case kMma: return reinterpret_cast<const void*>(block_attn_kernel<T, 2>);
+    case kMma3: return reinterpret_cast<const void*>(block_attn_kernel<T, 3>);
+    default: return reinterpret_cast<const void*>(decode_attn_kernel<T>);
+    }
 }
 
 template <typename T>
-kvd_status launch_attn(bool mma, dim3 grid, cudaStream_t st, bool pdl, unsigned cl,
+kvd_status launch_attn(int var, dim3 grid, cudaStream_t st, bool pdl, unsigned cl,
                        const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p) {
     const int slots = merge_slots(p.cluster, p.splits, p.msub);
-    if (mma)
-        return launch_ex(block_attn_kernel<T>, grid, dim3(kThreads),
-                         smem_layout(p.stages, 16, slots, p.append ? p.qlen : 0).total, st,
-                         pdl, cl, mk, mv, p);
+    const int app_rows = p.append ? p.qlen : 0;
+    if (var == kMma)
+        return launch_ex(block_attn_kernel<T, 2>, grid, dim3(kThreads),
+                         smem_layout(p.stages, 16, slots, app_rows).total, st, pdl, cl, mk, mv,
+                         p);
+    if (var == kMma3)
+        return launch_ex(block_attn_kernel<T, 3>, grid, dim3(kThreads),
+                         smem_layout(p.stages, 16, slots, app_rows).total, st, pdl, cl, mk, mv,
+                         p);
     return launch_ex(decode_attn_kernel<T>, grid, dim3(kThreads),
-                     smem_layout(p.stages, 1, slots, p.append ? p.qlen : 0).total, st, pdl, cl,
-                     mk, mv, p);
+                     smem_layout(p.stages, 1, slots, app_rows).total, st, pdl, cl, mk, mv, p);
 }
 
 size_t plan_smem(const AttnPlan& P, bool mma, int app_rows) {
@@ -1003,38 +1021,51 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
     const int len_bound = lens ? kv->capacity : fixed_len;
     const bool bf = dtype == KVD_BF16;
     const int group = n_q_heads / kv->n_kv_heads;
-    bool mma = verify || (int64_t)rows_per_kv * group * qlen >= 2;
-    int max_cluster = bf ? prepare<__nv_bfloat16>(mma) : prepare<__half>(mma);
-    if (max_cluster <= 0) return KVD_ERR_CUDA;
-    int kid = (mma ? 2 : 0) | (bf ? 1 : 0);
-    const void* kern = bf ? kernel_of<__nv_bfloat16>(mma) : kernel_of<__half>(mma);
     const int app_rows = app ? qlen : 0;
-    AttnPlan P = choose_plan(kern, kid, mma, nsm, batch, n_q_heads, kv->n_kv_heads,
-                             rows_per_kv, qlen, len_bound, max_cluster, app_rows);
-    if (!mma && P.tiles_per_split <= 2) {
+    // Plan for one kernel variant; false if it cannot be prepared.
+    auto plan_for = [&](int var, AttnPlan& out) -> bool {
+        const int mc = bf ? prepare<__nv_bfloat16>(var) : prepare<__half>(var);
+        if (mc <= 0) return false;
+        const void* kern = bf ? kernel_of<__nv_bfloat16>(var) : kernel_of<__half>(var);
+        out = choose_plan(kern, var * 2 + (bf ? 1 : 0), var != kSimt, nsm, batch, n_q_heads,
+                          kv->n_kv_heads, rows_per_kv, qlen, len_bound, mc, app_rows);
+        return true;
+    };
+    // Whether a tensor-core plan keeps all its blocks resident at once.
+    auto one_wave = [&](int var, const AttnPlan& Q) -> bool {
+        if (Q.cluster) return true;  // choose_plan checked the clusters' residency
+        if (Q.splits != 1) return false;
+        const void* kern = bf ? kernel_of<__nv_bfloat16>(var) : kernel_of<__half>(var);
+        return (int64_t)Q.units <=
+               resident(kern, var * 2 + (bf ? 1 : 0), plan_smem(Q, true, app_rows), 1, nsm);
+    };
+    int var = (verify || (int64_t)rows_per_kv * group * qlen >= 2) ? kMma : kSimt;
+    AttnPlan P;
+    if (!plan_for(var, P)) return KVD_ERR_CUDA;
+    if (var == kSimt && P.tiles_per_split <= 2) {
         // Each block has a single round of tiles: then the time is the chain after the
         // dependency wait, and the tensor-core kernel's per-tile chain (ldmatrix + mma,
         // two shuffles) is shorter than the CUDA-core one (a shuffle tree per position).
         // Measured for 20 heads: 3.70 vs 4.47 us over 1500 frames, 3.02 vs 3.31 us at 448
         // positions with the append. It has half the resident blocks per SM, so it is
         // taken only while its launch still fits in one wave.
-        const int mc2 = bf ? prepare<__nv_bfloat16>(true) : prepare<__half>(true);
-        const int kid2 = 2 | (bf ? 1 : 0);
-        const void* kern2 = bf ? kernel_of<__nv_bfloat16>(true) : kernel_of<__half>(true);
-        if (mc2 > 0) {
-            const AttnPlan P2 = choose_plan(kern2, kid2, true, nsm, batch, n_q_heads,
-                                            kv->n_kv_heads, rows_per_kv, qlen, len_bound, mc2,
-                                            app_rows);
-            const bool fits =
-                P2.cluster || (P2.splits == 1 && (int64_t)P2.units <=
-                                   resident(kern2, kid2, plan_smem(P2, true, app_rows), 1, nsm));
-            if (fits && P2.tiles_per_split <= 2) {
-                mma = true;
-                P = P2;
-                max_cluster = mc2;
-                kid = kid2;
-                kern = kern2;
-            }
+        AttnPlan P2;
+        if (plan_for(kMma, P2) && one_wave(kMma, P2) && P2.tiles_per_split <= 2) {
+            var = kMma;
+            P = P2;
+        }
+    }
+    if (var == kMma && P.tiles_per_split >= 8) {
+        // Residency limits the split count and blocks stream 4 or more rounds: the variant
+        // with 3 blocks per SM allows more splits, but each round is slower (spills), so it
+        // is taken only when it at least halves every block's tiles. Measured: beam cross
+        // attention (160 units over 1500 frames) 16.0 -> 13.2 us; with a smaller cut
+        // (GQA-LM: 8 -> 6 tiles per block) it lost, 6.9 -> 8.1 us per layer.
+        AttnPlan P3;
+        if (plan_for(kMma3, P3) && one_wave(kMma3, P3) &&
+            2 * P3.tiles_per_split <= P.tiles_per_split) {
+            var = kMma3;
+            P = P3;
         }
     }
     if ((int64_t)kv->n_kv_heads * P.nsub > 65535) return KVD_ERR_UNSUPPORTED;
@@ -1087,8 +1118,8 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
     const bool pdl = (flags & (KVD_FLAG_PDL | KVD_FLAG_EARLY_KV)) != 0;
     const dim3 grid(P.splits, kv->n_kv_heads * P.nsub, P.bkv);
     const unsigned cl = P.cluster ? (unsigned)P.splits : 1u;
-    return bf ? launch_attn<__nv_bfloat16>(mma, grid, stream, pdl, cl, mk, mv, p)
-              : launch_attn<__half>(mma, grid, stream, pdl, cl, mk, mv, p);
+    return bf ? launch_attn<__nv_bfloat16>(var, grid, stream, pdl, cl, mk, mv, p)
+              : launch_attn<__half>(var, grid, stream, pdl, cl, mk, mv, p);
 }
 
 }  // namespace
