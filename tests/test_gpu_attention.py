@@ -193,6 +193,14 @@ def test_workspace_too_small_is_rejected():
         kvd.kvd_decode_attn(q, kvd.make_cache(K, K), q.clone(), None, fixed_len=32768)
 
 
+def test_beam_cross_eight_windows_register_variant():
+    # 8 windows x beam 5 over 1500 frames: 160 (window, head) units, too many for
+    # cluster splits at 2 blocks per SM; the 3-blocks-per-SM build halves each block's
+    # tiles and runs instead
+    got, want = run_attention("f16", 40, 20, 20, 1500, fixed_len=1500, rpk=5, seed=173)
+    assert_attn_close(got, want, "f16", "beam cross, 8 windows")
+
+
 # One query vector per KV head runs on the CUDA-core kernel when blocks stream several
 # rounds of tiles (long caches); short caches go to the tensor-core kernel. These shapes
 # keep the CUDA-core kernel's cluster merge, single-split store and fused append covered.
