@@ -241,6 +241,37 @@ kvd_status kvd_verify_attn(kvd_dtype dtype, int32_t batch, int32_t n_q_heads, in
                            int32_t *dev_err, kvd_stream_t stream);
 
 /*
+ * kvd_prefill_attn -- prefill: the first forward pass over a prompt.
+ *
+ * [N] "KV キャッシュが推論を最適化する方法" (prefill fills the cache with the whole
+ * prompt, decoding then adds one token per step); [W] "Inference 抽象と KV キャッシュ"
+ * (the first pass covers the initial tokens). Two launches on `stream`: the prompt's
+ * K/V rows j < plens[b] are written at positions lens_in[b] + j and
+ * lens_out[b] = lens_in[b] + plens[b]; then, per head,
+ *
+ *   out[b,hq,j,:] = sum_{t <= lens_in[b] + j} softmax_t(scale * q[b,hq,j] . K[b,h,t]) V[b,h,t]
+ *
+ * for j < plens[b] (h = hq / (n_q_heads / n_kv_heads)); rows j >= plens[b] of `out` are
+ * written as zeros. lens_in > 0 continues a cached prefix (chunked prefill).
+ *
+ * q, out        : device [batch, n_q_heads, max_len, 64], contiguous, 16-byte aligned
+ * k_new, v_new  : device [batch, n_kv_heads, max_len, 64], contiguous, 16-byte aligned
+ * kv            : the layer's cache (any strides kvd_cache allows)
+ * lens_in       : device int32 [batch] or NULL (every row starts empty)
+ * plens         : device int32 [batch], prompt lengths in [0, max_len]
+ * lens_out      : device int32 [batch] or NULL; must not alias lens_in
+ * Q.K^T and P.V run on the tensor cores, fp32 accumulation, output rounded to nearest.
+ * Device errors: lens_in + plens outside [0, capacity] or plens outside [0, max_len] ->
+ * KVD_ERR_LEN_OVERFLOW; that row's cache is untouched, lens_out keeps lens_in and its
+ * output rows are zeros. No workspace; the buffers are caller-owned.
+ */
+kvd_status kvd_prefill_attn(kvd_dtype dtype, int32_t batch, int32_t n_q_heads, int32_t max_len,
+                            const void *q, const kvd_cache *kv, const void *k_new,
+                            const void *v_new, const int32_t *lens_in, const int32_t *plens,
+                            int32_t *lens_out, float scale, void *out, uint32_t flags,
+                            int32_t *dev_err, kvd_stream_t stream);
+
+/*
  * kvd_greedy_accept -- A6. Greedy verification of k draft tokens.
  *
  * [W] "Inference 抽象と KV キャッシュ" (GreedyDecoder: argmax at temperature 0);

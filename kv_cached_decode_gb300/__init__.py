@@ -87,6 +87,7 @@ def load_library(path: str = LIB_PATH):
             "kvd_decode_attn_noalloc": [I32, I32, I32, P, CP, P, I32, NP, I32, F, P, U32, P, P],
             "kvd_verify_attn": [I32, I32, I32, I32, P, CP, P, I32, NP, I32, I32, F, P, P, SZ,
                                 U32, P, P],
+            "kvd_prefill_attn": [I32, I32, I32, I32, P, CP, P, P, P, P, P, F, P, U32, P, P],
             "kvd_greedy_accept": [P, I32, I32, I32, P, P, P, P, P, P, SZ, U32, P, P],
             "kvd_beam_reorder_kv": [I32, CP, I32, I32, I32, P, P, I32, U32, P, P],
             "kvd_workspace_size": [I32, I32, I32, I32, I32, I32, I32, I32],
@@ -213,6 +214,19 @@ def kvd_verify_attn(q, cache: Cache, out, workspace, lens=None, fixed_len: int =
                                           scale, _ptr(out),
                                           _ptr(workspace), ws_bytes, flags, _ptr(dev_err),
                                           _stream(stream)), "kvd_verify_attn")
+
+
+def kvd_prefill_attn(q, cache: Cache, k_new, v_new, plens, out, lens_in=None, lens_out=None,
+                     scale: float = 0.125, flags: int = 0, dev_err=None, stream=None):
+    """Prefill: append the prompt's K/V (rows j < plens[b]) and run causal attention of
+    the prompt. q, out: [batch, n_q_heads, max_len, 64]; k_new, v_new: [batch,
+    n_kv_heads, max_len, 64]."""
+    B, Hq, T, D = q.shape
+    _check(load_library().kvd_prefill_attn(_dtype_code(q), B, Hq, T, _ptr(q),
+                                           ctypes.byref(cache), _ptr(k_new), _ptr(v_new),
+                                           _ptr(lens_in), _ptr(plens), _ptr(lens_out), scale,
+                                           _ptr(out), flags, _ptr(dev_err), _stream(stream)),
+           "kvd_prefill_attn")
 
 
 def kvd_greedy_accept(logits, draft, n_accepted, next_token, workspace, n_min=None,

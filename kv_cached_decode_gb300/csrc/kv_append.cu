@@ -16,7 +16,8 @@ struct AppendParams {
     int64_t sb, sh, st;  // bytes
     const uint8_t* k_new;
     const uint8_t* v_new;
-    const int32_t* lens_in;
+    const int32_t* lens_in;   // NULL: every row starts empty
+    const int32_t* counts;    // NULL: q rows for every batch row; else rows for row b
     int32_t* lens_out;
     int32_t* dev_err;
     int32_t capacity, heads, q;
@@ -35,18 +36,21 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
         const int64_t bh = row / p.q;
         const int h = (int)(bh % p.heads);
         const int b = (int)(bh / p.heads);
-        const int len = p.lens_in[b];
+        const int len = p.lens_in ? p.lens_in[b] : 0;
+        const int n = p.counts ? p.counts[b] : p.q;
         const bool first = !is_v && h == 0 && j == 0 && c == 0;
-        if (len < 0 || (int64_t)len + p.q > p.capacity) {
+        if (len < 0 || n < 0 || n > p.q || (int64_t)len + n > p.capacity) {
             if (first) {
                 flag_error(p.dev_err, KVD_ERR_LEN_OVERFLOW);
                 if (p.lens_out) p.lens_out[b] = len;
             }
-        } else {
+        } else if (j < n) {
             const uint4 val = *reinterpret_cast<const uint4*>((is_v ? p.v_new : p.k_new) + rem * 16);
             uint8_t* dst = (is_v ? p.v : p.k) + b * p.sb + h * p.sh + (int64_t)(len + j) * p.st + c * 16;
             *reinterpret_cast<uint4*>(dst) = val;
-            if (first && p.lens_out) p.lens_out[b] = len + p.q;
+            if (first && p.lens_out) p.lens_out[b] = len + n;
+        } else if (first && p.lens_out) {
+            p.lens_out[b] = len;  // n == 0
         }
     }
     pdl_trigger();
@@ -55,6 +59,35 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
 }  // namespace kvd
 
 using namespace kvd;
+
+namespace kvd {
+// Shared by kvd_kv_append and the prefill: arguments already validated.
+kvd_status launch_append(const kvd_cache* cache, int32_t batch, int32_t q, const void* k_new,
+                         const void* v_new, const int32_t* lens_in, const int32_t* counts,
+                         int32_t* lens_out, uint32_t flags, int32_t* dev_err,
+                         cudaStream_t stream) {
+    AppendParams p;
+    p.k = static_cast<uint8_t*>(cache->k);
+    p.v = static_cast<uint8_t*>(cache->v);
+    p.sb = cache->stride_b * 2;
+    p.sh = cache->stride_h * 2;
+    p.st = cache->stride_t * 2;
+    p.k_new = static_cast<const uint8_t*>(k_new);
+    p.v_new = static_cast<const uint8_t*>(v_new);
+    p.lens_in = lens_in;
+    p.counts = counts;
+    p.lens_out = lens_out;
+    p.dev_err = dev_err;
+    p.capacity = cache->capacity;
+    p.heads = cache->n_kv_heads;
+    p.q = q;
+    p.chunks = (int64_t)batch * cache->n_kv_heads * q * 8;
+    const int64_t blocks = (2 * p.chunks + 255) / 256;
+    if (blocks > 0x7fffffff) return KVD_ERR_UNSUPPORTED;
+    return launch(kv_append_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                  (flags & KVD_FLAG_PDL) != 0, p);
+}
+}  // namespace kvd
 
 extern "C" kvd_status kvd_kv_append(kvd_dtype dtype, const kvd_cache* cache, int32_t batch,
                                     int32_t q, const void* k_new, const void* v_new,
@@ -67,23 +100,6 @@ extern "C" kvd_status kvd_kv_append(kvd_dtype dtype, const kvd_cache* cache, int
     if (!k_new || !v_new || !lens_in || !aligned16(k_new) || !aligned16(v_new))
         return KVD_ERR_INVALID_ARG;
     if (lens_out && lens_out == lens_in) return KVD_ERR_INVALID_ARG;
-    AppendParams p;
-    p.k = static_cast<uint8_t*>(cache->k);
-    p.v = static_cast<uint8_t*>(cache->v);
-    p.sb = cache->stride_b * 2;
-    p.sh = cache->stride_h * 2;
-    p.st = cache->stride_t * 2;
-    p.k_new = static_cast<const uint8_t*>(k_new);
-    p.v_new = static_cast<const uint8_t*>(v_new);
-    p.lens_in = lens_in;
-    p.lens_out = lens_out;
-    p.dev_err = dev_err;
-    p.capacity = cache->capacity;
-    p.heads = cache->n_kv_heads;
-    p.q = q;
-    p.chunks = (int64_t)batch * cache->n_kv_heads * q * 8;
-    const int64_t blocks = (2 * p.chunks + 255) / 256;
-    if (blocks > 0x7fffffff) return KVD_ERR_UNSUPPORTED;
-    return launch(kv_append_kernel, dim3((unsigned)blocks), dim3(256), 0,
-                  reinterpret_cast<cudaStream_t>(stream), (flags & KVD_FLAG_PDL) != 0, p);
+    return launch_append(cache, batch, q, k_new, v_new, lens_in, nullptr, lens_out, flags,
+                         dev_err, reinterpret_cast<cudaStream_t>(stream));
 }

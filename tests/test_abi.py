@@ -30,7 +30,8 @@ def _declared():
 
 def test_header_declares_the_entry_points():
     want = {"kvd_kv_append", "kvd_decode_attn", "kvd_verify_attn", "kvd_greedy_accept",
-            "kvd_beam_reorder_kv", "kvd_workspace_size", "kvd_status_string", "kvd_version"}
+            "kvd_beam_reorder_kv", "kvd_workspace_size", "kvd_status_string", "kvd_version",
+            "kvd_prefill_attn"}
     assert want <= _declared()
 
 
@@ -136,3 +137,30 @@ def test_host_rejects_bad_shapes(lib):
     # empty batches are a no-op
     assert lib.kvd_decode_attn(0, 0, 20, None, ctypes.byref(c), None, 0, None, 1, 0.125, None,
                                None, 0, 0, None, None) == 0
+
+
+def test_prefill_host_rejects_bad_arguments(lib):
+    c = _fake_cache()
+    p = ctypes.c_void_p(0x30000)
+    lens = ctypes.c_void_p(0x40000)
+    # no prompt lengths
+    assert lib.kvd_prefill_attn(0, 1, 20, 16, p, ctypes.byref(c), p, p, None, None, None,
+                                0.125, p, 0, None, None) == 1
+    # query heads not a multiple of KV heads
+    assert lib.kvd_prefill_attn(0, 1, 30, 16, p, ctypes.byref(c), p, p, None, lens, None,
+                                0.125, p, 0, None, None) == 1
+    # lens_out aliasing lens_in, and a misaligned query pointer
+    assert lib.kvd_prefill_attn(0, 1, 20, 16, p, ctypes.byref(c), p, p, lens, lens, lens,
+                                0.125, p, 0, None, None) == 1
+    assert lib.kvd_prefill_attn(0, 1, 20, 16, ctypes.c_void_p(0x30008), ctypes.byref(c), p, p,
+                                None, lens, None, 0.125, p, 0, None, None) == 1
+    # a bad cache, a bad dtype, and the empty cases
+    bad = _fake_cache(head_dim=128)
+    assert lib.kvd_prefill_attn(0, 1, 20, 16, p, ctypes.byref(bad), p, p, None, lens, None,
+                                0.125, p, 0, None, None) == 2
+    assert lib.kvd_prefill_attn(7, 1, 20, 16, p, ctypes.byref(c), p, p, None, lens, None,
+                                0.125, p, 0, None, None) == 1
+    assert lib.kvd_prefill_attn(0, 0, 20, 16, None, ctypes.byref(c), None, None, None, None,
+                                None, 0.125, None, 0, None, None) == 0
+    assert lib.kvd_prefill_attn(0, 1, 20, 0, None, ctypes.byref(c), None, None, None, None,
+                                None, 0.125, None, 0, None, None) == 0

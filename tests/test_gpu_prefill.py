@@ -1,0 +1,111 @@
+"""Prefill on the GPU (kvd_prefill_attn) against the fp64 oracle.
+
+The prompt's K/V must land in the cache bit-exactly at lens_in + j; each prompt row j
+must match the oracle's causal attention at position lens_in + j (the oracle takes the
+prompt as a causal query block of plens[b] tokens over the appended cache); rows past a
+row's prompt length are zeros. Tolerance: max-abs 1e-2, rel-Frobenius 5e-3.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_attn_close, dev16, dev_i32, host16, new_err, require_gpu
+from workloads import gen_cache, gen_lens_uniform, gen_new_kv, gen_queries, make_rng
+
+pytestmark = pytest.mark.gpu
+D = 64
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def run_prefill(dtype, B, Hq, Hkv, cap, max_len, plens, lens_in=None, *, seed, flags=0):
+    import kv_cached_decode_gb300 as kvd
+
+    rng = make_rng(seed)
+    plens = np.asarray(plens, np.int32)
+    start = np.zeros(B, np.int32) if lens_in is None else np.asarray(lens_in, np.int32)
+    # cached prefix (NaN past it), the prompt's K/V and queries
+    K, V = gen_cache(rng, B, Hkv, cap, D, dtype, 0.125, lens=start)
+    kn, vn = gen_new_kv(rng, B, Hkv, max_len, D, dtype, 0.125)
+    q = gen_queries(rng, B, Hq, max_len, D, dtype, 0.125)
+    # expected cache and outputs
+    Kw, Vw = K.copy(), V.copy()
+    want = np.zeros((B, Hq, max_len, D))
+    ok = (start >= 0) & (plens >= 0) & (plens <= max_len) & (start + plens <= cap)
+    for b in range(B):
+        if not ok[b]:
+            continue
+        Kw[b, :, start[b]:start[b] + plens[b]] = kn[b, :, :plens[b]]
+        Vw[b, :, start[b]:start[b] + plens[b]] = vn[b, :, :plens[b]]
+        if plens[b] > 0:
+            w, err = oracle.attention(q[b:b + 1, :, :plens[b]], Kw[b:b + 1], Vw[b:b + 1], dtype,
+                                      lens=np.array([start[b] + plens[b]], np.int32),
+                                      causal=True)
+            assert not err
+            want[b, :, :plens[b]] = w[0]
+    Kd, Vd = dev16(K, dtype), dev16(V, dtype)
+    qd = dev16(q, dtype)
+    out = torch.full_like(qd, 3.0)
+    lens_out = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    e = new_err()
+    kvd.kvd_prefill_attn(qd, kvd.make_cache(Kd, Vd), dev16(kn, dtype), dev16(vn, dtype),
+                         dev_i32(plens), out, lens_in=None if lens_in is None else dev_i32(start),
+                         lens_out=lens_out, flags=flags, dev_err=e)
+    torch.cuda.synchronize()
+    want_lens = np.where(ok, start + plens, start)
+    return (host16(out), want, host16(Kd), host16(Vd), Kw, Vw, lens_out.cpu().numpy(),
+            want_lens, e.item(), ok)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_prefill_gqa_ragged(dtype):
+    # prompt lengths across 64-row tiles: full, one token, empty, a ragged tail
+    got, want, Kg, Vg, Kw, Vw, lo, wlo, e, ok = run_prefill(
+        dtype, 4, 9, 3, 256, 200, [200, 1, 0, 130], seed=800)
+    assert e == 0
+    assert np.array_equal(Kg, Kw) and np.array_equal(Vg, Vw) and np.array_equal(lo, wlo)
+    assert_attn_close(got, want, dtype, "prefill GQA")
+    assert np.all(got[2] == 0) and np.all(got[1][:, 1:] == 0) and np.all(got[3][:, 130:] == 0)
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_prefill_after_cached_prefix(flags):
+    # chunked prefill: prompts continue cached prefixes of 0, 50 and 100 positions
+    got, want, Kg, Vg, Kw, Vw, lo, wlo, e, ok = run_prefill(
+        "f16", 3, 4, 4, 192, 65, [64, 65, 37], [0, 50, 100], seed=801, flags=flags)
+    assert e == 0
+    assert np.array_equal(Kg, Kw) and np.array_equal(Vg, Vw) and np.array_equal(lo, wlo)
+    assert_attn_close(got, want, "f16", "prefill after a prefix")
+
+
+def test_prefill_whisper_initial_tokens():
+    # the first pass over the initial tokens of a Whisper-shaped decoder layer
+    got, want, Kg, Vg, Kw, Vw, lo, wlo, e, ok = run_prefill(
+        "f16", 1, 20, 20, 448, 4, [4], seed=802)
+    assert e == 0 and np.array_equal(Kg, Kw) and np.array_equal(lo, wlo)
+    assert_attn_close(got, want, "f16", "Whisper initial tokens")
+
+
+def test_prefill_long_prompts():
+    # prompts of 300..640 tokens over GQA heads: up to 10 query tiles per head
+    rng = make_rng(803)
+    plens = gen_lens_uniform(rng, 3, 300, 640)
+    got, want, Kg, Vg, Kw, Vw, lo, wlo, e, ok = run_prefill(
+        "bf16", 3, 6, 2, 704, 640, plens, seed=804)
+    assert e == 0 and np.array_equal(Kg, Kw) and np.array_equal(lo, wlo)
+    assert_attn_close(got, want, "bf16", "long prompts")
+
+
+def test_prefill_rejected_row_is_untouched():
+    # row 0 would run past the capacity: flagged, cache and length kept, output zeros
+    got, want, Kg, Vg, Kw, Vw, lo, wlo, e, ok = run_prefill(
+        "f16", 2, 2, 2, 128, 50, [50, 20], [100, 10], seed=805)
+    assert e == 16 and not ok[0] and ok[1]
+    assert np.array_equal(Kg, Kw) and np.array_equal(Vg, Vw) and np.array_equal(lo, wlo)
+    assert np.all(got[0] == 0)
+    assert_attn_close(got[1:], want[1:], "f16", "good row")
