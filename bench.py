@@ -757,6 +757,7 @@ def run_sweep(args):
                 torch.cuda.empty_cache()
     run_beam_step(torch, kvd, dev, stream, peak, flags)
     run_gqa_lm_step(torch, kvd, dev, stream, peak, flags)
+    run_prefill(torch, kvd, dev, stream, flags)
     run_tiny_layer(torch, kvd, dev, stream, flags)
     run_verify_ratio(torch, kvd, dev, stream, flags)
     return 0
@@ -865,6 +866,55 @@ def run_gqa_lm_step(torch, kvd, dev, stream, peak, flags):
                       "pct_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 1),
                       "pct_peak": round(100 * gbs / peak, 1),
                       "tokens_per_s": round(B / (t * 1e-3), 1)}), flush=True)
+
+
+def run_prefill(torch, kvd, dev, stream, flags):
+    """Prefill of the GQA decoder-LM prompts: 16 rows, 9 query heads on 3 KV heads, bf16,
+    prompt lengths uniform in [256, 2048] (the decode step's cache lengths), one layer per
+    call; 30 layers' caches in a graph. Reports tensor TFLOP/s of the causal attention
+    (Q.K^T and P.V over each prompt token's visible keys)."""
+    w = WORKLOADS["gqa_lm_step"]
+    NL, B, Hq, Hkv, cap = w["n_layers"], w["batch"], w["n_q_heads"], w["n_kv_heads"], w["capacity"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4040)
+    bf = torch.bfloat16
+    plens_np = gen_lens_uniform(make_rng(seed_for("gqa_lm_step", 0, 7)), B, w["len_lo"],
+                                w["len_hi"])
+    T = int(plens_np.max())
+    kv_tensors, caches = [], []
+    for _ in range(NL):
+        k = torch.empty(B, Hkv, cap, D, dtype=bf, device=dev)
+        v = torch.empty(B, Hkv, cap, D, dtype=bf, device=dev)
+        kv_tensors.append((k, v))
+        caches.append(kvd.make_cache(k, v))
+    q = torch.empty(B, Hq, T, D, dtype=bf, device=dev).normal_(0, w["qkv_std"], generator=gen)
+    kn = torch.empty(2, B, Hkv, T, D, dtype=bf, device=dev).normal_(0, w["qkv_std"],
+                                                                    generator=gen)
+    out = torch.empty_like(q)
+    plens = torch.from_numpy(plens_np).to(dev)
+    lens_out = torch.zeros_like(plens)
+
+    def prefill():
+        for l in range(NL):
+            kvd.kvd_prefill_attn(q, caches[l], kn[0], kn[1], plens, out, lens_out=lens_out,
+                                 scale=w["scale"], flags=flags & kvd.KVD_FLAG_PDL)
+
+    t = time_graph(torch, capture(torch, prefill, stream), stream, 20) / NL  # ms per layer
+    pairs = int(np.sum(plens_np.astype(np.int64) * (plens_np.astype(np.int64) + 1) // 2))
+    flops = 4 * D * Hq * pairs  # two products, 2 flops per multiply-add
+    tflops = flops / (t * 1e-3) / 1e12
+    peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        pass
+    print(json.dumps({"sweep": "prefill", "layers": NL, "batch": B, "heads": f"{Hq}/{Hkv}",
+                      "mean_prompt": round(float(plens_np.mean()), 1), "us_per_layer":
+                      round(t * 1e3, 2), "tflops": round(tflops, 1),
+                      "frac_of_bf16_peak": None if peak is None else round(tflops / peak, 4),
+                      "tokens_per_s": round(float(plens_np.sum()) / (t * 1e-3), 1)}),
+          flush=True)
 
 
 def run_tiny_layer(torch, kvd, dev, stream, flags):
