@@ -71,6 +71,8 @@ def _load():
             lib.kvo_greedy_accept.restype = ctypes.c_uint
             lib.kvo_beam_reorder.argtypes = [I, I, I, I, I, I, I, P, P, P, L, L, L]
             lib.kvo_beam_reorder.restype = ctypes.c_uint
+            lib.kvo_rope.argtypes = [I, I, I, I, I, P, P, ctypes.c_double, P]
+            lib.kvo_rope.restype = None
             _lib = lib
     return _lib
 
@@ -184,3 +186,17 @@ def beam_reorder(cache, parent, beam: int, length: int, dtype: str):
     m = lib.kvo_beam_reorder(DTYPE_CODE[dtype], R, beam, H, cap, D, int(length),
                              _ptr(parent), _ptr(cache), _ptr(dst), sb, sh, st)
     return dst, _errs(m)
+
+
+def rope(x, dtype: str, pos0=None, base: float = 10000.0):
+    """Rotary encoding of ``x [B,H,n,D]`` (fp16/bf16 bits, or float64 with dtype "f64"),
+    token j of row b at position ``pos0[b] + j``. Returns float64, same shape."""
+    lib = _load()
+    _check_storage(x, dtype)
+    B, H, n, D = x.shape
+    x = np.ascontiguousarray(x)
+    p0 = None if pos0 is None else np.ascontiguousarray(pos0, dtype=np.int32)
+    y = np.empty(x.shape, dtype=np.float64)
+    code = {"f16": 0, "bf16": 1, "f64": 2}[dtype]
+    lib.kvo_rope(code, B, H, n, D, _ptr(x), _ptr(p0), float(base), _ptr(y))
+    return y

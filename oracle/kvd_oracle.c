@@ -298,3 +298,34 @@ unsigned kvo_beam_reorder(int dtype, int rows, int beam, int heads, int capacity
     }
     return err;
 }
+
+/* ---- NEXT-3: rotary position encoding at absolute positions -----------------------
+ *
+ * [N] "nanoVLM における KV キャッシュ実装" (the LanguageModel passes start_pos so that the
+ * rotary position encoding of new tokens matches their absolute position in the
+ * sequence). The page gives no formula; this is the usual rotary encoding in its
+ * rotate-half form, with theta_i = base^(-2i/D) and a = pos * theta_i for i < D/2:
+ *   y[i]       = x[i] cos a - x[i + D/2] sin a
+ *   y[i + D/2] = x[i + D/2] cos a + x[i] sin a
+ * x: [batch, heads, n, head_dim], contiguous; token j of row b is at pos0[b] + j
+ * (pos0 NULL: 0). y: double, same shape. head_dim must be even.
+ */
+void kvo_rope(int dtype, int batch, int heads, int n, int head_dim, const void *x,
+              const int32_t *pos0, double base, double *y)
+{
+    int half = head_dim / 2;
+    for (int b = 0; b < batch; ++b)
+        for (int h = 0; h < heads; ++h)
+            for (int j = 0; j < n; ++j) {
+                double pos = (double)((pos0 ? pos0[b] : 0) + j);
+                int64_t row = (((int64_t)b * heads + h) * n + j) * head_dim;
+                for (int i = 0; i < half; ++i) {
+                    double theta = pow(base, -2.0 * i / head_dim);
+                    double a = pos * theta;
+                    double x0 = load(dtype, x, row + i);
+                    double x1 = load(dtype, x, row + i + half);
+                    y[row + i] = x0 * cos(a) - x1 * sin(a);
+                    y[row + i + half] = x1 * cos(a) + x0 * sin(a);
+                }
+            }
+}

@@ -19,6 +19,7 @@ ATT = "tests/test_oracle_attention.py"
 ACC = "tests/test_oracle_accept_beam.py"
 APP = "tests/test_oracle_formats_append.py"
 TINY = "tests/test_oracle_tiny_model.py"
+ROPE = "tests/test_oracle_rope.py"
 
 MUTANTS = [
     ("causal limit off by one", "int limit = causal ? len - nq + 1 + i : len;",
@@ -52,6 +53,14 @@ MUTANTS = [
      "mag = ldexp((double)(1024 + frac), expo - 24);", [APP]),
     ("bfloat16 subnormal scale wrong", "mag = ldexp((double)frac, -133);",
      "mag = ldexp((double)frac, -134);", [APP]),
+    ("rotary pairs taken as adjacent dims", "double x1 = load(dtype, x, row + i + half);",
+     "double x1 = load(dtype, x, row + (i ^ 1));", [ROPE]),
+    ("rotary frequency exponent halved", "double theta = pow(base, -2.0 * i / head_dim);",
+     "double theta = pow(base, -1.0 * i / head_dim);", [ROPE]),
+    ("rotary sine sign flipped", "y[row + i] = x0 * cos(a) - x1 * sin(a);",
+     "y[row + i] = x0 * cos(a) + x1 * sin(a);", [ROPE]),
+    ("rotary position not offset by the start", "double pos = (double)((pos0 ? pos0[b] : 0) + j);",
+     "double pos = (double)j;", [ROPE]),
 ]
 
 
