@@ -857,6 +857,16 @@ def run_gqa_lm_step(torch, kvd, dev, stream, peak, flags):
                                 flags=flags, append=(kn[l, 0], kn[l, 1], lens_out))
 
     t = time_graph(torch, capture(torch, step, stream), stream, 100)
+
+    # the same step with the rotary encoding of q and the new keys at their absolute
+    # positions (one more launch per layer; timing only: replays rotate again)
+    def step_rope():
+        for l in range(NL):
+            kvd.kvd_rope(q[l], kn[l, 0], lens_in, flags=flags & kvd.KVD_FLAG_PDL)
+            kvd.kvd_decode_attn(q[l], caches[l], out[l], ws, lens=lens_in, scale=w["scale"],
+                                flags=flags, append=(kn[l, 0], kn[l, 1], lens_out))
+
+    t_rope = time_graph(torch, capture(torch, step_rope, stream), stream, 100)
     kv_bytes = 2 * Hkv * int(np.sum(lens_np.astype(np.int64) + 1)) * D * 2
     step_bytes = NL * (kv_bytes + 2 * B * Hq * D * 2 + append_bytes(B, Hkv, 1))
     gbs = step_bytes / (t * 1e-3) / 1e9
@@ -865,7 +875,9 @@ def run_gqa_lm_step(torch, kvd, dev, stream, peak, flags):
                       "us_per_layer": round(t * 1e3 / NL, 3), "gbs": round(gbs, 1),
                       "pct_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 1),
                       "pct_peak": round(100 * gbs / peak, 1),
-                      "tokens_per_s": round(B / (t * 1e-3), 1)}), flush=True)
+                      "tokens_per_s": round(B / (t * 1e-3), 1),
+                      "with_rope_step_us": round(t_rope * 1e3, 2),
+                      "with_rope_us_per_layer": round(t_rope * 1e3 / NL, 3)}), flush=True)
 
 
 def run_prefill(torch, kvd, dev, stream, flags):

@@ -272,6 +272,26 @@ kvd_status kvd_prefill_attn(kvd_dtype dtype, int32_t batch, int32_t n_q_heads, i
                             int32_t *dev_err, kvd_stream_t stream);
 
 /*
+ * kvd_rope -- rotary position encoding at absolute positions (in place).
+ *
+ * [N] "nanoVLM における KV キャッシュ実装" (start_pos keeps the rotary encoding of new
+ * tokens at their absolute positions). The pages give no formula; this is the usual
+ * rotate-half form: for i < 32, theta_i = base^(-i/32) and a = pos * theta_i,
+ *   y[i] = x[i] cos a - x[i+32] sin a,   y[i+32] = x[i+32] cos a + x[i] sin a,
+ * with token j of row b at pos0[b] + j. Run it on a step's queries and new keys (before
+ * kvd_kv_append, the fused append, or kvd_prefill_attn).
+ *
+ * q : device [batch, n_q_heads, n, 64] or NULL;  k : device [batch, n_k_heads, n, 64]
+ *     or NULL; contiguous, 16-byte aligned, rotated in place (one launch for both).
+ * pos0 : device int32 [batch] or NULL (0). base > 0 (10000 for the usual encoding).
+ * fp32 arithmetic (sin/cos with full argument reduction), rounded to the storage type.
+ * No device errors; dev_err is accepted for symmetry.
+ */
+kvd_status kvd_rope(kvd_dtype dtype, int32_t batch, int32_t n, void *q, int32_t n_q_heads,
+                    void *k, int32_t n_k_heads, const int32_t *pos0, float base, uint32_t flags,
+                    int32_t *dev_err, kvd_stream_t stream);
+
+/*
  * kvd_greedy_accept -- A6. Greedy verification of k draft tokens.
  *
  * [W] "Inference 抽象と KV キャッシュ" (GreedyDecoder: argmax at temperature 0);

@@ -88,6 +88,7 @@ def load_library(path: str = LIB_PATH):
             "kvd_verify_attn": [I32, I32, I32, I32, P, CP, P, I32, NP, I32, I32, F, P, P, SZ,
                                 U32, P, P],
             "kvd_prefill_attn": [I32, I32, I32, I32, P, CP, P, P, P, P, P, F, P, U32, P, P],
+            "kvd_rope": [I32, I32, I32, P, I32, P, I32, P, F, U32, P, P],
             "kvd_greedy_accept": [P, I32, I32, I32, P, P, P, P, P, P, SZ, U32, P, P],
             "kvd_beam_reorder_kv": [I32, CP, I32, I32, I32, P, P, I32, U32, P, P],
             "kvd_workspace_size": [I32, I32, I32, I32, I32, I32, I32, I32],
@@ -227,6 +228,18 @@ def kvd_prefill_attn(q, cache: Cache, k_new, v_new, plens, out, lens_in=None, le
                                            _ptr(lens_in), _ptr(plens), _ptr(lens_out), scale,
                                            _ptr(out), flags, _ptr(dev_err), _stream(stream)),
            "kvd_prefill_attn")
+
+
+def kvd_rope(q=None, k=None, pos0=None, base: float = 10000.0, flags: int = 0, dev_err=None,
+             stream=None):
+    """Rotary encoding, in place, of q [batch, n_q_heads, n, 64] and/or k [batch,
+    n_k_heads, n, 64]; token j of row b at position pos0[b] + j."""
+    ref = q if q is not None else k
+    B, _, n, _ = ref.shape
+    _check(load_library().kvd_rope(_dtype_code(ref), B, n, _ptr(q),
+                                   0 if q is None else q.shape[1], _ptr(k),
+                                   0 if k is None else k.shape[1], _ptr(pos0), base, flags,
+                                   _ptr(dev_err), _stream(stream)), "kvd_rope")
 
 
 def kvd_greedy_accept(logits, draft, n_accepted, next_token, workspace, n_min=None,

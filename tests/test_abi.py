@@ -31,7 +31,7 @@ def _declared():
 def test_header_declares_the_entry_points():
     want = {"kvd_kv_append", "kvd_decode_attn", "kvd_verify_attn", "kvd_greedy_accept",
             "kvd_beam_reorder_kv", "kvd_workspace_size", "kvd_status_string", "kvd_version",
-            "kvd_prefill_attn"}
+            "kvd_prefill_attn", "kvd_rope"}
     assert want <= _declared()
 
 
@@ -164,3 +164,13 @@ def test_prefill_host_rejects_bad_arguments(lib):
                                 None, 0.125, None, 0, None, None) == 0
     assert lib.kvd_prefill_attn(0, 1, 20, 0, None, ctypes.byref(c), None, None, None, None,
                                 None, 0.125, None, 0, None, None) == 0
+
+
+def test_rope_host_rejects_bad_arguments(lib):
+    p = ctypes.c_void_p(0x30000)
+    assert lib.kvd_rope(0, 1, 4, p, 4, p, 2, None, 0.0, 0, None, None) == 1      # base 0
+    assert lib.kvd_rope(0, 1, 4, ctypes.c_void_p(0x30002), 4, None, 0, None, 1e4, 0, None,
+                        None) == 1                                               # misaligned
+    assert lib.kvd_rope(0, 1, 4, p, 0, None, 0, None, 1e4, 0, None, None) == 1   # no heads
+    assert lib.kvd_rope(5, 1, 4, p, 4, None, 0, None, 1e4, 0, None, None) == 1   # dtype
+    assert lib.kvd_rope(0, 1, 4, None, 0, None, 0, None, 1e4, 0, None, None) == 0  # nothing
