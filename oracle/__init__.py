@@ -5,7 +5,7 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 runs it, and it imports nothing from the product library.
 
 ``kvd_oracle.c`` holds the definitions (append, attention, greedy accept, beam
-reorder); this module marshals numpy arrays into it. ``tiny_model.py`` builds a
+reorder, rotary encoding, logit filters with the beam-search step); this module marshals numpy arrays into it. ``tiny_model.py`` builds a
 small fp64 transformer on top of these functions for the end-to-end invariants
 (cached == recomputed, speculative == greedy, beam reorder == per-beam recompute).
 
@@ -73,6 +73,9 @@ def _load():
             lib.kvo_beam_reorder.restype = ctypes.c_uint
             lib.kvo_rope.argtypes = [I, I, I, I, I, P, P, ctypes.c_double, P]
             lib.kvo_rope.restype = None
+            lib.kvo_beam_select.argtypes = [I, I, I, P, P, P, I, P, I, I, I, P, P, P, P, P, P,
+                                            P, P]
+            lib.kvo_beam_select.restype = ctypes.c_uint
             _lib = lib
     return _lib
 
@@ -200,3 +203,36 @@ def rope(x, dtype: str, pos0=None, base: float = 10000.0):
     code = {"f16": 0, "bf16": 1, "f64": 2}[dtype]
     lib.kvo_rope(code, B, H, n, D, _ptr(x), _ptr(p0), float(base), _ptr(y))
     return y
+
+
+def beam_select(logits, beam: int, *, cum=None, suppress=(), blank=(), eot: int = 0,
+                first_step: bool = False, walk: bool = True):
+    """Logit filters and one beam-search step on fp32 ``logits [rows, vocab]``.
+
+    Returns a dict: ``row_token``/``row_logprob [rows, beam+1]`` (each row's beam+1 best
+    tokens after the filters), and with ``walk``: ``parent``/``token``/``new_cum
+    [rows]`` (kept continuations, per window best first), ``n_fin [windows]``,
+    ``fin_parent``/``fin_score [rows]``; plus ``errors``.
+    """
+    lib = _load()
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    rows, V = logits.shape
+    assert rows % beam == 0
+    kk = beam + 1
+    cum_a = None if cum is None else np.ascontiguousarray(cum, dtype=np.float32)
+    sup = np.ascontiguousarray(suppress, dtype=np.int32)
+    blk = np.ascontiguousarray(blank, dtype=np.int32)
+    r = {"row_token": np.empty((rows, kk), np.int32),
+         "row_logprob": np.empty((rows, kk), np.float64)}
+    if walk:
+        r.update(parent=np.empty(rows, np.int32), token=np.empty(rows, np.int32),
+                 new_cum=np.empty(rows, np.float64), n_fin=np.empty(rows // beam, np.int32),
+                 fin_parent=np.empty(rows, np.int32), fin_score=np.empty(rows, np.float64))
+    g = r.get
+    m = lib.kvo_beam_select(rows, beam, V, _ptr(logits), _ptr(cum_a), _ptr(sup), sup.size,
+                            _ptr(blk), blk.size, int(eot), int(bool(first_step)),
+                            _ptr(r["row_token"]), _ptr(r["row_logprob"]), _ptr(g("parent")),
+                            _ptr(g("token")), _ptr(g("new_cum")), _ptr(g("n_fin")),
+                            _ptr(g("fin_parent")), _ptr(g("fin_score")))
+    r["errors"] = _errs(m)
+    return r

@@ -329,3 +329,132 @@ void kvo_rope(int dtype, int batch, int heads, int n, int head_dim, const void *
                 }
             }
 }
+
+/* ---- logit filters and one beam-search step ---------------------------------------
+ *
+ * [W] "LogitFilter チェーン": SuppressBlank sets the logits of the blank (space) ids and
+ * of EOT to -inf, at the first sampling position only; SuppressTokens sets the listed
+ * ids to -inf at every position. [W] "Inference 抽象と KV キャッシュ"
+ * (BeamSearchDecoder.update), for each window of `beam` rows:
+ *   1. per beam row, the beam+1 tokens of highest log-probability (log-softmax of the
+ *      filtered logits),
+ *   2. every continuation (row j, token t) scores cum[j] + logprob_j(t),
+ *   3. going from the highest score down, EOT continuations are collected as finished
+ *      and the others kept, until `beam` are kept,
+ *   4. the kept continuations' rows are the parents the caches are reordered by.
+ *
+ * Readings where the page is silent: a NaN logit or a NaN cum counts as -inf and sets
+ * the NaN bit; tokens of a row rank by logit, ties to the lower id; continuations of
+ * equal score keep the order (row, then rank in the row); a row whose filtered logits
+ * are all -inf has every log-probability -inf; a suppressed or blank id outside
+ * [0, vocab) is skipped and sets the bad-token bit; the EOT continuations collected are
+ * those ranked above the last kept one.
+ *
+ * logits: fp32 [rows, vocab], rows = windows * beam. cum: fp32 [rows] or NULL (zeros).
+ * Outputs, each optional (NULL):
+ *   row_token, row_logprob [rows, beam+1]: step 1, best first;
+ *   parent (absolute row), token, new_cum [rows]: kept continuation s of window w at
+ *   w*beam + s, best first;
+ *   n_fin [windows]; fin_parent, fin_score [rows]: finished continuation f of window w
+ *   at w*beam + f, best first; slots past n_fin[w] hold -1 and -inf.
+ */
+unsigned kvo_beam_select(int rows, int beam, int vocab, const float *logits, const float *cum,
+                         const int32_t *suppress, int n_suppress, const int32_t *blank,
+                         int n_blank, int eot, int first_step, int32_t *row_token,
+                         double *row_logprob, int32_t *parent, int32_t *token, double *new_cum,
+                         int32_t *n_fin, int32_t *fin_parent, double *fin_score)
+{
+    unsigned err = 0;
+    const int kk = beam + 1;
+    const int windows = rows / beam;
+    double *x = malloc(sizeof(double) * (size_t)vocab);
+    char *used = malloc((size_t)vocab);
+    double *score = malloc(sizeof(double) * (size_t)beam * kk);
+    int *tok = malloc(sizeof(int) * (size_t)beam * kk);
+    char *taken = malloc((size_t)beam * kk);
+    for (int w = 0; w < windows; ++w) {
+        for (int j = 0; j < beam; ++j) {
+            const int r = w * beam + j;
+            /* the filters */
+            for (int v = 0; v < vocab; ++v) {
+                x[v] = logits[(int64_t)r * vocab + v];
+                if (isnan(x[v])) {
+                    err |= KVO_ERR_NAN;
+                    x[v] = -INFINITY;
+                }
+            }
+            for (int i = 0; i < n_suppress; ++i) {
+                if (suppress[i] < 0 || suppress[i] >= vocab) err |= KVO_ERR_BAD_TOKEN;
+                else x[suppress[i]] = -INFINITY;
+            }
+            if (first_step) {
+                for (int i = 0; i < n_blank; ++i) {
+                    if (blank[i] < 0 || blank[i] >= vocab) err |= KVO_ERR_BAD_TOKEN;
+                    else x[blank[i]] = -INFINITY;
+                }
+                x[eot] = -INFINITY;
+            }
+            /* log-softmax: logprob(v) = x[v] - log(sum_u exp(x[u])) */
+            double mx = -INFINITY;
+            for (int v = 0; v < vocab; ++v)
+                if (x[v] > mx) mx = x[v];
+            double lse = -INFINITY;
+            if (mx > -INFINITY) {
+                double sum = 0.0;
+                for (int v = 0; v < vocab; ++v) sum += exp(x[v] - mx);
+                lse = mx + log(sum);
+            }
+            /* step 1: the beam+1 best tokens, by logit, ties to the lower id */
+            double c = cum ? (double)cum[r] : 0.0;
+            if (isnan(c)) {
+                err |= KVO_ERR_NAN;
+                c = -INFINITY;
+            }
+            memset(used, 0, (size_t)vocab);
+            for (int k = 0; k < kk; ++k) {
+                int best = -1;
+                for (int v = 0; v < vocab; ++v)
+                    if (!used[v] && (best < 0 || x[v] > x[best])) best = v;
+                used[best] = 1;
+                const double lp = mx > -INFINITY ? x[best] - lse : -INFINITY;
+                if (row_token) row_token[(int64_t)r * kk + k] = best;
+                if (row_logprob) row_logprob[(int64_t)r * kk + k] = lp;
+                /* step 2: the continuation's score */
+                score[j * kk + k] = c + lp;
+                tok[j * kk + k] = best;
+            }
+        }
+        if (!parent) continue;
+        /* step 3: walk the continuations from the highest score down */
+        int kept = 0, fin = 0;
+        memset(taken, 0, (size_t)beam * kk);
+        while (kept < beam) {
+            int best = -1;
+            for (int cnd = 0; cnd < beam * kk; ++cnd)
+                if (!taken[cnd] && (best < 0 || score[cnd] > score[best])) best = cnd;
+            taken[best] = 1;
+            const int src = w * beam + best / kk;
+            if (tok[best] == eot) {
+                fin_parent[w * beam + fin] = src;
+                fin_score[w * beam + fin] = score[best];
+                ++fin;
+            } else {
+                parent[w * beam + kept] = src;
+                token[w * beam + kept] = tok[best];
+                new_cum[w * beam + kept] = score[best];
+                ++kept;
+            }
+        }
+        n_fin[w] = fin;
+        for (int f = fin; f < beam; ++f) {
+            fin_parent[w * beam + f] = -1;
+            fin_score[w * beam + f] = -INFINITY;
+        }
+    }
+    free(x);
+    free(used);
+    free(score);
+    free(tok);
+    free(taken);
+    return err;
+}

@@ -20,6 +20,7 @@ ACC = "tests/test_oracle_accept_beam.py"
 APP = "tests/test_oracle_formats_append.py"
 TINY = "tests/test_oracle_tiny_model.py"
 ROPE = "tests/test_oracle_rope.py"
+SEL = "tests/test_oracle_beam_select.py"
 
 MUTANTS = [
     ("causal limit off by one", "int limit = causal ? len - nq + 1 + i : len;",
@@ -61,6 +62,19 @@ MUTANTS = [
      "y[row + i] = x0 * cos(a) + x1 * sin(a);", [ROPE]),
     ("rotary position not offset by the start", "double pos = (double)((pos0 ? pos0[b] : 0) + j);",
      "double pos = (double)j;", [ROPE]),
+    ("blank ids masked at every step", "            if (first_step) {\n                for (int i = 0; i < n_blank;",
+     "            if (1) {\n                for (int i = 0; i < n_blank;", [SEL]),
+    ("EOT not masked at the first step", "                x[eot] = -INFINITY;\n", "", [SEL]),
+    ("cumulative score dropped", "score[j * kk + k] = c + lp;", "score[j * kk + k] = lp;",
+     [SEL]),
+    ("EOT continuations kept as live beams", "if (tok[best] == eot) {", "if (0) {", [SEL]),
+    ("row tokens tie to the higher id", "(best < 0 || x[v] > x[best])) best = v;",
+     "(best < 0 || x[v] >= x[best])) best = v;", [SEL]),
+    ("log-softmax normaliser dropped", "lse = mx + log(sum);", "lse = mx;", [SEL]),
+    ("equal scores tie to the later beam", "score[cnd] > score[best])) best = cnd;",
+     "score[cnd] >= score[best])) best = cnd;", [SEL]),
+    ("suppression list ignored", "else x[suppress[i]] = -INFINITY;",
+     "else x[suppress[i]] = x[suppress[i]];", [SEL]),
 ]
 
 

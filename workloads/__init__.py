@@ -18,5 +18,6 @@ from .synth import (  # noqa: F401
     gen_lens_uniform,
     gen_accept_inputs,
     gen_parents,
+    gen_beam_select_inputs,
     seed_for,
 )

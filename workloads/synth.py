@@ -27,7 +27,12 @@ Shapes (head_dim 64 throughout):
 * beam search: 8 audio windows x beam 5 = 40 rows, 32 layers, 20 heads, fp16,
   capacity 448, parents uniform inside each window's block of 5 rows;
 * decode-attention sweep: batch {1,4,16,64} x length {128,512,2048,8192} x
-  heads {20/20, 20/4}.
+  heads {20/20, 20/4};
+* beam-search step selection: 8 audio windows x beam 5 = 40 rows of fp32 logits over
+  a 51865-id vocabulary, N(0, 2^2); in 30% of the rows the EOT logit is set near the
+  row's maximum (max + N(0, 0.5^2)) so that finished continuations occur; cumulative
+  log-probabilities -U(0, 20) per row; a synthetic suppression set of 88 distinct ids
+  and one blank id stand in for the tokenizer's lists (EOT is id 50257).
 
 Q, K and V are N(0, 1) / 8 (i.e. 1/sqrt(head_dim)); the score scale is 1/8.
 """
@@ -63,6 +68,10 @@ WORKLOADS = {
         n_layers=32, windows=8, beam=5, n_q_heads=20, n_kv_heads=20, head_dim=64,
         dtype="f16", capacity=448, cross_len=1500, lens=(32, 224, 440),
         qkv_std=0.125, scale=0.125,
+    ),
+    "beam_select": dict(
+        windows=8, beam=5, vocab=51865, logit_std=2.0, p_eot=0.3, eot=50257,
+        n_suppress=88, blank=(220,), cum_range=(0.0, 20.0),
     ),
     "decode_sweep": dict(
         batches=(1, 4, 16, 64), lens=(128, 512, 2048, 8192),
@@ -156,3 +165,30 @@ def gen_parents(rng, windows: int, beam: int) -> np.ndarray:
     """Beam parents ``[windows*beam]`` int32, uniform inside each window's block."""
     base = np.repeat(np.arange(windows) * beam, beam)
     return (base + rng.integers(0, beam, size=windows * beam)).astype(np.int32)
+
+
+def gen_beam_select_inputs(rng, windows: int, beam: int, vocab: int, *, logit_std: float = 2.0,
+                           p_eot: float = 0.3, eot: int = 50257, n_suppress: int = 88,
+                           cum_range=(0.0, 20.0)):
+    """Inputs of one beam-search selection step.
+
+    Returns ``(logits [windows*beam, vocab] fp32, cum [windows*beam] fp32,
+    suppress [n_suppress] int32)``. Logits are N(0, logit_std^2); with probability
+    ``p_eot`` a row's EOT logit is replaced by the row's maximum plus N(0, 0.5^2).
+    ``cum`` is -U(cum_range). ``suppress`` holds distinct ids drawn uniformly from the
+    vocabulary without EOT.
+    """
+    rows = windows * beam
+    logits = (rng.standard_normal(size=(rows, vocab)) * logit_std).astype(np.float32)
+    hit = rng.random(size=rows) < p_eot
+    bump = (logits.max(axis=1) + rng.standard_normal(size=rows) * 0.5).astype(np.float32)
+    if 0 <= eot < vocab:
+        logits[hit, eot] = bump[hit]
+    cum = (-rng.uniform(cum_range[0], cum_range[1], size=rows)).astype(np.float32)
+    pool = np.array([v for v in range(vocab) if v != eot]) if vocab < 4096 else None
+    if pool is None:
+        sup = rng.choice(vocab, size=n_suppress + 1, replace=False)
+        sup = sup[sup != eot][:n_suppress]
+    else:
+        sup = rng.choice(pool, size=min(n_suppress, pool.size), replace=False)
+    return logits, cum, np.sort(sup).astype(np.int32)
