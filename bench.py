@@ -39,8 +39,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from workloads import (WORKLOADS, gen_accept_inputs, gen_cache, gen_lens_uniform,  # noqa: E402
-                       gen_new_kv, gen_parents, gen_queries, make_rng, seed_for)
+from workloads import (WORKLOADS, gen_accept_inputs, gen_beam_select_inputs,  # noqa: E402
+                       gen_cache, gen_lens_uniform, gen_new_kv, gen_parents, gen_queries,
+                       make_rng, seed_for)
 
 METRIC = "decode-attn KV-read GB/s & % of 8 TB/s HBM; verified tokens/s per layer-step"
 NOMINAL_HBM_GBS = 8000.0
@@ -756,6 +757,7 @@ def run_sweep(args):
                 del pool, caches, g
                 torch.cuda.empty_cache()
     run_beam_step(torch, kvd, dev, stream, peak, flags)
+    run_beam_select(torch, kvd, dev, stream, peak, flags)
     run_gqa_lm_step(torch, kvd, dev, stream, peak, flags)
     run_prefill(torch, kvd, dev, stream, flags)
     run_tiny_layer(torch, kvd, dev, stream, flags)
@@ -825,6 +827,52 @@ def run_beam_step(torch, kvd, dev, stream, peak, flags):
                           "step_gbs": round(step_bytes / (t_step * 1e-3) / 1e9, 1),
                           "tokens_per_s": round(R / (t_step * 1e-3), 1),
                           "moved_rows": moved, "source_rows": srcs}), flush=True)
+
+
+def run_beam_select(torch, kvd, dev, stream, peak, flags):
+    """Logit filters + beam-search selection over fp32 logits of 51865 ids: the beam
+    workload (8 windows x beam 5 = 40 rows, 8.3 MB, suppression list of 88 ids) and
+    greedy mode (beam 1, no walk) on 1 and 16 rows. The graph cycles through distinct
+    copies of the logits holding more than twice the L2, so every launch reads HBM."""
+    w = WORKLOADS["beam_select"]
+    V, eot = w["vocab"], w["eot"]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    i32 = dict(dtype=torch.int32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    for kind, W, beam in (("beam", w["windows"], w["beam"]), ("greedy", 1, 1), ("greedy", 16, 1)):
+        rows, K = W * beam, beam + 1
+        rng = make_rng(seed_for("beam_select", salt=rows))
+        x, cum, sup = gen_beam_select_inputs(rng, W, beam, V, eot=eot,
+                                             n_suppress=w["n_suppress"])
+        one = rows * V * 4
+        n = max(1, min(2048, 2 * l2 // one + 1))
+        pool = torch.from_numpy(x).to(dev).unsqueeze(0).repeat(n, 1, 1)
+        cum_d = torch.from_numpy(cum).to(dev)
+        sup_d = torch.from_numpy(sup).to(dev)
+        out = {"row_token": torch.empty(rows, K, **i32), "row_logprob": torch.empty(rows, K, **f32)}
+        if kind == "beam":
+            out.update(parent=torch.empty(rows, **i32), token=torch.empty(rows, **i32),
+                       new_cum=torch.empty(rows, **f32), n_finished=torch.empty(W, **i32),
+                       fin_parent=torch.empty(rows, **i32), fin_score=torch.empty(rows, **f32))
+
+        def fn():
+            for i in range(n):
+                kvd.kvd_beam_select(pool[i], beam, cum=cum_d if kind == "beam" else None,
+                                    suppress=sup_d, eot=eot, flags=flags, **out)
+
+        g = capture(torch, fn, stream)
+        t = time_graph(torch, g, stream, max(3, int(4e-3 / (n * 3e-6)))) / n  # ms per launch
+        # algorithmic bytes: the logits, cum and the suppression list read once; outputs
+        nbytes = one + sup.size * 4 + (rows * 4 if kind == "beam" else 0) + rows * K * 8
+        if kind == "beam":
+            nbytes += rows * 20 + W * 4
+        gbs = nbytes / (t * 1e-3) / 1e9
+        print(json.dumps({"sweep": "beam_select", "mode": kind, "rows": rows, "beam": beam,
+                          "vocab": V, "us": round(t * 1e3, 3), "bytes": nbytes,
+                          "gbs": round(gbs, 1), "pct_peak": round(100 * gbs / peak, 1),
+                          "distinct_buffers": n, "flags": flags}), flush=True)
+        del pool, g
+        torch.cuda.empty_cache()
 
 
 def run_gqa_lm_step(torch, kvd, dev, stream, peak, flags):

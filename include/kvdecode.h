@@ -100,6 +100,7 @@ enum {
 #define KVD_HEAD_DIM 64
 #define KVD_MAX_QLEN 16
 #define KVD_MAX_BEAM 8
+#define KVD_MAX_VOCAB 524288
 #define KVD_MAX_LAYERS_PER_CALL 64
 
 /* The new tokens' K/V for a fused append inside an attention call. */
@@ -348,6 +349,47 @@ kvd_status kvd_beam_reorder_kv(kvd_dtype dtype, const kvd_cache *layers, int32_t
                                int32_t rows, int32_t beam, const int32_t *parent,
                                const int32_t *lens, int32_t fixed_len, uint32_t flags,
                                int32_t *dev_err, kvd_stream_t stream);
+
+/*
+ * kvd_beam_select -- NEXT-2. Logit filters and one beam-search selection step.
+ *
+ * [W] "LogitFilter チェーン" (SuppressBlank: blank ids and EOT -> -inf at the first
+ * sampling position only; SuppressTokens: listed ids -> -inf at every position) and
+ * [W] "Inference 抽象と KV キャッシュ" (BeamSearchDecoder.update). For every window w
+ * of `beam` rows r = w*beam + j:
+ *   x_r      = logits[r] with the masks applied (a NaN counts as -inf)
+ *   lp_r(t)  = x_r[t] - log sum_u exp(x_r[u])          (all -inf if x_r is all -inf)
+ *   step 1   : the beam+1 ids of largest x_r (ties: lower id) -> row_token, row_logprob
+ *   step 2   : continuation (j, t) scores cum[r] + lp_r(t) (a NaN cum counts as -inf)
+ *   step 3   : from the highest score down (ties: lower j, then better rank in the row)
+ *              EOT continuations are finished, the others kept until `beam` are kept
+ *   outputs  : kept continuation s at w*beam + s -> parent (absolute row, the input of
+ *              kvd_beam_reorder_kv), token, new_cum; n_finished[w]; finished f at
+ *              w*beam + f -> fin_parent, fin_score (slots past n_finished: -1, -inf)
+ * fp32 arithmetic; every id and parent is decided by exact comparisons of fp32 values.
+ * Greedy decoding with the filters: beam = 1, parent = NULL, token = row_token[r][0].
+ *
+ * logits      : device fp32 [windows*beam, vocab], contiguous; beam+1 <= vocab <=
+ *               KVD_MAX_VOCAB; windows <= 2^24
+ * cum         : device fp32 [windows*beam] or NULL (zeros)
+ * suppress    : device int32 [n_suppress] (duplicates allowed); blank: device int32
+ *               [n_blank], read only when first_step != 0; eot in [0, vocab) (host int)
+ * row_token, row_logprob : device [windows*beam, beam+1] or NULL
+ * parent, token, new_cum, fin_parent, fin_score : device [windows*beam];
+ * n_finished  : device int32 [windows] -- all NULL (no walk) or all non-NULL
+ * beam in 1..8 (KVD_ERR_UNSUPPORTED otherwise). No workspace: one thread-block cluster
+ * per window merges through distributed shared memory.
+ * Device errors: a suppress/blank id outside [0, vocab) -> KVD_ERR_BAD_TOKEN (skipped);
+ * a NaN logit or cum -> KVD_ERR_NAN (outputs still follow the rules above); a bounded
+ * wait for a copy that gave up -> KVD_ERR_TIMEOUT (outputs undefined).
+ */
+kvd_status kvd_beam_select(const float *logits, int32_t windows, int32_t beam, int32_t vocab,
+                           const float *cum, const int32_t *suppress, int32_t n_suppress,
+                           const int32_t *blank, int32_t n_blank, int32_t eot,
+                           int32_t first_step, int32_t *row_token, float *row_logprob,
+                           int32_t *parent, int32_t *token, float *new_cum,
+                           int32_t *n_finished, int32_t *fin_parent, float *fin_score,
+                           uint32_t flags, int32_t *dev_err, kvd_stream_t stream);
 
 /*
  * kvd_workspace_size -- bytes of workspace a call needs (always includes the

@@ -9,7 +9,8 @@ or a call fails, an exception is raised.
 Tensors: caches are ``[batch, n_kv_heads, capacity, 64]`` fp16/bf16 CUDA tensors with
 the last axis contiguous; queries/outputs are contiguous ``[batch, n_q_heads, qlen, 64]``;
 lengths, drafts, parents and outputs of ``kvd_greedy_accept`` are int32 CUDA tensors;
-logits are contiguous fp32 ``[batch, k+1, vocab]``.
+logits are contiguous fp32 ``[batch, k+1, vocab]`` (``kvd_greedy_accept``) or
+``[windows*beam, vocab]`` (``kvd_beam_select``).
 """
 
 from __future__ import annotations
@@ -36,7 +37,7 @@ HEAD_DIM = 64
 
 EXPORTED = ("kvd_kv_append", "kvd_decode_attn", "kvd_verify_attn", "kvd_greedy_accept",
             "kvd_beam_reorder_kv", "kvd_workspace_size", "kvd_status_string", "kvd_version",
-            "kvd_decode_attn_noalloc")
+            "kvd_decode_attn_noalloc", "kvd_prefill_attn", "kvd_rope", "kvd_beam_select")
 
 
 class KvdError(RuntimeError):
@@ -91,6 +92,8 @@ def load_library(path: str = LIB_PATH):
             "kvd_rope": [I32, I32, I32, P, I32, P, I32, P, F, U32, P, P],
             "kvd_greedy_accept": [P, I32, I32, I32, P, P, P, P, P, P, SZ, U32, P, P],
             "kvd_beam_reorder_kv": [I32, CP, I32, I32, I32, P, P, I32, U32, P, P],
+            "kvd_beam_select": [P, I32, I32, I32, P, P, I32, P, I32, I32, I32, P, P, P, P, P,
+                                P, P, P, U32, P, P],
             "kvd_workspace_size": [I32, I32, I32, I32, I32, I32, I32, I32],
             "kvd_status_string": [I32],
             "kvd_version": [],
@@ -260,3 +263,22 @@ def kvd_beam_reorder_kv(caches, rows: int, beam: int, parent, lens=None, fixed_l
                                               _ptr(parent), _ptr(lens), fixed_len, flags,
                                               _ptr(dev_err), _stream(stream)),
            "kvd_beam_reorder_kv")
+
+
+def kvd_beam_select(logits, beam: int, *, cum=None, suppress=None, blank=None,
+                    eot: int = 0, first_step: bool = False, row_token=None, row_logprob=None,
+                    parent=None, token=None, new_cum=None, n_finished=None, fin_parent=None,
+                    fin_score=None, flags: int = 0, dev_err=None, stream=None):
+    """Logit filters + one beam-search selection step over ``logits [windows*beam, V]``.
+
+    ``suppress``/``blank`` are int32 CUDA tensors of ids; the walk outputs (``parent``
+    ... ``fin_score``) are all given or all None.
+    """
+    rows, V = logits.shape
+    n_sup = 0 if suppress is None else suppress.numel()
+    n_blank = 0 if blank is None else blank.numel()
+    _check(load_library().kvd_beam_select(
+        _ptr(logits), rows // beam, beam, V, _ptr(cum), _ptr(suppress), n_sup, _ptr(blank),
+        n_blank, eot, int(bool(first_step)), _ptr(row_token), _ptr(row_logprob), _ptr(parent),
+        _ptr(token), _ptr(new_cum), _ptr(n_finished), _ptr(fin_parent), _ptr(fin_score),
+        flags, _ptr(dev_err), _stream(stream)), "kvd_beam_select")

@@ -133,14 +133,6 @@ __global__ void __launch_bounds__(kBeamThreads)
 // once all have arrived each moving row's span is copied back out from its parent's
 // copy. Loads of a tile finish before any of its stores, as in the per-thread path, so
 // the reorder stays in place; tiles of one block touch disjoint rows' spans.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-        "[%3];" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
 __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
                  "r"(src), "r"(bytes)

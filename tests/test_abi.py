@@ -31,7 +31,7 @@ def _declared():
 def test_header_declares_the_entry_points():
     want = {"kvd_kv_append", "kvd_decode_attn", "kvd_verify_attn", "kvd_greedy_accept",
             "kvd_beam_reorder_kv", "kvd_workspace_size", "kvd_status_string", "kvd_version",
-            "kvd_prefill_attn", "kvd_rope"}
+            "kvd_prefill_attn", "kvd_rope", "kvd_beam_select"}
     assert want <= _declared()
 
 
@@ -174,3 +174,27 @@ def test_rope_host_rejects_bad_arguments(lib):
     assert lib.kvd_rope(0, 1, 4, p, 0, None, 0, None, 1e4, 0, None, None) == 1   # no heads
     assert lib.kvd_rope(5, 1, 4, p, 4, None, 0, None, 1e4, 0, None, None) == 1   # dtype
     assert lib.kvd_rope(0, 1, 4, None, 0, None, 0, None, 1e4, 0, None, None) == 0  # nothing
+
+
+def test_beam_select_host_rejects_bad_arguments(lib):
+    p = ctypes.c_void_p(0x40000)
+
+    def call(windows=1, beam=5, vocab=100, eot=99, n_sup=0, parent=p, row_token=None,
+             logits=p):
+        return lib.kvd_beam_select(logits, windows, beam, vocab, None, p, n_sup, None, 0, eot,
+                                   0, row_token, None, parent, p, p, p, p, p, 0, None, None)
+
+    assert call(beam=9) == 2                         # beam above 8
+    assert call(beam=0) == 2
+    assert call(vocab=5) == 1                        # vocab must exceed beam
+    assert call(eot=100) == 1 and call(eot=-1) == 1  # EOT outside the vocabulary
+    assert call(windows=-1) == 1
+    assert call(windows=0) == 0                      # nothing to do
+    assert call(windows=(1 << 24) + 1) == 2          # too many windows
+    assert call(parent=None) == 1                    # no output at all
+    assert call(vocab=524289, eot=0) == 2            # vocabulary too large
+    assert call(logits=ctypes.c_void_p(0x40002)) == 1  # logits not 4-byte aligned
+    assert lib.kvd_beam_select(p, 1, 5, 100, None, None, 3, None, 0, 99, 0, None, None, p, p,
+                               p, p, p, p, 0, None, None) == 1  # suppression list missing
+    assert lib.kvd_beam_select(p, 1, 5, 100, None, None, 0, None, 0, 99, 0, None, None, p,
+                               None, p, p, p, p, 0, None, None) == 1  # partial walk outputs
