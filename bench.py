@@ -717,6 +717,11 @@ def run_sweep(args):
     flags = kvd.KVD_FLAG_PDL if (args.pdl or args.early_kv) else 0
     if args.early_kv:
         flags |= kvd.KVD_FLAG_EARLY_KV
+    parts = {"beam_step": run_beam_step, "beam_select": run_beam_select,
+             "gqa_lm_step": run_gqa_lm_step}
+    if args.sweep_part in parts:
+        parts[args.sweep_part](torch, kvd, dev, stream, peak, flags)
+        return 0
     w = WORKLOADS["decode_sweep"]
     for (Hq, Hkv) in w["heads"]:
         for B in w["batches"]:
@@ -1058,6 +1063,8 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true",
                     help="decode-attention batch x length sweep, the beam step, the GQA-LM "
                          "step, the tiny layer and the verify/decode ratio (JSON lines)")
+    ap.add_argument("--sweep-part", choices=["beam_step", "beam_select", "gqa_lm_step"],
+                    default=None, help="with --sweep: run only this part")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu DRAM bytes per launch of the dominant kernel, if measured")
