@@ -883,7 +883,8 @@ def run_beam_select(torch, kvd, dev, stream, peak, flags):
 def run_gqa_lm_step(torch, kvd, dev, stream, peak, flags):
     """GQA decoder-LM step: 30 layers, 16 rows, 9 query heads on 3 KV heads, bf16,
     ragged lengths uniform in [256, 2048]; per layer one fused call appends each row's
-    new token and attends over its len + 1 positions."""
+    new token and attends over its len + 1 positions. Also timed: the same step with the
+    rotary encoding of q and the new keys, as a separate launch and inside the call."""
     w = WORKLOADS["gqa_lm_step"]
     NL, B, Hq, Hkv, cap = w["n_layers"], w["batch"], w["n_q_heads"], w["n_kv_heads"], w["capacity"]
     gen = torch.Generator(device=dev)
@@ -920,6 +921,15 @@ def run_gqa_lm_step(torch, kvd, dev, stream, peak, flags):
                                 flags=flags, append=(kn[l, 0], kn[l, 1], lens_out))
 
     t_rope = time_graph(torch, capture(torch, step_rope, stream), stream, 100)
+
+    # the rotation done inside the attention launch (queries at load, the new keys as
+    # they are appended): no extra launch
+    def step_fused_rope():
+        for l in range(NL):
+            kvd.kvd_decode_attn(q[l], caches[l], out[l], ws, lens=lens_in, scale=w["scale"],
+                                flags=flags, append=(kn[l, 0], kn[l, 1], lens_out, 10000.0))
+
+    t_fused = time_graph(torch, capture(torch, step_fused_rope, stream), stream, 100)
     kv_bytes = 2 * Hkv * int(np.sum(lens_np.astype(np.int64) + 1)) * D * 2
     step_bytes = NL * (kv_bytes + 2 * B * Hq * D * 2 + append_bytes(B, Hkv, 1))
     gbs = step_bytes / (t * 1e-3) / 1e9
@@ -930,7 +940,10 @@ def run_gqa_lm_step(torch, kvd, dev, stream, peak, flags):
                       "pct_peak": round(100 * gbs / peak, 1),
                       "tokens_per_s": round(B / (t * 1e-3), 1),
                       "with_rope_step_us": round(t_rope * 1e3, 2),
-                      "with_rope_us_per_layer": round(t_rope * 1e3 / NL, 3)}), flush=True)
+                      "with_rope_us_per_layer": round(t_rope * 1e3 / NL, 3),
+                      "with_fused_rope_step_us": round(t_fused * 1e3, 2),
+                      "with_fused_rope_us_per_layer": round(t_fused * 1e3 / NL, 3)}),
+          flush=True)
 
 
 def run_prefill(torch, kvd, dev, stream, flags):

@@ -108,6 +108,11 @@ typedef struct kvd_new_tokens {
     const void *k_new;  /* device [kv_batch, n_kv_heads, qlen, 64], contiguous */
     const void *v_new;  /* same shape                                         */
     int32_t *lens_out;  /* device [kv_batch] or NULL: receives lens + qlen     */
+    float rope_base;    /* 0: no rotation. > 0: rotary encoding (kvd_rope's    */
+                        /* definition, this base) of the call's queries and    */
+                        /* new keys at the new tokens' absolute positions      */
+                        /* lens[b] + j, inside the attention launch; the       */
+                        /* cache receives the rotated keys, q is not written   */
 } kvd_new_tokens;
 
 /* One layer's cache: K and V share the shape and strides. */

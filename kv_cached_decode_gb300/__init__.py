@@ -60,7 +60,7 @@ class NewTokens(ctypes.Structure):
     """Mirror of ``kvd_new_tokens``: new K/V appended inside an attention call."""
 
     _fields_ = [("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
-                ("lens_out", ctypes.c_void_p)]
+                ("lens_out", ctypes.c_void_p), ("rope_base", ctypes.c_float)]
 
 
 _lock = threading.Lock()
@@ -126,12 +126,14 @@ def _stream(stream):
 
 
 def _append_arg(append):
-    """``append`` is None or ``(k_new, v_new, lens_out_or_None)`` device tensors."""
+    """``append`` is None or ``(k_new, v_new, lens_out_or_None[, rope_base])``: device
+    tensors, and the rotary base (0 or absent: no rotation)."""
     if append is None:
         return None
-    k_new, v_new, lens_out = append
+    k_new, v_new, lens_out = append[:3]
+    rope_base = float(append[3]) if len(append) > 3 else 0.0
     return ctypes.byref(NewTokens(k_new.data_ptr(), v_new.data_ptr(),
-                                  None if lens_out is None else lens_out.data_ptr()))
+                                  None if lens_out is None else lens_out.data_ptr(), rope_base))
 
 
 def _check(status: int, call: str):

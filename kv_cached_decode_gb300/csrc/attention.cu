@@ -81,6 +81,8 @@ struct AttnParams {
     int32_t early;
     int32_t cluster;   // 1: the splits of a unit form one thread-block cluster
     int32_t append;    // 1: k_new/v_new are written at positions lens[b] .. lens[b]+qlen-1
+    int32_t rope;      // 1: rotary encoding of the queries and the appended keys
+    float rope_log2_base;
     const uint8_t* k_new;
     const uint8_t* v_new;
     int32_t* lens_out;
@@ -102,7 +104,8 @@ struct AttnParams {
 struct SmemLayout {
     uint32_t bar_off, red_off, mrg_off, misc_off, qoff_off, app_off, total;
 };
-// app_rows: appended rows staged for the fused append (qlen, or 0 without append).
+// app_rows: 256-byte units staged for the fused append: qlen (the K and V rows), plus
+// qlen more with rotary encoding (the cos/sin table, 32 float2 per token), else 0.
 __host__ __device__ inline SmemLayout smem_layout(int stages, int rmax, int merge_slots,
                                                   int app_rows) {
     SmemLayout L;
@@ -113,12 +116,23 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int rmax, int merg
     L.mrg_off = (L.bar_off + (stages + 1) * 8 + 15) & ~15u;
     L.misc_off = L.mrg_off + merge_slots * kSlot * 4;
     L.qoff_off = L.misc_off + 16;  // element offsets of the block's query rows in q / out
-    L.app_off = L.qoff_off + kMmaQueryBlock * 8;  // appended rows: K [app_rows][128 B], V
+    L.app_off = L.qoff_off + kMmaQueryBlock * 8;  // appended rows: K [qlen][128 B], V, table
     L.total = L.app_off + app_rows * 2 * kRowBytes + 1024;  // + slack to align the base
     return L;
 }
 __host__ __device__ inline int merge_slots(int cluster, int splits, int msub) {
     return cluster ? splits * msub : 0;
+}
+__host__ __device__ inline int app_units(int append, int rope, int qlen) {
+    return append ? qlen * (rope ? 2 : 1) : 0;
+}
+__host__ __device__ inline int app_units(const AttnParams& p) {
+    return app_units(p.append, p.rope, p.qlen);
+}
+// The rotary cos/sin table of the call's new tokens: [qlen][32] float2, token j at
+// position len - qlen + j (its absolute position), after the appended rows.
+__device__ __forceinline__ const float2* rope_table(const AttnParams& p, const uint8_t* app) {
+    return reinterpret_cast<const float2*>(app + p.qlen * 2 * kRowBytes);
 }
 
 struct CtaCtx {
@@ -185,9 +199,10 @@ __device__ __forceinline__ void store_out(const AttnParams& p, const int64_t* qo
 // start, and waits for the previous one (before all of this unless the call was made
 // with KVD_FLAG_EARLY_KV). Returns false if the length is out of range: flagged,
 // nothing written.
+template <bool ROPE>
 __device__ __forceinline__ bool prologue(const AttnParams& p, CtaCtx& c, uint8_t* smem,
-                                         uint64_t* bars, int64_t* qoff, const CUtensorMap* tmk,
-                                         const CUtensorMap* tmv) {
+                                         uint64_t* bars, int64_t* qoff, uint8_t* app,
+                                         const CUtensorMap* tmk, const CUtensorMap* tmv) {
     const int tid = threadIdx.x;
     if (!p.early) pdl_wait();
     setup_ctx(p, c);
@@ -231,6 +246,14 @@ __device__ __forceinline__ bool prologue(const AttnParams& p, CtaCtx& c, uint8_t
             prefetch_l2((ai & 1 ? p.v_new : p.k_new) + row * kRowBytes);
         }
     }
+    // The rotary table of the new tokens' positions (with KVD_FLAG_EARLY_KV, before the
+    // wait: it depends only on the length).
+    if (ROPE) {
+        float2* tab = const_cast<float2*>(rope_table(p, app));
+        const int pos0 = c.len - p.qlen;
+        for (int x = tid; x < p.qlen * 32; x += kThreads)
+            tab[x] = rope_cos_sin(pos0 + (x >> 5), x & 31, p.rope_log2_base);
+    }
     __syncthreads();
     if (p.cluster) cluster_arrive_relaxed();  // the first CTA's merge barrier is ready
     pdl_trigger();
@@ -267,6 +290,22 @@ __device__ __forceinline__ void stage_appended(const AttnParams& p, const CtaCtx
                    (is_v ? p.v_new : p.k_new) + src);
     }
 }
+// Rotary encoding of 8 pairs: dims i0..i0+7 in lo, i0+32..i0+39 in hi, rounded back to
+// the storage type (the same bits as the stand-alone rotation).
+template <typename T>
+__device__ __forceinline__ void rope_rotate8(uint4& lo, uint4& hi, const float2* tr, int i0) {
+    uint32_t* a = reinterpret_cast<uint32_t*>(&lo);
+    uint32_t* b = reinterpret_cast<uint32_t*>(&hi);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        float2 x = Half16<T>::to_f2(a[w]), y = Half16<T>::to_f2(b[w]);
+        rope_rotate(x.x, y.x, tr[i0 + 2 * w]);
+        rope_rotate(x.y, y.y, tr[i0 + 2 * w + 1]);
+        a[w] = Half16<T>::from_f2(x.x, x.y);
+        b[w] = Half16<T>::from_f2(y.x, y.y);
+    }
+}
+template <typename T, bool ROPE>
 __device__ __forceinline__ void inject_slab(const AttnParams& p, const CtaCtx& c, uint8_t* sK,
                                             uint8_t* sV, const uint8_t* app, int tile0,
                                             int slab0) {
@@ -276,16 +315,42 @@ __device__ __forceinline__ void inject_slab(const AttnParams& p, const CtaCtx& c
     cp_async_wait_all();
     __syncwarp();
     const int lane = threadIdx.x & 31;
-    for (int x = lane; x < n2; x += 32) {
-        const bool is_v = x >= n2 / 2;
-        const int y = is_v ? x - n2 / 2 : x;
-        const int t = r0 + (y >> 3), ch = y & 7;
-        const uint4 val = *reinterpret_cast<const uint4*>(
-            app + (is_v ? p.qlen * kRowBytes : 0) + (t - c.new0) * kRowBytes + ch * 16);
+    auto put = [&](bool is_v, int t, int ch, const uint4& val) {
         *reinterpret_cast<uint4*>((is_v ? sV : sK) + swz(t - tile0, ch)) = val;
         if (c.sub == 0)
             *reinterpret_cast<uint4*>((is_v ? p.vc : p.kc) + c.bk * p.sb + c.h * p.sh +
                                       (int64_t)t * p.st + ch * 16) = val;
+    };
+    if (ROPE) {
+        // per row: 4 K chunk pairs (ch, ch + 4), rotated at the token's position, then
+        // the 8 V chunks as they are
+        const float2* tab = rope_table(p, app);
+        const int rows = n2 / 16;
+        for (int x = lane; x < rows * 12; x += 32) {
+            const int t = r0 + x / 12, y = x % 12, j = t - c.new0;
+            if (y < 4) {
+                const uint8_t* kr = app + j * kRowBytes;
+                uint4 lo = *reinterpret_cast<const uint4*>(kr + y * 16);
+                uint4 hi = *reinterpret_cast<const uint4*>(kr + (y + 4) * 16);
+                rope_rotate8<T>(lo, hi, tab + j * 32, y * 8);
+                put(false, t, y, lo);
+                put(false, t, y + 4, hi);
+            } else {
+                const int ch = y - 4;
+                put(true, t, ch,
+                    *reinterpret_cast<const uint4*>(app + p.qlen * kRowBytes + j * kRowBytes +
+                                                    ch * 16));
+            }
+        }
+    } else {
+        for (int x = lane; x < n2; x += 32) {
+            const bool is_v = x >= n2 / 2;
+            const int y = is_v ? x - n2 / 2 : x;
+            const int t = r0 + (y >> 3), ch = y & 7;
+            put(is_v, t, ch,
+                *reinterpret_cast<const uint4*>(app + (is_v ? p.qlen * kRowBytes : 0) +
+                                                (t - c.new0) * kRowBytes + ch * 16));
+        }
     }
     fence_proxy_async();  // the stage is refilled by TMA later
     __syncwarp();
@@ -322,7 +387,7 @@ __device__ void abort_after_timeout(const AttnParams& p, const CtaCtx& c, uint64
 // The tile loop shared by both kernels. Tiles are taken two at a time (a round); warp w
 // works on tile 2r + w/4, positions (w%4)*16 .. +15, through slab(sK, sV, tile0, slab0).
 // Returns false after a timeout (already handled: the caller just returns).
-template <typename Slab>
+template <typename T, bool ROPE, typename Slab>
 __device__ __forceinline__ bool run_tiles(const AttnParams& p, const CtaCtx& c, uint8_t* smem,
                                           uint64_t* bars, float* mrg, uint8_t* app,
                                           const CUtensorMap* tmk, const CUtensorMap* tmv,
@@ -351,7 +416,7 @@ __device__ __forceinline__ bool run_tiles(const AttnParams& p, const CtaCtx& c, 
                 uint8_t* sK = smem + st * 2 * kTileBytes;
                 uint8_t* sV = sK + kTileBytes;
                 const int tile0 = c.t_begin + j * kTile;
-                if (p.append) inject_slab(p, c, sK, sV, app, tile0, slab0);
+                if (p.append) inject_slab<T, ROPE>(p, c, sK, sV, app, tile0, slab0);
                 slab(sK, sV, tile0, slab0);
             }
         }
@@ -587,7 +652,7 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
 }
 
 // ------------------------------------------------- one query vector per KV head (SIMT) --
-template <typename T>
+template <typename T, bool ROPE>
 __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: 4 blocks per SM
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
@@ -595,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: 4 blocks per
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     const SmemLayout L = smem_layout(p.stages, RM, merge_slots(p.cluster, p.splits, p.msub),
-                                     p.append ? p.qlen : 0);
+                                     app_units(p));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
     float* red = reinterpret_cast<float*>(smem + L.red_off);
     float* mrg = reinterpret_cast<float*>(smem + L.mrg_off);
@@ -605,13 +670,33 @@ __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: 4 blocks per
     const int grp = lane >> 3, c8 = lane & 7;
 
     CtaCtx c;
-    if (!prologue(p, c, smem, bars, qoff, &tmk, &tmv)) return;
+    if (!prologue<ROPE>(p, c, smem, bars, qoff, smem + L.app_off, &tmk, &tmv)) return;
 
     float qf[8];
     {
         const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + qoff[0] +
                                                         c8 * 8);
         unpack8<T>(u, qf);
+    }
+    if (ROPE) {
+        // the one query token sits at position len - 1; lane c8 ^ 4 holds the other half
+        // of its rotation pairs
+        const float2* tab = rope_table(p, smem + L.app_off);
+        const bool hi = c8 >= 4;
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            float y[2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const float other = __shfl_xor_sync(0xffffffffu, qf[e + t], 4);
+                float x0 = hi ? other : qf[e + t], x1 = hi ? qf[e + t] : other;
+                rope_rotate(x0, x1, tab[(c8 & 3) * 8 + e + t]);
+                y[t] = hi ? x1 : x0;
+            }
+            const float2 r = Half16<T>::to_f2(Half16<T>::from_f2(y[0], y[1]));
+            qf[e] = r.x;
+            qf[e + 1] = r.y;
+        }
     }
     float mrun = -INFINITY, lrun = 0.f, acc[8];
 #pragma unroll
@@ -659,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: 4 blocks per
             for (int e = 0; e < 8; ++e) acc[e] = fmaf(sc[jj], valid ? vf[e] : 0.f, acc[e]);
         }
     };
-    if (!run_tiles(p, c, smem, bars, mrg, smem + L.app_off, &tmk, &tmv, slab)) return;
+    if (!run_tiles<T, ROPE>(p, c, smem, bars, mrg, smem + L.app_off, &tmk, &tmv, slab)) return;
 
     // Merge the four 8-lane groups of each warp (they saw different positions).
 #pragma unroll
@@ -694,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: 4 blocks per
 // MINB: blocks per SM the register budget is cut for. 2 (no cut) is the default; 3 gives
 // more resident blocks, hence more splits, when a launch is limited by residency, at the
 // price of a few spilled registers.
-template <typename T, int MINB>
+template <typename T, int MINB, bool ROPE>
 __global__ void __launch_bounds__(kThreads, MINB)
     block_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
@@ -702,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     const SmemLayout L = smem_layout(p.stages, RM, merge_slots(p.cluster, p.splits, p.msub),
-                                     p.append ? p.qlen : 0);
+                                     app_units(p));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
     float* red = reinterpret_cast<float*>(smem + L.red_off);
     float* mrg = reinterpret_cast<float*>(smem + L.mrg_off);
@@ -713,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const int jm = lane >> 3, rr = lane & 7;         // ldmatrix matrix / row
 
     CtaCtx c;
-    if (!prologue(p, c, smem, bars, qoff, &tmk, &tmv)) return;
+    if (!prologue<ROPE>(p, c, smem, bars, qoff, smem + L.app_off, &tmk, &tmv)) return;
 
     // Q as m16n8k16 A fragments for the four 16-dim k-steps (rows >= mcount are 0).
     uint32_t qa[4][4];
@@ -728,6 +813,24 @@ __global__ void __launch_bounds__(kThreads, MINB)
         qa[kk][1] = rowB ? *reinterpret_cast<const uint32_t*>(qbase + offB + d0) : 0u;
         qa[kk][2] = rowA ? *reinterpret_cast<const uint32_t*>(qbase + offA + d0 + 8) : 0u;
         qa[kk][3] = rowB ? *reinterpret_cast<const uint32_t*>(qbase + offB + d0 + 8) : 0u;
+    }
+    if (ROPE) {
+        // query m is token m % qlen of the new tokens; k-steps kk and kk + 2 hold the two
+        // halves of the same rotation pairs in this lane
+        const float2* tab = rope_table(p, smem + L.app_off);
+        const int jA = (c.m0 + qr) % p.qlen, jB = (c.m0 + qr + 8) % p.qlen;
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = kk * 16 + qc + (e >= 2 ? 8 : 0);
+                const float2* tr = tab + ((e & 1) ? jB : jA) * 32;
+                float2 lo = Half16<T>::to_f2(qa[kk][e]), hi = Half16<T>::to_f2(qa[kk + 2][e]);
+                rope_rotate(lo.x, hi.x, tr[i]);
+                rope_rotate(lo.y, hi.y, tr[i + 1]);
+                qa[kk][e] = Half16<T>::from_f2(lo.x, lo.y);
+                qa[kk + 2][e] = Half16<T>::from_f2(hi.x, hi.y);
+            }
     }
     auto limit_of = [&](int r, bool live) -> int {
         if (!live) return 0;
@@ -815,7 +918,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
             Mma<T>::run(oacc[2 * np + 1], pa, v2, v3);
         }
     };
-    if (!run_tiles(p, c, smem, bars, mrg, smem + L.app_off, &tmk, &tmv, slab)) return;
+    if (!run_tiles<T, ROPE>(p, c, smem, bars, mrg, smem + L.app_off, &tmk, &tmv, slab)) return;
 
     lA += __shfl_xor_sync(0xffffffffu, lA, 1);
     lA += __shfl_xor_sync(0xffffffffu, lA, 2);
@@ -875,28 +978,33 @@ int prepare_kernel(size_t smem_bytes) {
 }
 
 // Kernel variants: the CUDA-core kernel, and the tensor-core kernel built for 2 or 3
-// resident blocks per SM.
-enum Variant { kSimt = 1, kMma = 2, kMma3 = 3 };
+// resident blocks per SM; the first two also with the rotary encoding compiled in (the
+// rotation code is kept out of the other builds, whose register budgets it would raise).
+enum Variant { kSimt = 1, kMma = 2, kMma3 = 3, kSimtRope = 4, kMmaRope = 5 };
 
 template <typename T>
 int prepare(int var) {
     const uint32_t mma_smem =
-        smem_layout(kMaxStages, 16, kMaxClusterSplits * kMmaQueryBlock, KVD_MAX_QLEN).total;
+        smem_layout(kMaxStages, 16, kMaxClusterSplits * kMmaQueryBlock, 2 * KVD_MAX_QLEN).total;
+    const uint32_t simt_smem =
+        smem_layout(kMaxStages, 1, kMaxClusterSplits, 2 * KVD_MAX_QLEN).total;
     switch (var) {
-    case kMma: return prepare_kernel<block_attn_kernel<T, 2>>(mma_smem);
-    case kMma3: return prepare_kernel<block_attn_kernel<T, 3>>(mma_smem);
-    default:
-        return prepare_kernel<decode_attn_kernel<T>>(
-            smem_layout(kMaxStages, 1, kMaxClusterSplits, KVD_MAX_QLEN).total);
+    case kMma: return prepare_kernel<block_attn_kernel<T, 2, false>>(mma_smem);
+    case kMma3: return prepare_kernel<block_attn_kernel<T, 3, false>>(mma_smem);
+    case kMmaRope: return prepare_kernel<block_attn_kernel<T, 2, true>>(mma_smem);
+    case kSimtRope: return prepare_kernel<decode_attn_kernel<T, true>>(simt_smem);
+    default: return prepare_kernel<decode_attn_kernel<T, false>>(simt_smem);
     }
 }
 
 template <typename T>
 const void* kernel_of(int var) {
     switch (var) {
-    case kMma: return reinterpret_cast<const void*>(block_attn_kernel<T, 2>);
-    case kMma3: return reinterpret_cast<const void*>(block_attn_kernel<T, 3>);
-    default: return reinterpret_cast<const void*>(decode_attn_kernel<T>);
+    case kMma: return reinterpret_cast<const void*>(block_attn_kernel<T, 2, false>);
+    case kMma3: return reinterpret_cast<const void*>(block_attn_kernel<T, 3, false>);
+    case kMmaRope: return reinterpret_cast<const void*>(block_attn_kernel<T, 2, true>);
+    case kSimtRope: return reinterpret_cast<const void*>(decode_attn_kernel<T, true>);
+    default: return reinterpret_cast<const void*>(decode_attn_kernel<T, false>);
     }
 }
 
@@ -904,17 +1012,26 @@ template <typename T>
 kvd_status launch_attn(int var, dim3 grid, cudaStream_t st, bool pdl, unsigned cl,
                        const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p) {
     const int slots = merge_slots(p.cluster, p.splits, p.msub);
-    const int app_rows = p.append ? p.qlen : 0;
-    if (var == kMma)
-        return launch_ex(block_attn_kernel<T, 2>, grid, dim3(kThreads),
-                         smem_layout(p.stages, 16, slots, app_rows).total, st, pdl, cl, mk, mv,
-                         p);
-    if (var == kMma3)
-        return launch_ex(block_attn_kernel<T, 3>, grid, dim3(kThreads),
-                         smem_layout(p.stages, 16, slots, app_rows).total, st, pdl, cl, mk, mv,
-                         p);
-    return launch_ex(decode_attn_kernel<T>, grid, dim3(kThreads),
-                     smem_layout(p.stages, 1, slots, app_rows).total, st, pdl, cl, mk, mv, p);
+    const int app_rows = app_units(p);
+    const uint32_t mma_smem = smem_layout(p.stages, 16, slots, app_rows).total;
+    const uint32_t simt_smem = smem_layout(p.stages, 1, slots, app_rows).total;
+    switch (var) {
+    case kMma:
+        return launch_ex(block_attn_kernel<T, 2, false>, grid, dim3(kThreads), mma_smem, st, pdl,
+                         cl, mk, mv, p);
+    case kMma3:
+        return launch_ex(block_attn_kernel<T, 3, false>, grid, dim3(kThreads), mma_smem, st, pdl,
+                         cl, mk, mv, p);
+    case kMmaRope:
+        return launch_ex(block_attn_kernel<T, 2, true>, grid, dim3(kThreads), mma_smem, st, pdl,
+                         cl, mk, mv, p);
+    case kSimtRope:
+        return launch_ex(decode_attn_kernel<T, true>, grid, dim3(kThreads), simt_smem, st, pdl,
+                         cl, mk, mv, p);
+    default:
+        return launch_ex(decode_attn_kernel<T, false>, grid, dim3(kThreads), simt_smem, st, pdl,
+                         cl, mk, mv, p);
+    }
 }
 
 size_t plan_smem(const AttnPlan& P, bool mma, int app_rows) {
@@ -1014,20 +1131,23 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
         if (!lens || !app->k_new || !app->v_new || !aligned16(app->k_new) ||
             !aligned16(app->v_new) || app->lens_out == lens)
             return KVD_ERR_INVALID_ARG;
+        if (!(app->rope_base >= 0.f) || !(app->rope_base < INFINITY)) return KVD_ERR_INVALID_ARG;
     }
+    const bool rope = app && app->rope_base > 0.f;
     if (!(scale == scale)) return KVD_ERR_INVALID_ARG;
     const int nsm = sm_count();
     if (nsm <= 0) return KVD_ERR_CUDA;
     const int len_bound = lens ? kv->capacity : fixed_len;
     const bool bf = dtype == KVD_BF16;
     const int group = n_q_heads / kv->n_kv_heads;
-    const int app_rows = app ? qlen : 0;
+    const int app_rows = app_units(app ? 1 : 0, rope ? 1 : 0, qlen);
     // Plan for one kernel variant; false if it cannot be prepared.
     auto plan_for = [&](int var, AttnPlan& out) -> bool {
         const int mc = bf ? prepare<__nv_bfloat16>(var) : prepare<__half>(var);
         if (mc <= 0) return false;
         const void* kern = bf ? kernel_of<__nv_bfloat16>(var) : kernel_of<__half>(var);
-        out = choose_plan(kern, var * 2 + (bf ? 1 : 0), var != kSimt, nsm, batch, n_q_heads,
+        out = choose_plan(kern, var * 2 + (bf ? 1 : 0), var != kSimt && var != kSimtRope, nsm,
+                          batch, n_q_heads,
                           kv->n_kv_heads, rows_per_kv, qlen, len_bound, mc, app_rows);
         return true;
     };
@@ -1039,10 +1159,12 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
         return (int64_t)Q.units <=
                resident(kern, var * 2 + (bf ? 1 : 0), plan_smem(Q, true, app_rows), 1, nsm);
     };
-    int var = (verify || (int64_t)rows_per_kv * group * qlen >= 2) ? kMma : kSimt;
+    // the builds with the rotation compiled in stand for kSimt and kMma when it is on
+    const int simt = rope ? kSimtRope : kSimt, mma = rope ? kMmaRope : kMma;
+    int var = (verify || (int64_t)rows_per_kv * group * qlen >= 2) ? mma : simt;
     AttnPlan P;
     if (!plan_for(var, P)) return KVD_ERR_CUDA;
-    if (var == kSimt && P.tiles_per_split <= 2) {
+    if (var == simt && P.tiles_per_split <= 2) {
         // Each block has a single round of tiles: then the time is the chain after the
         // dependency wait, and the tensor-core kernel's per-tile chain (ldmatrix + mma,
         // two shuffles) is shorter than the CUDA-core one (a shuffle tree per position).
@@ -1050,8 +1172,8 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
         // positions with the append. It has half the resident blocks per SM, so it is
         // taken only while its launch still fits in one wave.
         AttnPlan P2;
-        if (plan_for(kMma, P2) && one_wave(kMma, P2) && P2.tiles_per_split <= 2) {
-            var = kMma;
+        if (plan_for(mma, P2) && one_wave(mma, P2) && P2.tiles_per_split <= 2) {
+            var = mma;
             P = P2;
         }
     }
@@ -1099,6 +1221,8 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
     p.early = (flags & KVD_FLAG_EARLY_KV) ? 1 : 0;
     p.cluster = P.cluster ? 1 : 0;
     p.append = app ? 1 : 0;
+    p.rope = rope ? 1 : 0;
+    p.rope_log2_base = rope ? log2f(app->rope_base) : 0.f;
     p.k_new = app ? static_cast<const uint8_t*>(app->k_new) : nullptr;
     p.v_new = app ? static_cast<const uint8_t*>(app->v_new) : nullptr;
     p.lens_out = app ? app->lens_out : nullptr;

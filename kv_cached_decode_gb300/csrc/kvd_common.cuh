@@ -62,6 +62,26 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
     f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
 }
 
+// ---------------------------------------------------------------- rotary encoding --
+// Rotate-half rotary encoding of 64-dim vectors: dims i and i + 32 form a pair rotated
+// by pos * theta_i, theta_i = base^(-i/32). One definition for every kernel that
+// rotates, so a rotation fused into another kernel gives the same bits as the stand-
+// alone one: the angle is formed in fp32 and sin/cos come from sincosf; the products are
+// rounded explicitly (no contraction choices left to the compiler).
+__device__ __forceinline__ float2 rope_cos_sin(int pos, int i, float log2_base) {
+    const float a = (float)pos * exp2f(-(float)i / 32.f * log2_base);
+    float sn, cs;
+    sincosf(a, &sn, &cs);
+    return make_float2(cs, sn);
+}
+// (x0, x1) = (x[i], x[i+32]) -> (x0 cos - x1 sin, x1 cos + x0 sin)
+__device__ __forceinline__ void rope_rotate(float& x0, float& x1, float2 cs) {
+    const float y0 = __fmaf_rn(x0, cs.x, -__fmul_rn(x1, cs.y));
+    const float y1 = __fmaf_rn(x1, cs.x, __fmul_rn(x0, cs.y));
+    x0 = y0;
+    x1 = y1;
+}
+
 // ---------------------------------------------------------------- shared memory ----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

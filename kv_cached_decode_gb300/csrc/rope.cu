@@ -8,9 +8,11 @@
 // keys of a step before they reach kv_append / decode_attn / verify_attn / prefill.
 //
 // Design: one thread per 8 rotation pairs (16-byte loads of x[i..i+7] and
-// x[i+32..i+39]); both tensors in one launch. The angle is formed in fp32 and sin/cos
-// come from sincosf (full argument reduction, accurate for positions in the
-// thousands); the result is rounded to the storage type.
+// x[i+32..i+39]); both tensors in one launch. The rotation itself (rope_cos_sin,
+// rope_rotate) is shared with the attention kernel, which can apply it to the queries
+// and the appended keys of a call instead of this launch, with the same bits: angle in
+// fp32, sin/cos from sincosf (full argument reduction, accurate for positions in the
+// thousands), the result rounded to the storage type.
 #include <algorithm>
 
 #include "kvd_common.cuh"
@@ -39,7 +41,7 @@ __global__ void __launch_bounds__(256) rope_kernel(const RopeParams p) {
         const int64_t row = idx >> 2;  // (b, h, j)
         const int j = (int)(row % p.n);
         const int b = (int)(row / p.n / p.heads[which]);
-        const float pos = (float)((p.pos0 ? p.pos0[b] : 0) + j);
+        const int pos = (p.pos0 ? p.pos0[b] : 0) + j;
         uint8_t* base = p.x[which] + row * kRowBytes;
         uint4* lo = reinterpret_cast<uint4*>(base + g * 16);
         uint4* hi = reinterpret_cast<uint4*>(base + 64 + g * 16);
@@ -49,20 +51,12 @@ __global__ void __launch_bounds__(256) rope_kernel(const RopeParams p) {
         uint32_t ol[4], oh[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float2 x0 = Half16<T>::to_f2(wl[e]), x1 = Half16<T>::to_f2(wh[e]);
-            float y0[2], y1[2];
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const int i = 8 * g + 2 * e + t;
-                const float a = pos * exp2f(-(float)i / 32.f * p.log2_base);
-                float s, c;
-                sincosf(a, &s, &c);
-                const float v0 = t ? x0.y : x0.x, v1 = t ? x1.y : x1.x;
-                y0[t] = v0 * c - v1 * s;
-                y1[t] = v1 * c + v0 * s;
-            }
-            ol[e] = Half16<T>::from_f2(y0[0], y0[1]);
-            oh[e] = Half16<T>::from_f2(y1[0], y1[1]);
+            float2 x0 = Half16<T>::to_f2(wl[e]), x1 = Half16<T>::to_f2(wh[e]);
+            const int i = 8 * g + 2 * e;
+            rope_rotate(x0.x, x1.x, rope_cos_sin(pos, i, p.log2_base));
+            rope_rotate(x0.y, x1.y, rope_cos_sin(pos, i + 1, p.log2_base));
+            ol[e] = Half16<T>::from_f2(x0.x, x0.y);
+            oh[e] = Half16<T>::from_f2(x1.x, x1.y);
         }
         *lo = make_uint4(ol[0], ol[1], ol[2], ol[3]);
         *hi = make_uint4(oh[0], oh[1], oh[2], oh[3]);

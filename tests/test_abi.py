@@ -134,6 +134,12 @@ def test_host_rejects_bad_shapes(lib):
     app_alias = NewTokens(0x50000, 0x60000, 0x40000)
     assert lib.kvd_decode_attn(0, 1, 20, q, ctypes.byref(c), lens, 10, ctypes.byref(app_alias),
                                1, 0.125, q, None, 0, 0, None, None) == 1
+    # a negative or NaN rotary base
+    for base in (-1.0, float("nan"), float("inf")):
+        app_rope = NewTokens(0x50000, 0x60000, None, base)
+        assert lib.kvd_decode_attn(0, 1, 20, q, ctypes.byref(c), lens, 10,
+                                   ctypes.byref(app_rope), 1, 0.125, q, None, 0, 0, None,
+                                   None) == 1
     # empty batches are a no-op
     assert lib.kvd_decode_attn(0, 0, 20, None, ctypes.byref(c), None, 0, None, 1, 0.125, None,
                                None, 0, 0, None, None) == 0

@@ -1,10 +1,15 @@
-"""Rotary encoding on the GPU (kvd_rope) against the fp64 oracle.
+"""Rotary encoding on the GPU (kvd_rope, and inside the attention call) against the
+fp64 oracle.
 
 Each rotated value must lie within one unit in the last place of the storage type of
-the oracle's value (plus 2e-4 of the pair's norm for the fp32 angle and sin/cos). End
-to end, a GQA decode step whose queries and new keys are rotated at their absolute
-positions must match the oracle's rotation (rounded to the storage type) followed by
-its append and attention, within the attention tolerance.
+the oracle's value, plus the fp32 angle's error times the pair's norm: the angle
+pos * theta (theta <= 1) is formed from exp2f (<= 2 ulp) and one rounded product, so
+its absolute error is below 2.5e-7 * pos; sin/cos add about 1e-6. End
+to end, a decode or verify step whose queries and new keys are rotated at their
+absolute positions must match the oracle's rotation (rounded to the storage type)
+followed by its append and attention, within the attention tolerance. The rotation
+inside the attention call must give the same bits as kvd_rope followed by the call:
+outputs, caches and lengths.
 """
 
 import numpy as np
@@ -39,6 +44,11 @@ def _round_bits(x, dtype):
     return r.astype(np.uint16)
 
 
+def _angle_tol(pos):
+    """Bound of the fp32 rotation's error per unit of pair norm at position pos."""
+    return 2.5e-7 * (np.asarray(pos, np.float64) + 1) + 1e-6
+
+
 def _ulp(y, dtype):
     mant = 10 if dtype == "f16" else 7
     e = np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** -14)))
@@ -62,7 +72,8 @@ def test_rope_matches_the_oracle(dtype):
         xf = _to_f64(x, dtype)
         pair = np.sqrt(xf[..., :32] ** 2 + xf[..., 32:] ** 2)
         pair = np.concatenate([pair, pair], axis=-1)
-        assert np.all(np.abs(got - want) <= _ulp(want, dtype) + 2e-4 * pair)
+        pos = (pos0[:, None, None, None] + np.arange(x.shape[2])[None, None, :, None])
+        assert np.all(np.abs(got - want) <= _ulp(want, dtype) + _angle_tol(pos) * pair)
     # position 0 leaves the first row's first token unchanged
     assert np.array_equal(host16(qd)[0, :, 0], q[0, :, 0])
 
@@ -97,3 +108,79 @@ def test_rope_then_gqa_decode_step():
     assert e.item() == 0 and not err
     assert np.array_equal(lens_out.cpu().numpy(), lens_w)
     assert_attn_close(host16(out), want, dtype, "rope + GQA decode")
+
+
+def _fused_vs_separate(dtype, B, Hq, Hkv, cap, lens, qlen, seed, *, verify=False):
+    """The rotation inside the attention call against kvd_rope + the same call: the
+    outputs, the caches and the lengths must be bit-identical."""
+    import kv_cached_decode_gb300 as kvd
+
+    rng = make_rng(seed)
+    lens = np.asarray(lens, np.int32)
+    K, V = gen_cache(rng, B, Hkv, cap, D, dtype, 0.125, lens=lens)
+    kn, vn = gen_new_kv(rng, B, Hkv, qlen, D, dtype, 0.125)
+    q = gen_queries(rng, B, Hq, qlen, D, dtype, 0.125)
+    results = []
+    for fused in (False, True):
+        qd, knd, vnd = dev16(q, dtype), dev16(kn, dtype), dev16(vn, dtype)
+        Kd, Vd = dev16(K, dtype), dev16(V, dtype)
+        lens_d = dev_i32(lens)
+        lens_out = torch.zeros_like(lens_d)
+        out = torch.full_like(qd, 7.0)
+        op = kvd.KVD_OP_VERIFY_ATTN if verify else kvd.KVD_OP_DECODE_ATTN
+        ws = kvd.new_workspace(kvd.kvd_workspace_size(op, B, Hq, Hkv, 1, qlen, cap))
+        e = new_err()
+        if not fused:
+            kvd.kvd_rope(qd, knd, lens_d)
+        app = (knd, vnd, lens_out, 10000.0) if fused else (knd, vnd, lens_out)
+        if verify:
+            kvd.kvd_verify_attn(qd, kvd.make_cache(Kd, Vd), out, ws, lens=lens_d, causal=True,
+                                dev_err=e, append=app)
+        else:
+            kvd.kvd_decode_attn(qd, kvd.make_cache(Kd, Vd), out, ws, lens=lens_d, dev_err=e,
+                                append=app)
+        torch.cuda.synchronize()
+        assert e.item() == 0
+        results.append((host16(out), host16(Kd), host16(Vd), lens_out.cpu().numpy()))
+    for a, b in zip(*results):
+        assert np.array_equal(a, b)
+    # and against the oracle: rotate (rounded to the storage type), append, attend
+    q_r = _round_bits(oracle.rope(q, dtype, lens), dtype)
+    kn_r = _round_bits(oracle.rope(kn, dtype, lens), dtype)
+    Kw, Vw = K.copy(), V.copy()
+    lens_w, err = oracle.kv_append(Kw, Vw, kn_r, vn, lens, dtype)
+    want, _ = oracle.attention(q_r, Kw, Vw, dtype, lens=lens_w, causal=verify)
+    assert not err
+    # the cache: unchanged outside the appended rows; there, the rotated keys within the
+    # tolerance of the stand-alone rotation (fp32 on the GPU, fp64 in the oracle)
+    Kg = results[1][1]
+    new_rows = np.zeros(Kg.shape, bool)
+    for b in range(B):
+        new_rows[b, :, lens[b]:lens[b] + qlen] = True
+    assert np.array_equal(Kg[~new_rows], Kw[~new_rows])
+    want_k = oracle.rope(kn, dtype, lens)
+    got_k = np.stack([_to_f64(Kg[b, :, lens[b]:lens[b] + qlen], dtype) for b in range(B)])
+    xf = _to_f64(kn, dtype)
+    pair = np.sqrt(xf[..., :32] ** 2 + xf[..., 32:] ** 2)
+    pair = np.concatenate([pair, pair], axis=-1)
+    pos = lens[:, None, None, None] + np.arange(qlen)[None, None, :, None]
+    assert np.all(np.abs(got_k - want_k) <= _ulp(want_k, dtype) + _angle_tol(pos) * pair)
+    assert_attn_close(results[1][0], want, dtype, "fused rotary encoding")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_fused_rope_gqa_decode(dtype):
+    # grouped heads: the tensor-core kernel
+    _fused_vs_separate(dtype, 4, 9, 3, 1100, [300, 1, 1000, 64], 1, seed=910)
+
+
+def test_fused_rope_mha_decode_short_and_long():
+    # one query per KV head: a short cache (one round of tiles) and a long one (the
+    # CUDA-core kernel streams several rounds)
+    _fused_vs_separate("f16", 2, 8, 8, 4200, [100, 40], 1, seed=911)
+    _fused_vs_separate("f16", 2, 8, 8, 4200, [4100, 3000], 1, seed=912)
+
+
+def test_fused_rope_causal_verify_block():
+    # five tokens at positions lens + 0..4, causal, GQA
+    _fused_vs_separate("bf16", 3, 6, 2, 700, [0, 250, 600], 5, seed=913, verify=True)
