@@ -153,6 +153,20 @@ kvd_status kvd_kv_append(kvd_dtype dtype, const kvd_cache *cache, int32_t batch,
                          kvd_stream_t stream);
 
 /*
+ * kvd_kv_append_rope -- A1 with the keys rotary-encoded as they are written (NEXT-3).
+ *
+ * [N] "nanoVLM における KV キャッシュ実装": the language model passes start_pos so that
+ * the rotary encoding of the new tokens matches their absolute positions. As
+ * kvd_kv_append, except that key row j of batch row b is written rotated at position
+ * lens_in[b] + j (kvd_rope's definition, base rope_base > 0; the same bits as kvd_rope
+ * followed by kvd_kv_append). V rows are written as they are.
+ */
+kvd_status kvd_kv_append_rope(kvd_dtype dtype, const kvd_cache *cache, int32_t batch, int32_t q,
+                              const void *k_new, const void *v_new, const int32_t *lens_in,
+                              int32_t *lens_out, float rope_base, uint32_t flags,
+                              int32_t *dev_err, kvd_stream_t stream);
+
+/*
  * kvd_decode_attn -- A2/A3 (+A4). One query token per row attends over the cache.
  *
  * [N] "KV キャッシュが推論を最適化する方法", step 4 (the current token's query meets the
@@ -266,6 +280,9 @@ kvd_status kvd_verify_attn(kvd_dtype dtype, int32_t batch, int32_t n_q_heads, in
  * lens_in       : device int32 [batch] or NULL (every row starts empty)
  * plens         : device int32 [batch], prompt lengths in [0, max_len]
  * lens_out      : device int32 [batch] or NULL; must not alias lens_in
+ * rope_base    : 0, or > 0 to rotary-encode the prompt (kvd_rope's definition): query
+ *                row j and key row j at position lens_in[b] + j; the cache receives the
+ *                rotated keys, q is not written (the same bits as kvd_rope first)
  * Q.K^T and P.V run on the tensor cores, fp32 accumulation, output rounded to nearest.
  * Device errors: lens_in + plens outside [0, capacity] or plens outside [0, max_len] ->
  * KVD_ERR_LEN_OVERFLOW; that row's cache is untouched, lens_out keeps lens_in and its
@@ -274,8 +291,8 @@ kvd_status kvd_verify_attn(kvd_dtype dtype, int32_t batch, int32_t n_q_heads, in
 kvd_status kvd_prefill_attn(kvd_dtype dtype, int32_t batch, int32_t n_q_heads, int32_t max_len,
                             const void *q, const kvd_cache *kv, const void *k_new,
                             const void *v_new, const int32_t *lens_in, const int32_t *plens,
-                            int32_t *lens_out, float scale, void *out, uint32_t flags,
-                            int32_t *dev_err, kvd_stream_t stream);
+                            int32_t *lens_out, float scale, float rope_base, void *out,
+                            uint32_t flags, int32_t *dev_err, kvd_stream_t stream);
 
 /*
  * kvd_rope -- rotary position encoding at absolute positions (in place).

@@ -37,7 +37,8 @@ HEAD_DIM = 64
 
 EXPORTED = ("kvd_kv_append", "kvd_decode_attn", "kvd_verify_attn", "kvd_greedy_accept",
             "kvd_beam_reorder_kv", "kvd_workspace_size", "kvd_status_string", "kvd_version",
-            "kvd_decode_attn_noalloc", "kvd_prefill_attn", "kvd_rope", "kvd_beam_select")
+            "kvd_decode_attn_noalloc", "kvd_prefill_attn", "kvd_rope", "kvd_beam_select",
+            "kvd_kv_append_rope")
 
 
 class KvdError(RuntimeError):
@@ -88,7 +89,8 @@ def load_library(path: str = LIB_PATH):
             "kvd_decode_attn_noalloc": [I32, I32, I32, P, CP, P, I32, NP, I32, F, P, U32, P, P],
             "kvd_verify_attn": [I32, I32, I32, I32, P, CP, P, I32, NP, I32, I32, F, P, P, SZ,
                                 U32, P, P],
-            "kvd_prefill_attn": [I32, I32, I32, I32, P, CP, P, P, P, P, P, F, P, U32, P, P],
+            "kvd_prefill_attn": [I32, I32, I32, I32, P, CP, P, P, P, P, P, F, F, P, U32, P, P],
+            "kvd_kv_append_rope": [I32, CP, I32, I32, P, P, P, P, F, U32, P, P],
             "kvd_rope": [I32, I32, I32, P, I32, P, I32, P, F, U32, P, P],
             "kvd_greedy_accept": [P, I32, I32, I32, P, P, P, P, P, P, SZ, U32, P, P],
             "kvd_beam_reorder_kv": [I32, CP, I32, I32, I32, P, P, I32, U32, P, P],
@@ -184,6 +186,15 @@ def kvd_kv_append(cache: Cache, k_new, v_new, lens_in, lens_out=None, flags: int
                                         _ptr(dev_err), _stream(stream)), "kvd_kv_append")
 
 
+def kvd_kv_append_rope(cache: Cache, k_new, v_new, lens_in, lens_out=None,
+                       rope_base: float = 10000.0, flags: int = 0, dev_err=None, stream=None):
+    B, H, q, D = k_new.shape
+    _check(load_library().kvd_kv_append_rope(_dtype_code(k_new), ctypes.byref(cache), B, q,
+                                             _ptr(k_new), _ptr(v_new), _ptr(lens_in),
+                                             _ptr(lens_out), rope_base, flags, _ptr(dev_err),
+                                             _stream(stream)), "kvd_kv_append_rope")
+
+
 def kvd_decode_attn(q, cache: Cache, out, workspace, lens=None, fixed_len: int = 0,
                     rows_per_kv: int = 1, scale: float = 0.125, flags: int = 0,
                     dev_err=None, stream=None, append=None):
@@ -223,15 +234,17 @@ def kvd_verify_attn(q, cache: Cache, out, workspace, lens=None, fixed_len: int =
 
 
 def kvd_prefill_attn(q, cache: Cache, k_new, v_new, plens, out, lens_in=None, lens_out=None,
-                     scale: float = 0.125, flags: int = 0, dev_err=None, stream=None):
+                     scale: float = 0.125, rope_base: float = 0.0, flags: int = 0,
+                     dev_err=None, stream=None):
     """Prefill: append the prompt's K/V (rows j < plens[b]) and run causal attention of
     the prompt. q, out: [batch, n_q_heads, max_len, 64]; k_new, v_new: [batch,
-    n_kv_heads, max_len, 64]."""
+    n_kv_heads, max_len, 64]. rope_base > 0: rotary encoding of the prompt."""
     B, Hq, T, D = q.shape
     _check(load_library().kvd_prefill_attn(_dtype_code(q), B, Hq, T, _ptr(q),
                                            ctypes.byref(cache), _ptr(k_new), _ptr(v_new),
                                            _ptr(lens_in), _ptr(plens), _ptr(lens_out), scale,
-                                           _ptr(out), flags, _ptr(dev_err), _stream(stream)),
+                                           rope_base, _ptr(out), flags, _ptr(dev_err),
+                                           _stream(stream)),
            "kvd_prefill_attn")
 
 

@@ -290,21 +290,6 @@ __device__ __forceinline__ void stage_appended(const AttnParams& p, const CtaCtx
                    (is_v ? p.v_new : p.k_new) + src);
     }
 }
-// Rotary encoding of 8 pairs: dims i0..i0+7 in lo, i0+32..i0+39 in hi, rounded back to
-// the storage type (the same bits as the stand-alone rotation).
-template <typename T>
-__device__ __forceinline__ void rope_rotate8(uint4& lo, uint4& hi, const float2* tr, int i0) {
-    uint32_t* a = reinterpret_cast<uint32_t*>(&lo);
-    uint32_t* b = reinterpret_cast<uint32_t*>(&hi);
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        float2 x = Half16<T>::to_f2(a[w]), y = Half16<T>::to_f2(b[w]);
-        rope_rotate(x.x, y.x, tr[i0 + 2 * w]);
-        rope_rotate(x.y, y.y, tr[i0 + 2 * w + 1]);
-        a[w] = Half16<T>::from_f2(x.x, x.y);
-        b[w] = Half16<T>::from_f2(y.x, y.y);
-    }
-}
 template <typename T, bool ROPE>
 __device__ __forceinline__ void inject_slab(const AttnParams& p, const CtaCtx& c, uint8_t* sK,
                                             uint8_t* sV, const uint8_t* app, int tile0,

@@ -82,6 +82,37 @@ __device__ __forceinline__ void rope_rotate(float& x0, float& x1, float2 cs) {
     x1 = y1;
 }
 
+// Rotary encoding of 8 pairs: dims i0..i0+7 in lo, i0+32..i0+39 in hi, rounded back to
+// the storage type (the same bits as the stand-alone rotation).
+template <typename T>
+__device__ __forceinline__ void rope_rotate8(uint4& lo, uint4& hi, const float2* tr, int i0) {
+    uint32_t* a = reinterpret_cast<uint32_t*>(&lo);
+    uint32_t* b = reinterpret_cast<uint32_t*>(&hi);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        float2 x = Half16<T>::to_f2(a[w]), y = Half16<T>::to_f2(b[w]);
+        rope_rotate(x.x, y.x, tr[i0 + 2 * w]);
+        rope_rotate(x.y, y.y, tr[i0 + 2 * w + 1]);
+        a[w] = Half16<T>::from_f2(x.x, x.y);
+        b[w] = Half16<T>::from_f2(y.x, y.y);
+    }
+}
+// As rope_rotate8, with the cos/sin of position pos computed here.
+template <typename T>
+__device__ __forceinline__ void rope_rotate8_at(uint4& lo, uint4& hi, int pos, int i0,
+                                                float log2_base) {
+    uint32_t* a = reinterpret_cast<uint32_t*>(&lo);
+    uint32_t* b = reinterpret_cast<uint32_t*>(&hi);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        float2 x = Half16<T>::to_f2(a[w]), y = Half16<T>::to_f2(b[w]);
+        rope_rotate(x.x, y.x, rope_cos_sin(pos, i0 + 2 * w, log2_base));
+        rope_rotate(x.y, y.y, rope_cos_sin(pos, i0 + 2 * w + 1, log2_base));
+        a[w] = Half16<T>::from_f2(x.x, x.y);
+        b[w] = Half16<T>::from_f2(y.x, y.y);
+    }
+}
+
 // ---------------------------------------------------------------- shared memory ----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -103,10 +103,11 @@ size_t accept_workspace_bytes(int batch, int k, int vocab, int target_ctas);
 
 // The append kernel's launcher (kv_append.cu), arguments already validated. counts:
 // NULL (q rows for every batch row) or device int32 [batch] rows per batch row (<= q).
-// lens_in NULL means every row starts empty.
+// lens_in NULL means every row starts empty. rope_base > 0: the keys are written with
+// rotary encoding at their absolute positions (dtype selects the element type).
 kvd_status launch_append(const kvd_cache* cache, int32_t batch, int32_t q, const void* k_new,
                          const void* v_new, const int32_t* lens_in, const int32_t* counts,
-                         int32_t* lens_out, uint32_t flags, int32_t* dev_err,
-                         cudaStream_t stream);
+                         int32_t* lens_out, kvd_dtype dtype, float rope_base, uint32_t flags,
+                         int32_t* dev_err, cudaStream_t stream);
 
 }  // namespace kvd

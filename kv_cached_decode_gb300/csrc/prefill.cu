@@ -39,13 +39,14 @@ struct PrefillParams {
     int32_t* dev_err;
     int32_t max_len, n_q_heads, group, capacity, q_tiles, box_rows;
     float scale_log2;
+    float rope_log2_base;     // > 0 sets the rotary variant's base (log2)
 };
 
 __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <typename T>
+template <typename T, bool ROPE>
 __global__ void __launch_bounds__(kPfThreads)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
@@ -111,6 +112,22 @@ __global__ void __launch_bounds__(kPfThreads)
         qa[kk][1] = liveB ? *reinterpret_cast<const uint32_t*>(bq) : 0u;
         qa[kk][2] = liveA ? *reinterpret_cast<const uint32_t*>(a + 8) : 0u;
         qa[kk][3] = liveB ? *reinterpret_cast<const uint32_t*>(bq + 8) : 0u;
+    }
+    if (ROPE) {
+        // prompt row r sits at position s0 + r; k-steps kk and kk + 2 hold the two halves
+        // of the same rotation pairs in this lane
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = kk * 16 + qc + (e >= 2 ? 8 : 0);
+                const int pos = s0 + ((e & 1) ? rowB : rowA);
+                float2 lo = Half16<T>::to_f2(qa[kk][e]), hi = Half16<T>::to_f2(qa[kk + 2][e]);
+                rope_rotate(lo.x, hi.x, rope_cos_sin(pos, i, p.rope_log2_base));
+                rope_rotate(lo.y, hi.y, rope_cos_sin(pos, i + 1, p.rope_log2_base));
+                qa[kk][e] = Half16<T>::from_f2(lo.x, lo.y);
+                qa[kk + 2][e] = Half16<T>::from_f2(hi.x, hi.y);
+            }
     }
     // keys t < lim are visible; rows past the prompt are clamped to the live rows' keys
     // (positions beyond hold other data) and written as zeros
@@ -247,19 +264,27 @@ __global__ void __launch_bounds__(kPfThreads)
 
 constexpr int kMaxDev = 64;
 
-template <typename T>
+template <typename T, bool ROPE>
 bool prepare_prefill() {
     static std::once_flag once[kMaxDev];
     static bool ok[kMaxDev];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
     std::call_once(once[dev], [dev] {
-        ok[dev] = cudaFuncSetAttribute(prefill_attn_kernel<T>,
+        ok[dev] = cudaFuncSetAttribute(prefill_attn_kernel<T, ROPE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kPfSmem) == cudaSuccess;
         cudaGetLastError();
     });
     return ok[dev];
+}
+
+template <typename T, bool ROPE>
+kvd_status launch_prefill(dim3 grid, cudaStream_t st, bool pdl, const CUtensorMap& mk,
+                          const CUtensorMap& mv, const PrefillParams& p) {
+    if (!prepare_prefill<T, ROPE>()) return KVD_ERR_CUDA;
+    return launch(prefill_attn_kernel<T, ROPE>, grid, dim3(kPfThreads), kPfSmem, st, pdl, mk,
+                  mv, p);
 }
 
 }  // namespace
@@ -271,8 +296,8 @@ extern "C" kvd_status kvd_prefill_attn(kvd_dtype dtype, int32_t batch, int32_t n
                                        int32_t max_len, const void* q, const kvd_cache* kv,
                                        const void* k_new, const void* v_new,
                                        const int32_t* lens_in, const int32_t* plens,
-                                       int32_t* lens_out, float scale, void* out,
-                                       uint32_t flags, int32_t* dev_err,
+                                       int32_t* lens_out, float scale, float rope_base,
+                                       void* out, uint32_t flags, int32_t* dev_err,
                                        kvd_stream_t stream) {
     if (dtype != KVD_F16 && dtype != KVD_BF16) return KVD_ERR_INVALID_ARG;
     if (kvd_status s = validate_cache(kv)) return s;
@@ -285,12 +310,13 @@ extern "C" kvd_status kvd_prefill_attn(kvd_dtype dtype, int32_t batch, int32_t n
         return KVD_ERR_INVALID_ARG;
     if (lens_out && lens_out == lens_in) return KVD_ERR_INVALID_ARG;
     if (!(scale == scale)) return KVD_ERR_INVALID_ARG;
+    if (!(rope_base >= 0.f) || !(rope_base < INFINITY)) return KVD_ERR_INVALID_ARG;
     const int64_t q_tiles = ((int64_t)max_len + kPfRows - 1) / kPfRows;
     if (q_tiles > 0x7fffffff || n_q_heads > 65535 || batch > 65535) return KVD_ERR_UNSUPPORTED;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // 1: the prompt's K/V into the cache (rows j < plens[b] at lens_in[b] + j)
     if (kvd_status s = launch_append(kv, batch, max_len, k_new, v_new, lens_in, plens, lens_out,
-                                     flags, dev_err, st))
+                                     dtype, rope_base, flags, dev_err, st))
         return s;
     // 2: causal attention of the prompt over the cache
     CUtensorMap mk, mv;
@@ -312,12 +338,11 @@ extern "C" kvd_status kvd_prefill_attn(kvd_dtype dtype, int32_t batch, int32_t n
     const dim3 grid((unsigned)q_tiles, (unsigned)n_q_heads, (unsigned)batch);
     // The attention waits for the append (a dependent launch when PDL is requested).
     const bool pdl = (flags & (KVD_FLAG_PDL | KVD_FLAG_EARLY_KV)) != 0;
-    if (dtype == KVD_BF16) {
-        if (!prepare_prefill<__nv_bfloat16>()) return KVD_ERR_CUDA;
-        return launch(prefill_attn_kernel<__nv_bfloat16>, grid, dim3(kPfThreads), kPfSmem, st,
-                      pdl, mk, mv, p);
-    }
-    if (!prepare_prefill<__half>()) return KVD_ERR_CUDA;
-    return launch(prefill_attn_kernel<__half>, grid, dim3(kPfThreads), kPfSmem, st, pdl, mk,
-                  mv, p);
+    const bool rope = rope_base > 0.f;
+    p.rope_log2_base = rope ? log2f(rope_base) : 0.f;
+    if (dtype == KVD_BF16)
+        return rope ? launch_prefill<__nv_bfloat16, true>(grid, st, pdl, mk, mv, p)
+                    : launch_prefill<__nv_bfloat16, false>(grid, st, pdl, mk, mv, p);
+    return rope ? launch_prefill<__half, true>(grid, st, pdl, mk, mv, p)
+                : launch_prefill<__half, false>(grid, st, pdl, mk, mv, p);
 }

@@ -31,7 +31,7 @@ def _declared():
 def test_header_declares_the_entry_points():
     want = {"kvd_kv_append", "kvd_decode_attn", "kvd_verify_attn", "kvd_greedy_accept",
             "kvd_beam_reorder_kv", "kvd_workspace_size", "kvd_status_string", "kvd_version",
-            "kvd_prefill_attn", "kvd_rope", "kvd_beam_select"}
+            "kvd_prefill_attn", "kvd_rope", "kvd_beam_select", "kvd_kv_append_rope"}
     assert want <= _declared()
 
 
@@ -151,25 +151,28 @@ def test_prefill_host_rejects_bad_arguments(lib):
     lens = ctypes.c_void_p(0x40000)
     # no prompt lengths
     assert lib.kvd_prefill_attn(0, 1, 20, 16, p, ctypes.byref(c), p, p, None, None, None,
-                                0.125, p, 0, None, None) == 1
+                                0.125, 0.0, p, 0, None, None) == 1
     # query heads not a multiple of KV heads
     assert lib.kvd_prefill_attn(0, 1, 30, 16, p, ctypes.byref(c), p, p, None, lens, None,
-                                0.125, p, 0, None, None) == 1
+                                0.125, 0.0, p, 0, None, None) == 1
     # lens_out aliasing lens_in, and a misaligned query pointer
     assert lib.kvd_prefill_attn(0, 1, 20, 16, p, ctypes.byref(c), p, p, lens, lens, lens,
-                                0.125, p, 0, None, None) == 1
+                                0.125, 0.0, p, 0, None, None) == 1
     assert lib.kvd_prefill_attn(0, 1, 20, 16, ctypes.c_void_p(0x30008), ctypes.byref(c), p, p,
-                                None, lens, None, 0.125, p, 0, None, None) == 1
+                                None, lens, None, 0.125, 0.0, p, 0, None, None) == 1
     # a bad cache, a bad dtype, and the empty cases
     bad = _fake_cache(head_dim=128)
     assert lib.kvd_prefill_attn(0, 1, 20, 16, p, ctypes.byref(bad), p, p, None, lens, None,
-                                0.125, p, 0, None, None) == 2
+                                0.125, 0.0, p, 0, None, None) == 2
     assert lib.kvd_prefill_attn(7, 1, 20, 16, p, ctypes.byref(c), p, p, None, lens, None,
-                                0.125, p, 0, None, None) == 1
+                                0.125, 0.0, p, 0, None, None) == 1
     assert lib.kvd_prefill_attn(0, 0, 20, 16, None, ctypes.byref(c), None, None, None, None,
-                                None, 0.125, None, 0, None, None) == 0
+                                None, 0.125, 0.0, None, 0, None, None) == 0
     assert lib.kvd_prefill_attn(0, 1, 20, 0, None, ctypes.byref(c), None, None, None, None,
-                                None, 0.125, None, 0, None, None) == 0
+                                None, 0.125, 0.0, None, 0, None, None) == 0
+    # a negative rotary base
+    assert lib.kvd_prefill_attn(0, 1, 20, 16, p, ctypes.byref(c), p, p, None, lens, None,
+                                0.125, -1.0, p, 0, None, None) == 1
 
 
 def test_rope_host_rejects_bad_arguments(lib):
@@ -204,3 +207,14 @@ def test_beam_select_host_rejects_bad_arguments(lib):
                                p, p, p, p, 0, None, None) == 1  # suppression list missing
     assert lib.kvd_beam_select(p, 1, 5, 100, None, None, 0, None, 0, 99, 0, None, None, p,
                                None, p, p, p, p, 0, None, None) == 1  # partial walk outputs
+
+
+def test_append_rope_host_rejects_bad_arguments(lib):
+    c = _fake_cache()
+    p = ctypes.c_void_p(0x30000)
+    lens = ctypes.c_void_p(0x40000)
+    for base in (0.0, -2.0, float("nan"), float("inf")):
+        assert lib.kvd_kv_append_rope(0, ctypes.byref(c), 1, 1, p, p, lens, None, base, 0,
+                                      None, None) == 1
+    assert lib.kvd_kv_append_rope(0, ctypes.byref(c), 0, 1, None, None, None, None, 1e4, 0,
+                                  None, None) == 0

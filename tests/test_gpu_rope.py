@@ -184,3 +184,84 @@ def test_fused_rope_mha_decode_short_and_long():
 def test_fused_rope_causal_verify_block():
     # five tokens at positions lens + 0..4, causal, GQA
     _fused_vs_separate("bf16", 3, 6, 2, 700, [0, 250, 600], 5, seed=913, verify=True)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_append_rope_equals_rope_then_append(dtype):
+    import kv_cached_decode_gb300 as kvd
+
+    rng = make_rng(920)
+    B, H, cap, q = 3, 4, 300, 5
+    lens = np.array([0, 17, 290], np.int32)
+    K, V = gen_cache(rng, B, H, cap, D, dtype, 0.125, lens=lens)
+    kn, vn = gen_new_kv(rng, B, H, q, D, dtype, 0.125)
+    caches = []
+    for fused in (False, True):
+        Kd, Vd = dev16(K, dtype), dev16(V, dtype)
+        knd, vnd = dev16(kn, dtype), dev16(vn, dtype)
+        lens_d, lens_out = dev_i32(lens), torch.zeros(B, dtype=torch.int32, device="cuda")
+        e = new_err()
+        if fused:
+            kvd.kvd_kv_append_rope(kvd.make_cache(Kd, Vd), knd, vnd, lens_d, lens_out,
+                                   rope_base=10000.0, dev_err=e)
+        else:
+            kvd.kvd_rope(None, knd, lens_d)
+            kvd.kvd_kv_append(kvd.make_cache(Kd, Vd), knd, vnd, lens_d, lens_out, dev_err=e)
+        torch.cuda.synchronize()
+        assert e.item() == 0
+        caches.append((host16(Kd), host16(Vd), lens_out.cpu().numpy()))
+    for a, b in zip(*caches):
+        assert np.array_equal(a, b)
+    assert np.array_equal(caches[1][2], lens + q)
+    # the appended keys against the oracle's rotation
+    want_k = oracle.rope(kn, dtype, lens)
+    got_k = np.stack([_to_f64(caches[1][0][b, :, lens[b]:lens[b] + q], dtype) for b in range(B)])
+    xf = _to_f64(kn, dtype)
+    pair = np.sqrt(xf[..., :32] ** 2 + xf[..., 32:] ** 2)
+    pair = np.concatenate([pair, pair], axis=-1)
+    pos = lens[:, None, None, None] + np.arange(q)[None, None, :, None]
+    assert np.all(np.abs(got_k - want_k) <= _ulp(want_k, dtype) + _angle_tol(pos) * pair)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_prefill_rope_equals_rope_then_prefill(dtype):
+    import kv_cached_decode_gb300 as kvd
+
+    rng = make_rng(921)
+    B, Hq, Hkv, cap, T = 3, 6, 2, 400, 150
+    lens_in = np.array([0, 40, 200], np.int32)
+    plens = np.array([150, 1, 97], np.int32)
+    K, V = gen_cache(rng, B, Hkv, cap, D, dtype, 0.125, lens=lens_in)
+    kn, vn = gen_new_kv(rng, B, Hkv, T, D, dtype, 0.125)
+    q = gen_queries(rng, B, Hq, T, D, dtype, 0.125)
+    res = []
+    for fused in (False, True):
+        Kd, Vd = dev16(K, dtype), dev16(V, dtype)
+        qd, knd, vnd = dev16(q, dtype), dev16(kn, dtype), dev16(vn, dtype)
+        li, pl = dev_i32(lens_in), dev_i32(plens)
+        lens_out = torch.zeros(B, dtype=torch.int32, device="cuda")
+        out = torch.full_like(qd, 3.0)
+        e = new_err()
+        if not fused:
+            kvd.kvd_rope(qd, knd, li)
+        kvd.kvd_prefill_attn(qd, kvd.make_cache(Kd, Vd), knd, vnd, pl, out, lens_in=li,
+                             lens_out=lens_out, rope_base=10000.0 if fused else 0.0, dev_err=e)
+        torch.cuda.synchronize()
+        assert e.item() == 0
+        res.append((host16(out), host16(Kd), host16(Vd), lens_out.cpu().numpy()))
+    for a, b in zip(*res):
+        assert np.array_equal(a, b)
+    # against the oracle: rotate (rounded), append, causal attention per row
+    q_r = _round_bits(oracle.rope(q, dtype, lens_in), dtype)
+    kn_r = _round_bits(oracle.rope(kn, dtype, lens_in), dtype)
+    Kw, Vw = K.copy(), V.copy()
+    want = np.zeros((B, Hq, T, D))
+    for b in range(B):
+        n = plens[b]
+        Kw[b, :, lens_in[b]:lens_in[b] + n] = kn_r[b, :, :n]
+        Vw[b, :, lens_in[b]:lens_in[b] + n] = vn[b, :, :n]
+        w, err = oracle.attention(q_r[b:b + 1, :, :n], Kw[b:b + 1], Vw[b:b + 1], dtype,
+                                  lens=np.array([lens_in[b] + n], np.int32), causal=True)
+        assert not err
+        want[b, :, :n] = w[0]
+    assert_attn_close(res[1][0], want, dtype, "prefill with rotary encoding")
