@@ -5,7 +5,8 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 runs it, and it imports nothing from the product library.
 
 ``kvd_oracle.c`` holds the definitions (append, attention, greedy accept, beam
-reorder, rotary encoding, logit filters with the beam-search step); this module marshals numpy arrays into it. ``tiny_model.py`` builds a
+reorder, rotary encoding, logit filters with the beam-search step, temperature sampling
+with stochastic speculative acceptance); this module marshals numpy arrays into it. ``tiny_model.py`` builds a
 small fp64 transformer on top of these functions for the end-to-end invariants
 (cached == recomputed, speculative == greedy, beam reorder == per-beam recompute).
 
@@ -76,6 +77,8 @@ def _load():
             lib.kvo_beam_select.argtypes = [I, I, I, P, P, P, I, P, I, I, I, P, P, P, P, P, P,
                                             P, P]
             lib.kvo_beam_select.restype = ctypes.c_uint
+            lib.kvo_sample_accept.argtypes = [I, I, I, P, P, P, ctypes.c_double, P, P, P, P]
+            lib.kvo_sample_accept.restype = ctypes.c_uint
             _lib = lib
     return _lib
 
@@ -236,3 +239,26 @@ def beam_select(logits, beam: int, *, cum=None, suppress=(), blank=(), eot: int 
                             _ptr(g("fin_parent")), _ptr(g("fin_score")))
     r["errors"] = _errs(m)
     return r
+
+
+def sample_accept(target, temperature: float, u, *, draft=None, drafts=None, r=None):
+    """Temperature sampling (k = 0) or stochastic speculative acceptance of k drafts.
+
+    target: fp32 [B, k+1, V]; draft: fp32 [B, k, V]; drafts: int32 [B, k]; r: fp32
+    [B, k] and u: fp32 [B] uniforms in [0, 1). Returns (n_accepted [B], next [B], errors).
+    """
+    lib = _load()
+    target = np.ascontiguousarray(target, dtype=np.float32)
+    B, k1, V = target.shape
+    k = k1 - 1
+    u = np.ascontiguousarray(u, dtype=np.float32)
+    if k:
+        draft = np.ascontiguousarray(draft, dtype=np.float32)
+        drafts = np.ascontiguousarray(drafts, dtype=np.int32)
+        r = np.ascontiguousarray(r, dtype=np.float32)
+        assert draft.shape == (B, k, V) and drafts.shape == (B, k) and r.shape == (B, k)
+    n = np.empty(B, np.int32)
+    nxt = np.empty(B, np.int32)
+    m = lib.kvo_sample_accept(B, k, V, _ptr(target), _ptr(draft), _ptr(drafts),
+                              float(temperature), _ptr(r), _ptr(u), _ptr(n), _ptr(nxt))
+    return n, nxt, _errs(m)

@@ -458,3 +458,97 @@ unsigned kvo_beam_select(int rows, int beam, int vocab, const float *logits, con
     free(taken);
     return err;
 }
+
+/* ---- temperature sampling and stochastic speculative acceptance -------------------
+ *
+ * [W] "Inference 抽象と KV キャッシュ": at a temperature above 0 GreedyDecoder samples
+ * from Categorical(logits / temperature). [S] "추측 디코딩이란?" names the speculative
+ * decoding of Leviathan et al. (2022); with sampling, its verification step is the
+ * rejection rule of that paper, written here from its definition:
+ *   p_i = softmax(target_i / T), q_i = softmax(draft_i / T), x_i the drafted token;
+ *   for i = 0, 1, ...: accept x_i when r_i * q_i(x_i) < p_i(x_i) (i.e. with probability
+ *   min(1, p/q)); at the first rejection n = i, the next token is drawn from the
+ *   residual max(0, p_n - q_n) (normalised); if all k are accepted, n = k and the next
+ *   token is drawn from p_k.
+ * A draw from weights w with uniform u in [0, 1) is the inverse CDF in id order: the
+ * smallest v whose running sum exceeds u * sum(w) (the last id with w > 0 if rounding
+ * leaves none). Readings: the uniforms r[b, i] and u[b] are inputs (the caller's random
+ * numbers); a NaN logit counts as -inf and sets the NaN bit; a drafted id outside the
+ * vocabulary sets the bad-token bit and is rejected; a residual that sums to 0 falls
+ * back to p_n. k = 0 is plain temperature sampling of target row 0.
+ *
+ * target: fp32 [batch, k+1, vocab]; draft: fp32 [batch, k, vocab] (unused when k = 0);
+ * drafts: int32 [batch, k]; r: fp32 [batch, k]; u: fp32 [batch].
+ * Outputs: n_acc[b] in 0..k, next[b].
+ */
+static void softmax_t(const float *x, int vocab, double temperature, double *p, unsigned *err)
+{
+    double mx = -INFINITY;
+    for (int v = 0; v < vocab; ++v) {
+        double y = x[v];
+        if (isnan(y)) {
+            *err |= KVO_ERR_NAN;
+            y = -INFINITY;
+        }
+        p[v] = y / temperature;
+        if (p[v] > mx) mx = p[v];
+    }
+    double s = 0.0;
+    for (int v = 0; v < vocab; ++v) {
+        p[v] = mx == -INFINITY ? 0.0 : exp(p[v] - mx);
+        s += p[v];
+    }
+    for (int v = 0; v < vocab; ++v) p[v] = s > 0.0 ? p[v] / s : 0.0;
+}
+
+static int inverse_cdf(const double *w, int vocab, double u)
+{
+    double total = 0.0;
+    for (int v = 0; v < vocab; ++v) total += w[v];
+    double run = 0.0;
+    int last = 0;
+    for (int v = 0; v < vocab; ++v) {
+        if (w[v] > 0.0) last = v;
+        run += w[v];
+        if (run > u * total) return v;
+    }
+    return last;
+}
+
+unsigned kvo_sample_accept(int batch, int k, int vocab, const float *target, const float *draft,
+                           const int32_t *drafts, double temperature, const float *r,
+                           const float *u, int32_t *n_acc, int32_t *next)
+{
+    unsigned err = 0;
+    double *p = malloc(sizeof(double) * (size_t)vocab);
+    double *q = malloc(sizeof(double) * (size_t)vocab);
+    double *w = malloc(sizeof(double) * (size_t)vocab);
+    for (int b = 0; b < batch; ++b) {
+        int n = k;
+        for (int i = 0; i < k; ++i) {
+            softmax_t(target + ((int64_t)b * (k + 1) + i) * vocab, vocab, temperature, p, &err);
+            softmax_t(draft + ((int64_t)b * k + i) * vocab, vocab, temperature, q, &err);
+            const int x = drafts[b * k + i];
+            const int ok = x >= 0 && x < vocab;
+            if (!ok) err |= KVO_ERR_BAD_TOKEN;
+            if (ok && (double)r[b * k + i] * q[x] < p[x]) continue;  /* accepted */
+            n = i;
+            double s = 0.0;
+            for (int v = 0; v < vocab; ++v) {
+                w[v] = p[v] - q[v] > 0.0 ? p[v] - q[v] : 0.0;
+                s += w[v];
+            }
+            next[b] = inverse_cdf(s > 0.0 ? w : p, vocab, (double)u[b]);
+            break;
+        }
+        if (n == k) {
+            softmax_t(target + ((int64_t)b * (k + 1) + k) * vocab, vocab, temperature, p, &err);
+            next[b] = inverse_cdf(p, vocab, (double)u[b]);
+        }
+        n_acc[b] = n;
+    }
+    free(p);
+    free(q);
+    free(w);
+    return err;
+}

@@ -21,6 +21,7 @@ APP = "tests/test_oracle_formats_append.py"
 TINY = "tests/test_oracle_tiny_model.py"
 ROPE = "tests/test_oracle_rope.py"
 SEL = "tests/test_oracle_beam_select.py"
+SMP = "tests/test_oracle_sample.py"
 
 MUTANTS = [
     ("causal limit off by one", "int limit = causal ? len - nq + 1 + i : len;",
@@ -75,6 +76,15 @@ MUTANTS = [
      "score[cnd] >= score[best])) best = cnd;", [SEL]),
     ("suppression list ignored", "else x[suppress[i]] = -INFINITY;",
      "else x[suppress[i]] = x[suppress[i]];", [SEL]),
+    ("residual not clamped at zero", "w[v] = p[v] - q[v] > 0.0 ? p[v] - q[v] : 0.0;",
+     "w[v] = p[v];", [SMP]),
+    ("acceptance ratio inverted", "(double)r[b * k + i] * q[x] < p[x]",
+     "(double)r[b * k + i] * p[x] < q[x]", [SMP]),
+    ("inverse CDF boundary not strict", "if (run > u * total) return v;",
+     "if (run >= u * total) return v;", [SMP]),
+    ("temperature ignored", "p[v] = y / temperature;", "p[v] = y;", [SMP]),
+    ("bonus token drawn from the last drafted row", "target + ((int64_t)b * (k + 1) + k) * vocab",
+     "target + ((int64_t)b * (k + 1) + (k > 0 ? k - 1 : 0)) * vocab", [SMP]),
 ]
 
 
