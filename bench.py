@@ -41,7 +41,7 @@ if ROOT not in sys.path:
 
 from workloads import (WORKLOADS, gen_accept_inputs, gen_beam_select_inputs,  # noqa: E402
                        gen_cache, gen_lens_uniform, gen_new_kv, gen_parents, gen_queries,
-                       make_rng, seed_for)
+                       gen_sample_inputs, make_rng, seed_for)
 
 METRIC = "decode-attn KV-read GB/s & % of 8 TB/s HBM; verified tokens/s per layer-step"
 NOMINAL_HBM_GBS = 8000.0
@@ -718,7 +718,7 @@ def run_sweep(args):
     if args.early_kv:
         flags |= kvd.KVD_FLAG_EARLY_KV
     parts = {"beam_step": run_beam_step, "beam_select": run_beam_select,
-             "gqa_lm_step": run_gqa_lm_step}
+             "gqa_lm_step": run_gqa_lm_step, "sample_accept": run_sample_accept}
     if args.sweep_part in parts:
         parts[args.sweep_part](torch, kvd, dev, stream, peak, flags)
         return 0
@@ -763,6 +763,7 @@ def run_sweep(args):
                 torch.cuda.empty_cache()
     run_beam_step(torch, kvd, dev, stream, peak, flags)
     run_beam_select(torch, kvd, dev, stream, peak, flags)
+    run_sample_accept(torch, kvd, dev, stream, peak, flags)
     run_gqa_lm_step(torch, kvd, dev, stream, peak, flags)
     run_prefill(torch, kvd, dev, stream, flags)
     run_tiny_layer(torch, kvd, dev, stream, flags)
@@ -877,6 +878,45 @@ def run_beam_select(torch, kvd, dev, stream, peak, flags):
                           "gbs": round(gbs, 1), "pct_peak": round(100 * gbs / peak, 1),
                           "distinct_buffers": n, "flags": flags}), flush=True)
         del pool, g
+        torch.cuda.empty_cache()
+
+
+def run_sample_accept(torch, kvd, dev, stream, peak, flags):
+    """Temperature sampling and stochastic speculative acceptance over fp32 logits of
+    51865 ids: k = 5 drafts (6 main-model rows + 5 draft rows per batch row) and plain
+    sampling (k = 0), at batch 1 and 16. Distinct copies of the inputs cycle through
+    more than twice the L2, so every launch reads HBM."""
+    V = 51865
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    i32 = dict(dtype=torch.int32, device=dev)
+    for k, B in ((5, 1), (5, 16), (0, 1), (0, 16)):
+        rng = make_rng(seed_for("whisper_verify", salt=100 + 10 * k + B))
+        target, draft, drafts, r, u = gen_sample_inputs(rng, B, k, V)
+        one = (target.size + draft.size) * 4
+        n = max(1, min(2048, 2 * l2 // one + 1))
+        tpool = torch.from_numpy(target).to(dev).unsqueeze(0).repeat(n, 1, 1, 1)
+        dpool = (torch.from_numpy(draft).to(dev).unsqueeze(0).repeat(n, 1, 1, 1) if k else None)
+        drafts_d = torch.from_numpy(drafts).to(dev) if k else None
+        r_d = torch.from_numpy(r).to(dev) if k else None
+        u_d = torch.from_numpy(u).to(dev)
+        n_acc = torch.empty(B, **i32)
+        nxt = torch.empty(B, **i32)
+
+        def fn():
+            for i in range(n):
+                kvd.kvd_sample_accept(tpool[i], u_d, n_acc, nxt, temperature=1.0,
+                                      draft=dpool[i] if k else None, drafts=drafts_d, r=r_d,
+                                      flags=flags)
+
+        g = capture(torch, fn, stream)
+        t = time_graph(torch, g, stream, max(3, int(4e-3 / (n * 5e-6)))) / n  # ms per launch
+        nbytes = one + B * (2 * k * 4 + 4 + 8) + B * k * 4
+        gbs = nbytes / (t * 1e-3) / 1e9
+        print(json.dumps({"sweep": "sample_accept", "k": k, "batch": B, "vocab": V,
+                          "us": round(t * 1e3, 3), "bytes": nbytes, "gbs": round(gbs, 1),
+                          "pct_peak": round(100 * gbs / peak, 1), "distinct_buffers": n,
+                          "flags": flags}), flush=True)
+        del tpool, dpool, g
         torch.cuda.empty_cache()
 
 
@@ -1076,7 +1116,8 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true",
                     help="decode-attention batch x length sweep, the beam step, the GQA-LM "
                          "step, the tiny layer and the verify/decode ratio (JSON lines)")
-    ap.add_argument("--sweep-part", choices=["beam_step", "beam_select", "gqa_lm_step"],
+    ap.add_argument("--sweep-part", choices=["beam_step", "beam_select", "gqa_lm_step",
+                                             "sample_accept"],
                     default=None, help="with --sweep: run only this part")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--traffic", type=float, default=None,

@@ -344,6 +344,41 @@ kvd_status kvd_greedy_accept(const float *logits, int32_t batch, int32_t k, int3
                              kvd_stream_t stream);
 
 /*
+ * kvd_sample_accept -- NEXT-4. Temperature sampling and stochastic speculative
+ * acceptance.
+ *
+ * [W] "Inference 抽象と KV キャッシュ" (GreedyDecoder above temperature 0 samples from
+ * Categorical(logits / T)); [S] "추측 디코딩이란?" (Leviathan et al.'s speculative
+ * decoding, whose sampling form is the rejection rule below). With
+ * p_i = softmax(target[b, i] / T), q_i = softmax(draft[b, i] / T), x_i = drafts[b, i]:
+ *
+ *   for i < k: accept x_i iff r[b, i] * q_i(x_i) < p_i(x_i); stop at the first rejection
+ *   n_accepted[b] = n (the first rejected i, or k)
+ *   next_token[b] = a draw with u[b] from max(0, p_n - q_n) normalised (p_n if that is
+ *                   all 0) when n < k, else from p_k
+ *   a draw from weights w with u in [0, 1): the smallest id whose running sum (id order)
+ *   exceeds u * sum(w); the last id with w > 0 if rounding leaves none
+ *
+ * The emitted tokens are drafts[b, 0..n-1] followed by next_token[b]; their joint
+ * distribution is the main model's. k = 0: plain temperature sampling of target row 0.
+ *
+ * target : device fp32 [batch, k+1, vocab]; draft: device fp32 [batch, k, vocab]
+ * drafts : device int32 [batch, k]; r: device fp32 [batch, k]; u: device fp32 [batch]
+ *          (the caller's uniforms in [0, 1); the library draws no random numbers)
+ * temperature > 0; 0 <= k <= 7 (KVD_ERR_UNSUPPORTED above).
+ * n_accepted, next_token : device int32 [batch]
+ * fp32 arithmetic; a draw whose u * sum(w) lies within fp32 rounding of a boundary may
+ * land on either neighbour. No workspace: one thread-block cluster per batch row.
+ * Device errors: a drafted id outside [0, vocab) -> KVD_ERR_BAD_TOKEN (rejected); a NaN
+ * logit -> KVD_ERR_NAN (counted as -inf).
+ */
+kvd_status kvd_sample_accept(const float *target, const float *draft, const int32_t *drafts,
+                             int32_t batch, int32_t k, int32_t vocab, float temperature,
+                             const float *r, const float *u, int32_t *n_accepted,
+                             int32_t *next_token, uint32_t flags, int32_t *dev_err,
+                             kvd_stream_t stream);
+
+/*
  * kvd_beam_reorder_kv -- A7. Reorder the self-attention caches of all layers.
  *
  * [W] "Inference 抽象と KV キャッシュ" (BeamSearchDecoder.update, rearrange_kv_cache):

@@ -38,7 +38,7 @@ HEAD_DIM = 64
 EXPORTED = ("kvd_kv_append", "kvd_decode_attn", "kvd_verify_attn", "kvd_greedy_accept",
             "kvd_beam_reorder_kv", "kvd_workspace_size", "kvd_status_string", "kvd_version",
             "kvd_decode_attn_noalloc", "kvd_prefill_attn", "kvd_rope", "kvd_beam_select",
-            "kvd_kv_append_rope")
+            "kvd_kv_append_rope", "kvd_sample_accept")
 
 
 class KvdError(RuntimeError):
@@ -91,6 +91,7 @@ def load_library(path: str = LIB_PATH):
                                 U32, P, P],
             "kvd_prefill_attn": [I32, I32, I32, I32, P, CP, P, P, P, P, P, F, F, P, U32, P, P],
             "kvd_kv_append_rope": [I32, CP, I32, I32, P, P, P, P, F, U32, P, P],
+            "kvd_sample_accept": [P, P, P, I32, I32, I32, F, P, P, P, P, U32, P, P],
             "kvd_rope": [I32, I32, I32, P, I32, P, I32, P, F, U32, P, P],
             "kvd_greedy_accept": [P, I32, I32, I32, P, P, P, P, P, P, SZ, U32, P, P],
             "kvd_beam_reorder_kv": [I32, CP, I32, I32, I32, P, P, I32, U32, P, P],
@@ -297,3 +298,15 @@ def kvd_beam_select(logits, beam: int, *, cum=None, suppress=None, blank=None,
         n_blank, eot, int(bool(first_step)), _ptr(row_token), _ptr(row_logprob), _ptr(parent),
         _ptr(token), _ptr(new_cum), _ptr(n_finished), _ptr(fin_parent), _ptr(fin_score),
         flags, _ptr(dev_err), _stream(stream)), "kvd_beam_select")
+
+
+def kvd_sample_accept(target, u, n_accepted, next_token, temperature: float = 1.0, draft=None,
+                      drafts=None, r=None, flags: int = 0, dev_err=None, stream=None):
+    """Temperature sampling (target [B, 1, V]) or stochastic speculative acceptance of k
+    drafts (target [B, k+1, V], draft [B, k, V], drafts and r [B, k]); u: [B] uniforms."""
+    B, k1, V = target.shape
+    _check(load_library().kvd_sample_accept(_ptr(target), _ptr(draft), _ptr(drafts), B,
+                                            k1 - 1, V, temperature, _ptr(r), _ptr(u),
+                                            _ptr(n_accepted), _ptr(next_token), flags,
+                                            _ptr(dev_err), _stream(stream)),
+           "kvd_sample_accept")

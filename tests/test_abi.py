@@ -31,7 +31,8 @@ def _declared():
 def test_header_declares_the_entry_points():
     want = {"kvd_kv_append", "kvd_decode_attn", "kvd_verify_attn", "kvd_greedy_accept",
             "kvd_beam_reorder_kv", "kvd_workspace_size", "kvd_status_string", "kvd_version",
-            "kvd_prefill_attn", "kvd_rope", "kvd_beam_select", "kvd_kv_append_rope"}
+            "kvd_prefill_attn", "kvd_rope", "kvd_beam_select", "kvd_kv_append_rope",
+            "kvd_sample_accept"}
     assert want <= _declared()
 
 
@@ -218,3 +219,18 @@ def test_append_rope_host_rejects_bad_arguments(lib):
                                       None, None) == 1
     assert lib.kvd_kv_append_rope(0, ctypes.byref(c), 0, 1, None, None, None, None, 1e4, 0,
                                   None, None) == 0
+
+
+def test_sample_accept_host_rejects_bad_arguments(lib):
+    p = ctypes.c_void_p(0x30000)
+
+    def call(k=2, vocab=100, T=1.0, draft=p, batch=1):
+        return lib.kvd_sample_accept(p, draft, p, batch, k, vocab, T, p, p, p, p, 0, None, None)
+
+    assert call(k=8) == 2                                  # more than 7 drafts
+    assert call(k=-1) == 1
+    for T in (0.0, -1.0, float("nan"), float("inf")):
+        assert call(T=T) == 1                              # temperature must be > 0
+    assert call(draft=None) == 1                           # drafts without a draft model
+    assert call(k=0, draft=None, batch=0) == 0             # nothing to do
+    assert call(vocab=0) == 1

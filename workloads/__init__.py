@@ -19,5 +19,6 @@ from .synth import (  # noqa: F401
     gen_accept_inputs,
     gen_parents,
     gen_beam_select_inputs,
+    gen_sample_inputs,
     seed_for,
 )

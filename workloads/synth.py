@@ -192,3 +192,24 @@ def gen_beam_select_inputs(rng, windows: int, beam: int, vocab: int, *, logit_st
     else:
         sup = rng.choice(pool, size=min(n_suppress, pool.size), replace=False)
     return logits, cum, np.sort(sup).astype(np.int32)
+
+
+def gen_sample_inputs(rng, batch: int, k: int, vocab: int, *, logit_std: float = 2.0,
+                      draft_noise: float = 1.0, p_match: float = 0.75):
+    """Inputs of temperature sampling / stochastic speculative acceptance.
+
+    Returns ``(target [batch, k+1, vocab] fp32, draft [batch, k, vocab] fp32, drafts
+    [batch, k] int32, r [batch, k] fp32, u [batch] fp32)``. The draft logits are the
+    target logits plus N(0, draft_noise^2); draft i is the draft row's largest logit with
+    probability p_match, else a uniform id. ``numpy.argmax`` only builds the drafts.
+    """
+    target = (rng.standard_normal(size=(batch, k + 1, vocab)) * logit_std).astype(np.float32)
+    noise = (rng.standard_normal(size=(batch, k, vocab)) * draft_noise).astype(np.float32)
+    draft = (target[:, :k] + noise).astype(np.float32)
+    top = np.argmax(draft, axis=-1) if k else np.zeros((batch, 0), np.int64)
+    match = rng.random(size=(batch, k)) < p_match
+    other = rng.integers(0, vocab, size=(batch, k))
+    drafts = np.where(match, top, other).astype(np.int32)
+    r = rng.random(size=(batch, k)).astype(np.float32)
+    u = rng.random(size=batch).astype(np.float32)
+    return target, draft, drafts, r, u
