@@ -901,10 +901,12 @@ def run_sample_accept(torch, kvd, dev, stream, peak, flags):
         u_d = torch.from_numpy(u).to(dev)
         n_acc = torch.empty(B, **i32)
         nxt = torch.empty(B, **i32)
+        ws = kvd.new_workspace(kvd.kvd_workspace_size(kvd.KVD_OP_SAMPLE_ACCEPT, B, qlen=k,
+                                                      vocab=V), device=dev)
 
         def fn():
             for i in range(n):
-                kvd.kvd_sample_accept(tpool[i], u_d, n_acc, nxt, temperature=1.0,
+                kvd.kvd_sample_accept(tpool[i], u_d, n_acc, nxt, ws, temperature=1.0,
                                       draft=dpool[i] if k else None, drafts=drafts_d, r=r_d,
                                       flags=flags)
 

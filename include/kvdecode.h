@@ -88,7 +88,8 @@ typedef enum kvd_dtype { KVD_F16 = 0, KVD_BF16 = 1 } kvd_dtype;
 typedef enum kvd_op {
     KVD_OP_DECODE_ATTN = 0,
     KVD_OP_VERIFY_ATTN = 1,
-    KVD_OP_GREEDY_ACCEPT = 2
+    KVD_OP_GREEDY_ACCEPT = 2,
+    KVD_OP_SAMPLE_ACCEPT = 3
 } kvd_op;
 
 enum {
@@ -367,16 +368,19 @@ kvd_status kvd_greedy_accept(const float *logits, int32_t batch, int32_t k, int3
  *          (the caller's uniforms in [0, 1); the library draws no random numbers)
  * temperature > 0; 0 <= k <= 7 (KVD_ERR_UNSUPPORTED above).
  * n_accepted, next_token : device int32 [batch]
+ * workspace : kvd_workspace_size(KVD_OP_SAMPLE_ACCEPT, batch, .., qlen = k, .., vocab)
+ *             bytes, 256-byte aligned (the rows' per-segment softmax sums)
  * fp32 arithmetic; a draw whose u * sum(w) lies within fp32 rounding of a boundary may
- * land on either neighbour. No workspace: one thread-block cluster per batch row.
+ * land on either neighbour. Two launches: the rows' softmax sums over the whole GPU,
+ * then one thread-block cluster per batch row for the decision and the draw.
  * Device errors: a drafted id outside [0, vocab) -> KVD_ERR_BAD_TOKEN (rejected); a NaN
  * logit -> KVD_ERR_NAN (counted as -inf).
  */
 kvd_status kvd_sample_accept(const float *target, const float *draft, const int32_t *drafts,
                              int32_t batch, int32_t k, int32_t vocab, float temperature,
                              const float *r, const float *u, int32_t *n_accepted,
-                             int32_t *next_token, uint32_t flags, int32_t *dev_err,
-                             kvd_stream_t stream);
+                             int32_t *next_token, void *workspace, size_t workspace_bytes,
+                             uint32_t flags, int32_t *dev_err, kvd_stream_t stream);
 
 /*
  * kvd_beam_reorder_kv -- A7. Reorder the self-attention caches of all layers.
@@ -454,6 +458,7 @@ kvd_status kvd_beam_select(const float *logits, int32_t windows, int32_t beam, i
  *   KVD_OP_DECODE_ATTN : batch, n_q_heads, n_kv_heads, rows_per_kv, max_len
  *   KVD_OP_VERIFY_ATTN : the same plus qlen
  *   KVD_OP_GREEDY_ACCEPT: batch, qlen = k, vocab
+ *   KVD_OP_SAMPLE_ACCEPT: batch, qlen = k, vocab
  * max_len is an upper bound of the attended length (the capacity, or fixed_len).
  * Returns 0 for invalid arguments.
  */

@@ -30,7 +30,7 @@ STATUS_NAMES = {0: "KVD_OK", 1: "KVD_ERR_INVALID_ARG", 2: "KVD_ERR_UNSUPPORTED",
                 17: "KVD_ERR_BAD_INDEX", 18: "KVD_ERR_BAD_TOKEN", 19: "KVD_ERR_NAN",
                 20: "KVD_ERR_TIMEOUT"}
 KVD_F16, KVD_BF16 = 0, 1
-KVD_OP_DECODE_ATTN, KVD_OP_VERIFY_ATTN, KVD_OP_GREEDY_ACCEPT = 0, 1, 2
+KVD_OP_DECODE_ATTN, KVD_OP_VERIFY_ATTN, KVD_OP_GREEDY_ACCEPT, KVD_OP_SAMPLE_ACCEPT = 0, 1, 2, 3
 KVD_FLAG_PDL, KVD_FLAG_EARLY_KV = 1, 2
 KVD_WS_COUNTER_BYTES = 65536
 HEAD_DIM = 64
@@ -91,7 +91,7 @@ def load_library(path: str = LIB_PATH):
                                 U32, P, P],
             "kvd_prefill_attn": [I32, I32, I32, I32, P, CP, P, P, P, P, P, F, F, P, U32, P, P],
             "kvd_kv_append_rope": [I32, CP, I32, I32, P, P, P, P, F, U32, P, P],
-            "kvd_sample_accept": [P, P, P, I32, I32, I32, F, P, P, P, P, U32, P, P],
+            "kvd_sample_accept": [P, P, P, I32, I32, I32, F, P, P, P, P, P, SZ, U32, P, P],
             "kvd_rope": [I32, I32, I32, P, I32, P, I32, P, F, U32, P, P],
             "kvd_greedy_accept": [P, I32, I32, I32, P, P, P, P, P, P, SZ, U32, P, P],
             "kvd_beam_reorder_kv": [I32, CP, I32, I32, I32, P, P, I32, U32, P, P],
@@ -300,13 +300,16 @@ def kvd_beam_select(logits, beam: int, *, cum=None, suppress=None, blank=None,
         flags, _ptr(dev_err), _stream(stream)), "kvd_beam_select")
 
 
-def kvd_sample_accept(target, u, n_accepted, next_token, temperature: float = 1.0, draft=None,
-                      drafts=None, r=None, flags: int = 0, dev_err=None, stream=None):
+def kvd_sample_accept(target, u, n_accepted, next_token, workspace, temperature: float = 1.0,
+                      draft=None, drafts=None, r=None, flags: int = 0, dev_err=None,
+                      stream=None):
     """Temperature sampling (target [B, 1, V]) or stochastic speculative acceptance of k
-    drafts (target [B, k+1, V], draft [B, k, V], drafts and r [B, k]); u: [B] uniforms."""
+    drafts (target [B, k+1, V], draft [B, k, V], drafts and r [B, k]); u: [B] uniforms;
+    workspace: kvd_workspace_size(KVD_OP_SAMPLE_ACCEPT, B, qlen=k, vocab=V) bytes."""
     B, k1, V = target.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
     _check(load_library().kvd_sample_accept(_ptr(target), _ptr(draft), _ptr(drafts), B,
                                             k1 - 1, V, temperature, _ptr(r), _ptr(u),
-                                            _ptr(n_accepted), _ptr(next_token), flags,
-                                            _ptr(dev_err), _stream(stream)),
+                                            _ptr(n_accepted), _ptr(next_token), _ptr(workspace),
+                                            ws_bytes, flags, _ptr(dev_err), _stream(stream)),
            "kvd_sample_accept")

@@ -129,6 +129,10 @@ extern "C" size_t kvd_workspace_size(kvd_op op, int32_t batch, int32_t n_q_heads
         if (batch <= 0 || qlen < 1 || qlen > KVD_MAX_QLEN || vocab <= 0) return 0;
         return accept_workspace_bytes(batch, qlen, vocab, kWsTargetBound);
     }
+    case KVD_OP_SAMPLE_ACCEPT: {
+        if (batch <= 0 || qlen < 0 || qlen > 7 || vocab <= 0) return 0;
+        return sample_workspace_bytes(batch, qlen, vocab);
+    }
     }
     return 0;
 }

@@ -101,6 +101,9 @@ bool workspace_merge_pays(int units, int rounds);
 constexpr int kWsTargetBound = 4096;
 size_t accept_workspace_bytes(int batch, int k, int vocab, int target_ctas);
 
+// Workspace bytes of kvd_sample_accept (sample_accept.cu).
+size_t sample_workspace_bytes(int batch, int k, int vocab);
+
 // The append kernel's launcher (kv_append.cu), arguments already validated. counts:
 // NULL (q rows for every batch row) or device int32 [batch] rows per batch row (<= q).
 // lens_in NULL means every row starts empty. rope_base > 0: the keys are written with

@@ -11,16 +11,15 @@
 //   next        =  the smallest id whose running sum of w exceeds u * sum(w), in id order
 //   w = max(0, p_n - q_n) (p_n if that sums to 0), or p_k when n = k
 //
-// Design: one thread-block cluster per batch row; CTA c owns the id slice
-// [c * slice, (c + 1) * slice) of all 2k + 1 rows (k + 1 main-model rows, k draft rows),
-// so the rows' softmax sums, the acceptance test and the draw all split the same way.
-//  1. Each thread streams its ids of every row (all rows' loads issued together) and
-//     keeps an online (max, sum of 2^(y - max)) per row, y = x * log2(e) / T; the block
-//     reduces them to the CTA's per-row pair.
-//  2. Cluster barrier; every CTA reads all CTAs' pairs through distributed shared
-//     memory and forms each row's log-sum-exp, so every CTA takes the same acceptance
-//     decision (the drafted ids' two logits are read directly).
-//  3. Each CTA sums the draw's weights over its slice and stores the sums into every
+// Design: two launches.
+//  A. The 2k + 1 rows (k + 1 main-model rows, k draft rows) are cut into 2048-id
+//     segments, one 256-thread block each over the whole GPU; a block reduces its
+//     segment to (max, sum of 2^(y - max)), y = x * log2(e) / T, into the workspace.
+//  B. One thread-block cluster per batch row; CTA c owns the id slice
+//     [c * slice, (c + 1) * slice). Every CTA reduces the segment pairs to each row's
+//     log-sum-exp (a warp per row) and takes the same acceptance decision (the drafted
+//     ids' logits are fetched by one thread each).
+//     Then each CTA sums the draw's weights over its slice and stores the sums into every
 //     CTA; cluster barrier (after it nothing is read remotely, so CTAs may exit); the
 //     prefix over the CTAs names the CTA whose slice holds u * sum(w); that CTA scans its slice
 //     (contiguous chunks per thread, a block-wide exclusive scan of the chunk sums) and
@@ -51,19 +50,19 @@ struct SampleParams {
     int32_t* n_acc;
     int32_t* next;
     int32_t* dev_err;
-    int32_t k, vocab, cluster, slice;
+    float2* ws_ml;        // [batch, 2k+1, segs] (max, sum) per 2048-id segment
+    int32_t k, vocab, cluster, slice, segs;
     float c2;  // log2(e) / T
 };
 
 struct SampleShared {
-    float wm[kSaWarps][kSaMaxRows], wl[kSaWarps][kSaMaxRows];
-    float rec_m[kSaMaxRows], rec_l[kSaMaxRows];  // this CTA's per-row pair (read by all)
     float row_m[kSaMaxRows], row_l[kSaMaxRows];  // each row's, over the whole vocabulary
     float warp_s[kSaWarps][2];
     float all_s[kSaMaxCluster][2];  // every CTA's sums of the draw weights: [0] w, [1]
                                     // the fallback p_n (each CTA writes its pair into all)
     float chunk_pre[kSaWarps];
     int n, use_p, owner, token, last_pos;
+    int acc[kSaMaxK], bad[kSaMaxK];
     float t_local;
 };
 
@@ -72,36 +71,74 @@ __device__ __forceinline__ void st_cluster_f32(float* local, int rank, float v) 
                  "f"(v)
                  : "memory");
 }
-__device__ __forceinline__ float ld_cluster_f32(const float* local, int rank) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];"
-                 : "=f"(v)
-                 : "r"(map_shared(smem_u32(local), (uint32_t)rank))
-                 : "memory");
-    return v;
-}
 // All threads of all CTAs of the cluster: writes before are visible to reads after.
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Online pair (m, l = sum 2^(y - m)), m = -inf for "nothing yet".
-__device__ __forceinline__ void online_add(float& m, float& l, float y) {
-    if (y > m) {
-        l = l * exp2f(m - y) + 1.f;
-        m = y;
-    } else if (y > -INFINITY) {
-        l += exp2f(y - m);
-    }
+// ---- kernel A: each row's (max, sum) per 2048-id segment, over the whole GPU ----
+constexpr int kStThreads = 256;
+constexpr int kStLoads = 8;
+constexpr int kSeg = kStThreads * kStLoads;
+
+__device__ __forceinline__ float exp2_or0(float a, float m) {
+    return a == -INFINITY ? 0.f : exp2f(a - m);  // 2^(a - m), 0 for an empty term
 }
-__device__ __forceinline__ void pair_combine(float& m, float& l, float m2, float l2) {
+// (m, l) = (m1, l1) + (m2, l2), branch-free (an empty pair has m = -inf, l = 0)
+__device__ __forceinline__ void pair_add(float& m, float& l, float m2, float l2) {
     const float M = fmaxf(m, m2);
-    if (M == -INFINITY) return;
-    l = (m == -INFINITY ? 0.f : l * exp2f(m - M)) + (m2 == -INFINITY ? 0.f : l2 * exp2f(m2 - M));
+    l = l * exp2_or0(m, M) + l2 * exp2_or0(m2, M);
     m = M;
 }
 
+__global__ void __launch_bounds__(kStThreads) sample_stats_kernel(const SampleParams p) {
+    __shared__ float s_m[kStThreads / 32], s_l[kStThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int seg = blockIdx.x, r = blockIdx.y, b = blockIdx.z;
+    const int k = p.k;
+    pdl_wait();
+    const float* row = r <= k ? p.target + ((int64_t)b * (k + 1) + r) * p.vocab
+                              : p.draft + ((int64_t)b * k + (r - k - 1)) * p.vocab;
+    const int lo = seg * kSeg, hi = min(p.vocab, lo + kSeg);
+    float y[kStLoads];
+    bool nan = false;
+#pragma unroll
+    for (int a = 0; a < kStLoads; ++a) {
+        const int e = lo + a * kStThreads + tid;
+        const float x = __ldcs(row + min(e, hi - 1));
+        nan |= e < hi && isnan(x);
+        y[a] = (e < hi && !isnan(x)) ? x * p.c2 : -INFINITY;
+    }
+    float m = y[0];
+#pragma unroll
+    for (int a = 1; a < kStLoads; ++a) m = fmaxf(m, y[a]);
+    float l = 0.f;
+#pragma unroll
+    for (int a = 0; a < kStLoads; ++a) l += exp2_or0(y[a], m);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        pair_add(m, l, __shfl_xor_sync(0xffffffffu, m, off), __shfl_xor_sync(0xffffffffu, l, off));
+    if (lane == 0) {
+        s_m[warp] = m;
+        s_l[warp] = l;
+    }
+    if (__syncthreads_or(nan) && tid == 0) flag_error(p.dev_err, KVD_ERR_NAN);
+    pdl_trigger();
+    if (warp == 0) {
+        m = lane < kStThreads / 32 ? s_m[lane] : -INFINITY;
+        l = lane < kStThreads / 32 ? s_l[lane] : 0.f;
+#pragma unroll
+        for (int off = 4; off > 0; off >>= 1)
+            pair_add(m, l, __shfl_xor_sync(0xffffffffu, m, off), __shfl_xor_sync(0xffffffffu, l, off));
+        if (lane == 0) {
+            const int64_t slot = ((int64_t)b * (2 * k + 1) + r) * p.segs + seg;
+            p.ws_ml[slot] = make_float2(m, l);
+        }
+    }
+}
+
+// ---- kernel B: the decision and the draw, one cluster per batch row ----
 template <int R>
 __global__ void __launch_bounds__(kSaThreads, 1) sample_accept_kernel(const SampleParams p) {
     __shared__ SampleShared S;
@@ -110,102 +147,56 @@ __global__ void __launch_bounds__(kSaThreads, 1) sample_accept_kernel(const Samp
     const int b = (int)(blockIdx.x / (unsigned)p.cluster);
     const int k = p.k;
     const int lo = rank * p.slice, hi = min(p.vocab, lo + p.slice);
-    pdl_wait();
     auto row_ptr = [&](int r) -> const float* {
         return r <= k ? p.target + ((int64_t)b * (k + 1) + r) * p.vocab
                       : p.draft + ((int64_t)b * k + (r - k - 1)) * p.vocab;
     };
+    pdl_wait();
 
-    // ---- 1. per-row online pairs over this CTA's slice ----
-    float m[R], l[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        m[r] = -INFINITY;
-        l[r] = 0.f;
-    }
-    bool nan = false;
-    // U ids per row per pass, all R * U loads issued before any is used
-    constexpr int U = R <= 7 ? 4 : 2;
-    for (int e0 = lo + tid; e0 < hi; e0 += U * kSaThreads) {
-        float x[U][R];
-#pragma unroll
-        for (int a = 0; a < U; ++a)
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int e = min(e0 + a * kSaThreads, hi - 1);
-                x[a][r] = __ldcs(row_ptr(r) + e);
-            }
-#pragma unroll
-        for (int a = 0; a < U; ++a) {
-            if (e0 + a * kSaThreads >= hi) break;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                nan |= isnan(x[a][r]);
-                online_add(m[r], l[r], isnan(x[a][r]) ? -INFINITY : x[a][r] * p.c2);
-            }
+    // ---- every row's log-sum-exp (log2 domain) from kernel A's segment pairs: one warp
+    // per row ----
+    if (warp < R) {
+        const float2* ml = p.ws_ml + ((int64_t)b * R + warp) * p.segs;
+        float m = -INFINITY, l = 0.f;
+        for (int sg = lane; sg < p.segs; sg += 32) {
+            const float2 v = __ldcg(ml + sg);
+            pair_add(m, l, v.x, v.y);
         }
-    }
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, m[r], off);
-            const float l2 = __shfl_xor_sync(0xffffffffu, l[r], off);
-            pair_combine(m[r], l[r], m2, l2);
-        }
+        for (int off = 16; off > 0; off >>= 1)
+            pair_add(m, l, __shfl_xor_sync(0xffffffffu, m, off), __shfl_xor_sync(0xffffffffu, l, off));
         if (lane == 0) {
-            S.wm[warp][r] = m[r];
-            S.wl[warp][r] = l[r];
+            S.row_m[warp] = m;
+            S.row_l[warp] = l;
         }
     }
-    if (__syncthreads_or(nan) && tid == 0) flag_error(p.dev_err, KVD_ERR_NAN);
-    if (tid < R) {
-        float mm = -INFINITY, ll = 0.f;
-        for (int w = 0; w < kSaWarps; ++w) pair_combine(mm, ll, S.wm[w][tid], S.wl[w][tid]);
-        S.rec_m[tid] = mm;
-        S.rec_l[tid] = ll;
-    }
-    if (p.cluster > 1) cluster_sync_all();
-    else __syncthreads();
-
-    // ---- 2. every row's log-sum-exp (log2 domain), then the acceptance decision ----
-    if (tid < R) {
-        float cm[kSaMaxCluster], cl[kSaMaxCluster];
-#pragma unroll
-        for (int c = 0; c < kSaMaxCluster; ++c) {  // all remote loads first
-            const bool on = c < p.cluster;
-            cm[c] = !on ? -INFINITY : p.cluster > 1 ? ld_cluster_f32(&S.rec_m[tid], c) : S.rec_m[tid];
-            cl[c] = !on ? 0.f : p.cluster > 1 ? ld_cluster_f32(&S.rec_l[tid], c) : S.rec_l[tid];
+    __syncthreads();
+    // the drafted ids' probabilities, all fetched at once (thread i: draft i)
+    if (tid < k) {
+        const int x = p.drafts[b * k + tid];
+        const bool ok = x >= 0 && x < p.vocab;
+        float pt = 0.f, qd = 0.f;
+        if (ok) {
+            const float xt = row_ptr(tid)[x], xd = row_ptr(k + 1 + tid)[x];
+            const float yt = isnan(xt) ? -INFINITY : xt * p.c2;
+            const float yd = isnan(xd) ? -INFINITY : xd * p.c2;
+            const int rd = k + 1 + tid;
+            pt = S.row_l[tid] > 0.f ? exp2f(yt - S.row_m[tid]) / S.row_l[tid] : 0.f;
+            qd = S.row_l[rd] > 0.f ? exp2f(yd - S.row_m[rd]) / S.row_l[rd] : 0.f;
         }
-        float mm = -INFINITY, ll = 0.f;
-#pragma unroll
-        for (int c = 0; c < kSaMaxCluster; ++c) pair_combine(mm, ll, cm[c], cl[c]);
-        S.row_m[tid] = mm;
-        S.row_l[tid] = ll;
+        // accepted iff the id is valid and r * q < p
+        S.acc[tid] = ok && p.r[b * k + tid] * qd < pt;
+        S.bad[tid] = !ok;
     }
     __syncthreads();
     if (tid == 0) {
         int n = k;
-        bool bad = false;
-        for (int i = 0; i < k; ++i) {
-            const int x = p.drafts[b * k + i];
-            if (x < 0 || x >= p.vocab) {
-                bad = true;
+        for (int i = 0; i < k; ++i)
+            if (!S.acc[i]) {
                 n = i;
                 break;
             }
-            const float xt = row_ptr(i)[x], xd = row_ptr(k + 1 + i)[x];
-            const float yt = isnan(xt) ? -INFINITY : xt * p.c2;
-            const float yd = isnan(xd) ? -INFINITY : xd * p.c2;
-            const float pt = S.row_l[i] > 0.f ? exp2f(yt - S.row_m[i]) / S.row_l[i] : 0.f;
-            const float qd =
-                S.row_l[k + 1 + i] > 0.f ? exp2f(yd - S.row_m[k + 1 + i]) / S.row_l[k + 1 + i] : 0.f;
-            if (!(p.r[b * k + i] * qd < pt)) {
-                n = i;
-                break;
-            }
-        }
-        if (bad && rank == 0) flag_error(p.dev_err, KVD_ERR_BAD_TOKEN);
+        if (n < k && S.bad[n] && rank == 0) flag_error(p.dev_err, KVD_ERR_BAD_TOKEN);
         S.n = n;
     }
     __syncthreads();
@@ -401,11 +392,23 @@ kvd_status launch_sample(int batch, cudaStream_t st, bool pdl, const SampleParam
         if (n > 0) break;
     }
     q.slice = (q.vocab + q.cluster - 1) / q.cluster;
+    // A: the rows' segment pairs, over the whole GPU; B: the decision and the draw (a
+    // dependent launch when PDL is requested: B waits for A either way)
+    if (kvd_status s = launch(sample_stats_kernel, dim3((unsigned)q.segs, (unsigned)R,
+                                                        (unsigned)batch),
+                              dim3(kStThreads), 0, st, pdl, q))
+        return s;
     return launch_ex(sample_accept_kernel<R>, dim3((unsigned)(batch * q.cluster)),
                      dim3(kSaThreads), 0, st, pdl, (unsigned)q.cluster, q);
 }
 
 }  // namespace
+
+size_t sample_workspace_bytes(int batch, int k, int vocab) {
+    const size_t segs = ((size_t)vocab + kSeg - 1) / kSeg;
+    return KVD_WS_COUNTER_BYTES + ((size_t)batch * (2 * k + 1) * segs * 8 + 255) / 256 * 256;
+}
+
 }  // namespace kvd
 
 using namespace kvd;
@@ -414,16 +417,22 @@ extern "C" kvd_status kvd_sample_accept(const float* target, const float* draft,
                                         const int32_t* drafts, int32_t batch, int32_t k,
                                         int32_t vocab, float temperature, const float* r,
                                         const float* u, int32_t* n_accepted,
-                                        int32_t* next_token, uint32_t flags, int32_t* dev_err,
-                                        kvd_stream_t stream) {
+                                        int32_t* next_token, void* workspace,
+                                        size_t workspace_bytes, uint32_t flags,
+                                        int32_t* dev_err, kvd_stream_t stream) {
     if (batch < 0 || vocab <= 0 || k < 0) return KVD_ERR_INVALID_ARG;
     if (k > kSaMaxK) return KVD_ERR_UNSUPPORTED;
     if (!(temperature > 0.f) || !(temperature < INFINITY)) return KVD_ERR_INVALID_ARG;
     if (batch == 0) return KVD_OK;
     if (!target || !u || !n_accepted || !next_token) return KVD_ERR_INVALID_ARG;
     if (k > 0 && (!draft || !drafts || !r)) return KVD_ERR_INVALID_ARG;
-    if ((int64_t)batch * kSaMaxCluster > 0x7fffffff) return KVD_ERR_UNSUPPORTED;
+    if ((int64_t)batch * kSaMaxCluster > 0x7fffffff || batch > 65535) return KVD_ERR_UNSUPPORTED;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) ||
+        workspace_bytes < sample_workspace_bytes(batch, k, vocab))
+        return KVD_ERR_WORKSPACE;
     SampleParams p;
+    p.ws_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + KVD_WS_COUNTER_BYTES);
+    p.segs = (vocab + kSeg - 1) / kSeg;
     p.target = target;
     p.draft = draft;
     p.drafts = drafts;

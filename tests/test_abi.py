@@ -224,8 +224,10 @@ def test_append_rope_host_rejects_bad_arguments(lib):
 def test_sample_accept_host_rejects_bad_arguments(lib):
     p = ctypes.c_void_p(0x30000)
 
-    def call(k=2, vocab=100, T=1.0, draft=p, batch=1):
-        return lib.kvd_sample_accept(p, draft, p, batch, k, vocab, T, p, p, p, p, 0, None, None)
+    def call(k=2, vocab=100, T=1.0, draft=p, batch=1, ws=ctypes.c_void_p(0x100000),
+             ws_bytes=1 << 20):
+        return lib.kvd_sample_accept(p, draft, p, batch, k, vocab, T, p, p, p, p, ws, ws_bytes,
+                                     0, None, None)
 
     assert call(k=8) == 2                                  # more than 7 drafts
     assert call(k=-1) == 1
@@ -234,3 +236,8 @@ def test_sample_accept_host_rejects_bad_arguments(lib):
     assert call(draft=None) == 1                           # drafts without a draft model
     assert call(k=0, draft=None, batch=0) == 0             # nothing to do
     assert call(vocab=0) == 1
+    assert call(ws=None) == 3 and call(ws_bytes=1024) == 3  # workspace missing / too small
+    from kv_cached_decode_gb300 import KVD_OP_SAMPLE_ACCEPT, KVD_WS_COUNTER_BYTES
+    n = lib.kvd_workspace_size(KVD_OP_SAMPLE_ACCEPT, 16, 0, 0, 0, 5, 0, 51865)
+    assert n >= KVD_WS_COUNTER_BYTES + 16 * 11 * 26 * 8  # (max, sum) per row and segment
+    assert lib.kvd_workspace_size(KVD_OP_SAMPLE_ACCEPT, 16, 0, 0, 0, 8, 0, 51865) == 0

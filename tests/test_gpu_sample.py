@@ -48,7 +48,10 @@ def run_gpu(target, T, u, draft=None, drafts=None, r=None, flags=0):
     n = torch.full((B,), -1, dtype=torch.int32, device="cuda")
     nxt = torch.full((B,), -1, dtype=torch.int32, device="cuda")
     e = new_err()
-    kvd.kvd_sample_accept(dev(target), dev(u), n, nxt, temperature=T, draft=dev(draft),
+    ws = kvd.new_workspace(kvd.kvd_workspace_size(kvd.KVD_OP_SAMPLE_ACCEPT, B,
+                                                  qlen=target.shape[1] - 1,
+                                                  vocab=target.shape[2]))
+    kvd.kvd_sample_accept(dev(target), dev(u), n, nxt, ws, temperature=T, draft=dev(draft),
                           drafts=dev(drafts), r=dev(r), flags=flags, dev_err=e)
     torch.cuda.synchronize()
     return n.cpu().numpy(), nxt.cpu().numpy(), e.item()
