@@ -834,6 +834,38 @@ def run_beam_step(torch, kvd, dev, stream, peak, flags):
                           "tokens_per_s": round(R / (t_step * 1e-3), 1),
                           "moved_rows": moved, "source_rows": srcs}), flush=True)
 
+    # the whole beam step at L = 224: the selection (logit filters, scores, parents) over
+    # 8 windows x 5 x 51865 logits, the reorder by its parents, then the 32 layers
+    sw = WORKLOADS["beam_select"]
+    x, cum, sup = gen_beam_select_inputs(make_rng(seed_for("beam_select", salt=7)), W, beam,
+                                         sw["vocab"], eot=sw["eot"],
+                                         n_suppress=sw["n_suppress"])
+    xd, cumd, supd = (torch.from_numpy(a).to(dev) for a in (x, cum, sup))
+    i32 = dict(dtype=torch.int32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    sel = dict(parent=torch.empty(R, **i32), token=torch.empty(R, **i32),
+               new_cum=torch.empty(R, **f32), n_finished=torch.empty(W, **i32),
+               fin_parent=torch.empty(R, **i32), fin_score=torch.empty(R, **f32))
+    L = 224
+    lens_in = torch.full((R,), L, dtype=torch.int32, device=dev)
+    lens = torch.full((R,), L + 1, dtype=torch.int32, device=dev)
+    self_flags = flags & kvd.KVD_FLAG_PDL
+
+    def full_step():
+        kvd.kvd_beam_select(xd, beam, cum=cumd, suppress=supd, eot=sw["eot"],
+                            flags=self_flags, **sel)
+        kvd.kvd_beam_reorder_kv(c_self, R, beam, sel["parent"], lens=lens_in, flags=self_flags)
+        for l in range(NL):
+            kvd.kvd_decode_attn(q, c_self[l], out, ws, lens=lens_in, flags=self_flags,
+                                append=(kn, kn, lens))
+            kvd.kvd_decode_attn(q, c_cross[l], out, ws, fixed_len=F, rows_per_kv=beam,
+                                flags=flags)
+
+    t_full = time_graph(torch, capture(torch, full_step, stream), stream, 50)
+    print(json.dumps({"sweep": "beam_step_with_selection", "rows": R, "len": L,
+                      "step_us": round(t_full * 1e3, 2),
+                      "tokens_per_s": round(R / (t_full * 1e-3), 1)}), flush=True)
+
 
 def run_beam_select(torch, kvd, dev, stream, peak, flags):
     """Logit filters + beam-search selection over fp32 logits of 51865 ids: the beam
