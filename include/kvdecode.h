@@ -130,7 +130,7 @@ typedef struct kvd_cache {
 } kvd_cache;
 
 /*
- * kvd_kv_append -- A1. Write the new tokens' K/V into the cache.
+ * kvd_kv_append -- write the new tokens' K/V into the cache.
  *
  * [N] "KV キャッシュが推論を最適化する方法", steps 2-3 (only the newest token's K/V are
  * computed and added to the cache); [W] "Inference 抽象と KV キャッシュ" (the
@@ -154,7 +154,7 @@ kvd_status kvd_kv_append(kvd_dtype dtype, const kvd_cache *cache, int32_t batch,
                          kvd_stream_t stream);
 
 /*
- * kvd_kv_append_rope -- A1 with the keys rotary-encoded as they are written (NEXT-3).
+ * kvd_kv_append_rope -- the append, with the keys rotary-encoded as they are written.
  *
  * [N] "nanoVLM における KV キャッシュ実装": the language model passes start_pos so that
  * the rotary encoding of the new tokens matches their absolute positions. As
@@ -168,7 +168,7 @@ kvd_status kvd_kv_append_rope(kvd_dtype dtype, const kvd_cache *cache, int32_t b
                               int32_t *dev_err, kvd_stream_t stream);
 
 /*
- * kvd_decode_attn -- A2/A3 (+A4). One query token per row attends over the cache.
+ * kvd_decode_attn -- one query token per row attends over the cache.
  *
  * [N] "KV キャッシュが推論を最適化する方法", step 4 (the current token's query meets the
  * cached K/V); [W] "Inference 抽象と KV キャッシュ" (attention sees the full
@@ -237,7 +237,7 @@ kvd_status kvd_decode_attn_noalloc(kvd_dtype dtype, int32_t batch, int32_t n_q_h
                                    int32_t *dev_err, kvd_stream_t stream);
 
 /*
- * kvd_verify_attn -- A5. A block of qlen query tokens per row in one pass.
+ * kvd_verify_attn -- a block of qlen query tokens per row in one pass.
  *
  * [S] "추측 디코딩이란?" and [A]: the main model checks all candidate tokens in a single
  * forward pass. The block's K/V are already appended (kvd_kv_append with q = qlen),
@@ -316,7 +316,7 @@ kvd_status kvd_rope(kvd_dtype dtype, int32_t batch, int32_t n, void *q, int32_t 
                     int32_t *dev_err, kvd_stream_t stream);
 
 /*
- * kvd_greedy_accept -- A6. Greedy verification of k draft tokens.
+ * kvd_greedy_accept -- greedy verification of k draft tokens.
  *
  * [W] "Inference 抽象と KV キャッシュ" (GreedyDecoder: argmax at temperature 0);
  * [S] "추측 디코딩이란?" and [A] (accept candidates up to the first mismatch, replace
@@ -345,7 +345,7 @@ kvd_status kvd_greedy_accept(const float *logits, int32_t batch, int32_t k, int3
                              kvd_stream_t stream);
 
 /*
- * kvd_sample_accept -- NEXT-4. Temperature sampling and stochastic speculative
+ * kvd_sample_accept -- temperature sampling and stochastic speculative
  * acceptance.
  *
  * [W] "Inference 抽象と KV キャッシュ" (GreedyDecoder above temperature 0 samples from
@@ -383,7 +383,7 @@ kvd_status kvd_sample_accept(const float *target, const float *draft, const int3
                              uint32_t flags, int32_t *dev_err, kvd_stream_t stream);
 
 /*
- * kvd_beam_reorder_kv -- A7. Reorder the self-attention caches of all layers.
+ * kvd_beam_reorder_kv -- reorder the self-attention caches of all layers.
  *
  * [W] "Inference 抽象と KV キャッシュ" (BeamSearchDecoder.update, rearrange_kv_cache):
  * after beams are re-ranked the key/value tensors are put in the new beam order, so
@@ -412,7 +412,7 @@ kvd_status kvd_beam_reorder_kv(kvd_dtype dtype, const kvd_cache *layers, int32_t
                                int32_t *dev_err, kvd_stream_t stream);
 
 /*
- * kvd_beam_select -- NEXT-2. Logit filters and one beam-search selection step.
+ * kvd_beam_select -- logit filters and one beam-search selection step.
  *
  * [W] "LogitFilter チェーン" (SuppressBlank: blank ids and EOT -> -inf at the first
  * sampling position only; SuppressTokens: listed ids -> -inf at every position) and

@@ -1,5 +1,5 @@
-// attention.cu -- decode attention (A2/A3), verify-block attention (A5), the split
-// merge (A4) and the optional fused append of the new tokens (A1) for sm_103a.
+// attention.cu -- decode attention (self and cross), verify-block attention, the split
+// merge and the optional fused append of the new tokens, for sm_103a.
 //
 // What is computed ("KV キャッシュが推論を最適化する方法" steps 2-4 of "nanoVLM における KV
 // キャッシュ実装"; "Inference 抽象と KV キャッシュ" of "Whisper のデコーダー内部"; "추측

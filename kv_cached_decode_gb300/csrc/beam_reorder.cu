@@ -1,4 +1,4 @@
-// beam_reorder.cu -- A7: reorder every layer's self-attention K/V by beam parent.
+// beam_reorder.cu -- reorder every layer's self-attention K/V by beam parent.
 //
 // BeamSearchDecoder.update and rearrange_kv_cache in "Inference 抽象と KV キャッシュ" of
 // "Whisper のデコーダー内部：Beam Search、Logit フィルター、KV キャッシュ": once the beams are

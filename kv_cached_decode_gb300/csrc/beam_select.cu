@@ -1,4 +1,4 @@
-// beam_select.cu -- logit filters and the beam-search selection step (NEXT-2).
+// beam_select.cu -- logit filters and the beam-search selection step.
 //
 // "Whisper のデコーダー内部" of readoss.com:
 //  * "LogitFilter チェーン": SuppressBlank masks the blank ids and EOT at the first

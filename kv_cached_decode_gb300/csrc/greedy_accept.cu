@@ -1,4 +1,4 @@
-// greedy_accept.cu -- A6: greedy verification of k draft tokens.
+// greedy_accept.cu -- greedy verification of k draft tokens.
 //
 // "추측 디코딩이란?" of "추측 디코딩으로 Whisper 추론 속도 2배 향상" and the aitime.ge
 // speculative-decoding article: the main model's token at every candidate position is

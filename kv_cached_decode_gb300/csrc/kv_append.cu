@@ -1,4 +1,4 @@
-// kv_append.cu -- A1: write the new tokens' K/V into the preallocated cache.
+// kv_append.cu -- write the new tokens' K/V into the preallocated cache.
 //
 // "KV キャッシュが推論を最適化する方法" (steps 2-3) of "nanoVLM における KV キャッシュ実装":
 // only the newest token's K/V are computed and added to the stored cache; "Inference 抽象

@@ -1,4 +1,4 @@
-// prefill.cu -- prefill: the first forward pass over a prompt (NEXT-1 of the hot path).
+// prefill.cu -- prefill: the first forward pass over a prompt.
 //
 // "KV キャッシュが推論を最適化する方法" of "nanoVLM における KV キャッシュ実装": the
 // prefill runs the whole prompt through the model once and fills the cache with every

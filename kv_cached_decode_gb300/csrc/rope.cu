@@ -1,4 +1,4 @@
-// rope.cu -- rotary position encoding at absolute positions (NEXT-3 of the hot path).
+// rope.cu -- rotary position encoding at absolute positions.
 //
 // "nanoVLM における KV キャッシュ実装" (the LanguageModel passes start_pos so that the
 // rotary encoding of the new tokens matches their absolute positions). Rotate-half form:

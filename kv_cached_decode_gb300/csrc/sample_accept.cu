@@ -1,4 +1,4 @@
-// sample_accept.cu -- temperature sampling and stochastic speculative acceptance (NEXT-4).
+// sample_accept.cu -- temperature sampling and stochastic speculative acceptance.
 //
 // "Inference 抽象と KV キャッシュ" of "Whisper のデコーダー内部": above temperature 0 the
 // decoder samples from Categorical(logits / T). "추측 디코딩이란?" of "추측 디코딩으로

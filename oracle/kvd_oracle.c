@@ -83,7 +83,7 @@ static void copy_elem(int dtype, void *dst, int64_t di, const void *src, int64_t
     memcpy((char *)dst + (size_t)di * n, (const char *)src + (size_t)si * n, n);
 }
 
-/* ---- A1: append the new tokens' K/V to the cache -----------------------------------
+/* ---- append the new tokens' K/V to the cache ---------------------------------------
  *
  * [N] "KV キャッシュが推論を最適化する方法", steps 2-3: after the first pass only the newest
  * token's K and V are computed, and they are added to the stored per-layer K/V whose
@@ -123,7 +123,7 @@ unsigned kvo_kv_append(int dtype, int batch, int heads, int capacity, int head_d
     return err;
 }
 
-/* ---- A2 / A3 / A5: attention of a query block over cached K/V ----------------------
+/* ---- attention of a query block over cached K/V --------------------------------
  *
  * [N] "KV キャッシュが推論を最適化する方法", step 4: the current token's query is combined
  * with the cached K and V to produce the output. [W] "Inference 抽象と KV キャッシュ": the
@@ -197,7 +197,7 @@ unsigned kvo_attention(int dtype, int batch, int n_q_heads, int nq, int head_dim
     return err;
 }
 
-/* ---- A6: greedy verification -- accept up to the first mismatch --------------------
+/* ---- greedy verification -- accept up to the first mismatch ------------------------
  *
  * [W] "Inference 抽象と KV キャッシュ" (GreedyDecoder): at temperature 0 the next token is
  * the argmax of the logits. [S] "추측 디코딩이란?" and [A]: the main model's token at each
@@ -259,7 +259,7 @@ unsigned kvo_greedy_accept(int batch, int k, int vocab, const float *logits,
     return err;
 }
 
-/* ---- A7: beam-search cache reorder ------------------------------------------------
+/* ---- beam-search cache reorder ----------------------------------------------------
  *
  * [W] "Inference 抽象と KV キャッシュ" (BeamSearchDecoder.update and rearrange_kv_cache):
  * after the beams are re-ranked the stored key/value tensors must be put in the new
@@ -299,7 +299,7 @@ unsigned kvo_beam_reorder(int dtype, int rows, int beam, int heads, int capacity
     return err;
 }
 
-/* ---- NEXT-3: rotary position encoding at absolute positions -----------------------
+/* ---- rotary position encoding at absolute positions ----------------------------
  *
  * [N] "nanoVLM における KV キャッシュ実装" (the LanguageModel passes start_pos so that the
  * rotary position encoding of new tokens matches their absolute position in the

@@ -1,5 +1,5 @@
-"""GPU parity, bit-exact, of the cache append (A1), greedy accept (A6) and beam cache
-reorder (A7) against the oracle, through the C ABI."""
+"""GPU parity, bit-exact, of the cache append, greedy accept and beam cache reorder
+against the oracle, through the C ABI."""
 
 import itertools
 import json

@@ -1,4 +1,4 @@
-"""GPU parity of decode attention (A2/A3/A4) and verify attention (A5) against the
+"""GPU parity of decode attention (self, cross, split merge) and verify attention against the
 fp64 oracle, through the C ABI. Tolerance: max-abs <= 1e-2, rel-Frobenius <= 5e-3."""
 
 import numpy as np
