@@ -230,6 +230,7 @@ __global__ void __launch_bounds__(kSaThreads, 1) sample_accept_kernel(const Samp
     };
     float sw = 0.f, sp = 0.f;
     int lw = -1, lp = -1;  // the chunk's last ids with a positive weight
+    auto chunk_pass = [&]() {
     for (int e0 = c0; e0 < c1; e0 += G) {
         float xt[G], xd[G];
         load_group(e0, xt, xd);
@@ -245,6 +246,26 @@ __global__ void __launch_bounds__(kSaThreads, 1) sample_accept_kernel(const Samp
             }
         }
     }
+    };
+    if (!resid) {
+        // The draw is from p (of row n = k): each slice's sum follows from kernel A's
+        // segment pairs (slices are whole segments), so every CTA finds the owner itself:
+        // no pass over the logits and no exchange; only the owner reads its slice.
+        if (tid < p.cluster) {
+            const float2* ml = p.ws_ml + ((int64_t)b * R + n) * p.segs;
+            const int s_lo = tid * (p.slice / kSeg);
+            const int s_hi = min(p.segs, s_lo + p.slice / kSeg);
+            float a = 0.f;
+            for (int sg = s_lo; sg < s_hi; ++sg) {
+                const float2 v = __ldcg(ml + sg);
+                a += v.x == -INFINITY || !(lt > 0.f) ? 0.f : v.y * exp2f(v.x - mt) / lt;
+            }
+            S.all_s[tid][0] = a;
+            S.all_s[tid][1] = a;
+        }
+        __syncthreads();
+    } else {
+    chunk_pass();
     float rw = sw, rp = sp;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -274,6 +295,7 @@ __global__ void __launch_bounds__(kSaThreads, 1) sample_accept_kernel(const Samp
     }
     if (p.cluster > 1) cluster_sync_all();
     else __syncthreads();
+    }
     if (tid == 0) {
         // the CTA whose slice holds u * sum(w): the first whose running sum exceeds it,
         // else the last with a positive sum (rounding), else CTA 0 (no weight at all)
@@ -310,6 +332,7 @@ __global__ void __launch_bounds__(kSaThreads, 1) sample_accept_kernel(const Samp
     }
     __syncthreads();
     if (S.owner != rank) return;
+    if (!resid) chunk_pass();  // the owner's slice, read now
 
     // ---- this CTA holds the draw: exclusive scan of the chunk sums, then one chunk ----
     const bool use_p = S.use_p != 0;
@@ -391,7 +414,8 @@ kvd_status launch_sample(int batch, cudaStream_t st, bool pdl, const SampleParam
         cudaGetLastError();
         if (n > 0) break;
     }
-    q.slice = (q.vocab + q.cluster - 1) / q.cluster;
+    q.slice = ((q.vocab + q.cluster - 1) / q.cluster + kSeg - 1) / kSeg * kSeg;  // whole segments
+    q.cluster = (q.vocab + q.slice - 1) / q.slice;
     // A: the rows' segment pairs, over the whole GPU; B: the decision and the draw (a
     // dependent launch when PDL is requested: B waits for A either way)
     if (kvd_status s = launch(sample_stats_kernel, dim3((unsigned)q.segs, (unsigned)R,
@@ -444,7 +468,8 @@ extern "C" kvd_status kvd_sample_accept(const float* target, const float* draft,
     p.k = k;
     p.vocab = vocab;
     p.cluster = std::max(1, std::min(kSaMaxCluster, (vocab + kSaMinSlice - 1) / kSaMinSlice));
-    p.slice = (vocab + p.cluster - 1) / p.cluster;
+    p.slice = ((vocab + p.cluster - 1) / p.cluster + kSeg - 1) / kSeg * kSeg;  // whole segments
+    p.cluster = (vocab + p.slice - 1) / p.slice;
     p.c2 = 1.4426950408889634f / temperature;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const bool pdl = (flags & KVD_FLAG_PDL) != 0;
