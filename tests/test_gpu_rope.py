@@ -265,3 +265,36 @@ def test_prefill_rope_equals_rope_then_prefill(dtype):
         assert not err
         want[b, :, :n] = w[0]
     assert_attn_close(res[1][0], want, dtype, "prefill with rotary encoding")
+
+
+def test_fused_rope_without_workspace():
+    # the no-workspace entry point takes the same rotation: same bits as with a workspace
+    import kv_cached_decode_gb300 as kvd
+
+    rng = make_rng(930)
+    B, Hq, Hkv, cap = 4, 9, 3, 700
+    lens = np.array([5, 640, 300, 64], np.int32)
+    K, V = gen_cache(rng, B, Hkv, cap, D, "bf16", 0.125, lens=lens)
+    kn, vn = gen_new_kv(rng, B, Hkv, 1, D, "bf16", 0.125)
+    q = gen_queries(rng, B, Hq, 1, D, "bf16", 0.125)
+    res = []
+    for noalloc in (False, True):
+        Kd, Vd = dev16(K, "bf16"), dev16(V, "bf16")
+        qd, knd, vnd = dev16(q, "bf16"), dev16(kn, "bf16"), dev16(vn, "bf16")
+        lens_d, lens_out = dev_i32(lens), torch.zeros(B, dtype=torch.int32, device="cuda")
+        out = torch.empty_like(qd)
+        e = new_err()
+        app = (knd, vnd, lens_out, 500000.0)
+        if noalloc:
+            kvd.kvd_decode_attn_noalloc(qd, kvd.make_cache(Kd, Vd), out, lens=lens_d, dev_err=e,
+                                        append=app)
+        else:
+            ws = kvd.new_workspace(kvd.kvd_workspace_size(kvd.KVD_OP_DECODE_ATTN, B, Hq, Hkv, 1,
+                                                          1, cap))
+            kvd.kvd_decode_attn(qd, kvd.make_cache(Kd, Vd), out, ws, lens=lens_d, dev_err=e,
+                                append=app)
+        torch.cuda.synchronize()
+        assert e.item() == 0
+        res.append((host16(out), host16(Kd), lens_out.cpu().numpy()))
+    for a, b in zip(*res):
+        assert np.array_equal(a, b)
