@@ -231,21 +231,21 @@ __global__ void __launch_bounds__(kSaThreads, 1) sample_accept_kernel(const Samp
     float sw = 0.f, sp = 0.f;
     int lw = -1, lp = -1;  // the chunk's last ids with a positive weight
     auto chunk_pass = [&]() {
-    for (int e0 = c0; e0 < c1; e0 += G) {
-        float xt[G], xd[G];
-        load_group(e0, xt, xd);
+        for (int e0 = c0; e0 < c1; e0 += G) {
+            float xt[G], xd[G];
+            load_group(e0, xt, xd);
 #pragma unroll
-        for (int a = 0; a < G; ++a) {
-            if (e0 + a < c1) {
-                float w, pw;
-                wp(xt[a], xd[a], w, pw);
-                sw += w;
-                sp += pw;
-                if (w > 0.f) lw = e0 + a;
-                if (pw > 0.f) lp = e0 + a;
+            for (int a = 0; a < G; ++a) {
+                if (e0 + a < c1) {
+                    float w, pw;
+                    wp(xt[a], xd[a], w, pw);
+                    sw += w;
+                    sp += pw;
+                    if (w > 0.f) lw = e0 + a;
+                    if (pw > 0.f) lp = e0 + a;
+                }
             }
         }
-    }
     };
     if (!resid) {
         // The draw is from p (of row n = k): each slice's sum follows from kernel A's
@@ -265,36 +265,36 @@ __global__ void __launch_bounds__(kSaThreads, 1) sample_accept_kernel(const Samp
         }
         __syncthreads();
     } else {
-    chunk_pass();
-    float rw = sw, rp = sp;
+        chunk_pass();
+        float rw = sw, rp = sp;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        rw += __shfl_xor_sync(0xffffffffu, rw, off);
-        rp += __shfl_xor_sync(0xffffffffu, rp, off);
-    }
-    if (lane == 0) {
-        S.warp_s[warp][0] = rw;
-        S.warp_s[warp][1] = rp;
-    }
-    __syncthreads();
-    if (tid < p.cluster) {
-        // this CTA's pair into every CTA (so that no shared memory is read remotely after
-        // the barrier, and a CTA may exit as soon as it is done)
-        float a = 0.f, c = 0.f;
-        for (int w = 0; w < kSaWarps; ++w) {
-            a += S.warp_s[w][0];
-            c += S.warp_s[w][1];
+        for (int off = 16; off > 0; off >>= 1) {
+            rw += __shfl_xor_sync(0xffffffffu, rw, off);
+            rp += __shfl_xor_sync(0xffffffffu, rp, off);
         }
-        if (p.cluster > 1) {
-            st_cluster_f32(&S.all_s[rank][0], tid, a);
-            st_cluster_f32(&S.all_s[rank][1], tid, c);
-        } else {
-            S.all_s[0][0] = a;
-            S.all_s[0][1] = c;
+        if (lane == 0) {
+            S.warp_s[warp][0] = rw;
+            S.warp_s[warp][1] = rp;
         }
-    }
-    if (p.cluster > 1) cluster_sync_all();
-    else __syncthreads();
+        __syncthreads();
+        if (tid < p.cluster) {
+            // this CTA's pair into every CTA (so that no shared memory is read remotely after
+            // the barrier, and a CTA may exit as soon as it is done)
+            float a = 0.f, c = 0.f;
+            for (int w = 0; w < kSaWarps; ++w) {
+                a += S.warp_s[w][0];
+                c += S.warp_s[w][1];
+            }
+            if (p.cluster > 1) {
+                st_cluster_f32(&S.all_s[rank][0], tid, a);
+                st_cluster_f32(&S.all_s[rank][1], tid, c);
+            } else {
+                S.all_s[0][0] = a;
+                S.all_s[0][1] = c;
+            }
+        }
+        if (p.cluster > 1) cluster_sync_all();
+        else __syncthreads();
     }
     if (tid == 0) {
         // the CTA whose slice holds u * sum(w): the first whose running sum exceeds it,
