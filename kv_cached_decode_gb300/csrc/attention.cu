@@ -105,7 +105,8 @@ struct SmemLayout {
     uint32_t bar_off, red_off, mrg_off, misc_off, qoff_off, app_off, total;
 };
 // app_rows: 256-byte units staged for the fused append: qlen (the K and V rows), plus
-// qlen more with rotary encoding (the cos/sin table, 32 float2 per token), else 0.
+// with rotary encoding qlen more (the cos/sin table, 32 float2 per token) and the
+// rotated query rows of the block, else 0.
 __host__ __device__ inline SmemLayout smem_layout(int stages, int rmax, int merge_slots,
                                                   int app_rows) {
     SmemLayout L;
@@ -123,8 +124,12 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int rmax, int merg
 __host__ __device__ inline int merge_slots(int cluster, int splits, int msub) {
     return cluster ? splits * msub : 0;
 }
+// The rotated query rows of a tensor-core block (16 rows, 144-byte stride so that the
+// ldmatrix rows fall in distinct banks): 2304 bytes = 9 units.
+constexpr int kQsStride = 144;
+constexpr int kQsUnits = 9;
 __host__ __device__ inline int app_units(int append, int rope, int qlen) {
-    return append ? qlen * (rope ? 2 : 1) : 0;
+    return append ? qlen * (rope ? 2 : 1) + (rope ? kQsUnits : 0) : 0;
 }
 __host__ __device__ inline int app_units(const AttnParams& p) {
     return app_units(p.append, p.rope, p.qlen);
@@ -789,33 +794,44 @@ __global__ void __launch_bounds__(kThreads, MINB)
     uint32_t qa[4][4];
     const T* qbase = static_cast<const T*>(p.q);
     const bool rowA = qr < c.mcount, rowB = qr + 8 < c.mcount;
-    const int64_t offA = rowA ? qoff[qr] : 0;
-    const int64_t offB = rowB ? qoff[qr + 8] : 0;
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        const int d0 = kk * 16 + qc;
-        qa[kk][0] = rowA ? *reinterpret_cast<const uint32_t*>(qbase + offA + d0) : 0u;
-        qa[kk][1] = rowB ? *reinterpret_cast<const uint32_t*>(qbase + offB + d0) : 0u;
-        qa[kk][2] = rowA ? *reinterpret_cast<const uint32_t*>(qbase + offA + d0 + 8) : 0u;
-        qa[kk][3] = rowB ? *reinterpret_cast<const uint32_t*>(qbase + offB + d0 + 8) : 0u;
-    }
     if (ROPE) {
-        // query m is token m % qlen of the new tokens; k-steps kk and kk + 2 hold the two
-        // halves of the same rotation pairs in this lane
+        // The block's query rows are rotated once, into shared memory (16 threads per
+        // row, 2 rotation pairs each; query m is token m % qlen of the new tokens), and
+        // every warp then loads its fragments from there with ldmatrix.
+        uint8_t* qs = smem + L.app_off + p.qlen * 4 * kRowBytes;
         const float2* tab = rope_table(p, smem + L.app_off);
-        const int jA = (c.m0 + qr) % p.qlen, jB = (c.m0 + qr + 8) % p.qlen;
+        const int m = tid >> 4, g = tid & 15;
+        uint32_t lo = 0u, hi = 0u;  // dims (2g, 2g + 1) and (2g + 32, 2g + 33)
+        if (m < c.mcount) {
+            const T* row = qbase + qoff[m];
+            lo = *reinterpret_cast<const uint32_t*>(row + 2 * g);
+            hi = *reinterpret_cast<const uint32_t*>(row + 32 + 2 * g);
+            const float2* tr = tab + ((c.m0 + m) % p.qlen) * 32;
+            float2 x0 = Half16<T>::to_f2(lo), x1 = Half16<T>::to_f2(hi);
+            rope_rotate(x0.x, x1.x, tr[2 * g]);
+            rope_rotate(x0.y, x1.y, tr[2 * g + 1]);
+            lo = Half16<T>::from_f2(x0.x, x0.y);
+            hi = Half16<T>::from_f2(x1.x, x1.y);
+        }
+        *reinterpret_cast<uint32_t*>(qs + m * kQsStride + 4 * g) = lo;
+        *reinterpret_cast<uint32_t*>(qs + m * kQsStride + 64 + 4 * g) = hi;
+        __syncthreads();
+        const uint32_t qb = smem_u32(qs) + (uint32_t)(((lane & 7) + ((lane >> 3) & 1) * 8) * kQsStride +
+                                                      (lane >> 4) * 16);
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
+        for (int kk = 0; kk < 4; ++kk)
+            ldsm_x4(qb + kk * 32, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+    } else {
+        const int64_t offA = rowA ? qoff[qr] : 0;
+        const int64_t offB = rowB ? qoff[qr + 8] : 0;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = kk * 16 + qc + (e >= 2 ? 8 : 0);
-                const float2* tr = tab + ((e & 1) ? jB : jA) * 32;
-                float2 lo = Half16<T>::to_f2(qa[kk][e]), hi = Half16<T>::to_f2(qa[kk + 2][e]);
-                rope_rotate(lo.x, hi.x, tr[i]);
-                rope_rotate(lo.y, hi.y, tr[i + 1]);
-                qa[kk][e] = Half16<T>::from_f2(lo.x, lo.y);
-                qa[kk + 2][e] = Half16<T>::from_f2(hi.x, hi.y);
-            }
+        for (int kk = 0; kk < 4; ++kk) {
+            const int d0 = kk * 16 + qc;
+            qa[kk][0] = rowA ? *reinterpret_cast<const uint32_t*>(qbase + offA + d0) : 0u;
+            qa[kk][1] = rowB ? *reinterpret_cast<const uint32_t*>(qbase + offB + d0) : 0u;
+            qa[kk][2] = rowA ? *reinterpret_cast<const uint32_t*>(qbase + offA + d0 + 8) : 0u;
+            qa[kk][3] = rowB ? *reinterpret_cast<const uint32_t*>(qbase + offB + d0 + 8) : 0u;
+        }
     }
     auto limit_of = [&](int r, bool live) -> int {
         if (!live) return 0;
@@ -970,9 +986,10 @@ enum Variant { kSimt = 1, kMma = 2, kMma3 = 3, kSimtRope = 4, kMmaRope = 5 };
 template <typename T>
 int prepare(int var) {
     const uint32_t mma_smem =
-        smem_layout(kMaxStages, 16, kMaxClusterSplits * kMmaQueryBlock, 2 * KVD_MAX_QLEN).total;
+        smem_layout(kMaxStages, 16, kMaxClusterSplits * kMmaQueryBlock,
+                    2 * KVD_MAX_QLEN + kQsUnits).total;
     const uint32_t simt_smem =
-        smem_layout(kMaxStages, 1, kMaxClusterSplits, 2 * KVD_MAX_QLEN).total;
+        smem_layout(kMaxStages, 1, kMaxClusterSplits, 2 * KVD_MAX_QLEN + kQsUnits).total;
     switch (var) {
     case kMma: return prepare_kernel<block_attn_kernel<T, 2, false>>(mma_smem);
     case kMma3: return prepare_kernel<block_attn_kernel<T, 3, false>>(mma_smem);
