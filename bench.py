@@ -722,6 +722,9 @@ def run_sweep(args):
     if args.sweep_part in parts:
         parts[args.sweep_part](torch, kvd, dev, stream, peak, flags)
         return 0
+    if args.sweep_part == "prefill":
+        run_prefill(torch, kvd, dev, stream, flags)
+        return 0
     w = WORKLOADS["decode_sweep"]
     for (Hq, Hkv) in w["heads"]:
         for B in w["batches"]:
@@ -1151,7 +1154,7 @@ def main(argv=None):
                     help="decode-attention batch x length sweep, the beam step, the GQA-LM "
                          "step, the tiny layer and the verify/decode ratio (JSON lines)")
     ap.add_argument("--sweep-part", choices=["beam_step", "beam_select", "gqa_lm_step",
-                                             "sample_accept"],
+                                             "sample_accept", "prefill"],
                     default=None, help="with --sweep: run only this part")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--traffic", type=float, default=None,

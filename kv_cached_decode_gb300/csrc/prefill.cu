@@ -182,16 +182,28 @@ __global__ void __launch_bounds__(kPfThreads)
             }
         }
         float tA = -INFINITY, tB = -INFINITY;
+        if (__all_sync(0xffffffffu, t0 + kTile <= min(limA, limB))) {
+            // the whole tile is visible to every row of the warp: no mask
 #pragma unroll
-        for (int n = 0; n < 8; ++n)
+            for (int n = 0; n < 8; ++n)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int key = t0 + n * 8 + qc + (e & 1);
-                const bool vis = key < (e < 2 ? limA : limB);
-                s[n][e] = vis ? s[n][e] * p.scale_log2 : -INFINITY;
-                if (e < 2) tA = fmaxf(tA, s[n][e]);
-                else tB = fmaxf(tB, s[n][e]);
-            }
+                for (int e = 0; e < 4; ++e) {
+                    s[n][e] *= p.scale_log2;
+                    if (e < 2) tA = fmaxf(tA, s[n][e]);
+                    else tB = fmaxf(tB, s[n][e]);
+                }
+        } else {
+#pragma unroll
+            for (int n = 0; n < 8; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int key = t0 + n * 8 + qc + (e & 1);
+                    const bool vis = key < (e < 2 ? limA : limB);
+                    s[n][e] = vis ? s[n][e] * p.scale_log2 : -INFINITY;
+                    if (e < 2) tA = fmaxf(tA, s[n][e]);
+                    else tB = fmaxf(tB, s[n][e]);
+                }
+        }
         tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 1));
         tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 2));
         tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 1));
