@@ -1,0 +1,126 @@
+// kvd_tc.cuh -- fifth-generation tensor core (tcgen05) helpers for sm_103a: tensor
+// memory allocation, shared-memory matrix descriptors, the instruction descriptor of
+// kind::f16 MMAs, single-thread MMA issue with completion on an mbarrier, and loads of
+// accumulator rows from tensor memory.
+//
+// Conventions used by every caller:
+//   * operands live in shared memory in the 128-byte-swizzled layout that TMA writes
+//     with CU_TENSOR_MAP_SWIZZLE_128B: rows of 64 16-bit elements (128 B), 16-byte chunk
+//     c of row r stored at chunk c ^ (r % 8), 8-row groups 1024 B apart, every tile
+//     1024-byte aligned;
+//   * an M = 128 accumulator occupies tensor-memory lanes 0..127 (lane = row), one
+//     32-bit column per fp32 element; warp w of the block reads lanes 32w..32w+31.
+#pragma once
+
+#include <cstdint>
+
+namespace kvd {
+
+// Allocate `ncols` tensor-memory columns (a power of two >= 32) for this CTA; the base
+// address is written to shared memory at `dst`. Executed by one whole warp.
+__device__ __forceinline__ void tc_alloc(uint32_t dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+// Free the allocation; executed by the warp that allocated it.
+__device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(ncols)
+                 : "memory");
+}
+// Order tensor-core operations around a thread barrier (before it / after it).
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a 128-byte-swizzled operand starting at `saddr`:
+// start address, leading and stride byte offsets (all in 16-byte units), the
+// descriptor version bit of this architecture (bit 46) and the swizzle mode (2 =
+// 128-byte swizzle, bits 61..63). Both offsets are 1024 B: the distance between 8-row
+// groups; the leading offset is not used by the shapes here (an operand's extent along
+// its contiguous dimension is at most one 128-byte row).
+__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(1024u >> 4) << 16) |
+           ((uint64_t)(1024u >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of a dense kind::f16 MMA with fp32 accumulation: A and B both
+// fp16 (bf16 = false) or both bf16; A K-major; B K-major or, with b_mn_major, MN-major;
+// M = 128 or 64, N a multiple of 16 up to 256.
+__host__ __device__ constexpr uint32_t tc_idesc_f16(bool bf16, int m, int n, bool b_mn_major) {
+    return (1u << 4)                                   // D: fp32
+           | ((bf16 ? 1u : 0u) << 7)                   // A type
+           | ((bf16 ? 1u : 0u) << 10)                  // B type
+           | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
+           | ((uint32_t)(n >> 3) << 17)                // N / 8
+           | ((uint32_t)(m >> 4) << 24);               // M / 16
+}
+
+// D[tmem] (+)= A[smem] . B[smem]^T for one K = 16 step; issued by a single thread.
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on the mbarrier when every MMA this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// This thread's lane of 32 consecutive fp32 columns starting at `taddr`, complete on
+// return (the load and its wait are one statement, so no use can move between them).
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+        "[%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Store 32 consecutive fp32 columns of this thread's lane at `taddr`, complete on return.
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const float* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
+}  // namespace kvd

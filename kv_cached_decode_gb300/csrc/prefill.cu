@@ -10,26 +10,33 @@
 // for j < plens[b] (rows past a row's prompt length are written as zeros).
 //
 // Design: the prompt's K/V are first written into the cache by the append kernel (with a
-// per-row count), then one block handles 64 query positions of one query head: four
-// warps of 16 rows each, with Q as m16n8k16 A fragments in registers. K/V tiles of 64
-// positions arrive by TMA (128-byte swizzle) through a 3-stage ring and are shared by
-// the four warps: S = Q.K^T and O = P.V run on the tensor cores (mma.sync, fp32
-// accumulate) with an online softmax in exp2 form; only the tiles a block's rows can see
-// are read (causal), and blocks with the most tiles start first.
+// per-row count), then one block of four warps handles 128 query positions of one query
+// head, one row per thread. The rows, rotated if asked, are staged once into shared
+// memory in the 128-byte-swizzled layout; K/V tiles of 64 positions arrive by TMA (the
+// same swizzle) through a 4-stage ring. Both products run on the fifth-generation tensor
+// cores: S = Q.K^T (M 128, N 64, K 64) and P.V (M 128, N 64, K 64, V read MN-major) are
+// issued by one thread as tcgen05.mma with fp32 accumulators in tensor memory, and each
+// thread reads its row of S back with tcgen05.ld, applies the causal mask and the online
+// softmax in exp2 form, and writes its row of P (rounded to the input type) to shared
+// memory for the second product; the output row accumulates in registers. Only the
+// tiles a block's rows can see are read, and blocks with the most tiles start first.
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "kvd_common.cuh"
 #include "kvd_internal.h"
+#include "kvd_tc.cuh"
 
 namespace kvd {
 namespace {
 
-constexpr int kPfWarps = 4;
-constexpr int kPfThreads = kPfWarps * 32;
-constexpr int kPfRows = kPfWarps * 16;  // query positions per block
-constexpr int kPfStages = 3;
-constexpr uint32_t kPfSmem = kPfStages * 2 * kTileBytes + kPfStages * 8 + 1024;
+constexpr int kPfThreads = 128;  // four warps: thread t owns query row t of the block
+constexpr int kPfRows = 128;     // query positions per block (the MMAs' M)
+constexpr int kPfStages = 4;     // K/V tiles in flight
+constexpr uint32_t kPfCols = 128;                    // tensor memory: S (64) + P.V (64)
+constexpr uint32_t kPfRowsBytes = kPfRows * kRowBytes;  // 16 KiB: the Q or the P block
+constexpr uint32_t kPfSmem = kPfStages * 2 * kTileBytes + 2 * kPfRowsBytes + 64 + 1024;
 
 struct PrefillParams {
     const void* q;            // [batch, n_q_heads, max_len, 64]
@@ -47,31 +54,34 @@ __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
 }
 
 template <typename T, bool ROPE>
-__global__ void __launch_bounds__(kPfThreads)
+__global__ void __launch_bounds__(kPfThreads, 2)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPfStages * 2 * kTileBytes);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint8_t* sQ = smem + kPfStages * 2 * kTileBytes;
+    uint8_t* sP = sQ + kPfRowsBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kPfRowsBytes);  // stages, then MMA
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kPfStages + 1);
+    const uint32_t mma_bar = smem_u32(&bars[kPfStages]);
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int qt = p.q_tiles - 1 - (int)blockIdx.x;  // the blocks with most tiles first
     const int hq = blockIdx.y, b = blockIdx.z, hk = hq / p.group;
     pdl_wait();
     const int s0 = p.lens_in ? p.lens_in[b] : 0;
     const int plen = p.plens[b];
     const int q0 = qt * kPfRows;
+    const int row = q0 + tid;
     const int64_t head_off = ((int64_t)b * p.n_q_heads + hq) * p.max_len * kHeadDim;
-    T* outp = static_cast<T*>(p.out) + head_off;
+    T* outr = static_cast<T*>(p.out) + head_off + (int64_t)row * kHeadDim;
     // a row the append rejected (length out of range) gets zeros, like padding rows
     const bool bad = s0 < 0 || plen < 0 || plen > p.max_len || (int64_t)s0 + plen > p.capacity;
     const int rows_live = bad ? 0 : max(0, min(kPfRows, plen - q0));
     if (rows_live == 0) {
-        for (int x = tid; x < kPfRows * 8; x += kPfThreads) {
-            const int r = q0 + (x >> 3);
-            if (r < p.max_len)
-                *reinterpret_cast<uint4*>(outp + (int64_t)r * kHeadDim + (x & 7) * 8) =
-                    make_uint4(0u, 0u, 0u, 0u);
-        }
+        if (row < p.max_len)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                reinterpret_cast<uint4*>(outr)[c] = make_uint4(0u, 0u, 0u, 0u);
         pdl_trigger();
         return;
     }
@@ -87,70 +97,61 @@ __global__ void __launch_bounds__(kPfThreads)
         tma_load_4d(dk + kTileBytes, &tmv, bar, 0, j * kTile, hk, b);
     };
     if (tid == 0) {
-        for (int j = 0; j < kPfStages; ++j) mbar_init(smem_u32(&bars[j]), 1);
+        for (int j = 0; j <= kPfStages; ++j) mbar_init(smem_u32(&bars[j]), 1);
         fence_barrier_init();
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
         for (int j = 0; j < min(kPfStages, n_tiles); ++j) issue(j);
     }
+    if (warp == 0) {
+        tc_alloc(smem_u32(tslot), kPfCols);
+        tc_relinquish();
+    }
+
+    // This thread's query row (zeros past the prompt), rotated at position s0 + row,
+    // into the swizzled A operand.
+    const bool live = row < plen;
+    uint4 qv[8];
+    const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + head_off +
+                                                       (int64_t)row * kHeadDim);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) qv[c] = live ? qrow[c] : make_uint4(0u, 0u, 0u, 0u);
+    if (ROPE && live) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) rope_rotate8_at<T>(qv[c], qv[c + 4], s0 + row, 8 * c, p.rope_log2_base);
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(sQ + swz(tid, c)) = qv[c];
+    fence_proxy_async();  // generic writes, read by the tensor cores
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
     pdl_trigger();
 
-    // This warp's 16 query rows as m16n8k16 A fragments (rows past the prompt are 0).
-    const int qr = lane >> 2, qc = (lane & 3) * 2;  // fragment row / column pair
-    const int jm = lane >> 3, rr = lane & 7;         // ldmatrix matrix / row
-    const int rowA = q0 + warp * 16 + qr, rowB = rowA + 8;
-    const bool liveA = rowA < plen, liveB = rowB < plen;
-    const T* qbase = static_cast<const T*>(p.q) + head_off;
-    uint32_t qa[4][4];
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        const int d0 = kk * 16 + qc;
-        const T* a = qbase + (int64_t)rowA * kHeadDim + d0;
-        const T* bq = qbase + (int64_t)rowB * kHeadDim + d0;
-        qa[kk][0] = liveA ? *reinterpret_cast<const uint32_t*>(a) : 0u;
-        qa[kk][1] = liveB ? *reinterpret_cast<const uint32_t*>(bq) : 0u;
-        qa[kk][2] = liveA ? *reinterpret_cast<const uint32_t*>(a + 8) : 0u;
-        qa[kk][3] = liveB ? *reinterpret_cast<const uint32_t*>(bq + 8) : 0u;
-    }
-    if (ROPE) {
-        // prompt row r sits at position s0 + r; k-steps kk and kk + 2 hold the two halves
-        // of the same rotation pairs in this lane
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = kk * 16 + qc + (e >= 2 ? 8 : 0);
-                const int pos = s0 + ((e & 1) ? rowB : rowA);
-                float2 lo = Half16<T>::to_f2(qa[kk][e]), hi = Half16<T>::to_f2(qa[kk + 2][e]);
-                rope_rotate(lo.x, hi.x, rope_cos_sin(pos, i, p.rope_log2_base));
-                rope_rotate(lo.y, hi.y, rope_cos_sin(pos, i + 1, p.rope_log2_base));
-                qa[kk][e] = Half16<T>::from_f2(lo.x, lo.y);
-                qa[kk + 2][e] = Half16<T>::from_f2(hi.x, hi.y);
-            }
-    }
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t kIdS = tc_idesc_f16(kBf16, kPfRows, kTile, false);
+    constexpr uint32_t kIdO = tc_idesc_f16(kBf16, kPfRows, kHeadDim, true);
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;  // this warp's 32 lanes
+    const uint32_t qaddr = smem_u32(sQ), paddr = smem_u32(sP);
     // keys t < lim are visible; rows past the prompt are clamped to the live rows' keys
-    // (positions beyond hold other data) and written as zeros
-    const int limA = min(s0 + rowA + 1, kv_end), limB = min(s0 + rowB + 1, kv_end);
+    // (positions beyond hold other data) and written as zeros. Rows ascend with the
+    // lane, so lane 0 holds the warp's smallest limit.
+    const int lim = min(s0 + row + 1, kv_end);
+    const int lim_warp = __shfl_sync(0xffffffffu, lim, 0);
 
-    float oacc[8][4];
+    float o[kHeadDim];
 #pragma unroll
-    for (int n = 0; n < 8; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) oacc[n][e] = 0.f;
-    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
-
-    for (int j = 0; j < n_tiles; ++j) {
+    for (int d = 0; d < kHeadDim; ++d) o[d] = 0.f;
+    float m = -INFINITY, l = 0.f;
+    uint32_t mph = 0;
+    bool failed = false;
+    int j = 0;
+    for (; j < n_tiles; ++j) {
         const int st = j % kPfStages;
-        const bool ok = mbar_wait_bounded(smem_u32(&bars[st]), (j / kPfStages) & 1);
-        if (__syncthreads_or(!ok)) {
-            // let the copies still in flight land, then leave; the outputs stay unwritten
-            if (tid == 0) {
-                flag_error(p.dev_err, KVD_ERR_TIMEOUT);
-                for (int jj = j; jj < min(n_tiles, j + kPfStages); ++jj)
-                    mbar_wait_bounded(smem_u32(&bars[jj % kPfStages]), (jj / kPfStages) & 1);
-            }
-            return;
+        if (__syncthreads_or(!mbar_wait_bounded(smem_u32(&bars[st]), (j / kPfStages) & 1))) {
+            failed = true;
+            break;
         }
         uint8_t* sK = smem + st * 2 * kTileBytes;
         uint8_t* sV = sK + kTileBytes;
@@ -162,115 +163,120 @@ __global__ void __launch_bounds__(kPfThreads)
             for (int x = tid; x < (kTile - first) * 8; x += kPfThreads)
                 *reinterpret_cast<uint4*>(sV + swz(first + (x >> 3), x & 7)) =
                     make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async();
             __syncthreads();
         }
-        const uint32_t kb = smem_u32(sK), vb = smem_u32(sV);
-        // S = Q . K^T over the 64 keys of the tile: 8 key blocks of 8
-        float s[8][4];
+        // S = Q . K^T for the tile's 64 keys
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t kaddr = smem_u32(sK);
 #pragma unroll
-        for (int n = 0; n < 8; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) s[n][e] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kb + swz(np * 16 + (jm >> 1) * 8 + rr, kk * 2 + (jm & 1)), b0, b1, b2, b3);
-                Mma<T>::run(s[2 * np], qa[kk], b0, b1);
-                Mma<T>::run(s[2 * np + 1], qa[kk], b2, b3);
-            }
+            for (int kk = 0; kk < 4; ++kk)
+                tc_mma_f16(tmem, tc_desc_sw128(qaddr + kk * 32), tc_desc_sw128(kaddr + kk * 32),
+                           kIdS, kk);
+            tc_commit(mma_bar);
         }
-        float tA = -INFINITY, tB = -INFINITY;
-        if (__all_sync(0xffffffffu, t0 + kTile <= min(limA, limB))) {
+        if (__syncthreads_or(!mbar_wait_bounded(mma_bar, mph))) {
+            failed = true;
+            break;
+        }
+        mph ^= 1;
+        tc_fence_after();
+        float s[kTile];
+        tc_ld32(tmem + lane_off, s);
+        tc_ld32(tmem + lane_off + 32, s + 32);
+        float tmax = -INFINITY;
+        if (t0 + kTile <= lim_warp) {
             // the whole tile is visible to every row of the warp: no mask
 #pragma unroll
-            for (int n = 0; n < 8; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    s[n][e] *= p.scale_log2;
-                    if (e < 2) tA = fmaxf(tA, s[n][e]);
-                    else tB = fmaxf(tB, s[n][e]);
-                }
+            for (int i = 0; i < kTile; ++i) {
+                s[i] *= p.scale_log2;
+                tmax = fmaxf(tmax, s[i]);
+            }
         } else {
 #pragma unroll
-            for (int n = 0; n < 8; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int key = t0 + n * 8 + qc + (e & 1);
-                    const bool vis = key < (e < 2 ? limA : limB);
-                    s[n][e] = vis ? s[n][e] * p.scale_log2 : -INFINITY;
-                    if (e < 2) tA = fmaxf(tA, s[n][e]);
-                    else tB = fmaxf(tB, s[n][e]);
-                }
-        }
-        tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 1));
-        tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 2));
-        tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 1));
-        tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 2));
-        const float nA = fmaxf(mA, tA), nB = fmaxf(mB, tB);
-        const float refA = nA == -INFINITY ? 0.f : nA, refB = nB == -INFINITY ? 0.f : nB;
-        const float aA = exp2f(mA - refA), aB = exp2f(mB - refB);
-        mA = nA;
-        mB = nB;
-        // P, rounded to the input type, as A fragments of the four 16-key steps; the
-        // normaliser sums the rounded weights that multiply V
-        uint32_t pa[4][4];
-        float sumA = 0.f, sumB = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            pa[ks][0] = Half16<T>::from_f2(exp2f(s[2 * ks][0] - refA), exp2f(s[2 * ks][1] - refA));
-            pa[ks][1] = Half16<T>::from_f2(exp2f(s[2 * ks][2] - refB), exp2f(s[2 * ks][3] - refB));
-            pa[ks][2] =
-                Half16<T>::from_f2(exp2f(s[2 * ks + 1][0] - refA), exp2f(s[2 * ks + 1][1] - refA));
-            pa[ks][3] =
-                Half16<T>::from_f2(exp2f(s[2 * ks + 1][2] - refB), exp2f(s[2 * ks + 1][3] - refB));
-            const float2 r0 = Half16<T>::to_f2(pa[ks][0]), r1 = Half16<T>::to_f2(pa[ks][1]);
-            const float2 r2 = Half16<T>::to_f2(pa[ks][2]), r3 = Half16<T>::to_f2(pa[ks][3]);
-            sumA += (r0.x + r0.y) + (r2.x + r2.y);
-            sumB += (r1.x + r1.y) + (r3.x + r3.y);
-        }
-        lA = fmaf(lA, aA, sumA);
-        lB = fmaf(lB, aB, sumB);
-#pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            oacc[n][0] *= aA;
-            oacc[n][1] *= aA;
-            oacc[n][2] *= aB;
-            oacc[n][3] *= aB;
-        }
-        // O += P . V: four 16-key steps x 8 blocks of 8 dims
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t v0, v1, v2, v3;
-                ldsm_x4_t(vb + swz(ks * 16 + (jm & 1) * 8 + rr, 2 * np + (jm >> 1)), v0, v1, v2, v3);
-                Mma<T>::run(oacc[2 * np], pa[ks], v0, v1);
-                Mma<T>::run(oacc[2 * np + 1], pa[ks], v2, v3);
+            for (int i = 0; i < kTile; ++i) {
+                s[i] = t0 + i < lim ? s[i] * p.scale_log2 : -INFINITY;
+                tmax = fmaxf(tmax, s[i]);
             }
         }
-        __syncthreads();  // every warp is done with this stage
+        const float mn = fmaxf(m, tmax);
+        const float ref = mn == -INFINITY ? 0.f : mn;
+        const float alpha = exp2f(m - ref);
+        m = mn;
+        // P, rounded to the input type, into this row of the swizzled A operand; the
+        // normaliser sums the rounded weights that multiply V
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                w[e] = Half16<T>::from_f2(exp2f(s[8 * c + 2 * e] - ref),
+                                          exp2f(s[8 * c + 2 * e + 1] - ref));
+                const float2 r = Half16<T>::to_f2(w[e]);
+                sum += r.x + r.y;
+            }
+            *reinterpret_cast<uint4*>(sP + swz(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        l = fmaf(l, alpha, sum);
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        // P.V for the tile, into its own accumulator
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t vaddr = smem_u32(sV);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                tc_mma_f16(tmem + kTile, tc_desc_sw128(paddr + kk * 32),
+                           tc_desc_sw128(vaddr + kk * 16 * kRowBytes), kIdO, kk);
+            tc_commit(mma_bar);
+        }
+        if (__syncthreads_or(!mbar_wait_bounded(mma_bar, mph))) {
+            failed = true;
+            break;
+        }
+        mph ^= 1;
+        tc_fence_after();
+        float pv[kHeadDim];
+        tc_ld32(tmem + lane_off + kTile, pv);
+        tc_ld32(tmem + lane_off + kTile + 32, pv + 32);
+#pragma unroll
+        for (int d = 0; d < kHeadDim; ++d) o[d] = fmaf(o[d], alpha, pv[d]);
+        // the stage's MMAs have completed (the wait above): refill it
         if (tid == 0 && j + kPfStages < n_tiles) {
-            fence_proxy_async();  // generic writes (cleared rows) before the refill
+            fence_proxy_async();
             issue(j + kPfStages);
         }
     }
 
-    lA += __shfl_xor_sync(0xffffffffu, lA, 1);
-    lA += __shfl_xor_sync(0xffffffffu, lA, 2);
-    lB += __shfl_xor_sync(0xffffffffu, lB, 1);
-    lB += __shfl_xor_sync(0xffffffffu, lB, 2);
-    const float invA = liveA && lA > 0.f ? 1.f / lA : 0.f;
-    const float invB = liveB && lB > 0.f ? 1.f / lB : 0.f;
+    if (failed) {
+        // let the copies still in flight land, then leave; the outputs stay unwritten
+        if (tid == 0) {
+            flag_error(p.dev_err, KVD_ERR_TIMEOUT);
+            for (int jj = j; jj < min(n_tiles, j + kPfStages); ++jj)
+                mbar_wait_bounded(smem_u32(&bars[jj % kPfStages]), (jj / kPfStages) & 1);
+        }
+    } else if (row < p.max_len) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-    for (int n = 0; n < 8; ++n) {
-        if (rowA < p.max_len)
-            *reinterpret_cast<uint32_t*>(outp + (int64_t)rowA * kHeadDim + n * 8 + qc) =
-                liveA ? Half16<T>::from_f2(oacc[n][0] * invA, oacc[n][1] * invA) : 0u;
-        if (rowB < p.max_len)
-            *reinterpret_cast<uint32_t*>(outp + (int64_t)rowB * kHeadDim + n * 8 + qc) =
-                liveB ? Half16<T>::from_f2(oacc[n][2] * invB, oacc[n][3] * invB) : 0u;
+        for (int c = 0; c < 8; ++c) {
+            uint4 w = make_uint4(0u, 0u, 0u, 0u);  // rows past the prompt: +0
+            if (live) {
+                w.x = Half16<T>::from_f2(o[8 * c] * inv, o[8 * c + 1] * inv);
+                w.y = Half16<T>::from_f2(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+                w.z = Half16<T>::from_f2(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+                w.w = Half16<T>::from_f2(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+            }
+            reinterpret_cast<uint4*>(outr)[c] = w;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tc_dealloc(tmem, kPfCols);
     }
 }
 
