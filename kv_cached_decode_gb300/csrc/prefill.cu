@@ -34,9 +34,12 @@ namespace {
 constexpr int kPfThreads = 128;  // four warps: thread t owns query row t of the block
 constexpr int kPfRows = 128;     // query positions per block (the MMAs' M)
 constexpr int kPfStages = 4;     // K/V tiles in flight
-constexpr uint32_t kPfCols = 128;                    // tensor memory: S (64) + P.V (64)
+constexpr uint32_t kPfCols = 256;  // tensor memory: two S buffers (64 + 64), O (64)
 constexpr uint32_t kPfRowsBytes = kPfRows * kRowBytes;  // 16 KiB: the Q or the P block
-constexpr uint32_t kPfSmem = kPfStages * 2 * kTileBytes + 2 * kPfRowsBytes + 64 + 1024;
+constexpr uint32_t kPfSmem = kPfStages * 2 * kTileBytes + 2 * kPfRowsBytes + 128 + 1024;
+// The softmax reference of a row moves only when its maximum grows by more than this
+// (log2 units): the weights then stay below 2^8 and the output is rescaled rarely.
+constexpr float kRescaleLog2 = 8.f;
 
 struct PrefillParams {
     const void* q;            // [batch, n_q_heads, max_len, 64]
@@ -61,9 +64,9 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     uint8_t* smem = align_1024(smem_raw);
     uint8_t* sQ = smem + kPfStages * 2 * kTileBytes;
     uint8_t* sP = sQ + kPfRowsBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kPfRowsBytes);  // stages, then MMA
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kPfStages + 1);
-    const uint32_t mma_bar = smem_u32(&bars[kPfStages]);
+    // barriers: one per stage, S buffers 0 and 1, O, and the drain after a failure
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kPfRowsBytes);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kPfStages + 4);
     const int tid = threadIdx.x, warp = tid >> 5;
     const int qt = p.q_tiles - 1 - (int)blockIdx.x;  // the blocks with most tiles first
     const int hq = blockIdx.y, b = blockIdx.z, hk = hq / p.group;
@@ -97,7 +100,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         tma_load_4d(dk + kTileBytes, &tmv, bar, 0, j * kTile, hk, b);
     };
     if (tid == 0) {
-        for (int j = 0; j <= kPfStages; ++j) mbar_init(smem_u32(&bars[j]), 1);
+        for (int j = 0; j < kPfStages + 4; ++j) mbar_init(smem_u32(&bars[j]), 1);
         fence_barrier_init();
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
@@ -133,58 +136,46 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     constexpr uint32_t kIdS = tc_idesc_f16(kBf16, kPfRows, kTile, false);
     constexpr uint32_t kIdO = tc_idesc_f16(kBf16, kPfRows, kHeadDim, true);
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;  // this warp's 32 lanes
+    const uint32_t t_o = tmem + 2 * kTile;                  // the output accumulator
     const uint32_t qaddr = smem_u32(sQ), paddr = smem_u32(sP);
+    const uint32_t bar_o = smem_u32(&bars[kPfStages + 2]);
+    const uint32_t bar_drain = smem_u32(&bars[kPfStages + 3]);
+    auto bar_s = [&](int j) { return smem_u32(&bars[kPfStages + (j & 1)]); };
+    // S_j = Q . K_j^T into S buffer j % 2, once tile j has landed (thread 0)
+    auto issue_s = [&](int j) -> bool {
+        const int st = j % kPfStages;
+        if (!mbar_wait_bounded(smem_u32(&bars[st]), (j / kPfStages) & 1)) return false;
+        tc_fence_after();
+        const uint32_t kaddr = smem_u32(smem + st * 2 * kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            tc_mma_f16(tmem + (j & 1) * kTile, tc_desc_sw128(qaddr + kk * 32),
+                       tc_desc_sw128(kaddr + kk * 32), kIdS, kk);
+        tc_commit(bar_s(j));
+        return true;
+    };
     // keys t < lim are visible; rows past the prompt are clamped to the live rows' keys
     // (positions beyond hold other data) and written as zeros. Rows ascend with the
     // lane, so lane 0 holds the warp's smallest limit.
     const int lim = min(s0 + row + 1, kv_end);
     const int lim_warp = __shfl_sync(0xffffffffu, lim, 0);
 
-    float o[kHeadDim];
-#pragma unroll
-    for (int d = 0; d < kHeadDim; ++d) o[d] = 0.f;
-    float m = -INFINITY, l = 0.f;
-    uint32_t mph = 0;
-    bool failed = false;
+    // Pipeline per tile j: thread 0 issues S_{j+1} while the rows turn S_j into P_j;
+    // P_j.V_j accumulates into O in tensor memory while the next tile's softmax runs.
+    float m = -INFINITY, l = 0.f;  // the row's reference (log2 units) and normaliser
+    bool stalled = false, failed = false;
+    int issued = min(kPfStages, n_tiles);  // tiles whose copies were started
+    if (tid == 0) stalled = !issue_s(0);
     int j = 0;
     for (; j < n_tiles; ++j) {
         const int st = j % kPfStages;
-        if (__syncthreads_or(!mbar_wait_bounded(smem_u32(&bars[st]), (j / kPfStages) & 1))) {
-            failed = true;
-            break;
-        }
-        uint8_t* sK = smem + st * 2 * kTileBytes;
-        uint8_t* sV = sK + kTileBytes;
         const int t0 = j * kTile;
-        if (t0 + kTile > kv_end) {
-            // Positions past the last visible key hold other data (or nothing): P is 0
-            // there, but 0 * NaN would still poison P.V, so clear those V rows first.
-            const int first = kv_end - t0;
-            for (int x = tid; x < (kTile - first) * 8; x += kPfThreads)
-                *reinterpret_cast<uint4*>(sV + swz(first + (x >> 3), x & 7)) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            fence_proxy_async();
-            __syncthreads();
-        }
-        // S = Q . K^T for the tile's 64 keys
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t kaddr = smem_u32(sK);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                tc_mma_f16(tmem, tc_desc_sw128(qaddr + kk * 32), tc_desc_sw128(kaddr + kk * 32),
-                           kIdS, kk);
-            tc_commit(mma_bar);
-        }
-        if (__syncthreads_or(!mbar_wait_bounded(mma_bar, mph))) {
-            failed = true;
-            break;
-        }
-        mph ^= 1;
+        if (tid == 0 && !stalled && j + 1 < n_tiles) stalled = !issue_s(j + 1);
+        if (!mbar_wait_bounded(bar_s(j), (j >> 1) & 1)) stalled = true;
         tc_fence_after();
         float s[kTile];
-        tc_ld32(tmem + lane_off, s);
-        tc_ld32(tmem + lane_off + 32, s + 32);
+        tc_ld32(tmem + lane_off + (j & 1) * kTile, s);
+        tc_ld32(tmem + lane_off + (j & 1) * kTile + 32, s + 32);
         float tmax = -INFINITY;
         if (t0 + kTile <= lim_warp) {
             // the whole tile is visible to every row of the warp: no mask
@@ -200,12 +191,38 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                 tmax = fmaxf(tmax, s[i]);
             }
         }
-        const float mn = fmaxf(m, tmax);
-        const float ref = mn == -INFINITY ? 0.f : mn;
-        const float alpha = exp2f(m - ref);
-        m = mn;
+        const float mc = fmaxf(m, tmax);
+        const bool grow = mc > m + kRescaleLog2;
+        float factor = 1.f;
+        if (grow) {
+            factor = exp2f(m - mc);  // 0 on the first tile
+            m = mc;
+        }
+        l *= factor;
+        if (j > 0) {
+            // P_{j-1}.V_{j-1} has completed: O can be rescaled, the P buffer rewritten
+            // and the stage of tile j - 1 refilled
+            if (!mbar_wait_bounded(bar_o, (j - 1) & 1)) stalled = true;
+            tc_fence_after();
+            if (__any_sync(0xffffffffu, grow)) {
+                float ov[32];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    tc_ld32(t_o + lane_off + h * 32, ov);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] *= factor;
+                    tc_st32(t_o + lane_off + h * 32, ov);
+                }
+            }
+            if (tid == 0 && j + kPfStages - 1 < n_tiles) {
+                fence_proxy_async();
+                issue(j + kPfStages - 1);
+                issued = j + kPfStages;
+            }
+        }
         // P, rounded to the input type, into this row of the swizzled A operand; the
         // normaliser sums the rounded weights that multiply V
+        const float ref = m == -INFINITY ? 0.f : m;
         float sum = 0.f;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -219,57 +236,69 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             }
             *reinterpret_cast<uint4*>(sP + swz(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        l = fmaf(l, alpha, sum);
-        fence_proxy_async();
+        l += sum;
+        uint8_t* sV = smem + st * 2 * kTileBytes + kTileBytes;
+        if (t0 + kTile > kv_end) {
+            // Positions past the last visible key hold other data (or nothing): P is 0
+            // there, but 0 * NaN would still poison P.V, so clear those V rows once the
+            // tile's copy has landed.
+            if (!mbar_wait_bounded(smem_u32(&bars[st]), (j / kPfStages) & 1)) {
+                stalled = true;
+            } else {
+                const int first = kv_end - t0;
+                for (int x = tid; x < (kTile - first) * 8; x += kPfThreads)
+                    *reinterpret_cast<uint4*>(sV + swz(first + (x >> 3), x & 7)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        fence_proxy_async();  // P (and cleared V rows) are read by the tensor cores
         tc_fence_before();
-        __syncthreads();
-        // P.V for the tile, into its own accumulator
+        if (__syncthreads_or(stalled)) {
+            failed = true;
+            break;
+        }
         if (tid == 0) {
             tc_fence_after();
             const uint32_t vaddr = smem_u32(sV);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                tc_mma_f16(tmem + kTile, tc_desc_sw128(paddr + kk * 32),
-                           tc_desc_sw128(vaddr + kk * 16 * kRowBytes), kIdO, kk);
-            tc_commit(mma_bar);
-        }
-        if (__syncthreads_or(!mbar_wait_bounded(mma_bar, mph))) {
-            failed = true;
-            break;
-        }
-        mph ^= 1;
-        tc_fence_after();
-        float pv[kHeadDim];
-        tc_ld32(tmem + lane_off + kTile, pv);
-        tc_ld32(tmem + lane_off + kTile + 32, pv + 32);
-#pragma unroll
-        for (int d = 0; d < kHeadDim; ++d) o[d] = fmaf(o[d], alpha, pv[d]);
-        // the stage's MMAs have completed (the wait above): refill it
-        if (tid == 0 && j + kPfStages < n_tiles) {
-            fence_proxy_async();
-            issue(j + kPfStages);
+                tc_mma_f16(t_o, tc_desc_sw128(paddr + kk * 32),
+                           tc_desc_sw128(vaddr + kk * 16 * kRowBytes), kIdO, j > 0 || kk > 0);
+            tc_commit(bar_o);
         }
     }
 
     if (failed) {
-        // let the copies still in flight land, then leave; the outputs stay unwritten
+        // let the MMAs and copies still in flight finish, then leave; the outputs stay
+        // unwritten
         if (tid == 0) {
             flag_error(p.dev_err, KVD_ERR_TIMEOUT);
-            for (int jj = j; jj < min(n_tiles, j + kPfStages); ++jj)
+            tc_commit(bar_drain);
+            mbar_wait_bounded(bar_drain, 0);
+            for (int jj = max(0, issued - kPfStages); jj < issued; ++jj)
                 mbar_wait_bounded(smem_u32(&bars[jj % kPfStages]), (jj / kPfStages) & 1);
         }
-    } else if (row < p.max_len) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+    } else {
+        const bool done = mbar_wait_bounded(bar_o, (n_tiles - 1) & 1);
+        tc_fence_after();
+        float o[kHeadDim];
+        tc_ld32(t_o + lane_off, o);
+        tc_ld32(t_o + lane_off + 32, o + 32);
+        if (!done) {
+            flag_error(p.dev_err, KVD_ERR_TIMEOUT);
+        } else if (row < p.max_len) {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint4 w = make_uint4(0u, 0u, 0u, 0u);  // rows past the prompt: +0
-            if (live) {
-                w.x = Half16<T>::from_f2(o[8 * c] * inv, o[8 * c + 1] * inv);
-                w.y = Half16<T>::from_f2(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
-                w.z = Half16<T>::from_f2(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
-                w.w = Half16<T>::from_f2(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+            for (int c = 0; c < 8; ++c) {
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);  // rows past the prompt: +0
+                if (live) {
+                    w.x = Half16<T>::from_f2(o[8 * c] * inv, o[8 * c + 1] * inv);
+                    w.y = Half16<T>::from_f2(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+                    w.z = Half16<T>::from_f2(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+                    w.w = Half16<T>::from_f2(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+                }
+                reinterpret_cast<uint4*>(outr)[c] = w;
             }
-            reinterpret_cast<uint4*>(outr)[c] = w;
         }
     }
     tc_fence_before();
