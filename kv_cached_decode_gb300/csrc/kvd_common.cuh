@@ -113,6 +113,14 @@ __device__ __forceinline__ void rope_rotate8_at(uint4& lo, uint4& hi, int pos, i
     }
 }
 
+// 2^x by the hardware approximation (ex2.approx.ftz: relative error near 2^-22, -inf
+// gives +0); for softmax weights that are rounded to 16 bits afterwards.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---------------------------------------------------------------- shared memory ----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -123,4 +123,23 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const float* v) {
         : "memory");
 }
 
+// One fp32 column of this thread's lane: load / store, complete on return.
+__device__ __forceinline__ float tc_ld1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r)
+        : "r"(taddr)
+        : "memory");
+    return __uint_as_float(r);
+}
+__device__ __forceinline__ void tc_st1(uint32_t taddr, float v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(__float_as_uint(v))
+        : "memory");
+}
+
 }  // namespace kvd

@@ -34,9 +34,10 @@ namespace {
 constexpr int kPfThreads = 128;  // four warps: thread t owns query row t of the block
 constexpr int kPfRows = 128;     // query positions per block (the MMAs' M)
 constexpr int kPfStages = 4;     // K/V tiles in flight
-constexpr uint32_t kPfCols = 256;  // tensor memory: two S buffers (64 + 64), O (64)
+constexpr uint32_t kPfCols = 256;  // tensor memory: two S buffers, O and L, 64 columns each
 constexpr uint32_t kPfRowsBytes = kPfRows * kRowBytes;  // 16 KiB: the Q or the P block
-constexpr uint32_t kPfSmem = kPfStages * 2 * kTileBytes + 2 * kPfRowsBytes + 128 + 1024;
+constexpr uint32_t kPfSmem =
+    kPfStages * 2 * kTileBytes + 2 * kPfRowsBytes + kTileBytes + 128 + 1024;
 // The softmax reference of a row moves only when its maximum grows by more than this
 // (log2 units): the weights then stay below 2^8 and the output is rescaled rarely.
 constexpr float kRescaleLog2 = 8.f;
@@ -64,8 +65,9 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     uint8_t* smem = align_1024(smem_raw);
     uint8_t* sQ = smem + kPfStages * 2 * kTileBytes;
     uint8_t* sP = sQ + kPfRowsBytes;
+    uint8_t* sOnes = sP + kPfRowsBytes;  // 64 x 64 ones: P . 1 gives the row sums
     // barriers: one per stage, S buffers 0 and 1, O, and the drain after a failure
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kPfRowsBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sOnes + kTileBytes);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kPfStages + 4);
     const int tid = threadIdx.x, warp = tid >> 5;
     const int qt = p.q_tiles - 1 - (int)blockIdx.x;  // the blocks with most tiles first
@@ -125,6 +127,11 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     }
 #pragma unroll
     for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(sQ + swz(tid, c)) = qv[c];
+    {
+        const uint32_t one2 = Half16<T>::from_f2(1.f, 1.f);
+        for (int x = tid; x < (int)(kTileBytes / 16); x += kPfThreads)
+            reinterpret_cast<uint4*>(sOnes)[x] = make_uint4(one2, one2, one2, one2);
+    }
     fence_proxy_async();  // generic writes, read by the tensor cores
     tc_fence_before();
     __syncthreads();
@@ -137,6 +144,14 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     constexpr uint32_t kIdO = tc_idesc_f16(kBf16, kPfRows, kHeadDim, true);
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;  // this warp's 32 lanes
     const uint32_t t_o = tmem + 2 * kTile;                  // the output accumulator
+    // the normaliser, the sum of the rounded weights: every column of P . 1 (same shape
+    // as P . V) holds it; column 0 is read
+    const uint32_t t_l = t_o + kHeadDim;
+    const uint32_t onesaddr = smem_u32(sOnes);
+    // With a positive scale the maximum is taken over the raw scores and the scale is
+    // folded into the exponent, one FFMA per weight.
+    const bool pos_scale = p.scale_log2 > 0.f;
+    const float cs = pos_scale ? p.scale_log2 : 1.f;
     const uint32_t qaddr = smem_u32(sQ), paddr = smem_u32(sP);
     const uint32_t bar_o = smem_u32(&bars[kPfStages + 2]);
     const uint32_t bar_drain = smem_u32(&bars[kPfStages + 3]);
@@ -162,7 +177,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
 
     // Pipeline per tile j: thread 0 issues S_{j+1} while the rows turn S_j into P_j;
     // P_j.V_j accumulates into O in tensor memory while the next tile's softmax runs.
-    float m = -INFINITY, l = 0.f;  // the row's reference (log2 units) and normaliser
+    float m = -INFINITY;  // the row's reference (log2 units)
     bool stalled = false, failed = false;
     int issued = min(kPfStages, n_tiles);  // tiles whose copies were started
     if (tid == 0) stalled = !issue_s(0);
@@ -176,21 +191,23 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         float s[kTile];
         tc_ld32(tmem + lane_off + (j & 1) * kTile, s);
         tc_ld32(tmem + lane_off + (j & 1) * kTile + 32, s + 32);
+        if (!pos_scale) {
+#pragma unroll
+            for (int i = 0; i < kTile; ++i) s[i] *= p.scale_log2;
+        }
         float tmax = -INFINITY;
         if (t0 + kTile <= lim_warp) {
             // the whole tile is visible to every row of the warp: no mask
 #pragma unroll
-            for (int i = 0; i < kTile; ++i) {
-                s[i] *= p.scale_log2;
-                tmax = fmaxf(tmax, s[i]);
-            }
+            for (int i = 0; i < kTile; ++i) tmax = fmaxf(tmax, s[i]);
         } else {
 #pragma unroll
             for (int i = 0; i < kTile; ++i) {
-                s[i] = t0 + i < lim ? s[i] * p.scale_log2 : -INFINITY;
+                s[i] = t0 + i < lim ? s[i] : -INFINITY;
                 tmax = fmaxf(tmax, s[i]);
             }
         }
+        tmax *= cs;
         const float mc = fmaxf(m, tmax);
         const bool grow = mc > m + kRescaleLog2;
         float factor = 1.f;
@@ -198,10 +215,9 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             factor = exp2f(m - mc);  // 0 on the first tile
             m = mc;
         }
-        l *= factor;
         if (j > 0) {
-            // P_{j-1}.V_{j-1} has completed: O can be rescaled, the P buffer rewritten
-            // and the stage of tile j - 1 refilled
+            // P_{j-1}.V_{j-1} has completed: O and L can be rescaled, the P buffer
+            // rewritten and the stage of tile j - 1 refilled
             if (!mbar_wait_bounded(bar_o, (j - 1) & 1)) stalled = true;
             tc_fence_after();
             if (__any_sync(0xffffffffu, grow)) {
@@ -213,6 +229,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                     for (int i = 0; i < 32; ++i) ov[i] *= factor;
                     tc_st32(t_o + lane_off + h * 32, ov);
                 }
+                tc_st1(t_l + lane_off, tc_ld1(t_l + lane_off) * factor);
             }
             if (tid == 0 && j + kPfStages - 1 < n_tiles) {
                 fence_proxy_async();
@@ -220,23 +237,17 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                 issued = j + kPfStages;
             }
         }
-        // P, rounded to the input type, into this row of the swizzled A operand; the
-        // normaliser sums the rounded weights that multiply V
-        const float ref = m == -INFINITY ? 0.f : m;
-        float sum = 0.f;
+        // P, rounded to the input type, into this row of the swizzled A operand
+        const float nref = m == -INFINITY ? 0.f : -m;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             uint32_t w[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                w[e] = Half16<T>::from_f2(exp2f(s[8 * c + 2 * e] - ref),
-                                          exp2f(s[8 * c + 2 * e + 1] - ref));
-                const float2 r = Half16<T>::to_f2(w[e]);
-                sum += r.x + r.y;
-            }
+            for (int e = 0; e < 4; ++e)
+                w[e] = Half16<T>::from_f2(ex2_approx(fmaf(s[8 * c + 2 * e], cs, nref)),
+                                          ex2_approx(fmaf(s[8 * c + 2 * e + 1], cs, nref)));
             *reinterpret_cast<uint4*>(sP + swz(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        l += sum;
         uint8_t* sV = smem + st * 2 * kTileBytes + kTileBytes;
         if (t0 + kTile > kv_end) {
             // Positions past the last visible key hold other data (or nothing): P is 0
@@ -264,6 +275,10 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             for (int kk = 0; kk < 4; ++kk)
                 tc_mma_f16(t_o, tc_desc_sw128(paddr + kk * 32),
                            tc_desc_sw128(vaddr + kk * 16 * kRowBytes), kIdO, j > 0 || kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                tc_mma_f16(t_l, tc_desc_sw128(paddr + kk * 32),
+                           tc_desc_sw128(onesaddr + kk * 16 * kRowBytes), kIdO, j > 0 || kk > 0);
             tc_commit(bar_o);
         }
     }
@@ -284,6 +299,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         float o[kHeadDim];
         tc_ld32(t_o + lane_off, o);
         tc_ld32(t_o + lane_off + 32, o + 32);
+        const float l = tc_ld1(t_l + lane_off);
         if (!done) {
             flag_error(p.dev_err, KVD_ERR_TIMEOUT);
         } else if (row < p.max_len) {
