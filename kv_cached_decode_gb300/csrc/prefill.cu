@@ -31,13 +31,15 @@
 namespace kvd {
 namespace {
 
-constexpr int kPfThreads = 128;  // four warps: thread t owns query row t of the block
-constexpr int kPfRows = 128;     // query positions per block (the MMAs' M)
-constexpr int kPfStages = 4;     // K/V tiles in flight
+constexpr int kPfSoftWarps = 4;                        // softmax warps: thread t owns row t
+constexpr int kPfThreads = (kPfSoftWarps + 1) * 32;    // + the producer warp
+constexpr int kPfRows = kPfSoftWarps * 32;             // query positions per block (MMA M)
+constexpr int kPfSlots = 3;                            // K tiles and V tiles in flight, each
 constexpr uint32_t kPfCols = 256;  // tensor memory: two S buffers, O and L, 64 columns each
-constexpr uint32_t kPfRowsBytes = kPfRows * kRowBytes;  // 16 KiB: the Q or the P block
+constexpr uint32_t kPfRowsBytes = kPfRows * kRowBytes;  // 16 KiB: the Q or a P block
+// shared memory: K slots | V slots | Q | P (two buffers) | ones | barriers
 constexpr uint32_t kPfSmem =
-    kPfStages * 2 * kTileBytes + 2 * kPfRowsBytes + kTileBytes + 128 + 1024;
+    2 * kPfSlots * kTileBytes + 3 * kPfRowsBytes + kTileBytes + 256 + 1024;
 // The softmax reference of a row moves only when its maximum grows by more than this
 // (log2 units): the weights then stay below 2^8 and the output is rescaled rarely.
 constexpr float kRescaleLog2 = 8.f;
@@ -57,33 +59,50 @@ __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+// Barrier indices inside the block's barrier array.
+enum PfBar {
+    kBarKFull = 0,                     // K slot s landed (TMA bytes)
+    kBarKEmpty = kBarKFull + kPfSlots, // S of the slot's tile done (MMA commit)
+    kBarVFull = kBarKEmpty + kPfSlots, // V slot s landed
+    kBarVEmpty = kBarVFull + kPfSlots, // P.V of the slot's tile done
+    kBarS = kBarVEmpty + kPfSlots,     // S buffer b written (MMA commit)
+    kBarSFree = kBarS + 2,             // S buffer b read by every row (128 arrivals)
+    kBarPFull = kBarSFree + 2,         // P buffer b written by every row (128 arrivals)
+    kBarO = kBarPFull + 2,             // P.V from P buffer b done (MMA commit)
+    kBarDrain = kBarO + 2,             // every MMA issued so far done (after a failure)
+    kBarCount = kBarDrain + 1
+};
+
 template <typename T, bool ROPE>
 __global__ void __launch_bounds__(kPfThreads, 2)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
-    uint8_t* sQ = smem + kPfStages * 2 * kTileBytes;
-    uint8_t* sP = sQ + kPfRowsBytes;
-    uint8_t* sOnes = sP + kPfRowsBytes;  // 64 x 64 ones: P . 1 gives the row sums
-    // barriers: one per stage, S buffers 0 and 1, O, and the drain after a failure
+    uint8_t* sK = smem;                               // kPfSlots x 8 KiB
+    uint8_t* sV = sK + kPfSlots * kTileBytes;         // kPfSlots x 8 KiB
+    uint8_t* sQ = sV + kPfSlots * kTileBytes;
+    uint8_t* sP = sQ + kPfRowsBytes;                  // two buffers
+    uint8_t* sOnes = sP + 2 * kPfRowsBytes;           // 64 x 64 ones: P . 1 = row sums
     uint64_t* bars = reinterpret_cast<uint64_t*>(sOnes + kTileBytes);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kPfStages + 4);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kBarCount);
+    auto bar = [&](int i) { return smem_u32(&bars[i]); };
     const int tid = threadIdx.x, warp = tid >> 5;
+    const bool producer = warp == kPfSoftWarps;
     const int qt = p.q_tiles - 1 - (int)blockIdx.x;  // the blocks with most tiles first
     const int hq = blockIdx.y, b = blockIdx.z, hk = hq / p.group;
     pdl_wait();
     const int s0 = p.lens_in ? p.lens_in[b] : 0;
     const int plen = p.plens[b];
     const int q0 = qt * kPfRows;
-    const int row = q0 + tid;
+    const int row = q0 + tid;  // meaningful for the softmax threads
     const int64_t head_off = ((int64_t)b * p.n_q_heads + hq) * p.max_len * kHeadDim;
     T* outr = static_cast<T*>(p.out) + head_off + (int64_t)row * kHeadDim;
     // a row the append rejected (length out of range) gets zeros, like padding rows
     const bool bad = s0 < 0 || plen < 0 || plen > p.max_len || (int64_t)s0 + plen > p.capacity;
     const int rows_live = bad ? 0 : max(0, min(kPfRows, plen - q0));
     if (rows_live == 0) {
-        if (row < p.max_len)
+        if (!producer && row < p.max_len)
 #pragma unroll
             for (int c = 0; c < 8; ++c)
                 reinterpret_cast<uint4*>(outr)[c] = make_uint4(0u, 0u, 0u, 0u);
@@ -92,47 +111,56 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     }
     const int kv_end = s0 + q0 + rows_live;  // exclusive: the last live row's limit
     const int n_tiles = (kv_end + kTile - 1) / kTile;
-    const uint32_t tx = 2u * p.box_rows * kRowBytes;
-    auto issue = [&](int j) {
-        const int st = j % kPfStages;
-        const uint32_t bar = smem_u32(&bars[st]);
-        mbar_expect_tx(bar, tx);
-        const uint32_t dk = smem_u32(smem + st * 2 * kTileBytes);
-        tma_load_4d(dk, &tmk, bar, 0, j * kTile, hk, b);
-        tma_load_4d(dk + kTileBytes, &tmv, bar, 0, j * kTile, hk, b);
+    const uint32_t tx = p.box_rows * kRowBytes;  // bytes of one K or V tile copy
+    auto load_k = [&](int j) {
+        const int s = j % kPfSlots;
+        mbar_expect_tx(bar(kBarKFull + s), tx);
+        tma_load_4d(smem_u32(sK + s * kTileBytes), &tmk, bar(kBarKFull + s), 0, j * kTile, hk, b);
     };
-    if (tid == 0) {
-        for (int j = 0; j < kPfStages + 4; ++j) mbar_init(smem_u32(&bars[j]), 1);
+    auto load_v = [&](int j) {
+        const int s = j % kPfSlots;
+        mbar_expect_tx(bar(kBarVFull + s), tx);
+        tma_load_4d(smem_u32(sV + s * kTileBytes), &tmv, bar(kBarVFull + s), 0, j * kTile, hk, b);
+    };
+    if (producer && (tid & 31) == 0) {
+        for (int i = 0; i < kBarCount; ++i)
+            mbar_init(bar(i), (i == kBarSFree || i == kBarSFree + 1 || i == kBarPFull ||
+                               i == kBarPFull + 1)
+                                  ? kPfRows
+                                  : 1);
         fence_barrier_init();
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
-        for (int j = 0; j < min(kPfStages, n_tiles); ++j) issue(j);
+        for (int j = 0; j < min(kPfSlots, n_tiles); ++j) {
+            load_k(j);
+            load_v(j);
+        }
     }
     if (warp == 0) {
         tc_alloc(smem_u32(tslot), kPfCols);
         tc_relinquish();
     }
-
-    // This thread's query row (zeros past the prompt), rotated at position s0 + row,
-    // into the swizzled A operand.
-    const bool live = row < plen;
-    uint4 qv[8];
-    const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + head_off +
-                                                       (int64_t)row * kHeadDim);
+    const bool live = !producer && row < plen;
+    if (!producer) {
+        // this thread's query row (zeros past the prompt), rotated at position s0 + row,
+        // into the swizzled A operand; and the ones operand
+        uint4 qv[8];
+        const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + head_off +
+                                                           (int64_t)row * kHeadDim);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) qv[c] = live ? qrow[c] : make_uint4(0u, 0u, 0u, 0u);
-    if (ROPE && live) {
+        for (int c = 0; c < 8; ++c) qv[c] = live ? qrow[c] : make_uint4(0u, 0u, 0u, 0u);
+        if (ROPE && live) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) rope_rotate8_at<T>(qv[c], qv[c + 4], s0 + row, 8 * c, p.rope_log2_base);
-    }
+            for (int c = 0; c < 4; ++c)
+                rope_rotate8_at<T>(qv[c], qv[c + 4], s0 + row, 8 * c, p.rope_log2_base);
+        }
 #pragma unroll
-    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(sQ + swz(tid, c)) = qv[c];
-    {
+        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(sQ + swz(tid, c)) = qv[c];
         const uint32_t one2 = Half16<T>::from_f2(1.f, 1.f);
-        for (int x = tid; x < (int)(kTileBytes / 16); x += kPfThreads)
+        for (int x = tid; x < (int)(kTileBytes / 16); x += kPfRows)
             reinterpret_cast<uint4*>(sOnes)[x] = make_uint4(one2, one2, one2, one2);
+        fence_proxy_async();  // generic writes, read by the tensor cores
     }
-    fence_proxy_async();  // generic writes, read by the tensor cores
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -142,85 +170,143 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kIdS = tc_idesc_f16(kBf16, kPfRows, kTile, false);
     constexpr uint32_t kIdO = tc_idesc_f16(kBf16, kPfRows, kHeadDim, true);
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;  // this warp's 32 lanes
-    const uint32_t t_o = tmem + 2 * kTile;                  // the output accumulator
+    const uint32_t t_o = tmem + 2 * kTile;  // the output accumulator
     // the normaliser, the sum of the rounded weights: every column of P . 1 (same shape
     // as P . V) holds it; column 0 is read
     const uint32_t t_l = t_o + kHeadDim;
-    const uint32_t onesaddr = smem_u32(sOnes);
-    // With a positive scale the maximum is taken over the raw scores and the scale is
-    // folded into the exponent, one FFMA per weight.
-    const bool pos_scale = p.scale_log2 > 0.f;
-    const float cs = pos_scale ? p.scale_log2 : 1.f;
-    const uint32_t qaddr = smem_u32(sQ), paddr = smem_u32(sP);
-    const uint32_t bar_o = smem_u32(&bars[kPfStages + 2]);
-    const uint32_t bar_drain = smem_u32(&bars[kPfStages + 3]);
-    auto bar_s = [&](int j) { return smem_u32(&bars[kPfStages + (j & 1)]); };
-    // S_j = Q . K_j^T into S buffer j % 2, once tile j has landed (thread 0)
-    auto issue_s = [&](int j) -> bool {
-        const int st = j % kPfStages;
-        if (!mbar_wait_bounded(smem_u32(&bars[st]), (j / kPfStages) & 1)) return false;
-        tc_fence_after();
-        const uint32_t kaddr = smem_u32(smem + st * 2 * kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            tc_mma_f16(tmem + (j & 1) * kTile, tc_desc_sw128(qaddr + kk * 32),
-                       tc_desc_sw128(kaddr + kk * 32), kIdS, kk);
-        tc_commit(bar_s(j));
-        return true;
-    };
-    // keys t < lim are visible; rows past the prompt are clamped to the live rows' keys
-    // (positions beyond hold other data) and written as zeros. Rows ascend with the
-    // lane, so lane 0 holds the warp's smallest limit.
-    const int lim = min(s0 + row + 1, kv_end);
-    const int lim_warp = __shfl_sync(0xffffffffu, lim, 0);
+    bool ok = true;
 
-    // Pipeline per tile j: thread 0 issues S_{j+1} while the rows turn S_j into P_j;
-    // P_j.V_j accumulates into O in tensor memory while the next tile's softmax runs.
-    float m = -INFINITY;  // the row's reference (log2 units)
-    bool stalled = false, failed = false;
-    int issued = min(kPfStages, n_tiles);  // tiles whose copies were started
-    if (tid == 0) stalled = !issue_s(0);
-    int j = 0;
-    for (; j < n_tiles; ++j) {
-        const int st = j % kPfStages;
-        const int t0 = j * kTile;
-        if (tid == 0 && !stalled && j + 1 < n_tiles) stalled = !issue_s(j + 1);
-        if (!mbar_wait_bounded(bar_s(j), (j >> 1) & 1)) stalled = true;
-        tc_fence_after();
-        float s[kTile];
-        tc_ld32(tmem + lane_off + (j & 1) * kTile, s);
-        tc_ld32(tmem + lane_off + (j & 1) * kTile + 32, s + 32);
-        if (!pos_scale) {
+    if (producer) {
+        // ---- producer: one thread issues every copy and every MMA ----
+        if ((tid & 31) == 0) {
+            const uint32_t qaddr = smem_u32(sQ), onesaddr = smem_u32(sOnes);
+            int k_issued = min(kPfSlots, n_tiles), v_issued = k_issued;
+            // S_j = Q . K_j^T into S buffer j % 2: K_j has landed and the rows have read
+            // S_{j-2} from that buffer
+            auto issue_s = [&](int j) -> bool {
+                const int s = j % kPfSlots;
+                if (!mbar_wait_bounded(bar(kBarKFull + s), (j / kPfSlots) & 1)) return false;
+                if (j >= 2 && !mbar_wait_bounded(bar(kBarSFree + (j & 1)), ((j - 2) >> 1) & 1))
+                    return false;
+                tc_fence_after();
+                const uint32_t kaddr = smem_u32(sK + s * kTileBytes);
 #pragma unroll
-            for (int i = 0; i < kTile; ++i) s[i] *= p.scale_log2;
-        }
-        float tmax = -INFINITY;
-        if (t0 + kTile <= lim_warp) {
-            // the whole tile is visible to every row of the warp: no mask
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_f16(tmem + (j & 1) * kTile, tc_desc_sw128(qaddr + kk * 32),
+                               tc_desc_sw128(kaddr + kk * 32), kIdS, kk);
+                tc_commit(bar(kBarS + (j & 1)));
+                tc_commit(bar(kBarKEmpty + s));
+                return true;
+            };
+            ok = issue_s(0);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                if (j + 1 < n_tiles && !(ok = issue_s(j + 1))) break;
+                // K slot of tile j: refilled with tile j + kPfSlots once S_j is done
+                if (j + kPfSlots < n_tiles) {
+                    if (!(ok = mbar_wait_bounded(bar(kBarKEmpty + j % kPfSlots),
+                                                 (j / kPfSlots) & 1)))
+                        break;
+                    load_k(j + kPfSlots);
+                    k_issued = j + kPfSlots + 1;
+                }
+                // P_j . V_j (and P_j . 1) once the rows have written P_j and V_j landed
+                const int pb = j & 1, vs = j % kPfSlots;
+                if (!(ok = mbar_wait_bounded(bar(kBarPFull + pb), (j >> 1) & 1))) break;
+                if (!(ok = mbar_wait_bounded(bar(kBarVFull + vs), (j / kPfSlots) & 1))) break;
+                tc_fence_after();
+                const uint32_t paddr = smem_u32(sP + pb * kPfRowsBytes);
+                const uint32_t vaddr = smem_u32(sV + vs * kTileBytes);
 #pragma unroll
-            for (int i = 0; i < kTile; ++i) tmax = fmaxf(tmax, s[i]);
-        } else {
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_f16(t_o, tc_desc_sw128(paddr + kk * 32),
+                               tc_desc_sw128(vaddr + kk * 16 * kRowBytes), kIdO, j > 0 || kk > 0);
 #pragma unroll
-            for (int i = 0; i < kTile; ++i) {
-                s[i] = t0 + i < lim ? s[i] : -INFINITY;
-                tmax = fmaxf(tmax, s[i]);
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_f16(t_l, tc_desc_sw128(paddr + kk * 32),
+                               tc_desc_sw128(onesaddr + kk * 16 * kRowBytes), kIdO,
+                               j > 0 || kk > 0);
+                tc_commit(bar(kBarO + pb));
+                tc_commit(bar(kBarVEmpty + vs));
+                // V slot of tile j - 1: refilled with tile j + kPfSlots - 1 once
+                // P_{j-1} . V_{j-1} is done
+                if (j >= 1 && j + kPfSlots - 1 < n_tiles) {
+                    const int j1 = j - 1;
+                    if (!(ok = mbar_wait_bounded(bar(kBarVEmpty + j1 % kPfSlots),
+                                                 (j1 / kPfSlots) & 1)))
+                        break;
+                    load_v(j + kPfSlots - 1);
+                    v_issued = j + kPfSlots;
+                }
+            }
+            if (!ok) {
+                // let the MMAs and copies in flight finish before the block leaves
+                flag_error(p.dev_err, KVD_ERR_TIMEOUT);
+                tc_commit(bar(kBarDrain));
+                mbar_wait_bounded(bar(kBarDrain), 0);
+                for (int jj = max(0, k_issued - kPfSlots); jj < k_issued; ++jj)
+                    mbar_wait_bounded(bar(kBarKFull + jj % kPfSlots), (jj / kPfSlots) & 1);
+                for (int jj = max(0, v_issued - kPfSlots); jj < v_issued; ++jj)
+                    mbar_wait_bounded(bar(kBarVFull + jj % kPfSlots), (jj / kPfSlots) & 1);
             }
         }
-        tmax *= cs;
-        const float mc = fmaxf(m, tmax);
-        const bool grow = mc > m + kRescaleLog2;
-        float factor = 1.f;
-        if (grow) {
-            factor = exp2f(m - mc);  // 0 on the first tile
-            m = mc;
-        }
-        if (j > 0) {
-            // P_{j-1}.V_{j-1} has completed: O and L can be rescaled, the P buffer
-            // rewritten and the stage of tile j - 1 refilled
-            if (!mbar_wait_bounded(bar_o, (j - 1) & 1)) stalled = true;
+    } else {
+        // ---- the rows: S_j into P_j, one row per thread ----
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;  // this warp's 32 lanes
+        // With a positive scale the maximum is taken over the raw scores and the scale is
+        // folded into the exponent, one FFMA per weight.
+        const bool pos_scale = p.scale_log2 > 0.f;
+        const float cs = pos_scale ? p.scale_log2 : 1.f;
+        // keys t < lim are visible; rows past the prompt are clamped to the live rows'
+        // keys (positions beyond hold other data) and written as zeros. Rows ascend with
+        // the lane, so lane 0 holds the warp's smallest limit.
+        const int lim = min(s0 + row + 1, kv_end);
+        const int lim_warp = __shfl_sync(0xffffffffu, lim, 0);
+        float m = -INFINITY;  // the row's reference (log2 units)
+        for (int j = 0; j < n_tiles; ++j) {
+            const int sb = j & 1;
+            const int t0 = j * kTile;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarS + sb), (j >> 1) & 1))) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
-            if (__any_sync(0xffffffffu, grow)) {
+            float s[kTile];
+            tc_ld32(tmem + lane_off + sb * kTile, s);
+            tc_ld32(tmem + lane_off + sb * kTile + 32, s + 32);
+            tc_fence_before();
+            mbar_arrive(bar(kBarSFree + sb));
+            if (!pos_scale) {
+#pragma unroll
+                for (int i = 0; i < kTile; ++i) s[i] *= p.scale_log2;
+            }
+            float tmax = -INFINITY;
+            if (t0 + kTile <= lim_warp) {
+                // the whole tile is visible to every row of the warp: no mask
+#pragma unroll
+                for (int i = 0; i < kTile; ++i) tmax = fmaxf(tmax, s[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < kTile; ++i) {
+                    s[i] = t0 + i < lim ? s[i] : -INFINITY;
+                    tmax = fmaxf(tmax, s[i]);
+                }
+            }
+            tmax *= cs;
+            const float mc = fmaxf(m, tmax);
+            const bool grow = mc > m + kRescaleLog2;
+            float factor = 1.f;
+            if (grow) {
+                factor = exp2f(m - mc);  // 0 on the first tile
+                m = mc;
+            }
+            if (j >= 1 && __any_sync(0xffffffffu, grow)) {
+                // O and L are rescaled once P_{j-1} . V_{j-1} is done
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarO + ((j - 1) & 1)),
+                                                                ((j - 1) >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
                 float ov[32];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -231,89 +317,70 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                 }
                 tc_st1(t_l + lane_off, tc_ld1(t_l + lane_off) * factor);
             }
-            if (tid == 0 && j + kPfStages - 1 < n_tiles) {
-                fence_proxy_async();
-                issue(j + kPfStages - 1);
-                issued = j + kPfStages;
+            // P buffer sb is free once P_{j-2} . V_{j-2} is done
+            if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarO + sb),
+                                                                     ((j - 2) >> 1) & 1))) {
+                ok = false;
+                break;
             }
-        }
-        // P, rounded to the input type, into this row of the swizzled A operand
-        const float nref = m == -INFINITY ? 0.f : -m;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                w[e] = Half16<T>::from_f2(ex2_approx(fmaf(s[8 * c + 2 * e], cs, nref)),
-                                          ex2_approx(fmaf(s[8 * c + 2 * e + 1], cs, nref)));
-            *reinterpret_cast<uint4*>(sP + swz(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        uint8_t* sV = smem + st * 2 * kTileBytes + kTileBytes;
-        if (t0 + kTile > kv_end) {
-            // Positions past the last visible key hold other data (or nothing): P is 0
-            // there, but 0 * NaN would still poison P.V, so clear those V rows once the
-            // tile's copy has landed.
-            if (!mbar_wait_bounded(smem_u32(&bars[st]), (j / kPfStages) & 1)) {
-                stalled = true;
-            } else {
-                const int first = kv_end - t0;
-                for (int x = tid; x < (kTile - first) * 8; x += kPfThreads)
-                    *reinterpret_cast<uint4*>(sV + swz(first + (x >> 3), x & 7)) =
-                        make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        fence_proxy_async();  // P (and cleared V rows) are read by the tensor cores
-        tc_fence_before();
-        if (__syncthreads_or(stalled)) {
-            failed = true;
-            break;
-        }
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t vaddr = smem_u32(sV);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                tc_mma_f16(t_o, tc_desc_sw128(paddr + kk * 32),
-                           tc_desc_sw128(vaddr + kk * 16 * kRowBytes), kIdO, j > 0 || kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                tc_mma_f16(t_l, tc_desc_sw128(paddr + kk * 32),
-                           tc_desc_sw128(onesaddr + kk * 16 * kRowBytes), kIdO, j > 0 || kk > 0);
-            tc_commit(bar_o);
-        }
-    }
-
-    if (failed) {
-        // let the MMAs and copies still in flight finish, then leave; the outputs stay
-        // unwritten
-        if (tid == 0) {
-            flag_error(p.dev_err, KVD_ERR_TIMEOUT);
-            tc_commit(bar_drain);
-            mbar_wait_bounded(bar_drain, 0);
-            for (int jj = max(0, issued - kPfStages); jj < issued; ++jj)
-                mbar_wait_bounded(smem_u32(&bars[jj % kPfStages]), (jj / kPfStages) & 1);
-        }
-    } else {
-        const bool done = mbar_wait_bounded(bar_o, (n_tiles - 1) & 1);
-        tc_fence_after();
-        float o[kHeadDim];
-        tc_ld32(t_o + lane_off, o);
-        tc_ld32(t_o + lane_off + 32, o + 32);
-        const float l = tc_ld1(t_l + lane_off);
-        if (!done) {
-            flag_error(p.dev_err, KVD_ERR_TIMEOUT);
-        } else if (row < p.max_len) {
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            // P, rounded to the input type, into this row of the swizzled A operand
+            uint8_t* pbuf = sP + sb * kPfRowsBytes;
+            const float nref = m == -INFINITY ? 0.f : -m;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                uint4 w = make_uint4(0u, 0u, 0u, 0u);  // rows past the prompt: +0
-                if (live) {
-                    w.x = Half16<T>::from_f2(o[8 * c] * inv, o[8 * c + 1] * inv);
-                    w.y = Half16<T>::from_f2(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
-                    w.z = Half16<T>::from_f2(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
-                    w.w = Half16<T>::from_f2(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w[e] = Half16<T>::from_f2(ex2_approx(fmaf(s[8 * c + 2 * e], cs, nref)),
+                                              ex2_approx(fmaf(s[8 * c + 2 * e + 1], cs, nref)));
+                *reinterpret_cast<uint4*>(pbuf + swz(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            if (t0 + kTile > kv_end) {
+                // Positions past the last visible key hold other data (or nothing): P is
+                // 0 there, but 0 * NaN would still poison P.V, so clear those V rows once
+                // the tile's copy has landed.
+                const int vs = j % kPfSlots;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarVFull + vs),
+                                                                (j / kPfSlots) & 1))) {
+                    ok = false;
+                    break;
                 }
-                reinterpret_cast<uint4*>(outr)[c] = w;
+                uint8_t* vt = sV + vs * kTileBytes;
+                const int first = kv_end - t0;
+                for (int x = tid; x < (kTile - first) * 8; x += kPfRows)
+                    *reinterpret_cast<uint4*>(vt + swz(first + (x >> 3), x & 7)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async();  // P (and cleared V rows) are read by the tensor cores
+            tc_fence_before();
+            mbar_arrive(bar(kBarPFull + sb));
+        }
+        if (!ok) {
+            if ((tid & 31) == 0) flag_error(p.dev_err, KVD_ERR_TIMEOUT);
+        } else {
+            const int jl = n_tiles - 1;
+            const bool done =
+                __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarO + (jl & 1)), (jl >> 1) & 1));
+            tc_fence_after();
+            float o[kHeadDim];
+            tc_ld32(t_o + lane_off, o);
+            tc_ld32(t_o + lane_off + 32, o + 32);
+            const float l = tc_ld1(t_l + lane_off);
+            if (!done) {
+                if ((tid & 31) == 0) flag_error(p.dev_err, KVD_ERR_TIMEOUT);
+            } else if (row < p.max_len) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 w = make_uint4(0u, 0u, 0u, 0u);  // rows past the prompt: +0
+                    if (live) {
+                        w.x = Half16<T>::from_f2(o[8 * c] * inv, o[8 * c + 1] * inv);
+                        w.y = Half16<T>::from_f2(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+                        w.z = Half16<T>::from_f2(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+                        w.w = Half16<T>::from_f2(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+                    }
+                    reinterpret_cast<uint4*>(outr)[c] = w;
+                }
             }
         }
     }
