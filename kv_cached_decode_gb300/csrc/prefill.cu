@@ -35,11 +35,10 @@ constexpr int kPfSoftWarps = 4;                        // softmax warps: thread 
 constexpr int kPfThreads = (kPfSoftWarps + 1) * 32;    // + the producer warp
 constexpr int kPfRows = kPfSoftWarps * 32;             // query positions per block (MMA M)
 constexpr int kPfSlots = 3;                            // K tiles and V tiles in flight, each
-constexpr uint32_t kPfCols = 256;  // tensor memory: two S buffers, O and L, 64 columns each
+constexpr uint32_t kPfCols = 256;  // tensor memory: two S buffers and O, 64 columns each
 constexpr uint32_t kPfRowsBytes = kPfRows * kRowBytes;  // 16 KiB: the Q or a P block
-// shared memory: K slots | V slots | Q | P (two buffers) | ones | barriers
-constexpr uint32_t kPfSmem =
-    2 * kPfSlots * kTileBytes + 3 * kPfRowsBytes + kTileBytes + 256 + 1024;
+// shared memory: K slots | V slots | Q | P (two buffers) | barriers
+constexpr uint32_t kPfSmem = 2 * kPfSlots * kTileBytes + 3 * kPfRowsBytes + 256 + 1024;
 // The softmax reference of a row moves only when its maximum grows by more than this
 // (log2 units): the weights then stay below 2^8 and the output is rescaled rarely.
 constexpr float kRescaleLog2 = 8.f;
@@ -83,8 +82,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     uint8_t* sV = sK + kPfSlots * kTileBytes;         // kPfSlots x 8 KiB
     uint8_t* sQ = sV + kPfSlots * kTileBytes;
     uint8_t* sP = sQ + kPfRowsBytes;                  // two buffers
-    uint8_t* sOnes = sP + 2 * kPfRowsBytes;           // 64 x 64 ones: P . 1 = row sums
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sOnes + kTileBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * kPfRowsBytes);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kBarCount);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -143,7 +141,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     const bool live = !producer && row < plen;
     if (!producer) {
         // this thread's query row (zeros past the prompt), rotated at position s0 + row,
-        // into the swizzled A operand; and the ones operand
+        // into the swizzled A operand
         uint4 qv[8];
         const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + head_off +
                                                            (int64_t)row * kHeadDim);
@@ -156,9 +154,6 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         }
 #pragma unroll
         for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(sQ + swz(tid, c)) = qv[c];
-        const uint32_t one2 = Half16<T>::from_f2(1.f, 1.f);
-        for (int x = tid; x < (int)(kTileBytes / 16); x += kPfRows)
-            reinterpret_cast<uint4*>(sOnes)[x] = make_uint4(one2, one2, one2, one2);
         fence_proxy_async();  // generic writes, read by the tensor cores
     }
     tc_fence_before();
@@ -171,15 +166,12 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     constexpr uint32_t kIdS = tc_idesc_f16(kBf16, kPfRows, kTile, false);
     constexpr uint32_t kIdO = tc_idesc_f16(kBf16, kPfRows, kHeadDim, true);
     const uint32_t t_o = tmem + 2 * kTile;  // the output accumulator
-    // the normaliser, the sum of the rounded weights: every column of P . 1 (same shape
-    // as P . V) holds it; column 0 is read
-    const uint32_t t_l = t_o + kHeadDim;
     bool ok = true;
 
     if (producer) {
         // ---- producer: one thread issues every copy and every MMA ----
         if ((tid & 31) == 0) {
-            const uint32_t qaddr = smem_u32(sQ), onesaddr = smem_u32(sOnes);
+            const uint32_t qaddr = smem_u32(sQ);
             int k_issued = min(kPfSlots, n_tiles), v_issued = k_issued;
             // S_j = Q . K_j^T into S buffer j % 2: K_j has landed and the rows have read
             // S_{j-2} from that buffer
@@ -209,7 +201,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                     load_k(j + kPfSlots);
                     k_issued = j + kPfSlots + 1;
                 }
-                // P_j . V_j (and P_j . 1) once the rows have written P_j and V_j landed
+                // P_j . V_j once the rows have written P_j and V_j landed
                 const int pb = j & 1, vs = j % kPfSlots;
                 if (!(ok = mbar_wait_bounded(bar(kBarPFull + pb), (j >> 1) & 1))) break;
                 if (!(ok = mbar_wait_bounded(bar(kBarVFull + vs), (j / kPfSlots) & 1))) break;
@@ -220,11 +212,6 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                 for (int kk = 0; kk < 4; ++kk)
                     tc_mma_f16(t_o, tc_desc_sw128(paddr + kk * 32),
                                tc_desc_sw128(vaddr + kk * 16 * kRowBytes), kIdO, j > 0 || kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    tc_mma_f16(t_l, tc_desc_sw128(paddr + kk * 32),
-                               tc_desc_sw128(onesaddr + kk * 16 * kRowBytes), kIdO,
-                               j > 0 || kk > 0);
                 tc_commit(bar(kBarO + pb));
                 tc_commit(bar(kBarVEmpty + vs));
                 // V slot of tile j - 1: refilled with tile j + kPfSlots - 1 once
@@ -261,7 +248,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         // the lane, so lane 0 holds the warp's smallest limit.
         const int lim = min(s0 + row + 1, kv_end);
         const int lim_warp = __shfl_sync(0xffffffffu, lim, 0);
-        float m = -INFINITY;  // the row's reference (log2 units)
+        float m = -INFINITY, l = 0.f;  // the row's reference (log2 units) and normaliser
         for (int j = 0; j < n_tiles; ++j) {
             const int sb = j & 1;
             const int t0 = j * kTile;
@@ -299,8 +286,9 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                 factor = exp2f(m - mc);  // 0 on the first tile
                 m = mc;
             }
+            l *= factor;
             if (j >= 1 && __any_sync(0xffffffffu, grow)) {
-                // O and L are rescaled once P_{j-1} . V_{j-1} is done
+                // O is rescaled once P_{j-1} . V_{j-1} is done
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarO + ((j - 1) & 1)),
                                                                 ((j - 1) >> 1) & 1))) {
                     ok = false;
@@ -315,7 +303,6 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                     for (int i = 0; i < 32; ++i) ov[i] *= factor;
                     tc_st32(t_o + lane_off + h * 32, ov);
                 }
-                tc_st1(t_l + lane_off, tc_ld1(t_l + lane_off) * factor);
             }
             // P buffer sb is free once P_{j-2} . V_{j-2} is done
             if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarO + sb),
@@ -323,18 +310,25 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                 ok = false;
                 break;
             }
-            // P, rounded to the input type, into this row of the swizzled A operand
+            // P, rounded to the input type, into this row of the swizzled A operand; the
+            // normaliser sums the unrounded weights (rounding to nearest leaves no bias)
             uint8_t* pbuf = sP + sb * kPfRowsBytes;
             const float nref = m == -INFINITY ? 0.f : -m;
+            float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 uint32_t w[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    w[e] = Half16<T>::from_f2(ex2_approx(fmaf(s[8 * c + 2 * e], cs, nref)),
-                                              ex2_approx(fmaf(s[8 * c + 2 * e + 1], cs, nref)));
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = ex2_approx(fmaf(s[8 * c + 2 * e], cs, nref));
+                    const float p1 = ex2_approx(fmaf(s[8 * c + 2 * e + 1], cs, nref));
+                    sum0 += p0;
+                    sum1 += p1;
+                    w[e] = Half16<T>::from_f2(p0, p1);
+                }
                 *reinterpret_cast<uint4*>(pbuf + swz(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
+            l += sum0 + sum1;
             if (t0 + kTile > kv_end) {
                 // Positions past the last visible key hold other data (or nothing): P is
                 // 0 there, but 0 * NaN would still poison P.V, so clear those V rows once
@@ -365,7 +359,6 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             float o[kHeadDim];
             tc_ld32(t_o + lane_off, o);
             tc_ld32(t_o + lane_off + 32, o + 32);
-            const float l = tc_ld1(t_l + lane_off);
             if (!done) {
                 if ((tid & 31) == 0) flag_error(p.dev_err, KVD_ERR_TIMEOUT);
             } else if (row < p.max_len) {
