@@ -34,11 +34,17 @@ namespace {
 constexpr int kPfSoftWarps = 4;                        // softmax warps: thread t owns row t
 constexpr int kPfThreads = (kPfSoftWarps + 1) * 32;    // + the producer warp
 constexpr int kPfRows = kPfSoftWarps * 32;             // query positions per block (MMA M)
-constexpr int kPfSlots = 3;                            // K tiles and V tiles in flight, each
-constexpr uint32_t kPfCols = 256;  // tensor memory: two S buffers and O, 64 columns each
+constexpr int kPfKSlots = 3;   // K tiles in flight
+constexpr int kPfVSlots = 2;   // V tiles in flight
+constexpr int kPfSBufs = 1;    // S buffers in tensor memory (the rows read S first)
+constexpr int kPfPBufs = 1;    // P buffers in shared memory
+constexpr int kPfMinBlocks = 2;  // blocks per SM the sizes below are chosen for
+constexpr uint32_t kPfCols = 128;  // tensor memory: S buffers and O, 64 columns each
+static_assert(kPfCols >= (kPfSBufs + 1) * 64, "tensor memory columns");
 constexpr uint32_t kPfRowsBytes = kPfRows * kRowBytes;  // 16 KiB: the Q or a P block
-// shared memory: K slots | V slots | Q | P (two buffers) | barriers
-constexpr uint32_t kPfSmem = 2 * kPfSlots * kTileBytes + 3 * kPfRowsBytes + 256 + 1024;
+// shared memory: K slots | V slots | Q | P buffers | barriers
+constexpr uint32_t kPfSmem = (kPfKSlots + kPfVSlots) * kTileBytes +
+                             (1 + kPfPBufs) * kPfRowsBytes + 256 + 1024;
 // The softmax reference of a row moves only when its maximum grows by more than this
 // (log2 units): the weights then stay below 2^8 and the output is rescaled rarely.
 constexpr float kRescaleLog2 = 8.f;
@@ -61,34 +67,41 @@ __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
 // Barrier indices inside the block's barrier array.
 enum PfBar {
     kBarKFull = 0,                     // K slot s landed (TMA bytes)
-    kBarKEmpty = kBarKFull + kPfSlots, // S of the slot's tile done (MMA commit)
-    kBarVFull = kBarKEmpty + kPfSlots, // V slot s landed
-    kBarVEmpty = kBarVFull + kPfSlots, // P.V of the slot's tile done
-    kBarS = kBarVEmpty + kPfSlots,     // S buffer b written (MMA commit)
-    kBarSFree = kBarS + 2,             // S buffer b read by every row (128 arrivals)
-    kBarPFull = kBarSFree + 2,         // P buffer b written by every row (128 arrivals)
-    kBarO = kBarPFull + 2,             // P.V from P buffer b done (MMA commit)
-    kBarDrain = kBarO + 2,             // every MMA issued so far done (after a failure)
+    kBarKEmpty = kBarKFull + kPfKSlots,  // S of the slot's tile done (MMA commit)
+    kBarVFull = kBarKEmpty + kPfKSlots,  // V slot s landed
+    kBarVEmpty = kBarVFull + kPfVSlots,  // P.V of the slot's tile done
+    kBarS = kBarVEmpty + kPfVSlots,      // S buffer b written (MMA commit)
+    kBarSFree = kBarS + kPfSBufs,        // S buffer b read by every row (128 arrivals)
+    kBarPFull = kBarSFree + kPfSBufs,    // P buffer b written by every row (128 arrivals)
+    kBarO = kBarPFull + kPfPBufs,        // P.V from P buffer b done (MMA commit)
+    kBarDrain = kBarO + kPfPBufs,        // every MMA issued so far done (after a failure)
     kBarCount = kBarDrain + 1
 };
 
 template <typename T, bool ROPE>
-__global__ void __launch_bounds__(kPfThreads, 2)
+__global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
-    uint8_t* sK = smem;                               // kPfSlots x 8 KiB
-    uint8_t* sV = sK + kPfSlots * kTileBytes;         // kPfSlots x 8 KiB
-    uint8_t* sQ = sV + kPfSlots * kTileBytes;
-    uint8_t* sP = sQ + kPfRowsBytes;                  // two buffers
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * kPfRowsBytes);
+    uint8_t* sK = smem;                        // kPfKSlots x 8 KiB
+    uint8_t* sV = sK + kPfKSlots * kTileBytes;  // kPfVSlots x 8 KiB
+    uint8_t* sQ = sV + kPfVSlots * kTileBytes;
+    uint8_t* sP = sQ + kPfRowsBytes;           // kPfPBufs x 16 KiB
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kPfPBufs * kPfRowsBytes);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kBarCount);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
     const int tid = threadIdx.x, warp = tid >> 5;
     const bool producer = warp == kPfSoftWarps;
-    const int qt = p.q_tiles - 1 - (int)blockIdx.x;  // the blocks with most tiles first
-    const int hq = blockIdx.y, b = blockIdx.z, hk = hq / p.group;
+    // Blocks are dispatched in linear order; the linear index runs over the query tiles
+    // last to first, then over (head, row), so the blocks with the most K/V tiles of
+    // every row start first and the short ones fill in behind them.
+    const int64_t lin =
+        blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
+    const int64_t per_tile = (int64_t)gridDim.y * gridDim.z;
+    const int qt = p.q_tiles - 1 - (int)(lin / per_tile);
+    const int hq = (int)(lin % per_tile % gridDim.y), b = (int)(lin % per_tile / gridDim.y);
+    const int hk = hq / p.group;
     pdl_wait();
     const int s0 = p.lens_in ? p.lens_in[b] : 0;
     const int plen = p.plens[b];
@@ -111,28 +124,26 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     const int n_tiles = (kv_end + kTile - 1) / kTile;
     const uint32_t tx = p.box_rows * kRowBytes;  // bytes of one K or V tile copy
     auto load_k = [&](int j) {
-        const int s = j % kPfSlots;
+        const int s = j % kPfKSlots;
         mbar_expect_tx(bar(kBarKFull + s), tx);
         tma_load_4d(smem_u32(sK + s * kTileBytes), &tmk, bar(kBarKFull + s), 0, j * kTile, hk, b);
     };
     auto load_v = [&](int j) {
-        const int s = j % kPfSlots;
+        const int s = j % kPfVSlots;
         mbar_expect_tx(bar(kBarVFull + s), tx);
         tma_load_4d(smem_u32(sV + s * kTileBytes), &tmv, bar(kBarVFull + s), 0, j * kTile, hk, b);
     };
     if (producer && (tid & 31) == 0) {
         for (int i = 0; i < kBarCount; ++i)
-            mbar_init(bar(i), (i == kBarSFree || i == kBarSFree + 1 || i == kBarPFull ||
-                               i == kBarPFull + 1)
+            mbar_init(bar(i), ((i >= kBarSFree && i < kBarSFree + kPfSBufs) ||
+                               (i >= kBarPFull && i < kBarPFull + kPfPBufs))
                                   ? kPfRows
                                   : 1);
         fence_barrier_init();
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
-        for (int j = 0; j < min(kPfSlots, n_tiles); ++j) {
-            load_k(j);
-            load_v(j);
-        }
+        for (int j = 0; j < min(kPfKSlots, n_tiles); ++j) load_k(j);
+        for (int j = 0; j < min(kPfVSlots, n_tiles); ++j) load_v(j);
     }
     if (warp == 0) {
         tc_alloc(smem_u32(tslot), kPfCols);
@@ -165,46 +176,47 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kIdS = tc_idesc_f16(kBf16, kPfRows, kTile, false);
     constexpr uint32_t kIdO = tc_idesc_f16(kBf16, kPfRows, kHeadDim, true);
-    const uint32_t t_o = tmem + 2 * kTile;  // the output accumulator
+    const uint32_t t_o = tmem + kPfSBufs * kTile;  // the output accumulator
     bool ok = true;
 
     if (producer) {
         // ---- producer: one thread issues every copy and every MMA ----
         if ((tid & 31) == 0) {
             const uint32_t qaddr = smem_u32(sQ);
-            int k_issued = min(kPfSlots, n_tiles), v_issued = k_issued;
-            // S_j = Q . K_j^T into S buffer j % 2: K_j has landed and the rows have read
-            // S_{j-2} from that buffer
+            int k_issued = min(kPfKSlots, n_tiles), v_issued = min(kPfVSlots, n_tiles);
+            // S_j = Q . K_j^T into S buffer j % kPfSBufs: K_j has landed and the rows have
+            // read S_{j - kPfSBufs} from that buffer
             auto issue_s = [&](int j) -> bool {
-                const int s = j % kPfSlots;
-                if (!mbar_wait_bounded(bar(kBarKFull + s), (j / kPfSlots) & 1)) return false;
-                if (j >= 2 && !mbar_wait_bounded(bar(kBarSFree + (j & 1)), ((j - 2) >> 1) & 1))
+                const int s = j % kPfKSlots, sb = j % kPfSBufs;
+                if (!mbar_wait_bounded(bar(kBarKFull + s), (j / kPfKSlots) & 1)) return false;
+                if (j >= kPfSBufs && !mbar_wait_bounded(bar(kBarSFree + sb),
+                                                        ((j - kPfSBufs) / kPfSBufs) & 1))
                     return false;
                 tc_fence_after();
                 const uint32_t kaddr = smem_u32(sK + s * kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    tc_mma_f16(tmem + (j & 1) * kTile, tc_desc_sw128(qaddr + kk * 32),
+                    tc_mma_f16(tmem + sb * kTile, tc_desc_sw128(qaddr + kk * 32),
                                tc_desc_sw128(kaddr + kk * 32), kIdS, kk);
-                tc_commit(bar(kBarS + (j & 1)));
+                tc_commit(bar(kBarS + sb));
                 tc_commit(bar(kBarKEmpty + s));
                 return true;
             };
             ok = issue_s(0);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (j + 1 < n_tiles && !(ok = issue_s(j + 1))) break;
-                // K slot of tile j: refilled with tile j + kPfSlots once S_j is done
-                if (j + kPfSlots < n_tiles) {
-                    if (!(ok = mbar_wait_bounded(bar(kBarKEmpty + j % kPfSlots),
-                                                 (j / kPfSlots) & 1)))
+                // K slot of tile j: refilled with tile j + kPfKSlots once S_j is done
+                if (j + kPfKSlots < n_tiles) {
+                    if (!(ok = mbar_wait_bounded(bar(kBarKEmpty + j % kPfKSlots),
+                                                 (j / kPfKSlots) & 1)))
                         break;
-                    load_k(j + kPfSlots);
-                    k_issued = j + kPfSlots + 1;
+                    load_k(j + kPfKSlots);
+                    k_issued = j + kPfKSlots + 1;
                 }
                 // P_j . V_j once the rows have written P_j and V_j landed
-                const int pb = j & 1, vs = j % kPfSlots;
-                if (!(ok = mbar_wait_bounded(bar(kBarPFull + pb), (j >> 1) & 1))) break;
-                if (!(ok = mbar_wait_bounded(bar(kBarVFull + vs), (j / kPfSlots) & 1))) break;
+                const int pb = j % kPfPBufs, vs = j % kPfVSlots;
+                if (!(ok = mbar_wait_bounded(bar(kBarPFull + pb), (j / kPfPBufs) & 1))) break;
+                if (!(ok = mbar_wait_bounded(bar(kBarVFull + vs), (j / kPfVSlots) & 1))) break;
                 tc_fence_after();
                 const uint32_t paddr = smem_u32(sP + pb * kPfRowsBytes);
                 const uint32_t vaddr = smem_u32(sV + vs * kTileBytes);
@@ -214,15 +226,15 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                                tc_desc_sw128(vaddr + kk * 16 * kRowBytes), kIdO, j > 0 || kk > 0);
                 tc_commit(bar(kBarO + pb));
                 tc_commit(bar(kBarVEmpty + vs));
-                // V slot of tile j - 1: refilled with tile j + kPfSlots - 1 once
+                // V slot of tile j - 1: refilled with tile j - 1 + kPfVSlots once
                 // P_{j-1} . V_{j-1} is done
-                if (j >= 1 && j + kPfSlots - 1 < n_tiles) {
+                if (j >= 1 && j - 1 + kPfVSlots < n_tiles) {
                     const int j1 = j - 1;
-                    if (!(ok = mbar_wait_bounded(bar(kBarVEmpty + j1 % kPfSlots),
-                                                 (j1 / kPfSlots) & 1)))
+                    if (!(ok = mbar_wait_bounded(bar(kBarVEmpty + j1 % kPfVSlots),
+                                                 (j1 / kPfVSlots) & 1)))
                         break;
-                    load_v(j + kPfSlots - 1);
-                    v_issued = j + kPfSlots;
+                    load_v(j1 + kPfVSlots);
+                    v_issued = j1 + kPfVSlots + 1;
                 }
             }
             if (!ok) {
@@ -230,10 +242,10 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                 flag_error(p.dev_err, KVD_ERR_TIMEOUT);
                 tc_commit(bar(kBarDrain));
                 mbar_wait_bounded(bar(kBarDrain), 0);
-                for (int jj = max(0, k_issued - kPfSlots); jj < k_issued; ++jj)
-                    mbar_wait_bounded(bar(kBarKFull + jj % kPfSlots), (jj / kPfSlots) & 1);
-                for (int jj = max(0, v_issued - kPfSlots); jj < v_issued; ++jj)
-                    mbar_wait_bounded(bar(kBarVFull + jj % kPfSlots), (jj / kPfSlots) & 1);
+                for (int jj = max(0, k_issued - kPfKSlots); jj < k_issued; ++jj)
+                    mbar_wait_bounded(bar(kBarKFull + jj % kPfKSlots), (jj / kPfKSlots) & 1);
+                for (int jj = max(0, v_issued - kPfVSlots); jj < v_issued; ++jj)
+                    mbar_wait_bounded(bar(kBarVFull + jj % kPfVSlots), (jj / kPfVSlots) & 1);
             }
         }
     } else {
@@ -250,9 +262,10 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         const int lim_warp = __shfl_sync(0xffffffffu, lim, 0);
         float m = -INFINITY, l = 0.f;  // the row's reference (log2 units) and normaliser
         for (int j = 0; j < n_tiles; ++j) {
-            const int sb = j & 1;
+            const int sb = j % kPfSBufs, pb = j % kPfPBufs;
             const int t0 = j * kTile;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarS + sb), (j >> 1) & 1))) {
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait_bounded(bar(kBarS + sb), (j / kPfSBufs) & 1))) {
                 ok = false;
                 break;
             }
@@ -266,19 +279,24 @@ __global__ void __launch_bounds__(kPfThreads, 2)
 #pragma unroll
                 for (int i = 0; i < kTile; ++i) s[i] *= p.scale_log2;
             }
-            float tmax = -INFINITY;
+            // (eight independent partial maxima: short dependency chains)
+            float pm[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pm[e] = -INFINITY;
             if (t0 + kTile <= lim_warp) {
                 // the whole tile is visible to every row of the warp: no mask
 #pragma unroll
-                for (int i = 0; i < kTile; ++i) tmax = fmaxf(tmax, s[i]);
+                for (int i = 0; i < kTile; ++i) pm[i & 7] = fmaxf(pm[i & 7], s[i]);
             } else {
 #pragma unroll
                 for (int i = 0; i < kTile; ++i) {
                     s[i] = t0 + i < lim ? s[i] : -INFINITY;
-                    tmax = fmaxf(tmax, s[i]);
+                    pm[i & 7] = fmaxf(pm[i & 7], s[i]);
                 }
             }
-            tmax *= cs;
+            const float tmax =
+                fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                      fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * cs;
             const float mc = fmaxf(m, tmax);
             const bool grow = mc > m + kRescaleLog2;
             float factor = 1.f;
@@ -289,8 +307,9 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             l *= factor;
             if (j >= 1 && __any_sync(0xffffffffu, grow)) {
                 // O is rescaled once P_{j-1} . V_{j-1} is done
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarO + ((j - 1) & 1)),
-                                                                ((j - 1) >> 1) & 1))) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_bounded(bar(kBarO + (j - 1) % kPfPBufs),
+                                                  ((j - 1) / kPfPBufs) & 1))) {
                     ok = false;
                     break;
                 }
@@ -304,17 +323,20 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                     tc_st32(t_o + lane_off + h * 32, ov);
                 }
             }
-            // P buffer sb is free once P_{j-2} . V_{j-2} is done
-            if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarO + sb),
-                                                                     ((j - 2) >> 1) & 1))) {
+            // P buffer pb is free once P_{j - kPfPBufs} . V is done
+            if (j >= kPfPBufs &&
+                !__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarO + pb),
+                                                           ((j - kPfPBufs) / kPfPBufs) & 1))) {
                 ok = false;
                 break;
             }
             // P, rounded to the input type, into this row of the swizzled A operand; the
             // normaliser sums the unrounded weights (rounding to nearest leaves no bias)
-            uint8_t* pbuf = sP + sb * kPfRowsBytes;
+            uint8_t* pbuf = sP + pb * kPfRowsBytes;
             const float nref = m == -INFINITY ? 0.f : -m;
-            float sum0 = 0.f, sum1 = 0.f;
+            float ps[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ps[e] = 0.f;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 uint32_t w[4];
@@ -322,20 +344,20 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                 for (int e = 0; e < 4; ++e) {
                     const float p0 = ex2_approx(fmaf(s[8 * c + 2 * e], cs, nref));
                     const float p1 = ex2_approx(fmaf(s[8 * c + 2 * e + 1], cs, nref));
-                    sum0 += p0;
-                    sum1 += p1;
+                    ps[2 * e] += p0;
+                    ps[2 * e + 1] += p1;
                     w[e] = Half16<T>::from_f2(p0, p1);
                 }
                 *reinterpret_cast<uint4*>(pbuf + swz(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            l += sum0 + sum1;
+            l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             if (t0 + kTile > kv_end) {
                 // Positions past the last visible key hold other data (or nothing): P is
                 // 0 there, but 0 * NaN would still poison P.V, so clear those V rows once
                 // the tile's copy has landed.
-                const int vs = j % kPfSlots;
+                const int vs = j % kPfVSlots;
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarVFull + vs),
-                                                                (j / kPfSlots) & 1))) {
+                                                                (j / kPfVSlots) & 1))) {
                     ok = false;
                     break;
                 }
@@ -347,14 +369,15 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             }
             fence_proxy_async();  // P (and cleared V rows) are read by the tensor cores
             tc_fence_before();
-            mbar_arrive(bar(kBarPFull + sb));
+            mbar_arrive(bar(kBarPFull + pb));
         }
         if (!ok) {
             if ((tid & 31) == 0) flag_error(p.dev_err, KVD_ERR_TIMEOUT);
         } else {
             const int jl = n_tiles - 1;
             const bool done =
-                __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarO + (jl & 1)), (jl >> 1) & 1));
+                __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarO + jl % kPfPBufs),
+                                                          (jl / kPfPBufs) & 1));
             tc_fence_after();
             float o[kHeadDim];
             tc_ld32(t_o + lane_off, o);
