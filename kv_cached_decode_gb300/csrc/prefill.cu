@@ -38,6 +38,10 @@ constexpr int kPfKSlots = 3;   // K tiles in flight
 constexpr int kPfVSlots = 2;   // V tiles in flight
 constexpr int kPfSBufs = 1;    // S buffers in tensor memory (the rows read S first)
 constexpr int kPfPBufs = 1;    // P buffers in shared memory
+// With one S and one P buffer, the rows' hand-offs also free the K and V slots: the rows
+// read S_j only after S_j (and so every read of K_j) completed, and write P_j only after
+// P_{j-1} . V_{j-1} completed.
+static_assert(kPfSBufs == 1 && kPfPBufs == 1, "slot reuse follows the rows' hand-offs");
 constexpr int kPfMinBlocks = 2;  // blocks per SM the sizes below are chosen for
 constexpr uint32_t kPfCols = 128;  // tensor memory: S buffers and O, 64 columns each
 static_assert(kPfCols >= (kPfSBufs + 1) * 64, "tensor memory columns");
@@ -66,11 +70,9 @@ __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
 
 // Barrier indices inside the block's barrier array.
 enum PfBar {
-    kBarKFull = 0,                     // K slot s landed (TMA bytes)
-    kBarKEmpty = kBarKFull + kPfKSlots,  // S of the slot's tile done (MMA commit)
-    kBarVFull = kBarKEmpty + kPfKSlots,  // V slot s landed
-    kBarVEmpty = kBarVFull + kPfVSlots,  // P.V of the slot's tile done
-    kBarS = kBarVEmpty + kPfVSlots,      // S buffer b written (MMA commit)
+    kBarKFull = 0,                       // K slot s landed (TMA bytes)
+    kBarVFull = kBarKFull + kPfKSlots,   // V slot s landed
+    kBarS = kBarVFull + kPfVSlots,       // S buffer b written (MMA commit)
     kBarSFree = kBarS + kPfSBufs,        // S buffer b read by every row (128 arrivals)
     kBarPFull = kBarSFree + kPfSBufs,    // P buffer b written by every row (128 arrivals)
     kBarO = kBarPFull + kPfPBufs,        // P.V from P buffer b done (MMA commit)
@@ -199,23 +201,26 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
                     tc_mma_f16(tmem + sb * kTile, tc_desc_sw128(qaddr + kk * 32),
                                tc_desc_sw128(kaddr + kk * 32), kIdS, kk);
                 tc_commit(bar(kBarS + sb));
-                tc_commit(bar(kBarKEmpty + s));
                 return true;
             };
             ok = issue_s(0);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (j + 1 < n_tiles && !(ok = issue_s(j + 1))) break;
-                // K slot of tile j: refilled with tile j + kPfKSlots once S_j is done
+                // K slot of tile j: refilled with tile j + kPfKSlots. S_j is done, since
+                // issuing S_{j+1} waited for the rows to read S_j.
                 if (j + kPfKSlots < n_tiles) {
-                    if (!(ok = mbar_wait_bounded(bar(kBarKEmpty + j % kPfKSlots),
-                                                 (j / kPfKSlots) & 1)))
-                        break;
                     load_k(j + kPfKSlots);
                     k_issued = j + kPfKSlots + 1;
                 }
                 // P_j . V_j once the rows have written P_j and V_j landed
                 const int pb = j % kPfPBufs, vs = j % kPfVSlots;
                 if (!(ok = mbar_wait_bounded(bar(kBarPFull + pb), (j / kPfPBufs) & 1))) break;
+                // V slot of tile j - 1: refilled with tile j - 1 + kPfVSlots. P_{j-1} . V_{j-1}
+                // is done, since the rows waited for it before writing P_j.
+                if (j >= 1 && j - 1 + kPfVSlots < n_tiles) {
+                    load_v(j - 1 + kPfVSlots);
+                    v_issued = j + kPfVSlots;
+                }
                 if (!(ok = mbar_wait_bounded(bar(kBarVFull + vs), (j / kPfVSlots) & 1))) break;
                 tc_fence_after();
                 const uint32_t paddr = smem_u32(sP + pb * kPfRowsBytes);
@@ -225,17 +230,6 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
                     tc_mma_f16(t_o, tc_desc_sw128(paddr + kk * 32),
                                tc_desc_sw128(vaddr + kk * 16 * kRowBytes), kIdO, j > 0 || kk > 0);
                 tc_commit(bar(kBarO + pb));
-                tc_commit(bar(kBarVEmpty + vs));
-                // V slot of tile j - 1: refilled with tile j - 1 + kPfVSlots once
-                // P_{j-1} . V_{j-1} is done
-                if (j >= 1 && j - 1 + kPfVSlots < n_tiles) {
-                    const int j1 = j - 1;
-                    if (!(ok = mbar_wait_bounded(bar(kBarVEmpty + j1 % kPfVSlots),
-                                                 (j1 / kPfVSlots) & 1)))
-                        break;
-                    load_v(j1 + kPfVSlots);
-                    v_issued = j1 + kPfVSlots + 1;
-                }
             }
             if (!ok) {
                 // let the MMAs and copies in flight finish before the block leaves
