@@ -242,25 +242,6 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// ---------------------------------------------------------------- named barriers ---
-// Barrier `id` (1..15) among `n` threads (a multiple of 32), whole warps converged.
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-// The same barrier, returning the OR of every participating thread's `v`.
-__device__ __forceinline__ bool named_bar_or(int id, int n, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %3, 0;\n\t"
-        "bar.red.or.pred po, %1, %2, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"(id), "r"(n), "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-}
-
 // ---------------------------------------------------------------- PDL --------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
