@@ -12,7 +12,9 @@ import torch
 
 import oracle
 from gpu_util import assert_attn_close, dev16, dev_i32, host16, new_err, require_gpu
-from workloads import gen_cache, gen_lens_uniform, gen_new_kv, gen_queries, make_rng
+from gpu_util import f64
+from workloads import (gen_cache, gen_lens_uniform, gen_new_kv, gen_queries, make_rng,
+                       round_half_bits)
 
 pytestmark = pytest.mark.gpu
 D = 64
@@ -23,16 +25,22 @@ def _gpu():
     require_gpu()
 
 
-def run_prefill(dtype, B, Hq, Hkv, cap, max_len, plens, lens_in=None, *, seed, flags=0):
+def run_prefill(dtype, B, Hq, Hkv, cap, max_len, plens, lens_in=None, *, seed, flags=0,
+                q_std=0.125, kv_std=0.125, key_growth=None):
     import kv_cached_decode_gb300 as kvd
 
     rng = make_rng(seed)
     plens = np.asarray(plens, np.int32)
     start = np.zeros(B, np.int32) if lens_in is None else np.asarray(lens_in, np.int32)
     # cached prefix (NaN past it), the prompt's K/V and queries
-    K, V = gen_cache(rng, B, Hkv, cap, D, dtype, 0.125, lens=start)
-    kn, vn = gen_new_kv(rng, B, Hkv, max_len, D, dtype, 0.125)
-    q = gen_queries(rng, B, Hq, max_len, D, dtype, 0.125)
+    K, V = gen_cache(rng, B, Hkv, cap, D, dtype, kv_std, lens=start)
+    kn, vn = gen_new_kv(rng, B, Hkv, max_len, D, dtype, kv_std)
+    q = gen_queries(rng, B, Hq, max_len, D, dtype, q_std)
+    if key_growth is not None:
+        # prompt key j scaled by 1 + j / key_growth: later keys score ever higher, so a
+        # row's running maximum keeps growing across key tiles
+        grow = 1.0 + np.arange(max_len) / key_growth
+        kn = round_half_bits(f64(kn, dtype) * grow[None, None, :, None], dtype)
     # expected cache and outputs
     Kw, Vw = K.copy(), V.copy()
     want = np.zeros((B, Hq, max_len, D))
@@ -109,3 +117,32 @@ def test_prefill_rejected_row_is_untouched():
     assert np.array_equal(Kg, Kw) and np.array_equal(Vg, Vw) and np.array_equal(lo, wlo)
     assert np.all(got[0] == 0)
     assert_attn_close(got[1:], want[1:], "f16", "good row")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_prefill_growing_maximum(dtype):
+    # Peaked scores whose maximum grows by many units (log2) from tile to tile: every
+    # change of a row's softmax reference (and the rescaling of the accumulated output
+    # it brings) is exercised, against the oracle's exact softmax.
+    got, want, Kg, Vg, Kw, Vw, lo, wlo, e, ok = run_prefill(
+        dtype, 2, 4, 2, 320, 300, [300, 257], seed=806, q_std=1.0, kv_std=0.5,
+        key_growth=16.0)
+    assert e == 0 and np.array_equal(Kg, Kw) and np.array_equal(lo, wlo)
+    assert_attn_close(got, want, dtype, "growing maximum")
+
+
+def test_prefill_cache_smaller_than_a_tile():
+    # a 40-position cache: the K/V copies are boxes of 40 rows, the tile's other rows
+    # stay unwritten and must not reach the output
+    got, want, Kg, Vg, Kw, Vw, lo, wlo, e, ok = run_prefill(
+        "f16", 3, 2, 1, 40, 33, [33, 7, 1], [0, 30, 39], seed=807)
+    assert e == 0 and np.array_equal(Kg, Kw) and np.array_equal(lo, wlo)
+    assert_attn_close(got, want, "f16", "small cache")
+
+
+def test_prefill_prompts_on_tile_boundaries():
+    # prompt ends exactly at 64- and 128-position boundaries (no partial key tile)
+    got, want, Kg, Vg, Kw, Vw, lo, wlo, e, ok = run_prefill(
+        "bf16", 4, 3, 1, 512, 384, [128, 256, 64, 384], [0, 0, 64, 128], seed=808)
+    assert e == 0 and np.array_equal(Kg, Kw) and np.array_equal(lo, wlo)
+    assert_attn_close(got, want, "bf16", "tile boundaries")

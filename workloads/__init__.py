@@ -12,6 +12,7 @@ from .synth import (  # noqa: F401
     WORKLOADS,
     make_rng,
     normal_half,
+    round_half_bits,
     gen_cache,
     gen_queries,
     gen_new_kv,

@@ -97,14 +97,19 @@ def _f32_to_bf16_bits(x32: np.ndarray) -> np.ndarray:
     return rounded.astype(np.uint16)
 
 
-def normal_half(rng: np.random.Generator, shape, std: float, dtype: str) -> np.ndarray:
-    """N(0, std^2) drawn in fp64, rounded to fp16/bf16, returned as uint16 bits."""
-    x = rng.standard_normal(size=shape) * std
+def round_half_bits(x, dtype: str) -> np.ndarray:
+    """fp64 values rounded to fp16/bf16 (nearest even), returned as uint16 bits."""
+    x = np.asarray(x, dtype=np.float64)
     if dtype == "f16":
         return x.astype(np.float16).view(np.uint16)
     if dtype == "bf16":
         return _f32_to_bf16_bits(x.astype(np.float32))
     raise ValueError(f"unknown dtype {dtype!r}")
+
+
+def normal_half(rng: np.random.Generator, shape, std: float, dtype: str) -> np.ndarray:
+    """N(0, std^2) drawn in fp64, rounded to fp16/bf16, returned as uint16 bits."""
+    return round_half_bits(rng.standard_normal(size=shape) * std, dtype)
 
 
 def gen_cache(rng, batch: int, n_kv_heads: int, capacity: int, head_dim: int,
