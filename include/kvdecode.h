@@ -94,7 +94,13 @@ typedef enum kvd_op {
 
 enum {
     KVD_FLAG_PDL = 1u << 0,
-    KVD_FLAG_EARLY_KV = 1u << 1
+    KVD_FLAG_EARLY_KV = 1u << 1,
+    /* Test only (kvd_prefill_attn): the attention kernel's producer does not issue the
+     * copy of the first K tile, so that copy's wait and the rows' waits run out after
+     * about one second each. The call must then report KVD_ERR_TIMEOUT through dev_err,
+     * leave the outputs unwritten, release its tensor memory and leave the stream
+     * usable. It exercises the bounded-wait failure path without any fault. */
+    KVD_FLAG_TEST_STALL = 1u << 8
 };
 
 #define KVD_WS_COUNTER_BYTES 65536

@@ -32,6 +32,7 @@ STATUS_NAMES = {0: "KVD_OK", 1: "KVD_ERR_INVALID_ARG", 2: "KVD_ERR_UNSUPPORTED",
 KVD_F16, KVD_BF16 = 0, 1
 KVD_OP_DECODE_ATTN, KVD_OP_VERIFY_ATTN, KVD_OP_GREEDY_ACCEPT, KVD_OP_SAMPLE_ACCEPT = 0, 1, 2, 3
 KVD_FLAG_PDL, KVD_FLAG_EARLY_KV = 1, 2
+KVD_FLAG_TEST_STALL = 1 << 8  # test only: see include/kvdecode.h
 KVD_WS_COUNTER_BYTES = 65536
 HEAD_DIM = 64
 

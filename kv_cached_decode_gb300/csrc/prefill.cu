@@ -62,6 +62,7 @@ struct PrefillParams {
     int32_t max_len, n_q_heads, group, capacity, q_tiles, box_rows;
     float scale_log2;
     float rope_log2_base;     // > 0 sets the rotary variant's base (log2)
+    int32_t test_stall;       // KVD_FLAG_TEST_STALL: the first K copy is never issued
 };
 
 __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
         fence_barrier_init();
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
-        for (int j = 0; j < min(kPfKSlots, n_tiles); ++j) load_k(j);
+        for (int j = p.test_stall ? 1 : 0; j < min(kPfKSlots, n_tiles); ++j) load_k(j);
         for (int j = 0; j < min(kPfVSlots, n_tiles); ++j) load_v(j);
     }
     if (warp == 0) {
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
                 flag_error(p.dev_err, KVD_ERR_TIMEOUT);
                 tc_commit(bar(kBarDrain));
                 mbar_wait_bounded(bar(kBarDrain), 0);
-                for (int jj = max(0, k_issued - kPfKSlots); jj < k_issued; ++jj)
+                for (int jj = max(p.test_stall ? 1 : 0, k_issued - kPfKSlots); jj < k_issued; ++jj)
                     mbar_wait_bounded(bar(kBarKFull + jj % kPfKSlots), (jj / kPfKSlots) & 1);
                 for (int jj = max(0, v_issued - kPfVSlots); jj < v_issued; ++jj)
                     mbar_wait_bounded(bar(kBarVFull + jj % kPfVSlots), (jj / kPfVSlots) & 1);
@@ -475,6 +476,7 @@ extern "C" kvd_status kvd_prefill_attn(kvd_dtype dtype, int32_t batch, int32_t n
     p.q_tiles = (int)q_tiles;
     p.box_rows = std::min(64, kv->capacity);
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.test_stall = (flags & KVD_FLAG_TEST_STALL) ? 1 : 0;
     const dim3 grid((unsigned)q_tiles, (unsigned)n_q_heads, (unsigned)batch);
     // The attention waits for the append (a dependent launch when PDL is requested).
     const bool pdl = (flags & (KVD_FLAG_PDL | KVD_FLAG_EARLY_KV)) != 0;

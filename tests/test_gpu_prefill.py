@@ -146,3 +146,31 @@ def test_prefill_prompts_on_tile_boundaries():
         "bf16", 4, 3, 1, 512, 384, [128, 256, 64, 384], [0, 0, 64, 128], seed=808)
     assert e == 0 and np.array_equal(Kg, Kw) and np.array_equal(lo, wlo)
     assert_attn_close(got, want, "bf16", "tile boundaries")
+
+
+def test_prefill_wait_that_runs_out_is_reported():
+    # The test-only stall flag withholds the first K copy: every wait on it runs out
+    # after about a second. The call must report KVD_ERR_TIMEOUT, leave the outputs
+    # unwritten and free its tensor memory; the same stream then serves a normal call.
+    import kv_cached_decode_gb300 as kvd
+
+    dtype, B, H, cap, max_len = "f16", 1, 1, 128, 100
+    rng = make_rng(809)
+    K, V = gen_cache(rng, B, H, cap, D, dtype, 0.125, lens=[0])
+    kn, vn = gen_new_kv(rng, B, H, max_len, D, dtype, 0.125)
+    q = gen_queries(rng, B, H, max_len, D, dtype, 0.125)
+    plens = np.array([max_len], np.int32)
+    Kd, Vd = dev16(K, dtype), dev16(V, dtype)
+    qd = dev16(q, dtype)
+    out = torch.full_like(qd, 3.0)
+    e = new_err()
+    kvd.kvd_prefill_attn(qd, kvd.make_cache(Kd, Vd), dev16(kn, dtype), dev16(vn, dtype),
+                         dev_i32(plens), out, flags=kvd.KVD_FLAG_TEST_STALL, dev_err=e)
+    torch.cuda.synchronize()
+    assert e.item() == 20  # KVD_ERR_TIMEOUT
+    assert torch.all(out == 3.0)
+    # the context and stream are usable: a normal call on fresh buffers matches the oracle
+    got, want, Kg, Vg, Kw, Vw, lo, wlo, e2, ok = run_prefill(
+        dtype, 2, 4, 2, 256, 150, [150, 77], seed=810)
+    assert e2 == 0 and np.array_equal(Kg, Kw) and np.array_equal(lo, wlo)
+    assert_attn_close(got, want, dtype, "after a timeout")
