@@ -1,7 +1,7 @@
 // kvd_tc.cuh -- fifth-generation tensor core (tcgen05) helpers for sm_103a: tensor
 // memory allocation, shared-memory matrix descriptors, the instruction descriptor of
-// kind::f16 MMAs, single-thread MMA issue with completion on an mbarrier, and loads of
-// accumulator rows from tensor memory.
+// kind::f16 MMAs, single-thread MMA issue with completion on an mbarrier, and loads and
+// stores of accumulator rows in tensor memory.
 //
 // Conventions used by every caller:
 //   * operands live in shared memory in the 128-byte-swizzled layout that TMA writes
@@ -120,25 +120,6 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const float* v) {
         "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
         "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
         "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-        : "memory");
-}
-
-// One fp32 column of this thread's lane: load / store, complete on return.
-__device__ __forceinline__ float tc_ld1(uint32_t taddr) {
-    uint32_t r;
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r)
-        : "r"(taddr)
-        : "memory");
-    return __uint_as_float(r);
-}
-__device__ __forceinline__ void tc_st1(uint32_t taddr, float v) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n\t"
-        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-        "r"(__float_as_uint(v))
         : "memory");
 }
 
