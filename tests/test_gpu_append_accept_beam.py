@@ -132,7 +132,8 @@ def test_accept_worked_example():
     assert e == 0 and int(n[0]) == 3 and fx["vocab"][int(nxt[0])] == "fox"
 
 
-@pytest.mark.parametrize("k,V", [(1, 1), (1, 7), (16, 2049), (3, 51865), (5, 100_003)])
+@pytest.mark.parametrize("k,V", [(1, 1), (1, 7), (16, 2049), (3, 51865), (5, 100_003),
+                                 (5, 524288)])
 def test_accept_shapes(k, V):
     logits, draft = gen_accept_inputs(make_rng(500 + k), 7, k, V, p_match=0.9) if V > 1 else (
         np.zeros((7, k + 1, 1), np.float32), np.zeros((7, k), np.int32))

@@ -153,11 +153,12 @@ def test_whisper_beam_step(first):
 
 @pytest.mark.parametrize("windows,beam,vocab", [(3, 1, 37), (2, 2, 1000), (5, 3, 2049),
                                                 (4, 4, 5000), (2, 8, 4097), (1, 4, 152064),
-                                                (1, 8, 400000), (64, 5, 51865)])
+                                                (1, 8, 400000), (64, 5, 51865),
+                                                (2, 8, 524288)])
 def test_shapes(windows, beam, vocab):
     # one piece per row (37 and 1000 ids), a piece boundary + 1, several pieces per row,
     # a large vocabulary, pieces staged in several passes (400000 ids, 2 pieces of 200000),
-    # many windows (64 clusters)
+    # many windows (64 clusters), the largest vocabulary and beam the call takes
     rng = make_rng(1100 + vocab + beam)
     eot = vocab - 3
     x, cum, sup = gen_beam_select_inputs(rng, windows, beam, vocab, eot=eot,

@@ -108,9 +108,10 @@ def test_speculative_acceptance(k):
     assert len(set(n.tolist())) > 1  # the case mixes accept counts
 
 
-@pytest.mark.parametrize("V", [37, 2049, 4097, 152064])
+@pytest.mark.parametrize("V", [37, 2049, 4097, 152064, 524288])
 def test_vocab_sizes(V):
-    # one CTA, a slice boundary + 1, three slices, sixteen slices of 9504 ids
+    # one CTA, a slice boundary + 1, three slices, sixteen slices of 9504 ids, a
+    # 524288-id vocabulary (the largest the beam selection takes)
     rng = make_rng(1720 + V)
     target, draft, drafts, r, u = gen_sample_inputs(rng, 6, 3, V)
     n, nxt, err = run_gpu(target, 0.8, u, draft, drafts, r, flags=1)
