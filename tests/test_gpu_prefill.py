@@ -174,3 +174,52 @@ def test_prefill_wait_that_runs_out_is_reported():
         dtype, 2, 4, 2, 256, 150, [150, 77], seed=810)
     assert e2 == 0 and np.array_equal(Kg, Kw) and np.array_equal(lo, wlo)
     assert_attn_close(got, want, dtype, "after a timeout")
+
+
+def test_prefill_bench_shape_sampled():
+    # The prefill at the size bench.py times (16 rows, 9 query heads on 3 KV heads, bf16,
+    # prompt lengths uniform in [256, 2048] from the bench's seed, PDL), checked on 48
+    # sampled (row, head, position) outputs, each against the oracle's attention of that
+    # one query over its visible keys; every cached K/V row bit-exact.
+    import kv_cached_decode_gb300 as kvd
+    from workloads import WORKLOADS, seed_for
+
+    w = WORKLOADS["gqa_lm_step"]
+    B, Hq, Hkv, cap, dtype = w["batch"], w["n_q_heads"], w["n_kv_heads"], w["capacity"], "bf16"
+    plens = gen_lens_uniform(make_rng(seed_for("gqa_lm_step", 0, 7)), B, w["len_lo"], w["len_hi"])
+    T = int(plens.max())
+    rng = make_rng(811)
+    K, V = gen_cache(rng, B, Hkv, cap, D, dtype, w["qkv_std"], lens=np.zeros(B, np.int32))
+    kn, vn = gen_new_kv(rng, B, Hkv, T, D, dtype, w["qkv_std"])
+    q = gen_queries(rng, B, Hq, T, D, dtype, w["qkv_std"])
+    Kd, Vd = dev16(K, dtype), dev16(V, dtype)
+    out = torch.full_like(dev16(q, dtype), 3.0)
+    lens_out = torch.zeros(B, dtype=torch.int32, device="cuda")
+    e = new_err()
+    kvd.kvd_prefill_attn(dev16(q, dtype), kvd.make_cache(Kd, Vd), dev16(kn, dtype),
+                         dev16(vn, dtype), dev_i32(plens), out, lens_out=lens_out,
+                         scale=w["scale"], flags=kvd.KVD_FLAG_PDL, dev_err=e)
+    torch.cuda.synchronize()
+    assert e.item() == 0 and np.array_equal(lens_out.cpu().numpy(), plens)
+    Kw, Vw = K.copy(), V.copy()
+    for b in range(B):
+        Kw[b, :, : plens[b]] = kn[b, :, : plens[b]]
+        Vw[b, :, : plens[b]] = vn[b, :, : plens[b]]
+    assert np.array_equal(host16(Kd), Kw) and np.array_equal(host16(Vd), Vw)
+    got = host16(out)
+    pick = make_rng(812)
+    for _ in range(48):
+        b = int(pick.integers(B))
+        h = int(pick.integers(Hq))
+        j = int(pick.integers(plens[b]))
+        if _ % 4 == 0:
+            j = int(plens[b]) - 1  # the last prompt row sees every key
+        hk = h // (Hq // Hkv)
+        want, err = oracle.attention(q[b:b + 1, h:h + 1, j:j + 1], Kw[b:b + 1, hk:hk + 1],
+                                     Vw[b:b + 1, hk:hk + 1], dtype,
+                                     lens=np.array([j + 1], np.int32))
+        assert not err
+        assert_attn_close(got[b:b + 1, h:h + 1, j:j + 1], want, dtype, f"row {b} head {h} pos {j}")
+    # rows past each prompt are zeros
+    for b in range(B):
+        assert np.all(got[b, :, plens[b]:] == 0)
