@@ -120,8 +120,34 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"expected float16 or bfloat16, got {t.dtype}")
 
 
-def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+_I32, _F32 = torch.int32, torch.float32
+
+
+def _ptr(t, dtype=None, what="tensor"):
+    """The device address of a contiguous CUDA tensor (None stays None). Anything else is
+    refused here: the library would read a host address or a strided view as a dense
+    device array."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, what):
+    return _ptr(t, None, what)
+
+
+def _i32(t, what):
+    return _ptr(t, _I32, what)
+
+
+def _f32(t, what):
+    return _ptr(t, _F32, what)
 
 
 def _stream(stream):
@@ -136,8 +162,10 @@ def _append_arg(append):
         return None
     k_new, v_new, lens_out = append[:3]
     rope_base = float(append[3]) if len(append) > 3 else 0.0
-    return ctypes.byref(NewTokens(k_new.data_ptr(), v_new.data_ptr(),
-                                  None if lens_out is None else lens_out.data_ptr(), rope_base))
+    kp, vp = _dev(k_new, "k_new"), _dev(v_new, "v_new")
+    lp = _i32(lens_out, "lens_out")
+    return ctypes.byref(NewTokens(kp.value, vp.value, None if lp is None else lp.value,
+                                  rope_base))
 
 
 def _check(status: int, call: str):
@@ -170,8 +198,8 @@ def kvd_status_string(status: int) -> str:
 def kvd_workspace_size(op: int, batch: int, n_q_heads: int = 1, n_kv_heads: int = 1,
                        rows_per_kv: int = 1, qlen: int = 1, max_len: int = 0,
                        vocab: int = 0) -> int:
-    return load_library().kvd_workspace_size(op, batch, n_q_heads, n_kv_heads, rows_per_kv,
-                                             qlen, max_len, vocab)
+    return load_library().kvd_workspace_size(op, batch, n_q_heads, n_kv_heads, rows_per_kv, qlen,
+                                             max_len, vocab)
 
 
 def new_workspace(nbytes: int, device=None) -> torch.Tensor:
@@ -183,17 +211,19 @@ def new_workspace(nbytes: int, device=None) -> torch.Tensor:
 def kvd_kv_append(cache: Cache, k_new, v_new, lens_in, lens_out=None, flags: int = 0,
                   dev_err=None, stream=None):
     B, H, q, D = k_new.shape
-    _check(load_library().kvd_kv_append(_dtype_code(k_new), ctypes.byref(cache), B, q, _ptr(k_new),
-                                        _ptr(v_new), _ptr(lens_in), _ptr(lens_out), flags,
-                                        _ptr(dev_err), _stream(stream)), "kvd_kv_append")
+    _check(load_library().kvd_kv_append(_dtype_code(k_new), ctypes.byref(cache), B, q,
+                                        _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+                                        _i32(lens_in, "lens_in"), _i32(lens_out, "lens_out"), flags,
+                                        _i32(dev_err, "dev_err"), _stream(stream)), "kvd_kv_append")
 
 
 def kvd_kv_append_rope(cache: Cache, k_new, v_new, lens_in, lens_out=None,
                        rope_base: float = 10000.0, flags: int = 0, dev_err=None, stream=None):
     B, H, q, D = k_new.shape
     _check(load_library().kvd_kv_append_rope(_dtype_code(k_new), ctypes.byref(cache), B, q,
-                                             _ptr(k_new), _ptr(v_new), _ptr(lens_in),
-                                             _ptr(lens_out), rope_base, flags, _ptr(dev_err),
+                                             _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+                                             _i32(lens_in, "lens_in"), _i32(lens_out, "lens_out"),
+                                             rope_base, flags, _i32(dev_err, "dev_err"),
                                              _stream(stream)), "kvd_kv_append_rope")
 
 
@@ -202,10 +232,11 @@ def kvd_decode_attn(q, cache: Cache, out, workspace, lens=None, fixed_len: int =
                     dev_err=None, stream=None, append=None):
     B, Hq, ql, D = q.shape
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load_library().kvd_decode_attn(_dtype_code(q), B, Hq, _ptr(q), ctypes.byref(cache),
-                                          _ptr(lens), fixed_len, _append_arg(append),
-                                          rows_per_kv, scale, _ptr(out), _ptr(workspace),
-                                          ws_bytes, flags, _ptr(dev_err), _stream(stream)),
+    _check(load_library().kvd_decode_attn(_dtype_code(q), B, Hq, _dev(q, "q"), ctypes.byref(cache),
+                                          _i32(lens, "lens"), fixed_len, _append_arg(append),
+                                          rows_per_kv, scale, _dev(out, "out"),
+                                          _dev(workspace, "workspace"), ws_bytes, flags,
+                                          _i32(dev_err, "dev_err"), _stream(stream)),
            "kvd_decode_attn")
 
 
@@ -214,11 +245,11 @@ def kvd_decode_attn_noalloc(q, cache: Cache, out, lens=None, fixed_len: int = 0,
                             dev_err=None, stream=None, append=None):
     """kvd_decode_attn without a workspace: the library's built-in scratch is used."""
     B, Hq, ql, D = q.shape
-    _check(load_library().kvd_decode_attn_noalloc(_dtype_code(q), B, Hq, _ptr(q),
-                                                  ctypes.byref(cache), _ptr(lens), fixed_len,
-                                                  _append_arg(append), rows_per_kv, scale,
-                                                  _ptr(out), flags, _ptr(dev_err),
-                                                  _stream(stream)),
+    _check(load_library().kvd_decode_attn_noalloc(_dtype_code(q), B, Hq, _dev(q, "q"),
+                                                  ctypes.byref(cache), _i32(lens, "lens"),
+                                                  fixed_len, _append_arg(append), rows_per_kv,
+                                                  scale, _dev(out, "out"), flags,
+                                                  _i32(dev_err, "dev_err"), _stream(stream)),
            "kvd_decode_attn_noalloc")
 
 
@@ -227,11 +258,11 @@ def kvd_verify_attn(q, cache: Cache, out, workspace, lens=None, fixed_len: int =
                     flags: int = 0, dev_err=None, stream=None, append=None):
     B, Hq, ql, D = q.shape
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load_library().kvd_verify_attn(_dtype_code(q), B, Hq, ql, _ptr(q),
-                                          ctypes.byref(cache), _ptr(lens), fixed_len,
+    _check(load_library().kvd_verify_attn(_dtype_code(q), B, Hq, ql, _dev(q, "q"),
+                                          ctypes.byref(cache), _i32(lens, "lens"), fixed_len,
                                           _append_arg(append), rows_per_kv, int(bool(causal)),
-                                          scale, _ptr(out),
-                                          _ptr(workspace), ws_bytes, flags, _ptr(dev_err),
+                                          scale, _dev(out, "out"), _dev(workspace, "workspace"),
+                                          ws_bytes, flags, _i32(dev_err, "dev_err"),
                                           _stream(stream)), "kvd_verify_attn")
 
 
@@ -242,11 +273,12 @@ def kvd_prefill_attn(q, cache: Cache, k_new, v_new, plens, out, lens_in=None, le
     the prompt. q, out: [batch, n_q_heads, max_len, 64]; k_new, v_new: [batch,
     n_kv_heads, max_len, 64]. rope_base > 0: rotary encoding of the prompt."""
     B, Hq, T, D = q.shape
-    _check(load_library().kvd_prefill_attn(_dtype_code(q), B, Hq, T, _ptr(q),
-                                           ctypes.byref(cache), _ptr(k_new), _ptr(v_new),
-                                           _ptr(lens_in), _ptr(plens), _ptr(lens_out), scale,
-                                           rope_base, _ptr(out), flags, _ptr(dev_err),
-                                           _stream(stream)),
+    _check(load_library().kvd_prefill_attn(_dtype_code(q), B, Hq, T, _dev(q, "q"),
+                                           ctypes.byref(cache), _dev(k_new, "k_new"),
+                                           _dev(v_new, "v_new"), _i32(lens_in, "lens_in"),
+                                           _i32(plens, "plens"), _i32(lens_out, "lens_out"), scale,
+                                           rope_base, _dev(out, "out"), flags,
+                                           _i32(dev_err, "dev_err"), _stream(stream)),
            "kvd_prefill_attn")
 
 
@@ -256,20 +288,22 @@ def kvd_rope(q=None, k=None, pos0=None, base: float = 10000.0, flags: int = 0, d
     n_k_heads, n, 64]; token j of row b at position pos0[b] + j."""
     ref = q if q is not None else k
     B, _, n, _ = ref.shape
-    _check(load_library().kvd_rope(_dtype_code(ref), B, n, _ptr(q),
-                                   0 if q is None else q.shape[1], _ptr(k),
-                                   0 if k is None else k.shape[1], _ptr(pos0), base, flags,
-                                   _ptr(dev_err), _stream(stream)), "kvd_rope")
+    _check(load_library().kvd_rope(_dtype_code(ref), B, n, _dev(q, "q"),
+                                   0 if q is None else q.shape[1], _dev(k, "k"),
+                                   0 if k is None else k.shape[1], _i32(pos0, "pos0"), base, flags,
+                                   _i32(dev_err, "dev_err"), _stream(stream)), "kvd_rope")
 
 
 def kvd_greedy_accept(logits, draft, n_accepted, next_token, workspace, n_min=None,
                       argmax=None, flags: int = 0, dev_err=None, stream=None):
     B, k1, V = logits.shape
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(load_library().kvd_greedy_accept(_ptr(logits), B, k1 - 1, V, _ptr(draft),
-                                            _ptr(n_accepted), _ptr(next_token), _ptr(n_min),
-                                            _ptr(argmax), _ptr(workspace), ws_bytes, flags,
-                                            _ptr(dev_err), _stream(stream)), "kvd_greedy_accept")
+    _check(load_library().kvd_greedy_accept(_f32(logits, "logits"), B, k1 - 1, V,
+                                            _i32(draft, "draft"), _i32(n_accepted, "n_accepted"),
+                                            _i32(next_token, "next_token"), _i32(n_min, "n_min"),
+                                            _i32(argmax, "argmax"), _dev(workspace, "workspace"),
+                                            ws_bytes, flags, _i32(dev_err, "dev_err"),
+                                            _stream(stream)), "kvd_greedy_accept")
 
 
 def kvd_beam_reorder_kv(caches, rows: int, beam: int, parent, lens=None, fixed_len: int = 0,
@@ -277,8 +311,8 @@ def kvd_beam_reorder_kv(caches, rows: int, beam: int, parent, lens=None, fixed_l
     arr = (Cache * len(caches))(*caches)
     code = KVD_F16 if dtype == torch.float16 else KVD_BF16
     _check(load_library().kvd_beam_reorder_kv(code, arr, len(caches), rows, beam,
-                                              _ptr(parent), _ptr(lens), fixed_len, flags,
-                                              _ptr(dev_err), _stream(stream)),
+                                              _i32(parent, "parent"), _i32(lens, "lens"), fixed_len,
+                                              flags, _i32(dev_err, "dev_err"), _stream(stream)),
            "kvd_beam_reorder_kv")
 
 
@@ -294,11 +328,17 @@ def kvd_beam_select(logits, beam: int, *, cum=None, suppress=None, blank=None,
     rows, V = logits.shape
     n_sup = 0 if suppress is None else suppress.numel()
     n_blank = 0 if blank is None else blank.numel()
-    _check(load_library().kvd_beam_select(
-        _ptr(logits), rows // beam, beam, V, _ptr(cum), _ptr(suppress), n_sup, _ptr(blank),
-        n_blank, eot, int(bool(first_step)), _ptr(row_token), _ptr(row_logprob), _ptr(parent),
-        _ptr(token), _ptr(new_cum), _ptr(n_finished), _ptr(fin_parent), _ptr(fin_score),
-        flags, _ptr(dev_err), _stream(stream)), "kvd_beam_select")
+    _check(load_library().kvd_beam_select(_f32(logits, "logits"), rows // beam, beam, V,
+                                          _f32(cum, "cum"), _i32(suppress, "suppress"), n_sup,
+                                          _i32(blank, "blank"), n_blank, eot, int(bool(first_step)),
+                                          _i32(row_token, "row_token"),
+                                          _f32(row_logprob, "row_logprob"), _i32(parent, "parent"),
+                                          _i32(token, "token"), _f32(new_cum, "new_cum"),
+                                          _i32(n_finished, "n_finished"),
+                                          _i32(fin_parent, "fin_parent"),
+                                          _f32(fin_score, "fin_score"), flags,
+                                          _i32(dev_err, "dev_err"), _stream(stream)),
+           "kvd_beam_select")
 
 
 def kvd_sample_accept(target, u, n_accepted, next_token, workspace, temperature: float = 1.0,
@@ -309,8 +349,11 @@ def kvd_sample_accept(target, u, n_accepted, next_token, workspace, temperature:
     workspace: kvd_workspace_size(KVD_OP_SAMPLE_ACCEPT, B, qlen=k, vocab=V) bytes."""
     B, k1, V = target.shape
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(load_library().kvd_sample_accept(_ptr(target), _ptr(draft), _ptr(drafts), B,
-                                            k1 - 1, V, temperature, _ptr(r), _ptr(u),
-                                            _ptr(n_accepted), _ptr(next_token), _ptr(workspace),
-                                            ws_bytes, flags, _ptr(dev_err), _stream(stream)),
+    _check(load_library().kvd_sample_accept(_f32(target, "target"), _f32(draft, "draft"),
+                                            _i32(drafts, "drafts"), B, k1 - 1, V, temperature,
+                                            _f32(r, "r"), _f32(u, "u"),
+                                            _i32(n_accepted, "n_accepted"),
+                                            _i32(next_token, "next_token"),
+                                            _dev(workspace, "workspace"), ws_bytes, flags,
+                                            _i32(dev_err, "dev_err"), _stream(stream)),
            "kvd_sample_accept")

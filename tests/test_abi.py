@@ -241,3 +241,22 @@ def test_sample_accept_host_rejects_bad_arguments(lib):
     n = lib.kvd_workspace_size(KVD_OP_SAMPLE_ACCEPT, 16, 0, 0, 0, 5, 0, 51865)
     assert n >= KVD_WS_COUNTER_BYTES + 16 * 11 * 26 * 8  # (max, sum) per row and segment
     assert lib.kvd_workspace_size(KVD_OP_SAMPLE_ACCEPT, 16, 0, 0, 0, 8, 0, 51865) == 0
+
+
+def test_binding_refuses_host_and_mistyped_tensors(lib):
+    # The binding passes raw device addresses: a host tensor would reach a kernel as a
+    # pointer into host memory, so it is refused before the library is called.
+    import torch
+
+    import kv_cached_decode_gb300 as kvd
+
+    logits = torch.zeros(1, 3, 10, dtype=torch.float32)
+    draft = torch.zeros(1, 2, dtype=torch.int32)
+    n, nxt = torch.zeros(1, dtype=torch.int32), torch.zeros(1, dtype=torch.int32)
+    ws = torch.zeros(1 << 16, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="logits must be a CUDA tensor"):
+        kvd.kvd_greedy_accept(logits, draft, n, nxt, ws)
+    with pytest.raises(ValueError, match="target must be a CUDA tensor"):
+        kvd.kvd_sample_accept(logits[:, :1], torch.zeros(1), n, nxt, ws)
+    with pytest.raises(ValueError, match="logits must be a CUDA tensor"):
+        kvd.kvd_beam_select(torch.zeros(2, 10), 2)

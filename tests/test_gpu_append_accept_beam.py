@@ -246,3 +246,24 @@ def test_beam_padded_rows_take_the_per_thread_path():
         for r in range(10):
             want[r, :, : lens[r]] = layer[kv][parent[r], :, : lens[r]]
         assert np.array_equal(host16(devs[kv].contiguous()), want)
+
+
+def test_binding_refuses_mistyped_and_strided_tensors():
+    import kv_cached_decode_gb300 as kvd
+
+    dev = "cuda"
+    logits = torch.zeros(2, 4, 64, dtype=torch.float32, device=dev)
+    draft = torch.zeros(2, 3, dtype=torch.int32, device=dev)
+    n = torch.zeros(2, dtype=torch.int32, device=dev)
+    nxt = torch.zeros(2, dtype=torch.int32, device=dev)
+    ws = kvd.new_workspace(kvd.kvd_workspace_size(kvd.KVD_OP_GREEDY_ACCEPT, 2, qlen=3,
+                                                  vocab=64), device=dev)
+    with pytest.raises(TypeError, match="logits must be torch.float32"):
+        kvd.kvd_greedy_accept(logits.half(), draft, n, nxt, ws)
+    with pytest.raises(TypeError, match="draft must be torch.int32"):
+        kvd.kvd_greedy_accept(logits, draft.long(), n, nxt, ws)
+    with pytest.raises(ValueError, match="draft must be contiguous"):
+        kvd.kvd_greedy_accept(logits, torch.zeros(3, 2, dtype=torch.int32, device=dev).t(),
+                              n, nxt, ws)
+    kvd.kvd_greedy_accept(logits, draft, n, nxt, ws)  # the same call, well formed
+    torch.cuda.synchronize()
