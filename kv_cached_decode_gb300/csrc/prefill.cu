@@ -10,16 +10,20 @@
 // for j < plens[b] (rows past a row's prompt length are written as zeros).
 //
 // Design: the prompt's K/V are first written into the cache by the append kernel (with a
-// per-row count), then one block of four warps handles 128 query positions of one query
-// head, one row per thread. The rows, rotated if asked, are staged once into shared
-// memory in the 128-byte-swizzled layout; K/V tiles of 64 positions arrive by TMA (the
-// same swizzle) through a 4-stage ring. Both products run on the fifth-generation tensor
-// cores: S = Q.K^T (M 128, N 64, K 64) and P.V (M 128, N 64, K 64, V read MN-major) are
-// issued by one thread as tcgen05.mma with fp32 accumulators in tensor memory, and each
-// thread reads its row of S back with tcgen05.ld, applies the causal mask and the online
-// softmax in exp2 form, and writes its row of P (rounded to the input type) to shared
-// memory for the second product; the output row accumulates in registers. Only the
-// tiles a block's rows can see are read, and blocks with the most tiles start first.
+// per-row count); then the attention kernel runs on the fifth-generation tensor cores.
+// A block takes 128 query positions of one query head: four softmax warps own the rows
+// (thread t: row t, tensor-memory lane t) and one producer thread issues every TMA copy
+// and every tcgen05.mma. The rows, rotated if asked, are staged once into shared memory
+// in the 128-byte-swizzled layout; K/V tiles of 64 positions arrive by TMA (the same
+// swizzle) through 3 K and 2 V slots.
+//   S = Q . K^T   M 128, N 64, K 64 (Q and K K-major)          -> tensor memory
+//   O += P . V    M 128, N 64, K 64 (P K-major, V MN-major)     -> tensor memory
+// Each row reads its S with tcgen05.ld, applies the causal mask where the tile is not
+// wholly visible to its warp, forms the weights exp2(s * scale * log2 e - m) rounded to
+// the input type into the swizzled P operand, and sums them. A row's reference m moves
+// only when its maximum grows by more than 2^8; the rows then rescale their O in tensor
+// memory. Hand-offs run through mbarriers, every wait bounded. Only the tiles a block's
+// rows can see are read, and the blocks with the most tiles start first.
 #include <algorithm>
 #include <mutex>
 #include <type_traits>
