@@ -719,6 +719,9 @@ def run_sweep(args):
         flags |= kvd.KVD_FLAG_EARLY_KV
     parts = {"beam_step": run_beam_step, "beam_select": run_beam_select,
              "gqa_lm_step": run_gqa_lm_step, "sample_accept": run_sample_accept}
+    if args.sweep_part == "beam_step" and args.beam_len is not None:
+        run_beam_step(torch, kvd, dev, stream, peak, flags, only_len=args.beam_len)
+        return 0
     if args.sweep_part in parts:
         parts[args.sweep_part](torch, kvd, dev, stream, peak, flags)
         return 0
@@ -774,7 +777,7 @@ def run_sweep(args):
     return 0
 
 
-def run_beam_step(torch, kvd, dev, stream, peak, flags):
+def run_beam_step(torch, kvd, dev, stream, peak, flags, only_len=None):
     """Beam search step: 8 windows x beam 5 = 40 rows, 32 layers, 20 heads, fp16,
     capacity 448: beam_reorder_kv over all layers, then per layer self decode over
     len+1 positions with the new token appended in the same call, and cross decode over
@@ -801,7 +804,7 @@ def run_beam_step(torch, kvd, dev, stream, peak, flags):
     ws = kvd.new_workspace(kvd.kvd_workspace_size(kvd.KVD_OP_DECODE_ATTN, R, H, H, beam, 1, F),
                            device=dev)
     moved = int(np.sum(parent_np != np.arange(R)))
-    for L in w["lens"]:
+    for L in w["lens"] if only_len is None else (only_len,):
         lens_in = torch.full((R,), L, dtype=torch.int32, device=dev)
         lens = torch.full((R,), L + 1, dtype=torch.int32, device=dev)
 
@@ -1156,6 +1159,8 @@ def main(argv=None):
     ap.add_argument("--sweep-part", choices=["beam_step", "beam_select", "gqa_lm_step",
                                              "sample_accept", "prefill"],
                     default=None, help="with --sweep: run only this part")
+    ap.add_argument("--beam-len", type=int, default=None,
+                    help="with --sweep --sweep-part beam_step: only this cached length")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu DRAM bytes per launch of the dominant kernel, if measured")
