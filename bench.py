@@ -680,7 +680,7 @@ def run_ours(args):
     verified = (e_n + 1) * 1 / (ms_ver * 1e-3 / step.NL)
 
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:  # the CPU baseline is taken at N = 1 only
         gbs, layers, secs = oracle_sample(seconds=args.cpu_seconds)
         cpu = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"{layers} of the 32 layers of one step (append, self/cross decode, "
