@@ -223,3 +223,39 @@ def test_prefill_bench_shape_sampled():
     # rows past each prompt are zeros
     for b in range(B):
         assert np.all(got[b, :, plens[b]:] == 0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_prefill_long_prompt_sampled(dtype):
+    # one 8000-token prompt after a 150-token cached prefix (8192-position cache): the
+    # last query blocks stream 128 key tiles; 24 sampled positions against the oracle,
+    # the cache bit-exact
+    import kv_cached_decode_gb300 as kvd
+
+    B, Hq, Hkv, cap, plen, s0 = 1, 2, 1, 8192, 8000, 150
+    rng = make_rng(813)
+    K, V = gen_cache(rng, B, Hkv, cap, D, dtype, 0.125, lens=[s0])
+    kn, vn = gen_new_kv(rng, B, Hkv, plen, D, dtype, 0.125)
+    q = gen_queries(rng, B, Hq, plen, D, dtype, 0.5)  # sharper rows than N(0, 1/64)
+    Kd, Vd = dev16(K, dtype), dev16(V, dtype)
+    out = torch.full_like(dev16(q, dtype), 3.0)
+    lens_out = torch.zeros(B, dtype=torch.int32, device="cuda")
+    e = new_err()
+    kvd.kvd_prefill_attn(dev16(q, dtype), kvd.make_cache(Kd, Vd), dev16(kn, dtype),
+                         dev16(vn, dtype), dev_i32([plen]), out, lens_in=dev_i32([s0]),
+                         lens_out=lens_out, dev_err=e)
+    torch.cuda.synchronize()
+    assert e.item() == 0 and lens_out.item() == s0 + plen
+    Kw, Vw = K.copy(), V.copy()
+    Kw[0, :, s0:s0 + plen] = kn[0]
+    Vw[0, :, s0:s0 + plen] = vn[0]
+    assert np.array_equal(host16(Kd), Kw) and np.array_equal(host16(Vd), Vw)
+    got = host16(out)
+    pick = make_rng(814)
+    js = sorted(set([0, 127, 128, plen - 1] + [int(x) for x in pick.integers(0, plen, 20)]))
+    for j in js:
+        for h in range(Hq):
+            want, err = oracle.attention(q[:, h:h + 1, j:j + 1], Kw[:, :1], Vw[:, :1], dtype,
+                                         lens=np.array([s0 + j + 1], np.int32))
+            assert not err
+            assert_attn_close(got[:, h:h + 1, j:j + 1], want, dtype, f"head {h} pos {j}")
