@@ -95,11 +95,20 @@ typedef enum kvd_op {
 enum {
     KVD_FLAG_PDL = 1u << 0,
     KVD_FLAG_EARLY_KV = 1u << 1,
-    /* Test only (kvd_prefill_attn): the attention kernel's producer does not issue the
+    /* Test only. kvd_prefill_attn: the attention kernel's producer does not issue the
      * copy of the first K tile, so that copy's wait and the rows' waits run out after
-     * about one second each. The call must then report KVD_ERR_TIMEOUT through dev_err,
+     * about one second each; the call must then report KVD_ERR_TIMEOUT through dev_err,
      * leave the outputs unwritten, release its tensor memory and leave the stream
-     * usable. It exercises the bounded-wait failure path without any fault. */
+     * usable. kvd_decode_attn / kvd_verify_attn / kvd_decode_attn_noalloc: in the last
+     * split of every (row, KV head) unit the first stage of K/V tiles expects more
+     * bytes than its copies bring (a split whose range starts past the row's length
+     * has no stage), so that stage never completes and the split's tile waits run out
+     * after about one second; it drains, gives up,
+     * and (in a cluster merge) sends its partial marked as given up; the call must
+     * report KVD_ERR_TIMEOUT, leave those units' outputs unwritten, and leave the
+     * stream usable (a workspace merge also leaves that unit's arrival counter
+     * non-zero: re-zero the workspace). The timeout paths are exercised without any
+     * fault. */
     KVD_FLAG_TEST_STALL = 1u << 8
 };
 
@@ -225,15 +234,24 @@ kvd_status kvd_decode_attn(kvd_dtype dtype, int32_t batch, int32_t n_q_heads, co
  * cudaMalloc, cudaFree or other allocating routine.
  *
  *  - Set-up: the first call on each device looks up the scratch address there
- *    (cudaGetSymbolAddress, with that device current). Make that first call before
- *    any stream capture.
- *  - Every call first clears the scratch's arrival counters on `stream` (a 64 KiB
- *    memset of the library's own buffer; nothing else), then launches the kernel.
+ *    (cudaGetSymbolAddress, with that device current), after the host checks below
+ *    have passed. Make that first call before any stream capture. The address is kept
+ *    for the life of the process: do not call this entry point again after a
+ *    cudaDeviceReset (or anything else that destroys the device's primary context)
+ *    in the same process.
+ *  - Host checks come first, exactly as for kvd_decode_attn: an invalid argument, or a
+ *    shape whose split merge needs more than the buffer holds (KVD_ERR_WORKSPACE; use
+ *    kvd_decode_attn with a workspace), returns with nothing enqueued on `stream`.
+ *  - Only a plan that merges splits through the buffer (a handful of (row, KV head)
+ *    units over a long range) uses its arrival counters. For such a plan the call first
+ *    clears those counters on `stream` (a memset of the library's own buffer, a few
+ *    bytes per unit), then launches the kernel. That memset sits between the previous
+ *    kernel on the stream and this one, so for those shapes KVD_FLAG_PDL and
+ *    KVD_FLAG_EARLY_KV give no overlap with the previous kernel. Other shapes launch
+ *    the kernel alone, and the flags behave as in kvd_decode_attn.
  *  - All calls on a device share the one buffer: calls that can overlap on the GPU
  *    (different streams, or graphs replayed concurrently) race and give wrong results.
  *    Serialise them on one stream.
- *  - Shapes whose split merge needs more than the buffer holds return
- *    KVD_ERR_WORKSPACE and launch no kernel; use kvd_decode_attn with a workspace.
  */
 #define KVD_NOALLOC_SCRATCH_BYTES (512u * 1024u)
 kvd_status kvd_decode_attn_noalloc(kvd_dtype dtype, int32_t batch, int32_t n_q_heads,
@@ -241,6 +259,17 @@ kvd_status kvd_decode_attn_noalloc(kvd_dtype dtype, int32_t batch, int32_t n_q_h
                                    int32_t fixed_len, const kvd_new_tokens *append,
                                    int32_t rows_per_kv, float scale, void *out, uint32_t flags,
                                    int32_t *dev_err, kvd_stream_t stream);
+
+/*
+ * kvd_noalloc_test_fill_counters -- test support for kvd_decode_attn_noalloc.
+ *
+ * No counterpart on the pages. Fills the arrival counters of the built-in scratch
+ * buffer (its first KVD_WS_COUNTER_BYTES) with `byte_value` on `stream`, as a call that
+ * stopped early after a timed-out wait could leave them, so that a test can check that
+ * the next kvd_decode_attn_noalloc call still starts its merge from zero. Not for use
+ * while a kvd_decode_attn_noalloc call may be running on another stream.
+ */
+kvd_status kvd_noalloc_test_fill_counters(uint8_t byte_value, kvd_stream_t stream);
 
 /*
  * kvd_verify_attn -- a block of qlen query tokens per row in one pass.

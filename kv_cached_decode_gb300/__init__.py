@@ -39,7 +39,7 @@ HEAD_DIM = 64
 EXPORTED = ("kvd_kv_append", "kvd_decode_attn", "kvd_verify_attn", "kvd_greedy_accept",
             "kvd_beam_reorder_kv", "kvd_workspace_size", "kvd_status_string", "kvd_version",
             "kvd_decode_attn_noalloc", "kvd_prefill_attn", "kvd_rope", "kvd_beam_select",
-            "kvd_kv_append_rope", "kvd_sample_accept")
+            "kvd_kv_append_rope", "kvd_sample_accept", "kvd_noalloc_test_fill_counters")
 
 
 class KvdError(RuntimeError):
@@ -88,6 +88,7 @@ def load_library(path: str = LIB_PATH):
             "kvd_kv_append": [I32, CP, I32, I32, P, P, P, P, U32, P, P],
             "kvd_decode_attn": [I32, I32, I32, P, CP, P, I32, NP, I32, F, P, P, SZ, U32, P, P],
             "kvd_decode_attn_noalloc": [I32, I32, I32, P, CP, P, I32, NP, I32, F, P, U32, P, P],
+            "kvd_noalloc_test_fill_counters": [ctypes.c_uint8, P],
             "kvd_verify_attn": [I32, I32, I32, I32, P, CP, P, I32, NP, I32, I32, F, P, P, SZ,
                                 U32, P, P],
             "kvd_prefill_attn": [I32, I32, I32, I32, P, CP, P, P, P, P, P, F, F, P, U32, P, P],
@@ -251,6 +252,12 @@ def kvd_decode_attn_noalloc(q, cache: Cache, out, lens=None, fixed_len: int = 0,
                                                   scale, _dev(out, "out"), flags,
                                                   _i32(dev_err, "dev_err"), _stream(stream)),
            "kvd_decode_attn_noalloc")
+
+
+def kvd_noalloc_test_fill_counters(byte_value: int, stream=None):
+    """Test support: fill the built-in scratch's arrival counters with ``byte_value``."""
+    _check(load_library().kvd_noalloc_test_fill_counters(byte_value, _stream(stream)),
+           "kvd_noalloc_test_fill_counters")
 
 
 def kvd_verify_attn(q, cache: Cache, out, workspace, lens=None, fixed_len: int = 0,

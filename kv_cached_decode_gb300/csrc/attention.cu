@@ -80,6 +80,7 @@ struct AttnParams {
     int32_t box_rows;
     int32_t early;
     int32_t cluster;   // 1: the splits of a unit form one thread-block cluster
+    int32_t test_stall;  // test only: the last split of every unit never sees its first stage
     int32_t append;    // 1: k_new/v_new are written at positions lens[b] .. lens[b]+qlen-1
     int32_t rope;      // 1: rotary encoding of the queries and the appended keys
     float rope_log2_base;
@@ -144,6 +145,27 @@ struct CtaCtx {
     int bk, h, sub, s, m0, mcount, len, new0, t_begin, t_end, n_tiles, unit;
     bool bad;
 };
+
+// Give-up points of the block's waits. Every wait is bounded relative to its own start
+// (kWaitNs, 1 s, in the mbarrier helpers; the timer is read only once a wait turns
+// slow), and they are ordered so that a first CTA that receives its cluster peers'
+// partials never exits while a peer can still send:
+//  * a thread's tile waits: at most one per round, each within 1 s, and none after the
+//    first that runs out -- at most `rounds` seconds in all;
+//  * a block that gave up drains its copies in flight: at most one wait per stage, each
+//    within 1 s -- `stages` seconds; only then does it send its partial (zeros, marked
+//    as given up);
+//  * so every peer has sent within (rounds + stages) seconds of passing the dependency
+//    wait, and the first CTA waits for the partials (rounds + stages + 1) seconds after
+//    it starts waiting, which is after it passed that wait too. All CTAs of a cluster
+//    are resident together and pass the dependency wait within microseconds of one
+//    another, far inside the 1 s margin.
+__device__ __forceinline__ unsigned long long merge_wait_ns(const AttnParams& p) {
+    return (unsigned long long)((p.tiles_per_split + 1) / 2 + p.stages + 1) * kWaitNs;
+}
+// The (max, sum) slot of a split that gave up carries this maximum; a merge that sees it
+// writes no output (a real maximum is finite or -inf).
+constexpr float kAbortedMax = INFINITY;
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -230,6 +252,11 @@ __device__ __forceinline__ bool prologue(const AttnParams& p, CtaCtx& c, uint8_t
         prefetch_tensormap(tmv);
         const uint32_t tx = 2u * p.box_rows * kRowBytes;
         const int first = min(p.stages, c.n_tiles);
+        // test only: the last split's first stage expects 16 bytes more than its copies
+        // bring (set before they are issued), so that phase never completes and every wait
+        // on it runs out; the copies themselves all land
+        if (p.test_stall && c.s == p.splits - 1 && first > 0)
+            mbar_expect_tx_only(smem_u32(&bars[0]), 16);
         for (int j = 0; j < first; ++j)
             issue_tile(tmk, tmv, smem, bars, j, c.t_begin + j * kTile, c.h, c.bk, tx);
     }
@@ -260,6 +287,8 @@ __device__ __forceinline__ bool prologue(const AttnParams& p, CtaCtx& c, uint8_t
             tab[x] = rope_cos_sin(pos0 + (x >> 5), x & 31, p.rope_log2_base);
     }
     __syncthreads();
+    // Every CTA of a cluster arrives here, before any wait of its own: the cluster
+    // barrier waits below (merge, abort) therefore always complete.
     if (p.cluster) cluster_arrive_relaxed();  // the first CTA's merge barrier is ready
     pdl_trigger();
     if (p.early) pdl_wait();
@@ -346,11 +375,17 @@ __device__ __forceinline__ void inject_slab(const AttnParams& p, const CtaCtx& c
     __syncwarp();
 }
 
-// After a timed-out wait: wait (bounded) for the latest copy issued into every stage, so
-// that none is still writing shared memory when the block exits; then keep the cluster's
-// merge consistent -- a non-first CTA still sends its (meaningless) bytes so the first
-// CTA's barrier completes, and the first CTA waits for them, since they land in its
-// shared memory, before it exits.
+// After a timed-out wait: wait (each within 1 s) for the latest copy issued into every
+// stage, so that none is still writing shared memory when the block exits; then keep
+// the cluster's merge consistent -- a non-first CTA still sends its bytes, marked as
+// given up, so the first CTA's barrier completes, and the first CTA waits for them
+// (merge_wait_ns after its drain), since they land in its shared memory, before it
+// exits.
+//
+// Every wait on this path ends: the drain waits and the first CTA's wait are bounded;
+// __syncthreads is reached by all threads (the caller's __syncthreads_or is
+// block-uniform); the cluster barrier wait completes because every CTA of the cluster
+// arrived on it in the prologue, before any wait.
 __device__ void abort_after_timeout(const AttnParams& p, const CtaCtx& c, uint64_t* bars,
                                     float* mrg, int issued) {
     const int tid = threadIdx.x;
@@ -365,11 +400,13 @@ __device__ void abort_after_timeout(const AttnParams& p, const CtaCtx& c, uint64
         if (c.s != 0) {
             const uint32_t dst = map_shared(smem_u32(mrg), 0);
             const uint32_t rbar = map_shared(smem_u32(&bars[p.stages]), 0);
-            for (int it = tid; it < kSlotQuads * c.mcount; it += blockDim.x)
+            for (int it = tid; it < kSlotQuads * c.mcount; it += blockDim.x) {
+                const bool ml = it % kSlotQuads == kHeadDim / 4;  // the (max, sum) quad
                 st_async_v4(dst + ((c.s * p.msub) * kSlot + 4 * it) * 4,
-                            make_float4(0.f, 0.f, 0.f, 0.f), rbar);
+                            make_float4(ml ? kAbortedMax : 0.f, 0.f, 0.f, 0.f), rbar);
+            }
         } else if (tid == 0) {
-            mbar_wait_bounded_cluster(smem_u32(&bars[p.stages]), 0);
+            mbar_wait_bounded_cluster(smem_u32(&bars[p.stages]), 0, merge_wait_ns(p));
         }
     }
 }
@@ -500,9 +537,11 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
                 st_async_v4(dst + slot * 4, v, rbar);
         }
         if (!leader) return;
-        // One warp waits for the other CTAs' bytes; the block barrier then orders those
-        // bytes, and the slots this CTA's own threads wrote, before every thread's reads.
-        const bool ok = tid >= 32 || mbar_wait_bounded_cluster(smem_u32(merge_bar), 0);
+        // One warp waits for the other CTAs' bytes (merge_wait_ns: longer than any peer
+        // can take to send); the block barrier then orders those bytes, and the slots
+        // this CTA's own threads wrote, before every thread's reads.
+        const bool ok =
+            tid >= 32 || mbar_wait_bounded_cluster(smem_u32(merge_bar), 0, merge_wait_ns(p));
         if (__syncthreads_or(!ok)) {
             if (tid == 0) flag_error(p.dev_err, KVD_ERR_TIMEOUT);
             return;
@@ -518,6 +557,7 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
 #pragma unroll
             for (int r = 0; r < kMaxClusterSplits; ++r)
                 mx = fmaxf(mx, sl0[min(r, S - 1) * stride + kHeadDim]);
+            if (mx == kAbortedMax) continue;  // a split gave up: no output
             const float ref = mx == -INFINITY ? 0.f : mx;
             float l = 0.f;
             float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -769,11 +809,18 @@ __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: 4 blocks per
 // MINB: blocks per SM the register budget is cut for. 2 (no cut) is the default; 3 gives
 // more resident blocks, hence more splits, when a launch is limited by residency, at the
 // price of a few spilled registers.
-template <typename T, int MINB, bool ROPE>
+// RM: query vectors a block holds, 16 or 8. With at most 8 (decode of one token, a
+// verify block of up to 8, grouped heads of up to 8, up to 8 beam rows on one window)
+// rows 8..15 of every m16n8k16 product are zero: the A fragments of those rows are the
+// constant 0, their S and O accumulators are not kept, and the block needs about 30
+// fewer registers -- three blocks per SM without spilling, so that more of the next
+// launch's blocks (and its thread-block clusters) fit beside a running launch.
+template <typename T, int MINB, bool ROPE, int RM = 16>
 __global__ void __launch_bounds__(kThreads, MINB)
     block_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
-    constexpr int RM = 16;
+    static_assert(RM == 16 || (RM == 8 && !ROPE), "the 8-row build has no rotation");
+    constexpr bool kFull = RM == 16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     const SmemLayout L = smem_layout(p.stages, RM, merge_slots(p.cluster, p.splits, p.msub),
@@ -793,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     // Q as m16n8k16 A fragments for the four 16-dim k-steps (rows >= mcount are 0).
     uint32_t qa[4][4];
     const T* qbase = static_cast<const T*>(p.q);
-    const bool rowA = qr < c.mcount, rowB = qr + 8 < c.mcount;
+    const bool rowA = qr < c.mcount, rowB = kFull && qr + 8 < c.mcount;
     if (ROPE) {
         // The block's query rows are rotated once, into shared memory (16 threads per
         // row, 2 rotation pairs each; query m is token m % qlen of the new tokens), and
@@ -833,6 +880,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
             qa[kk][3] = rowB ? *reinterpret_cast<const uint32_t*>(qbase + offB + d0 + 8) : 0u;
         }
     }
+    // One product: the full m16n8k16, or with RM == 8 the rows 0..7 only (rows 8..15 of
+    // A are zero and their accumulators are not kept).
+    auto mma = [&](float* acc, const uint32_t* a, uint32_t b0, uint32_t b1) {
+        if (kFull) Mma<T>::run(acc, a, b0, b1);
+        else Mma<T>::run_top(acc, a[0], a[2], b0, b1);
+    };
     auto limit_of = [&](int r, bool live) -> int {
         if (!live) return 0;
         const int lim = p.causal ? c.len - p.qlen + 1 + (c.m0 + r) % p.qlen : c.len;
@@ -840,11 +893,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
     };
     const int limA = limit_of(qr, rowA), limB = limit_of(qr + 8, rowB);
 
-    float oacc[8][4];
+    constexpr int kAcc = kFull ? 4 : 2;  // accumulator elements kept per n8 block
+    float oacc[8][kAcc];
 #pragma unroll
     for (int n = 0; n < 8; ++n)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) oacc[n][e] = 0.f;
+        for (int e = 0; e < kAcc; ++e) oacc[n][e] = 0.f;
     float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
 
     auto slab = [&](uint8_t* sK, uint8_t* sV, int tile0, int slab0) {
@@ -861,70 +915,93 @@ __global__ void __launch_bounds__(kThreads, MINB)
             __syncwarp();
         }
         const uint32_t kb = smem_u32(sK), vb = smem_u32(sV);
-        float sacc[2][4];
+        float sacc[2][kAcc];
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[n][e] = 0.f;
+            for (int e = 0; e < kAcc; ++e) sacc[n][e] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
             const int krow = slab0 + (jm >> 1) * 8 + rr;
             uint32_t b0, b1, b2, b3;
             ldsm_x4(kb + swz(krow, kk * 2 + (jm & 1)), b0, b1, b2, b3);
-            Mma<T>::run(sacc[0], qa[kk], b0, b1);
-            Mma<T>::run(sacc[1], qa[kk], b2, b3);
+            mma(sacc[0], qa[kk], b0, b1);
+            mma(sacc[1], qa[kk], b2, b3);
         }
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < kAcc; ++e) {
                 const int key = tile0 + slab0 + n * 8 + qc + (e & 1);
                 const int lim = e < 2 ? limA : limB;
                 sacc[n][e] = key < lim ? sacc[n][e] * p.scale_log2 : -INFINITY;
             }
-        float tA = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
-        float tB = fmaxf(fmaxf(sacc[0][2], sacc[0][3]), fmaxf(sacc[1][2], sacc[1][3]));
-        tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 1));
-        tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 2));
-        tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 1));
-        tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 2));
-        const float nA = fmaxf(mA, tA), nB = fmaxf(mB, tB);
-        const float refA = nA == -INFINITY ? 0.f : nA, refB = nB == -INFINITY ? 0.f : nB;
-        const float aA = exp2f(mA - refA), aB = exp2f(mB - refB);
-        mA = nA;
-        mB = nB;
         uint32_t pa[4];
-        pa[0] = Half16<T>::from_f2(exp2f(sacc[0][0] - refA), exp2f(sacc[0][1] - refA));
-        pa[1] = Half16<T>::from_f2(exp2f(sacc[0][2] - refB), exp2f(sacc[0][3] - refB));
-        pa[2] = Half16<T>::from_f2(exp2f(sacc[1][0] - refA), exp2f(sacc[1][1] - refA));
-        pa[3] = Half16<T>::from_f2(exp2f(sacc[1][2] - refB), exp2f(sacc[1][3] - refB));
-        // The normaliser sums the rounded weights that actually multiply V.
-        const float2 r0 = Half16<T>::to_f2(pa[0]), r1 = Half16<T>::to_f2(pa[1]);
-        const float2 r2 = Half16<T>::to_f2(pa[2]), r3 = Half16<T>::to_f2(pa[3]);
-        lA = fmaf(lA, aA, (r0.x + r0.y) + (r2.x + r2.y));
-        lB = fmaf(lB, aB, (r1.x + r1.y) + (r3.x + r3.y));
+        if constexpr (kFull) {
+            // rows 0..7 (A) and 8..15 (B): two independent chains, interleaved
+            float tA = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
+            float tB = fmaxf(fmaxf(sacc[0][2], sacc[0][3]), fmaxf(sacc[1][2], sacc[1][3]));
+            tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 1));
+            tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 2));
+            tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 1));
+            tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 2));
+            const float nA = fmaxf(mA, tA), nB = fmaxf(mB, tB);
+            const float refA = nA == -INFINITY ? 0.f : nA, refB = nB == -INFINITY ? 0.f : nB;
+            const float aA = exp2f(mA - refA), aB = exp2f(mB - refB);
+            mA = nA;
+            mB = nB;
+            pa[0] = Half16<T>::from_f2(exp2f(sacc[0][0] - refA), exp2f(sacc[0][1] - refA));
+            pa[1] = Half16<T>::from_f2(exp2f(sacc[0][2] - refB), exp2f(sacc[0][3] - refB));
+            pa[2] = Half16<T>::from_f2(exp2f(sacc[1][0] - refA), exp2f(sacc[1][1] - refA));
+            pa[3] = Half16<T>::from_f2(exp2f(sacc[1][2] - refB), exp2f(sacc[1][3] - refB));
+            // The normaliser sums the rounded weights that actually multiply V.
+            const float2 r0 = Half16<T>::to_f2(pa[0]), r1 = Half16<T>::to_f2(pa[1]);
+            const float2 r2 = Half16<T>::to_f2(pa[2]), r3 = Half16<T>::to_f2(pa[3]);
+            lA = fmaf(lA, aA, (r0.x + r0.y) + (r2.x + r2.y));
+            lB = fmaf(lB, aB, (r1.x + r1.y) + (r3.x + r3.y));
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            oacc[n][0] *= aA;
-            oacc[n][1] *= aA;
-            oacc[n][2] *= aB;
-            oacc[n][3] *= aB;
+            for (int n = 0; n < 8; ++n) {
+                oacc[n][0] *= aA;
+                oacc[n][1] *= aA;
+                oacc[n][kAcc - 2] *= aB;
+                oacc[n][kAcc - 1] *= aB;
+            }
+        } else {
+            float tA = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
+            tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 1));
+            tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 2));
+            const float nA = fmaxf(mA, tA);
+            const float refA = nA == -INFINITY ? 0.f : nA;
+            const float aA = exp2f(mA - refA);
+            mA = nA;
+            pa[0] = Half16<T>::from_f2(exp2f(sacc[0][0] - refA), exp2f(sacc[0][1] - refA));
+            pa[2] = Half16<T>::from_f2(exp2f(sacc[1][0] - refA), exp2f(sacc[1][1] - refA));
+            pa[1] = pa[3] = 0u;
+            const float2 r0 = Half16<T>::to_f2(pa[0]), r2 = Half16<T>::to_f2(pa[2]);
+            lA = fmaf(lA, aA, (r0.x + r0.y) + (r2.x + r2.y));
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+                oacc[n][0] *= aA;
+                oacc[n][1] *= aA;
+            }
         }
 #pragma unroll
         for (int np = 0; np < 4; ++np) {
             const int vrow = slab0 + (jm & 1) * 8 + rr;
             uint32_t v0, v1, v2, v3;
             ldsm_x4_t(vb + swz(vrow, 2 * np + (jm >> 1)), v0, v1, v2, v3);
-            Mma<T>::run(oacc[2 * np], pa, v0, v1);
-            Mma<T>::run(oacc[2 * np + 1], pa, v2, v3);
+            mma(oacc[2 * np], pa, v0, v1);
+            mma(oacc[2 * np + 1], pa, v2, v3);
         }
     };
     if (!run_tiles<T, ROPE>(p, c, smem, bars, mrg, smem + L.app_off, &tmk, &tmv, slab)) return;
 
     lA += __shfl_xor_sync(0xffffffffu, lA, 1);
     lA += __shfl_xor_sync(0xffffffffu, lA, 2);
-    lB += __shfl_xor_sync(0xffffffffu, lB, 1);
-    lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+    if (kFull) {
+        lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+        lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+    }
     {
         constexpr int RS = red_stride(RM);
         float* red_o = red;
@@ -938,18 +1015,46 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     make_float2(oacc[n][0], oacc[n][1]);
             if (rowB)
                 *reinterpret_cast<float2*>(red_o + (warp * RM + qr + 8) * RS + n * 8 + qc) =
-                    make_float2(oacc[n][2], oacc[n][3]);
+                    make_float2(oacc[n][kAcc - 2], oacc[n][kAcc - 1]);
         }
         if ((lane & 3) == 0) {
             red_m[warp * RM + qr] = mA;
-            red_m[warp * RM + qr + 8] = mB;
             red_l[warp * RM + qr] = lA;
-            red_l[warp * RM + qr + 8] = lB;
+            if (kFull) {
+                red_m[warp * RM + qr + 8] = mB;
+                red_l[warp * RM + qr + 8] = lB;
+            }
         }
     }
     __syncthreads();
     finish_cta<T, RM>(p, c, red, mrg, &bars[p.stages], misc, qoff, smem + L.bar_off - 4096);
 }
+
+// ---------------------------------------------------------------- no-allocation scratch
+// kvd_decode_attn_noalloc merges split results in this buffer compiled into the library
+// instead of a caller's workspace (see kvdecode.h). Host code must never pass
+// `g_noalloc_scratch` itself to a kernel: on the host that name is only a stand-in for
+// the device symbol. The device address is looked up once per device with
+// cudaGetSymbolAddress while that device is current.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[KVD_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::once_flag g_noalloc_once[64];
+void* g_noalloc_ptr[64];
+cudaError_t g_noalloc_err[64];
+
+kvd_status noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return KVD_ERR_CUDA;
+    std::call_once(g_noalloc_once[dev], [dev] {
+        g_noalloc_err[dev] = cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_noalloc_scratch);
+    });
+    if (g_noalloc_err[dev] != cudaSuccess || !g_noalloc_ptr[dev]) return KVD_ERR_CUDA;
+    *out = g_noalloc_ptr[dev];
+    return KVD_OK;
+}
+}  // namespace
 
 // ---------------------------------------------------------------- host side --------
 namespace {
@@ -978,24 +1083,30 @@ int prepare_kernel(size_t smem_bytes) {
     return result[dev];
 }
 
-// Kernel variants: the CUDA-core kernel, and the tensor-core kernel built for 2 or 3
-// resident blocks per SM; the first two also with the rotary encoding compiled in (the
-// rotation code is kept out of the other builds, whose register budgets it would raise).
-enum Variant { kSimt = 1, kMma = 2, kMma3 = 3, kSimtRope = 4, kMmaRope = 5 };
+// Kernel variants: the CUDA-core kernel; the tensor-core kernel built for 2 or 3
+// resident blocks per SM; its build for blocks of at most 8 query vectors (3 per SM);
+// the first two also with the rotary encoding compiled in (the rotation code is kept out
+// of the other builds, whose register budgets it would raise).
+enum Variant { kSimt = 1, kMma = 2, kMma3 = 3, kSimtRope = 4, kMmaRope = 5, kMma8 = 6 };
+
+// Rows of the warp partials (the red area) of a variant: 16 for the tensor-core builds,
+// 8 for the 8-vector build, 1 for the CUDA-core kernel.
+constexpr int variant_rmax(int var) {
+    return (var == kSimt || var == kSimtRope) ? 1 : var == kMma8 ? 8 : 16;
+}
 
 template <typename T>
 int prepare(int var) {
-    const uint32_t mma_smem =
-        smem_layout(kMaxStages, 16, kMaxClusterSplits * kMmaQueryBlock,
-                    2 * KVD_MAX_QLEN + kQsUnits).total;
-    const uint32_t simt_smem =
-        smem_layout(kMaxStages, 1, kMaxClusterSplits, 2 * KVD_MAX_QLEN + kQsUnits).total;
+    const int rmax = variant_rmax(var);
+    const uint32_t smem = smem_layout(kMaxStages, rmax, kMaxClusterSplits * std::min(rmax, 16),
+                                      2 * KVD_MAX_QLEN + kQsUnits).total;
     switch (var) {
-    case kMma: return prepare_kernel<block_attn_kernel<T, 2, false>>(mma_smem);
-    case kMma3: return prepare_kernel<block_attn_kernel<T, 3, false>>(mma_smem);
-    case kMmaRope: return prepare_kernel<block_attn_kernel<T, 2, true>>(mma_smem);
-    case kSimtRope: return prepare_kernel<decode_attn_kernel<T, true>>(simt_smem);
-    default: return prepare_kernel<decode_attn_kernel<T, false>>(simt_smem);
+    case kMma: return prepare_kernel<block_attn_kernel<T, 2, false>>(smem);
+    case kMma3: return prepare_kernel<block_attn_kernel<T, 3, false>>(smem);
+    case kMmaRope: return prepare_kernel<block_attn_kernel<T, 2, true>>(smem);
+    case kMma8: return prepare_kernel<block_attn_kernel<T, 3, false, 8>>(smem);
+    case kSimtRope: return prepare_kernel<decode_attn_kernel<T, true>>(smem);
+    default: return prepare_kernel<decode_attn_kernel<T, false>>(smem);
     }
 }
 
@@ -1005,6 +1116,7 @@ const void* kernel_of(int var) {
     case kMma: return reinterpret_cast<const void*>(block_attn_kernel<T, 2, false>);
     case kMma3: return reinterpret_cast<const void*>(block_attn_kernel<T, 3, false>);
     case kMmaRope: return reinterpret_cast<const void*>(block_attn_kernel<T, 2, true>);
+    case kMma8: return reinterpret_cast<const void*>(block_attn_kernel<T, 3, false, 8>);
     case kSimtRope: return reinterpret_cast<const void*>(decode_attn_kernel<T, true>);
     default: return reinterpret_cast<const void*>(decode_attn_kernel<T, false>);
     }
@@ -1018,6 +1130,9 @@ kvd_status launch_attn(int var, dim3 grid, cudaStream_t st, bool pdl, unsigned c
     const uint32_t mma_smem = smem_layout(p.stages, 16, slots, app_rows).total;
     const uint32_t simt_smem = smem_layout(p.stages, 1, slots, app_rows).total;
     switch (var) {
+    case kMma8:
+        return launch_ex(block_attn_kernel<T, 3, false, 8>, grid, dim3(kThreads),
+                         smem_layout(p.stages, 8, slots, app_rows).total, st, pdl, cl, mk, mv, p);
     case kMma:
         return launch_ex(block_attn_kernel<T, 2, false>, grid, dim3(kThreads), mma_smem, st, pdl,
                          cl, mk, mv, p);
@@ -1036,8 +1151,8 @@ kvd_status launch_attn(int var, dim3 grid, cudaStream_t st, bool pdl, unsigned c
     }
 }
 
-size_t plan_smem(const AttnPlan& P, bool mma, int app_rows) {
-    return smem_layout(P.stages, mma ? 16 : 1, merge_slots(P.cluster, P.splits, P.msub),
+size_t plan_smem(const AttnPlan& P, int var, int app_rows) {
+    return smem_layout(P.stages, variant_rmax(var), merge_slots(P.cluster, P.splits, P.msub),
                        app_rows)
         .total;
 }
@@ -1088,17 +1203,17 @@ int resident(const void* kern, int kid, size_t smem, int cluster, int nsm) {
 // when none fits (many units fill the GPU by themselves). Only for a handful of units
 // over a long range, where even 16-block clusters leave each block streaming many
 // tiles, split further and merge through the workspace.
-AttnPlan choose_plan(const void* kern, int kid, bool mma, int nsm, int batch, int n_q_heads,
+AttnPlan choose_plan(const void* kern, int kid, int var, int nsm, int batch, int n_q_heads,
                      int n_kv_heads, int rows_per_kv, int qlen, int len_bound, int max_cluster,
                      int app_rows) {
-    const int mmax = mma ? kMmaQueryBlock : 1;
+    const int mmax = variant_rmax(var) > 1 ? kMmaQueryBlock : 1;
     const AttnPlan P1 = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, qlen, len_bound,
                                        mmax, 1, max_cluster);
     if (P1.rounds <= 1) return P1;
     if (workspace_merge_pays(P1.units, P1.rounds)) {
         AttnPlan W = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, qlen, len_bound,
                                     mmax, kMaxSplits, 1);
-        const int blocks = resident(kern, kid, plan_smem(W, mma, app_rows), 1, nsm);
+        const int blocks = resident(kern, kid, plan_smem(W, var, app_rows), 1, nsm);
         return plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, qlen, len_bound, mmax,
                               std::max(1, blocks / P1.units), max_cluster);
     }
@@ -1109,7 +1224,7 @@ AttnPlan choose_plan(const void* kern, int kid, bool mma, int nsm, int batch, in
         if (P.splits == last) continue;
         last = P.splits;
         if (P.splits < 2) break;
-        if (P.cluster && resident(kern, kid, plan_smem(P, mma, app_rows), P.splits, nsm) >= P.units)
+        if (P.cluster && resident(kern, kid, plan_smem(P, var, app_rows), P.splits, nsm) >= P.units)
             return P;
     }
     return P1;
@@ -1119,7 +1234,8 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
                      int32_t qlen, const void* q, const kvd_cache* kv, const int32_t* lens,
                      int32_t fixed_len, const kvd_new_tokens* app, int32_t rows_per_kv,
                      int32_t causal, float scale, void* out, void* ws, size_t ws_bytes,
-                     uint32_t flags, int32_t* dev_err, cudaStream_t stream) {
+                     uint32_t flags, int32_t* dev_err, cudaStream_t stream,
+                     bool noalloc = false) {
     if (dtype != KVD_F16 && dtype != KVD_BF16) return KVD_ERR_INVALID_ARG;
     if (kvd_status s = validate_cache(kv)) return s;
     if (batch < 0 || n_q_heads <= 0 || rows_per_kv <= 0) return KVD_ERR_INVALID_ARG;
@@ -1139,6 +1255,10 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
     if (!(scale == scale)) return KVD_ERR_INVALID_ARG;
     const int nsm = sm_count();
     if (nsm <= 0) return KVD_ERR_CUDA;
+    if (noalloc) {  // the built-in scratch stands in for the workspace
+        if (kvd_status s = noalloc_scratch(&ws)) return s;
+        ws_bytes = KVD_NOALLOC_SCRATCH_BYTES;
+    }
     const int len_bound = lens ? kv->capacity : fixed_len;
     const bool bf = dtype == KVD_BF16;
     const int group = n_q_heads / kv->n_kv_heads;
@@ -1148,7 +1268,7 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
         const int mc = bf ? prepare<__nv_bfloat16>(var) : prepare<__half>(var);
         if (mc <= 0) return false;
         const void* kern = bf ? kernel_of<__nv_bfloat16>(var) : kernel_of<__half>(var);
-        out = choose_plan(kern, var * 2 + (bf ? 1 : 0), var != kSimt && var != kSimtRope, nsm,
+        out = choose_plan(kern, var * 2 + (bf ? 1 : 0), var, nsm,
                           batch, n_q_heads,
                           kv->n_kv_heads, rows_per_kv, qlen, len_bound, mc, app_rows);
         return true;
@@ -1159,7 +1279,7 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
         if (Q.splits != 1) return false;
         const void* kern = bf ? kernel_of<__nv_bfloat16>(var) : kernel_of<__half>(var);
         return (int64_t)Q.units <=
-               resident(kern, var * 2 + (bf ? 1 : 0), plan_smem(Q, true, app_rows), 1, nsm);
+               resident(kern, var * 2 + (bf ? 1 : 0), plan_smem(Q, var, app_rows), 1, nsm);
     };
     // the builds with the rotation compiled in stand for kSimt and kMma when it is on
     const int simt = rope ? kSimtRope : kSimt, mma = rope ? kMmaRope : kMma;
@@ -1180,15 +1300,21 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
         }
     }
     if (var == kMma && P.tiles_per_split >= 8) {
-        // Residency limits the split count and blocks stream 4 or more rounds: the variant
-        // with 3 blocks per SM allows more splits, but each round is slower (spills), so it
-        // is taken only when it at least halves every block's tiles. Measured: beam cross
-        // attention (160 units over 1500 frames) 16.0 -> 13.2 us; with a smaller cut
-        // (GQA-LM: 8 -> 6 tiles per block) it lost, 6.9 -> 8.1 us per layer.
+        // Residency limits the split count and blocks stream 4 or more rounds: a build
+        // with 3 blocks per SM allows more splits. For blocks of at most 8 query vectors
+        // that is the 8-vector build (no spill); otherwise the full build cut to 80
+        // registers, whose rounds are slower (spills). Either is taken only when it at
+        // least halves every block's tiles. Measured: beam cross attention (160 units over
+        // 1500 frames) 16.0 -> 13.2 us with the cut full build, and the beam step 1211 ->
+        // 1159 us with the 8-vector build instead; with a smaller cut (GQA-LM: 8 -> 6
+        // tiles per block) it lost, 6.9 -> 8.1 us per layer. Three blocks per SM do not
+        // pay for launches that are latency chains: packed more densely, the blocks of
+        // one launch slow one another (Whisper step 0.441 -> 0.492 ms with the 8-vector
+        // build used for every launch of at most 8 vectors).
+        const int v3 = (int64_t)P.msub <= 8 ? kMma8 : kMma3;
         AttnPlan P3;
-        if (plan_for(kMma3, P3) && one_wave(kMma3, P3) &&
-            2 * P3.tiles_per_split <= P.tiles_per_split) {
-            var = kMma3;
+        if (plan_for(v3, P3) && one_wave(v3, P3) && 2 * P3.tiles_per_split <= P.tiles_per_split) {
+            var = v3;
             P = P3;
         }
     }
@@ -1222,6 +1348,7 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
     p.box_rows = std::min(64, kv->capacity);
     p.early = (flags & KVD_FLAG_EARLY_KV) ? 1 : 0;
     p.cluster = P.cluster ? 1 : 0;
+    p.test_stall = (flags & KVD_FLAG_TEST_STALL) ? 1 : 0;
     p.append = app ? 1 : 0;
     p.rope = rope ? 1 : 0;
     p.rope_log2_base = rope ? log2f(app->rope_base) : 0.f;
@@ -1241,6 +1368,12 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
     p.ws_ml = wsb ? reinterpret_cast<float2*>(wsb + P.ml_offset) : nullptr;
     p.dev_err = dev_err;
 
+    // The built-in scratch keeps whatever the previous call left; a plan that merges
+    // through it needs its units' arrival counters at zero (a call that stopped early
+    // could have left them non-zero). Cleared here, after every check has passed.
+    if (noalloc && P.splits > 1 && !P.cluster &&
+        cudaMemsetAsync(ws, 0, (size_t)P.units * sizeof(int32_t), stream) != cudaSuccess)
+        return KVD_ERR_CUDA;
     const bool pdl = (flags & (KVD_FLAG_PDL | KVD_FLAG_EARLY_KV)) != 0;
     const dim3 grid(P.splits, kv->n_kv_heads * P.nsub, P.bkv);
     const unsigned cl = P.cluster ? (unsigned)P.splits : 1u;
@@ -1275,45 +1408,28 @@ extern "C" kvd_status kvd_verify_attn(kvd_dtype dtype, int32_t batch, int32_t n_
 }
 
 // ---------------------------------------------------------------- no-allocation entry
-// kvd_decode_attn_noalloc: the decode kernels with their split-merge scratch in a buffer
-// compiled into the library, for callers that cannot allocate a workspace (see
-// kvdecode.h). Host code must never pass `g_noalloc_scratch` itself to a kernel: on the
-// host that name is only a stand-in for the device symbol. The device address is looked
-// up once per device with cudaGetSymbolAddress while that device is current.
-static __device__ __align__(256) uint8_t g_noalloc_scratch[KVD_NOALLOC_SCRATCH_BYTES];
-
-namespace kvd {
-namespace {
-std::once_flag g_noalloc_once[kMaxDev];
-void* g_noalloc_ptr[kMaxDev];
-cudaError_t g_noalloc_err[kMaxDev];
-
-kvd_status noalloc_scratch(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return KVD_ERR_CUDA;
-    std::call_once(g_noalloc_once[dev], [dev] {
-        g_noalloc_err[dev] = cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_noalloc_scratch);
-    });
-    if (g_noalloc_err[dev] != cudaSuccess || !g_noalloc_ptr[dev]) return KVD_ERR_CUDA;
-    *out = g_noalloc_ptr[dev];
-    return KVD_OK;
-}
-}  // namespace
-}  // namespace kvd
-
+// kvd_decode_attn_noalloc: the decode kernels with their split-merge scratch in the
+// buffer compiled into the library, for callers that cannot allocate a workspace (see
+// kvdecode.h). Every host check and the plan come first; the scratch's arrival counters
+// are cleared only for a plan that merges through them, right before the launch.
 extern "C" kvd_status kvd_decode_attn_noalloc(kvd_dtype dtype, int32_t batch, int32_t n_q_heads,
                                               const void* q, const kvd_cache* kv,
                                               const int32_t* lens, int32_t fixed_len,
                                               const kvd_new_tokens* append, int32_t rows_per_kv,
                                               float scale, void* out, uint32_t flags,
                                               int32_t* dev_err, kvd_stream_t stream) {
+    return kvd::attention(false, dtype, batch, n_q_heads, 1, q, kv, lens, fixed_len, append,
+                          rows_per_kv, 0, scale, out, nullptr, 0, flags, dev_err,
+                          reinterpret_cast<cudaStream_t>(stream), /*noalloc=*/true);
+}
+
+// Test support: overwrite the built-in scratch's arrival counters on `stream`, as a call
+// that stopped early (a timed-out wait) could leave them.
+extern "C" kvd_status kvd_noalloc_test_fill_counters(uint8_t byte_value, kvd_stream_t stream) {
     void* scratch = nullptr;
     if (kvd_status s = kvd::noalloc_scratch(&scratch)) return s;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // The buffer keeps whatever the previous call left; its arrival counters must start
-    // at zero, so clear them (a call that stopped early could have left them non-zero).
-    if (cudaMemsetAsync(scratch, 0, KVD_WS_COUNTER_BYTES, st) != cudaSuccess) return KVD_ERR_CUDA;
-    return kvd::attention(false, dtype, batch, n_q_heads, 1, q, kv, lens, fixed_len, append,
-                          rows_per_kv, 0, scale, out, scratch, KVD_NOALLOC_SCRATCH_BYTES, flags,
-                          dev_err, st);
+    return cudaMemsetAsync(scratch, byte_value, KVD_WS_COUNTER_BYTES,
+                           reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KVD_OK
+               : KVD_ERR_CUDA;
 }

@@ -147,6 +147,11 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                  "r"(bytes)
                  : "memory");
 }
+// Raise the transaction count of the current phase by `bytes`, without an arrival.
+__device__ __forceinline__ void mbar_expect_tx_only(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
 // One arrival (release) on the barrier.
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -178,15 +183,16 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
         : "memory");
     return ok != 0;
 }
-// As mbar_wait_bounded, for a barrier that other CTAs of the cluster arrive on: the
-// acquire covers their writes to this CTA's shared memory.
-__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity) {
+// As mbar_wait_bounded, for a barrier that other CTAs of the cluster arrive on (the
+// acquire covers their writes to this CTA's shared memory), with a bound of `budget_ns`.
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                          unsigned long long budget_ns = kWaitNs) {
     // the clock is read every 64 polls only: polling threads then stay cheap
     unsigned long long t0 = 0;
     for (unsigned n = 1; !mbar_try_wait_cluster(bar, parity); ++n) {
         if (n % 64 == 0) {
             if (t0 == 0) t0 = global_ns();
-            else if (global_ns() - t0 > kWaitNs) return false;
+            else if (global_ns() - t0 > budget_ns) return false;
         }
     }
     return true;
@@ -300,6 +306,17 @@ template <> struct Mma<__half> {
             : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
             : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
     }
+    // Rows 0..7 only: A rows 8..15 are zero (a1 = a3 = 0), the accumulator of rows
+    // 0..7 is c[0..1]; rows 8..15 start from 0 and their results are discarded.
+    static __device__ __forceinline__ void run_top(float* c, uint32_t a0, uint32_t a2,
+                                                   uint32_t b0, uint32_t b1) {
+        float d2, d3;
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %10, %10};"
+            : "+f"(c[0]), "+f"(c[1]), "=f"(d2), "=f"(d3)
+            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+    }
 };
 template <> struct Mma<__nv_bfloat16> {
     static __device__ __forceinline__ void run(float* c, const uint32_t* a, uint32_t b0,
@@ -309,6 +326,17 @@ template <> struct Mma<__nv_bfloat16> {
             "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
             : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
             : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    // Rows 0..7 only: A rows 8..15 are zero (a1 = a3 = 0), the accumulator of rows
+    // 0..7 is c[0..1]; rows 8..15 start from 0 and their results are discarded.
+    static __device__ __forceinline__ void run_top(float* c, uint32_t a0, uint32_t a2,
+                                                   uint32_t b0, uint32_t b1) {
+        float d2, d3;
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %10, %10};"
+            : "+f"(c[0]), "+f"(c[1]), "=f"(d2), "=f"(d3)
+            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
     }
 };
 

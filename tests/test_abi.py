@@ -146,6 +146,26 @@ def test_host_rejects_bad_shapes(lib):
                                None, 0, 0, None, None) == 0
 
 
+def test_noalloc_rejects_bad_arguments_before_any_cuda_call(lib):
+    # The no-workspace entry point runs every host check before it looks up its built-in
+    # scratch or enqueues anything: on this GPU-less host, fake pointers with a bad
+    # argument must come back as KVD_ERR_INVALID_ARG (a CUDA call would give
+    # KVD_ERR_CUDA instead).
+    c = _fake_cache()
+    q = ctypes.c_void_p(0x30000)
+    call = lib.kvd_decode_attn_noalloc
+    assert call(0, 1, 30, q, ctypes.byref(c), None, 10, None, 1, 0.125, q, 0, None, None) == 1
+    assert call(0, 1, 20, ctypes.c_void_p(0x30008), ctypes.byref(c), None, 10, None, 1, 0.125,
+                q, 0, None, None) == 1                       # misaligned query
+    assert call(0, 1, 20, q, ctypes.byref(c), None, 449, None, 1, 0.125, q, 0, None,
+                None) == 1                                   # fixed length past capacity
+    bad = _fake_cache(k=0)
+    assert call(0, 1, 20, q, ctypes.byref(bad), None, 10, None, 1, 0.125, q, 0, None,
+                None) == 1                                   # no K buffer
+    assert call(0, 0, 20, None, ctypes.byref(c), None, 0, None, 1, 0.125, None, 0, None,
+                None) == 0                                   # nothing to do
+
+
 def test_prefill_host_rejects_bad_arguments(lib):
     c = _fake_cache()
     p = ctypes.c_void_p(0x30000)

@@ -92,3 +92,63 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     assert ei.value.status == 3  # KVD_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.all(out == 5.0)
+
+
+def test_noalloc_recovers_from_counters_left_non_zero():
+    """A call that stopped early (a timed-out wait) can leave the built-in scratch's
+    arrival counters non-zero. The counters are overwritten here from the host (no fault,
+    no stalled kernel), then the next call must still merge from zero: its output equals
+    the workspace entry point's bit for bit (same plan, same merge order)."""
+    import kv_cached_decode_gb300 as kvd
+
+    dtype, B, Hq, Hkv, cap, lens, fixed = CASES[0]  # merges through the scratch
+    rng = make_rng(9100)
+    K, V = gen_cache(rng, B, Hkv, cap, D, dtype, 0.125, lens=lens)
+    q = gen_queries(rng, B, Hq, 1, D, dtype, 0.125)
+    Kd, Vd, qd = dev16(K, dtype), dev16(V, dtype), dev16(q, dtype)
+    cache = kvd.make_cache(Kd, Vd)
+    lens_d = dev_i32(lens)
+    ref = torch.empty_like(qd)
+    ws = kvd.new_workspace(kvd.kvd_workspace_size(kvd.KVD_OP_DECODE_ATTN, B, Hq, Hkv, 1, 1, cap))
+    kvd.kvd_decode_attn(qd, cache, ref, ws, lens=lens_d)
+    err = new_err()
+    for fill in (0x01, 0x7F):
+        kvd.kvd_noalloc_test_fill_counters(fill)
+        o = torch.full_like(qd, 3.0)
+        kvd.kvd_decode_attn_noalloc(qd, cache, o, lens=lens_d, dev_err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        assert np.array_equal(host16(o), host16(ref)), f"fill {fill:#x}"
+
+
+def test_noalloc_after_a_call_that_gave_up():
+    """A call that really stopped early: with KVD_FLAG_TEST_STALL the last split of the
+    unit gives up after a bounded wait (KVD_ERR_TIMEOUT, output unwritten), leaving the
+    built-in scratch's arrival counter part-way. The next call, with nothing re-zeroed by
+    the caller, must still equal the workspace entry point bit for bit."""
+    import kv_cached_decode_gb300 as kvd
+
+    dtype, B, Hq, Hkv, cap, _, fixed = CASES[0]  # merges through the scratch
+    lens = [cap]  # a full row: the last split has tiles, so its first stage is the one stalled
+    rng = make_rng(9200)
+    K, V = gen_cache(rng, B, Hkv, cap, D, dtype, 0.125, lens=lens)
+    q = gen_queries(rng, B, Hq, 1, D, dtype, 0.125)
+    Kd, Vd, qd = dev16(K, dtype), dev16(V, dtype), dev16(q, dtype)
+    cache = kvd.make_cache(Kd, Vd)
+    lens_d = dev_i32(lens)
+    ref = torch.empty_like(qd)
+    ws = kvd.new_workspace(kvd.kvd_workspace_size(kvd.KVD_OP_DECODE_ATTN, B, Hq, Hkv, 1, 1, cap))
+    kvd.kvd_decode_attn(qd, cache, ref, ws, lens=lens_d)
+    stalled = torch.full_like(qd, 3.0)
+    err = new_err()
+    kvd.kvd_decode_attn_noalloc(qd, cache, stalled, lens=lens_d, dev_err=err,
+                                flags=kvd.KVD_FLAG_TEST_STALL)
+    torch.cuda.synchronize()
+    assert err.item() == 20  # KVD_ERR_TIMEOUT
+    assert torch.all(stalled == 3.0)
+    o = torch.full_like(qd, 3.0)
+    err2 = new_err()
+    kvd.kvd_decode_attn_noalloc(qd, cache, o, lens=lens_d, dev_err=err2)
+    torch.cuda.synchronize()
+    assert err2.item() == 0
+    assert np.array_equal(host16(o), host16(ref))
