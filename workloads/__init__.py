@@ -14,6 +14,7 @@ from .synth import (  # noqa: F401
     normal_half,
     round_half_bits,
     gen_cache,
+    gen_cache_device,
     gen_queries,
     gen_new_kv,
     gen_lens_uniform,

@@ -218,3 +218,21 @@ def gen_sample_inputs(rng, batch: int, k: int, vocab: int, *, logit_std: float =
     r = rng.random(size=(batch, k)).astype(np.float32)
     u = rng.random(size=batch).astype(np.float32)
     return target, draft, drafts, r, u
+
+
+def gen_cache_device(seed: int, batch: int, n_kv_heads: int, capacity: int, head_dim: int,
+                     dtype: str, std: float, device="cuda"):
+    """Full-size K and V caches ``[batch, n_kv_heads, capacity, head_dim]`` drawn on the
+    device: torch's seeded Philox generator on ``device``, N(0, std^2) rounded by torch to
+    fp16/bf16. For caches too large to draw on the host in reasonable time (gigabytes);
+    a test copies the rows it checks back to the host, so both sides see the same bits.
+    Returns two torch tensors (the caller keeps them alive)."""
+    import torch
+
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    shape = (batch, n_kv_heads, capacity, head_dim)
+    k = torch.empty(shape, dtype=tdt, device=device).normal_(0.0, std, generator=gen)
+    v = torch.empty(shape, dtype=tdt, device=device).normal_(0.0, std, generator=gen)
+    return k, v
