@@ -176,7 +176,13 @@ __global__ void __launch_bounds__(kBulkThreads)
                               bytes, bar);
             if (!mbar_wait_bounded(bar, phase)) {
                 flag_error(p.dev_err, KVD_ERR_TIMEOUT);
-                mbar_wait_bounded(bar, phase);  // let copies in flight land before exit
+                // Let copies in flight land before the block exits, for at most another
+                // second. If that wait runs out too, the block still exits (the error is
+                // already flagged): a copy that has not landed in two seconds is not
+                // waited for without bound, and could then write into shared memory the
+                // next block on this SM receives.
+                const bool drained = mbar_wait_bounded(bar, phase);
+                (void)drained;
                 break;
             }
             fence_proxy_async();
