@@ -103,9 +103,9 @@ enum {
      * split of every (row, KV head) unit the first stage of K/V tiles expects more
      * bytes than its copies bring (a split whose range starts past the row's length
      * has no stage), so that stage never completes and the split's tile waits run out
-     * after about one second; it drains, gives up,
-     * and (in a cluster merge) sends its partial marked as given up; the call must
-     * report KVD_ERR_TIMEOUT, leave those units' outputs unwritten, and leave the
+     * after about one second; it drains and gives up without sending its partial
+     * (in a cluster merge the first CTA's bounded wait for it then runs out); the call
+     * must report KVD_ERR_TIMEOUT, leave those units' outputs unwritten, and leave the
      * stream usable (a workspace merge also leaves that unit's arrival counter
      * non-zero: re-zero the workspace). The timeout paths are exercised without any
      * fault. */

@@ -81,6 +81,7 @@ struct AttnParams {
     int32_t early;
     int32_t cluster;   // 1: the splits of a unit form one thread-block cluster
     int32_t test_stall;  // test only: the last split of every unit never sees its first stage
+    unsigned long long merge_wait_ns;  // the first CTA's bound on its wait for the partials
     int32_t append;    // 1: k_new/v_new are written at positions lens[b] .. lens[b]+qlen-1
     int32_t rope;      // 1: rotary encoding of the queries and the appended keys
     float rope_log2_base;
@@ -152,20 +153,19 @@ struct CtaCtx {
 // partials never exits while a peer can still send:
 //  * a thread's tile waits: at most one per round, each within 1 s, and none after the
 //    first that runs out -- at most `rounds` seconds in all;
-//  * a block that gave up drains its copies in flight: at most one wait per stage, each
-//    within 1 s -- `stages` seconds; only then does it send its partial (zeros, marked
-//    as given up);
-//  * so every peer has sent within (rounds + stages) seconds of passing the dependency
-//    wait, and the first CTA waits for the partials (rounds + stages + 1) seconds after
-//    it starts waiting, which is after it passed that wait too. All CTAs of a cluster
-//    are resident together and pass the dependency wait within microseconds of one
-//    another, far inside the 1 s margin.
-__device__ __forceinline__ unsigned long long merge_wait_ns(const AttnParams& p) {
-    return (unsigned long long)((p.tiles_per_split + 1) / 2 + p.stages + 1) * kWaitNs;
+//  * a block that gave up drains its copies in flight (at most one wait per stage, each
+//    within 1 s) and sends nothing;
+//  * so every peer that sends has sent within `rounds` seconds of passing the
+//    dependency wait, and the first CTA waits for the partials (rounds + stages + 1)
+//    seconds after it starts waiting, which is after it passed that wait too: it is
+//    still waiting when the last partial lands, and a unit with a peer that gave up
+//    ends in the first CTA's timeout (no output). All CTAs of a cluster are resident
+//    together and pass the dependency wait within microseconds of one another, far
+//    inside the 1 s margin.
+// (rounds + stages + 1) seconds, computed on the host into AttnParams::merge_wait_ns.
+inline unsigned long long merge_wait_budget(int tiles_per_split, int stages) {
+    return (unsigned long long)((tiles_per_split + 1) / 2 + stages + 1) * kWaitNs;
 }
-// The (max, sum) slot of a split that gave up carries this maximum; a merge that sees it
-// writes no output (a real maximum is finite or -inf).
-constexpr float kAbortedMax = INFINITY;
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -376,11 +376,11 @@ __device__ __forceinline__ void inject_slab(const AttnParams& p, const CtaCtx& c
 }
 
 // After a timed-out wait: wait (each within 1 s) for the latest copy issued into every
-// stage, so that none is still writing shared memory when the block exits; then keep
-// the cluster's merge consistent -- a non-first CTA still sends its bytes, marked as
-// given up, so the first CTA's barrier completes, and the first CTA waits for them
-// (merge_wait_ns after its drain), since they land in its shared memory, before it
-// exits.
+// stage, so that none is still writing shared memory when the block exits. A non-first
+// CTA of a cluster then sends nothing: the first CTA's wait for the partials runs out,
+// so it flags the timeout and writes no output for the unit. A first CTA that gave up
+// still waits (merge_wait_ns) for the others' partials, since they land in its shared
+// memory, before it exits.
 //
 // Every wait on this path ends: the drain waits and the first CTA's wait are bounded;
 // __syncthreads is reached by all threads (the caller's __syncthreads_or is
@@ -397,17 +397,8 @@ __device__ void abort_after_timeout(const AttnParams& p, const CtaCtx& c, uint64
     __syncthreads();
     if (p.cluster) {
         cluster_wait();
-        if (c.s != 0) {
-            const uint32_t dst = map_shared(smem_u32(mrg), 0);
-            const uint32_t rbar = map_shared(smem_u32(&bars[p.stages]), 0);
-            for (int it = tid; it < kSlotQuads * c.mcount; it += blockDim.x) {
-                const bool ml = it % kSlotQuads == kHeadDim / 4;  // the (max, sum) quad
-                st_async_v4(dst + ((c.s * p.msub) * kSlot + 4 * it) * 4,
-                            make_float4(ml ? kAbortedMax : 0.f, 0.f, 0.f, 0.f), rbar);
-            }
-        } else if (tid == 0) {
-            mbar_wait_bounded_cluster(smem_u32(&bars[p.stages]), 0, merge_wait_ns(p));
-        }
+        if (c.s == 0 && tid == 0)
+            mbar_wait_bounded_cluster(smem_u32(&bars[p.stages]), 0, p.merge_wait_ns);
     }
 }
 
@@ -541,7 +532,7 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
         // can take to send); the block barrier then orders those bytes, and the slots
         // this CTA's own threads wrote, before every thread's reads.
         const bool ok =
-            tid >= 32 || mbar_wait_bounded_cluster(smem_u32(merge_bar), 0, merge_wait_ns(p));
+            tid >= 32 || mbar_wait_bounded_cluster(smem_u32(merge_bar), 0, p.merge_wait_ns);
         if (__syncthreads_or(!ok)) {
             if (tid == 0) flag_error(p.dev_err, KVD_ERR_TIMEOUT);
             return;
@@ -557,7 +548,6 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
 #pragma unroll
             for (int r = 0; r < kMaxClusterSplits; ++r)
                 mx = fmaxf(mx, sl0[min(r, S - 1) * stride + kHeadDim]);
-            if (mx == kAbortedMax) continue;  // a split gave up: no output
             const float ref = mx == -INFINITY ? 0.f : mx;
             float l = 0.f;
             float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1349,6 +1339,7 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
     p.early = (flags & KVD_FLAG_EARLY_KV) ? 1 : 0;
     p.cluster = P.cluster ? 1 : 0;
     p.test_stall = (flags & KVD_FLAG_TEST_STALL) ? 1 : 0;
+    p.merge_wait_ns = merge_wait_budget(P.tiles_per_split, p.stages);
     p.append = app ? 1 : 0;
     p.rope = rope ? 1 : 0;
     p.rope_log2_base = rope ? log2f(app->rope_base) : 0.f;

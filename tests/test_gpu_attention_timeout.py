@@ -6,10 +6,10 @@ about one second. The call must then report KVD_ERR_TIMEOUT, leave the output
 unwritten, and leave the context and stream usable: the next normal call on the same
 stream matches the fp64 oracle. Every
 merge path is covered: one split per unit, the cluster merge (the split that gives up
-is a non-first CTA, which sends its partial marked as given up only after its drain; the
-first CTA must still be waiting for it), and the workspace merge (the unit's arrival
+is a non-first CTA, which sends nothing, so the first CTA's bounded wait for the
+partials runs out and it writes no output), and the workspace merge (the unit's arrival
 counter is left non-zero and the workspace is re-zeroed, as the header says). Each stall
-costs about two seconds of waiting.
+costs a few seconds of waiting.
 """
 
 import numpy as np
