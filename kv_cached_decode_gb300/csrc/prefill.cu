@@ -12,15 +12,16 @@
 // Design: the prompt's K/V are first written into the cache by the append kernel (with a
 // per-row count); then the attention kernel runs on the fifth-generation tensor cores.
 // A block takes 128 query positions of one query head: four softmax warps own the rows
-// (thread t: row t, tensor-memory lane t) and one producer thread issues every TMA copy
+// (thread t: row t, tensor-memory lane t) and one producer warp issues every TMA copy
 // and every tcgen05.mma. The rows, rotated if asked, are staged once into shared memory
 // in the 128-byte-swizzled layout; K/V tiles of 64 positions arrive by TMA (the same
-// swizzle) through 3 K and 2 V slots.
-//   S = Q . K^T   M 128, N 64, K 64 (Q and K K-major)          -> tensor memory
-//   O += P . V    M 128, N 64, K 64 (P K-major, V MN-major)     -> tensor memory
+// swizzle) through 5 slots of K/V pairs.
+//   S = Q . K^T   M 128, N 64, K 64 (Q and K K-major, shared memory) -> tensor memory
+//   O += P . V    M 128, N 64, K 64 (P in tensor memory, V MN-major)  -> tensor memory
 // Each row reads its S with tcgen05.ld, applies the causal mask where the tile is not
 // wholly visible to its warp, forms the weights exp2(s * scale * log2 e - m) rounded to
-// the input type into the swizzled P operand, and sums them. A row's reference m moves
+// the input type in registers, sums them, and stores them into its lane of the P
+// operand (two buffers) with tcgen05.st. A row's reference m moves
 // only when its maximum grows by more than 2^8; the rows then rescale their O in tensor
 // memory. Hand-offs run through mbarriers, every wait bounded. Only the tiles a block's
 // rows can see are read, and the blocks with the most tiles start first.
@@ -38,21 +39,29 @@ namespace {
 constexpr int kPfSoftWarps = 4;                        // softmax warps: thread t owns row t
 constexpr int kPfThreads = (kPfSoftWarps + 1) * 32;    // + the producer warp
 constexpr int kPfRows = kPfSoftWarps * 32;             // query positions per block (MMA M)
-constexpr int kPfKSlots = 3;   // K tiles in flight
-constexpr int kPfVSlots = 2;   // V tiles in flight
-constexpr int kPfSBufs = 1;    // S buffers in tensor memory (the rows read S first)
-constexpr int kPfPBufs = 1;    // P buffers in shared memory
-// With one S and one P buffer, the rows' hand-offs also free the K and V slots: the rows
-// read S_j only after S_j (and so every read of K_j) completed, and write P_j only after
-// P_{j-1} . V_{j-1} completed.
-static_assert(kPfSBufs == 1 && kPfPBufs == 1, "slot reuse follows the rows' hand-offs");
+constexpr int kPfSlots = 5;    // K/V tile pairs in flight (one barrier per pair)
+constexpr int kPfSBufs = 2;    // S buffers in tensor memory: S is issued two tiles ahead
+constexpr int kPfPBufs = 2;    // P buffers in tensor memory
+// The hand-offs, per tile j (one producer iteration per tile):
+//  * the rows wait for S_j, write P_j into P buffer j % 2 and signal P_j;
+//  * the producer waits for that signal, issues P_j . V_j and then S_{j+2} into S buffer
+//    j % 2 (the rows have read S_j), and refills the slot of tile j - 1 with tile
+//    j - 1 + kPfSlots once P_{j-1} . V_{j-1} has completed.
+// A commit tracks every MMA its thread issued before it, and P_{j-2} . V_{j-2} is issued
+// before S_j, so a row that sees S_j complete may overwrite P buffer j % 2 without a wait
+// of its own. The refilled pair is needed kPfSlots - 3 iterations later.
+static_assert(kPfSBufs == 2 && kPfPBufs == 2 && kPfSlots >= 4, "the hand-offs above");
 constexpr int kPfMinBlocks = 2;  // blocks per SM the sizes below are chosen for
-constexpr uint32_t kPfCols = 128;  // tensor memory: S buffers and O, 64 columns each
-static_assert(kPfCols >= (kPfSBufs + 1) * 64, "tensor memory columns");
-constexpr uint32_t kPfRowsBytes = kPfRows * kRowBytes;  // 16 KiB: the Q or a P block
-// shared memory: K slots | V slots | Q | P buffers | barriers
-constexpr uint32_t kPfSmem = (kPfKSlots + kPfVSlots) * kTileBytes +
-                             (1 + kPfPBufs) * kPfRowsBytes + 256 + 1024;
+// tensor memory: S buffers (64 fp32 columns each), O (64), then P buffers (32 columns
+// each: a row's 64 weights, two 16-bit values per column)
+constexpr uint32_t kPfColsO = kPfSBufs * kTile;
+constexpr uint32_t kPfColsP = kPfColsO + kHeadDim;
+constexpr uint32_t kPfCols = 256;  // allocated (a power of two)
+static_assert(kPfCols >= kPfColsP + kPfPBufs * (kTile / 2), "tensor memory columns");
+static_assert(kPfMinBlocks * kPfCols <= 512, "the resident blocks' tensor memory");
+constexpr uint32_t kPfRowsBytes = kPfRows * kRowBytes;  // 16 KiB: the Q block
+// shared memory: K slots | V slots | Q | barriers
+constexpr uint32_t kPfSmem = 2 * kPfSlots * kTileBytes + kPfRowsBytes + 256 + 1024;
 // The softmax reference of a row moves only when its maximum grows by more than this
 // (log2 units): the weights then stay below 2^8 and the output is rescaled rarely.
 constexpr float kRescaleLog2 = 8.f;
@@ -69,17 +78,43 @@ struct PrefillParams {
     int32_t test_stall;       // KVD_FLAG_TEST_STALL: the first K copy is never issued
 };
 
+// Three-input maximum and two-lane fp32 arithmetic of this architecture: one instruction
+// for what takes two otherwise; each lane rounds as the scalar instruction does.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// (a.x * b.x + c.x, a.y * b.y + c.y), each fused and rounded to nearest
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+// (a.x + b.x, a.y + b.y), each rounded to nearest
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
 // Barrier indices inside the block's barrier array.
 enum PfBar {
-    kBarKFull = 0,                       // K slot s landed (TMA bytes)
-    kBarVFull = kBarKFull + kPfKSlots,   // V slot s landed
-    kBarS = kBarVFull + kPfVSlots,       // S buffer b written (MMA commit)
-    kBarSFree = kBarS + kPfSBufs,        // S buffer b read by every row (128 arrivals)
-    kBarPFull = kBarSFree + kPfSBufs,    // P buffer b written by every row (128 arrivals)
+    kBarKV = 0,                          // K and V of slot s landed (TMA bytes)
+    kBarS = kBarKV + kPfSlots,           // S buffer b written (MMA commit)
+    kBarPFull = kBarS + kPfSBufs,        // P buffer b written by every row (128 arrivals)
     kBarO = kBarPFull + kPfPBufs,        // P.V from P buffer b done (MMA commit)
     kBarDrain = kBarO + kPfPBufs,        // every MMA issued so far done (after a failure)
     kBarCount = kBarDrain + 1
@@ -91,11 +126,10 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
                         const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
-    uint8_t* sK = smem;                        // kPfKSlots x 8 KiB
-    uint8_t* sV = sK + kPfKSlots * kTileBytes;  // kPfVSlots x 8 KiB
-    uint8_t* sQ = sV + kPfVSlots * kTileBytes;
-    uint8_t* sP = sQ + kPfRowsBytes;           // kPfPBufs x 16 KiB
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kPfPBufs * kPfRowsBytes);
+    uint8_t* sK = smem;                        // kPfSlots x 8 KiB
+    uint8_t* sV = sK + kPfSlots * kTileBytes;   // kPfSlots x 8 KiB
+    uint8_t* sQ = sV + kPfSlots * kTileBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sQ + kPfRowsBytes);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kBarCount);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -130,27 +164,20 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
     const int kv_end = s0 + q0 + rows_live;  // exclusive: the last live row's limit
     const int n_tiles = (kv_end + kTile - 1) / kTile;
     const uint32_t tx = p.box_rows * kRowBytes;  // bytes of one K or V tile copy
-    auto load_k = [&](int j) {
-        const int s = j % kPfKSlots;
-        mbar_expect_tx(bar(kBarKFull + s), tx);
-        tma_load_4d(smem_u32(sK + s * kTileBytes), &tmk, bar(kBarKFull + s), 0, j * kTile, hk, b);
-    };
-    auto load_v = [&](int j) {
-        const int s = j % kPfVSlots;
-        mbar_expect_tx(bar(kBarVFull + s), tx);
-        tma_load_4d(smem_u32(sV + s * kTileBytes), &tmv, bar(kBarVFull + s), 0, j * kTile, hk, b);
+    // K_j and V_j into slot j % kPfSlots, both completing on the slot's barrier
+    auto load_kv = [&](int j) {
+        const int s = j % kPfSlots;
+        mbar_expect_tx(bar(kBarKV + s), 2 * tx);
+        tma_load_4d(smem_u32(sK + s * kTileBytes), &tmk, bar(kBarKV + s), 0, j * kTile, hk, b);
+        tma_load_4d(smem_u32(sV + s * kTileBytes), &tmv, bar(kBarKV + s), 0, j * kTile, hk, b);
     };
     if (producer && (tid & 31) == 0) {
         for (int i = 0; i < kBarCount; ++i)
-            mbar_init(bar(i), ((i >= kBarSFree && i < kBarSFree + kPfSBufs) ||
-                               (i >= kBarPFull && i < kBarPFull + kPfPBufs))
-                                  ? kPfRows
-                                  : 1);
+            mbar_init(bar(i), (i >= kBarPFull && i < kBarPFull + kPfPBufs) ? kPfRows : 1);
         fence_barrier_init();
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
-        for (int j = p.test_stall ? 1 : 0; j < min(kPfKSlots, n_tiles); ++j) load_k(j);
-        for (int j = 0; j < min(kPfVSlots, n_tiles); ++j) load_v(j);
+        for (int j = p.test_stall ? 1 : 0; j < min(kPfSlots, n_tiles); ++j) load_kv(j);
     }
     if (warp == 0) {
         tc_alloc(smem_u32(tslot), kPfCols);
@@ -183,70 +210,72 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kIdS = tc_idesc_f16(kBf16, kPfRows, kTile, false);
     constexpr uint32_t kIdO = tc_idesc_f16(kBf16, kPfRows, kHeadDim, true);
-    const uint32_t t_o = tmem + kPfSBufs * kTile;  // the output accumulator
+    const uint32_t t_o = tmem + kPfColsO;  // the output accumulator
     bool ok = true;
 
     if (producer) {
-        // ---- producer: one thread issues every copy and every MMA ----
-        if ((tid & 31) == 0) {
-            const uint32_t qaddr = smem_u32(sQ);
-            int k_issued = min(kPfKSlots, n_tiles), v_issued = min(kPfVSlots, n_tiles);
-            // S_j = Q . K_j^T into S buffer j % kPfSBufs: K_j has landed and the rows have
-            // read S_{j - kPfSBufs} from that buffer
-            auto issue_s = [&](int j) -> bool {
-                const int s = j % kPfKSlots, sb = j % kPfSBufs;
-                if (!mbar_wait_bounded(bar(kBarKFull + s), (j / kPfKSlots) & 1)) return false;
-                if (j >= kPfSBufs && !mbar_wait_bounded(bar(kBarSFree + sb),
-                                                        ((j - kPfSBufs) / kPfSBufs) & 1))
-                    return false;
-                tc_fence_after();
-                const uint32_t kaddr = smem_u32(sK + s * kTileBytes);
+        // ---- producer warp: the whole warp runs the loop, so its control flow and the
+        // operand descriptors stay warp-uniform; one elected lane (the same one every
+        // time, so its commits track its own MMAs) issues each copy, MMA and commit ----
+        const uint32_t qaddr = smem_u32(sQ);
+        int kv_issued = min(kPfSlots, n_tiles);
+        auto wait_all = [&](int i, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait_bounded(bar(i), parity));
+        };
+        // S_j = Q . K_j^T into S buffer j % 2 once tile j has landed
+        auto issue_s = [&](int j) -> bool {
+            const int s = j % kPfSlots, sb = j % kPfSBufs;
+            if (!wait_all(kBarKV + s, (j / kPfSlots) & 1)) return false;
+            tc_fence_after();
+            const uint32_t kaddr = smem_u32(sK + s * kTileBytes);
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     tc_mma_f16(tmem + sb * kTile, tc_desc_sw128(qaddr + kk * 32),
                                tc_desc_sw128(kaddr + kk * 32), kIdS, kk);
                 tc_commit(bar(kBarS + sb));
-                return true;
-            };
-            ok = issue_s(0);
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                if (j + 1 < n_tiles && !(ok = issue_s(j + 1))) break;
-                // K slot of tile j: refilled with tile j + kPfKSlots. S_j is done, since
-                // issuing S_{j+1} waited for the rows to read S_j.
-                if (j + kPfKSlots < n_tiles) {
-                    load_k(j + kPfKSlots);
-                    k_issued = j + kPfKSlots + 1;
-                }
-                // P_j . V_j once the rows have written P_j and V_j landed
-                const int pb = j % kPfPBufs, vs = j % kPfVSlots;
-                if (!(ok = mbar_wait_bounded(bar(kBarPFull + pb), (j / kPfPBufs) & 1))) break;
-                // V slot of tile j - 1: refilled with tile j - 1 + kPfVSlots. P_{j-1} . V_{j-1}
-                // is done, since the rows waited for it before writing P_j.
-                if (j >= 1 && j - 1 + kPfVSlots < n_tiles) {
-                    load_v(j - 1 + kPfVSlots);
-                    v_issued = j + kPfVSlots;
-                }
-                if (!(ok = mbar_wait_bounded(bar(kBarVFull + vs), (j / kPfVSlots) & 1))) break;
-                tc_fence_after();
-                const uint32_t paddr = smem_u32(sP + pb * kPfRowsBytes);
-                const uint32_t vaddr = smem_u32(sV + vs * kTileBytes);
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int j = 0; ok && j < min(kPfSBufs, n_tiles); ++j) ok = issue_s(j);
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            // P_j . V_j once the rows have written P_j (V_j landed before S_j was issued)
+            const int pb = j % kPfPBufs;
+            if (!(ok = wait_all(kBarPFull + pb, (j / kPfPBufs) & 1))) break;
+            tc_fence_after();
+            const uint32_t t_p = tmem + kPfColsP + pb * (kTile / 2);
+            const uint32_t vaddr = smem_u32(sV + (j % kPfSlots) * kTileBytes);
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    tc_mma_f16(t_o, tc_desc_sw128(paddr + kk * 32),
-                               tc_desc_sw128(vaddr + kk * 16 * kRowBytes), kIdO, j > 0 || kk > 0);
+                    tc_mma_f16_tmem_a(t_o, t_p + kk * 8,
+                                      tc_desc_sw128(vaddr + kk * 16 * kRowBytes), kIdO,
+                                      j > 0 || kk > 0);
                 tc_commit(bar(kBarO + pb));
             }
-            if (!ok) {
-                // let the MMAs and copies in flight finish before the block leaves
-                flag_error(p.dev_err, KVD_ERR_TIMEOUT);
-                tc_commit(bar(kBarDrain));
-                mbar_wait_bounded(bar(kBarDrain), 0);
-                for (int jj = max(p.test_stall ? 1 : 0, k_issued - kPfKSlots); jj < k_issued; ++jj)
-                    mbar_wait_bounded(bar(kBarKFull + jj % kPfKSlots), (jj / kPfKSlots) & 1);
-                for (int jj = max(0, v_issued - kPfVSlots); jj < v_issued; ++jj)
-                    mbar_wait_bounded(bar(kBarVFull + jj % kPfVSlots), (jj / kPfVSlots) & 1);
+            __syncwarp();
+            // S_{j+2} into the S buffer the rows have read S_j from
+            if (j + kPfSBufs < n_tiles && !(ok = issue_s(j + kPfSBufs))) break;
+            // the slot of tile j - 1 takes tile j - 1 + kPfSlots once P_{j-1} . V_{j-1}
+            // (the last reader of that slot) has completed
+            if (j >= 1 && j - 1 + kPfSlots < n_tiles) {
+                if (!(ok = wait_all(kBarO + (j - 1) % kPfPBufs, ((j - 1) / kPfPBufs) & 1)))
+                    break;
+                if (elect_one()) load_kv(j - 1 + kPfSlots);
+                __syncwarp();
+                kv_issued = j + kPfSlots;
             }
         }
+        if (!ok && elect_one()) {
+            // let the MMAs and copies in flight finish before the block leaves
+            flag_error(p.dev_err, KVD_ERR_TIMEOUT);
+            tc_commit(bar(kBarDrain));
+            mbar_wait_bounded(bar(kBarDrain), 0);
+            for (int jj = max(p.test_stall ? 1 : 0, kv_issued - kPfSlots); jj < kv_issued; ++jj)
+                mbar_wait_bounded(bar(kBarKV + jj % kPfSlots), (jj / kPfSlots) & 1);
+        }
+        __syncwarp();
     } else {
         // ---- the rows: S_j into P_j, one row per thread ----
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;  // this warp's 32 lanes
@@ -272,30 +301,27 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
             float s[kTile];
             tc_ld32(tmem + lane_off + sb * kTile, s);
             tc_ld32(tmem + lane_off + sb * kTile + 32, s + 32);
-            tc_fence_before();
-            mbar_arrive(bar(kBarSFree + sb));
             if (!pos_scale) {
 #pragma unroll
                 for (int i = 0; i < kTile; ++i) s[i] *= p.scale_log2;
             }
-            // (eight independent partial maxima: short dependency chains)
+            if (t0 + kTile > lim_warp) {
+                // the tile is not wholly visible to every row of the warp: mask it
+#pragma unroll
+                for (int i = 0; i < kTile; ++i) s[i] = t0 + i < lim ? s[i] : -INFINITY;
+            }
+            // (eight independent partial maxima over eight scores each: short chains)
             float pm[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) pm[e] = -INFINITY;
-            if (t0 + kTile <= lim_warp) {
-                // the whole tile is visible to every row of the warp: no mask
-#pragma unroll
-                for (int i = 0; i < kTile; ++i) pm[i & 7] = fmaxf(pm[i & 7], s[i]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < kTile; ++i) {
-                    s[i] = t0 + i < lim ? s[i] : -INFINITY;
-                    pm[i & 7] = fmaxf(pm[i & 7], s[i]);
-                }
+            for (int e = 0; e < 8; ++e) {
+                float a = fmax3(s[e], s[e + 8], s[e + 16]);
+                a = fmax3(a, s[e + 24], s[e + 32]);
+                a = fmax3(a, s[e + 40], s[e + 48]);
+                pm[e] = fmaxf(a, s[e + 56]);
             }
             const float tmax =
-                fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                      fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * cs;
+                fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], fmaxf(pm[5],
+                      fmaxf(pm[6], pm[7])))) * cs;
             const float mc = fmaxf(m, tmax);
             const bool grow = mc > m + kRescaleLog2;
             float factor = 1.f;
@@ -322,41 +348,34 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
                     tc_st32(t_o + lane_off + h * 32, ov);
                 }
             }
-            // P buffer pb is free once P_{j - kPfPBufs} . V is done
-            if (j >= kPfPBufs &&
-                !__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarO + pb),
-                                                           ((j - kPfPBufs) / kPfPBufs) & 1))) {
-                ok = false;
-                break;
-            }
-            // P, rounded to the input type, into this row of the swizzled A operand; the
-            // normaliser sums the unrounded weights (rounding to nearest leaves no bias)
-            uint8_t* pbuf = sP + pb * kPfRowsBytes;
+            // The weights, rounded to the input type; the normaliser sums the unrounded
+            // weights (rounding to nearest leaves no bias).
             const float nref = m == -INFINITY ? 0.f : -m;
-            float ps[8];
+            // eight partial sums, as four lane pairs
+            float2 ps[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ps[e] = 0.f;
+            for (int e = 0; e < 4; ++e) ps[e] = make_float2(0.f, 0.f);
+            uint32_t w[kTile / 2];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = ex2_approx(fmaf(s[8 * c + 2 * e], cs, nref));
-                    const float p1 = ex2_approx(fmaf(s[8 * c + 2 * e + 1], cs, nref));
-                    ps[2 * e] += p0;
-                    ps[2 * e + 1] += p1;
-                    w[e] = Half16<T>::from_f2(p0, p1);
-                }
-                *reinterpret_cast<uint4*>(pbuf + swz(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int i = 0; i < kTile / 2; ++i) {
+                const float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), make_float2(cs, cs),
+                                       make_float2(nref, nref));
+                const float2 pw = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                ps[i & 3] = fadd2(ps[i & 3], pw);
+                w[i] = Half16<T>::from_f2(pw.x, pw.y);
             }
-            l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+            l += ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y)) +
+                 ((ps[2].x + ps[2].y) + (ps[3].x + ps[3].y));
+            // this row of the A operand, in this thread's lane of tensor memory (its last
+            // reader, P_{j-2} . V_{j-2}, completed before S_j did)
+            tc_st32_u(tmem + lane_off + kPfColsP + pb * (kTile / 2), w);
             if (t0 + kTile > kv_end) {
                 // Positions past the last visible key hold other data (or nothing): P is
                 // 0 there, but 0 * NaN would still poison P.V, so clear those V rows once
                 // the tile's copy has landed.
-                const int vs = j % kPfVSlots;
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarVFull + vs),
-                                                                (j / kPfVSlots) & 1))) {
+                const int vs = j % kPfSlots;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarKV + vs),
+                                                                (j / kPfSlots) & 1))) {
                     ok = false;
                     break;
                 }
@@ -365,8 +384,8 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
                 for (int x = tid; x < (kTile - first) * 8; x += kPfRows)
                     *reinterpret_cast<uint4*>(vt + swz(first + (x >> 3), x & 7)) =
                         make_uint4(0u, 0u, 0u, 0u);
+                fence_proxy_async();  // the cleared rows are read by the tensor cores
             }
-            fence_proxy_async();  // P (and cleared V rows) are read by the tensor cores
             tc_fence_before();
             mbar_arrive(bar(kBarPFull + pb));
         }
