@@ -55,6 +55,34 @@ kvd_status encode_cache_map(CUtensorMap* map, kvd_dtype dtype, void* base, const
     return r == CUDA_SUCCESS ? KVD_OK : KVD_ERR_INVALID_ARG;
 }
 
+kvd_status encode_rows_map(CUtensorMap* map, kvd_dtype dtype, void* base, int rows, int heads,
+                           int batch, int box_rows) {
+    kvd_cache c = {};
+    c.head_dim = KVD_HEAD_DIM;
+    c.capacity = rows;
+    c.n_kv_heads = heads;
+    c.batch = batch;
+    c.stride_t = KVD_HEAD_DIM;
+    c.stride_h = (int64_t)rows * KVD_HEAD_DIM;
+    c.stride_b = (int64_t)heads * rows * KVD_HEAD_DIM;
+    if (kvd_status s = encode_cache_map(map, dtype, base, &c)) return s;
+    if (box_rows == std::min(64, rows)) return KVD_OK;
+    // the same map with a taller box
+    const cuuint64_t dims[4] = {(cuuint64_t)KVD_HEAD_DIM, (cuuint64_t)rows, (cuuint64_t)heads,
+                                (cuuint64_t)batch};
+    const cuuint64_t strides[3] = {(cuuint64_t)c.stride_t * 2, (cuuint64_t)c.stride_h * 2,
+                                   (cuuint64_t)c.stride_b * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)KVD_HEAD_DIM, (cuuint32_t)box_rows, 1, 1};
+    const cuuint32_t elem[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(map,
+                          dtype == KVD_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          4, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? KVD_OK : KVD_ERR_INVALID_ARG;
+}
+
 kvd_status validate_cache(const kvd_cache* c) {
     if (!c || !c->k || !c->v) return KVD_ERR_INVALID_ARG;
     if (c->head_dim != KVD_HEAD_DIM) return KVD_ERR_UNSUPPORTED;

@@ -138,13 +138,6 @@ __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t byt
                  "r"(src), "r"(bytes)
                  : "memory");
 }
-__device__ __forceinline__ void bulk_commit() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// the stores have read shared memory (it may be refilled)
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 // the stores are complete
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");

@@ -18,6 +18,11 @@ int sm_count();
 // range.
 kvd_status encode_cache_map(CUtensorMap* map, kvd_dtype dtype, void* base, const kvd_cache* c);
 
+// 4-D TMA descriptor over dense rows of 64 16-bit values [batch, heads, rows, 64]: dims
+// (64, rows, heads, batch), box (64, box_rows, 1, 1), 128-byte swizzle.
+kvd_status encode_rows_map(CUtensorMap* map, kvd_dtype dtype, void* base, int rows, int heads,
+                           int batch, int box_rows);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 kvd_status validate_cache(const kvd_cache* c);

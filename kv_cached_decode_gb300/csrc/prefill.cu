@@ -123,7 +123,8 @@ enum PfBar {
 template <typename T, bool ROPE>
 __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tmk,
-                        const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
+                        const __grid_constant__ CUtensorMap tmv,
+                        const __grid_constant__ CUtensorMap tmo, const PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     uint8_t* sK = smem;                        // kPfSlots x 8 KiB
@@ -149,15 +150,28 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
     const int q0 = qt * kPfRows;
     const int row = q0 + tid;  // meaningful for the softmax threads
     const int64_t head_off = ((int64_t)b * p.n_q_heads + hq) * p.max_len * kHeadDim;
-    T* outr = static_cast<T*>(p.out) + head_off + (int64_t)row * kHeadDim;
     // a row the append rejected (length out of range) gets zeros, like padding rows
     const bool bad = s0 < 0 || plen < 0 || plen > p.max_len || (int64_t)s0 + plen > p.capacity;
     const int rows_live = bad ? 0 : max(0, min(kPfRows, plen - q0));
+    // The block's 128 output rows leave through the Q tile's shared memory (free once every
+    // S has completed) and one tensor store; rows past max_len fall outside the tensor.
+    auto store_rows = [&]() {
+        fence_proxy_async();  // the rows' generic writes, read by the tensor store
+        asm volatile("bar.sync 1, %0;" ::"n"(kPfRows) : "memory");
+        if (tid == 0 && tslot[1] == 0) {
+            tma_store_4d(&tmo, smem_u32(sQ), 0, q0, hq, b);
+            bulk_commit();
+            bulk_wait_read();
+        }
+    };
     if (rows_live == 0) {
-        if (!producer && row < p.max_len)
+        if (!producer) {
+            if (tid == 0) tslot[1] = 0;
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-                reinterpret_cast<uint4*>(outr)[c] = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(sQ + swz(tid, c)) = make_uint4(0u, 0u, 0u, 0u);
+            store_rows();
+        }
         pdl_trigger();
         return;
     }
@@ -183,6 +197,7 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
         tc_alloc(smem_u32(tslot), kPfCols);
         tc_relinquish();
     }
+    if (tid == kPfRows - 1) tslot[1] = 0;  // set when a row could not produce its output
     const bool live = !producer && row < plen;
     if (!producer) {
         // this thread's query row (zeros past the prompt), rotated at position s0 + row,
@@ -389,6 +404,7 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
             tc_fence_before();
             mbar_arrive(bar(kBarPFull + pb));
         }
+        bool wrote = false;
         if (!ok) {
             if ((tid & 31) == 0) flag_error(p.dev_err, KVD_ERR_TIMEOUT);
         } else {
@@ -402,7 +418,8 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
             tc_ld32(t_o + lane_off + 32, o + 32);
             if (!done) {
                 if ((tid & 31) == 0) flag_error(p.dev_err, KVD_ERR_TIMEOUT);
-            } else if (row < p.max_len) {
+            } else {
+                // every MMA has completed, so this row of the Q tile is free
                 const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -413,10 +430,14 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
                         w.z = Half16<T>::from_f2(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
                         w.w = Half16<T>::from_f2(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
                     }
-                    reinterpret_cast<uint4*>(outr)[c] = w;
+                    *reinterpret_cast<uint4*>(sQ + swz(tid, c)) = w;
                 }
+                wrote = true;
             }
         }
+        // a warp that gave up leaves the whole tile unwritten
+        if ((tid & 31) == 0 && !wrote) atomicOr(reinterpret_cast<int*>(&tslot[1]), 1);
+        store_rows();
     }
     tc_fence_before();
     __syncthreads();
@@ -445,10 +466,10 @@ bool prepare_prefill() {
 
 template <typename T, bool ROPE>
 kvd_status launch_prefill(dim3 grid, cudaStream_t st, bool pdl, const CUtensorMap& mk,
-                          const CUtensorMap& mv, const PrefillParams& p) {
+                          const CUtensorMap& mv, const CUtensorMap& mo, const PrefillParams& p) {
     if (!prepare_prefill<T, ROPE>()) return KVD_ERR_CUDA;
     return launch(prefill_attn_kernel<T, ROPE>, grid, dim3(kPfThreads), kPfSmem, st, pdl, mk,
-                  mv, p);
+                  mv, mo, p);
 }
 
 }  // namespace
@@ -483,9 +504,12 @@ extern "C" kvd_status kvd_prefill_attn(kvd_dtype dtype, int32_t batch, int32_t n
                                      dtype, rope_base, flags, dev_err, st))
         return s;
     // 2: causal attention of the prompt over the cache
-    CUtensorMap mk, mv;
+    CUtensorMap mk, mv, mo;
     if (kvd_status s = encode_cache_map(&mk, dtype, kv->k, kv)) return s;
     if (kvd_status s = encode_cache_map(&mv, dtype, kv->v, kv)) return s;
+    if (kvd_status s = encode_rows_map(&mo, dtype, out, max_len, n_q_heads, batch,
+                                       std::min(kPfRows, max_len)))
+        return s;
     PrefillParams p;
     p.q = q;
     p.out = out;
@@ -506,8 +530,8 @@ extern "C" kvd_status kvd_prefill_attn(kvd_dtype dtype, int32_t batch, int32_t n
     const bool rope = rope_base > 0.f;
     p.rope_log2_base = rope ? log2f(rope_base) : 0.f;
     if (dtype == KVD_BF16)
-        return rope ? launch_prefill<__nv_bfloat16, true>(grid, st, pdl, mk, mv, p)
-                    : launch_prefill<__nv_bfloat16, false>(grid, st, pdl, mk, mv, p);
-    return rope ? launch_prefill<__half, true>(grid, st, pdl, mk, mv, p)
-                : launch_prefill<__half, false>(grid, st, pdl, mk, mv, p);
+        return rope ? launch_prefill<__nv_bfloat16, true>(grid, st, pdl, mk, mv, mo, p)
+                    : launch_prefill<__nv_bfloat16, false>(grid, st, pdl, mk, mv, mo, p);
+    return rope ? launch_prefill<__half, true>(grid, st, pdl, mk, mv, mo, p)
+                : launch_prefill<__half, false>(grid, st, pdl, mk, mv, mo, p);
 }
