@@ -1117,14 +1117,18 @@ def run_beam_step(torch, kvd, dev, stream, peak, flags, only_len=None, with_sele
         def reorder():
             kvd.kvd_beam_reorder_kv(c_self, R, beam, parent, lens=lens_in, flags=flags)
 
-        # The reorder rewrites the self caches, so the self calls must not stage K/V
-        # before their dependency wait: PDL only. Cross K/V are never rewritten.
+        # The reorder rewrites the self caches, so the first self call after it must not
+        # stage K/V before its dependency wait: PDL only. That call lets the next launch
+        # start only after its wait, so the reorder has completed before any later self
+        # call starts, and those stage early like the cross calls (cross K/V are never
+        # rewritten).
         self_flags = flags & kvd.KVD_FLAG_PDL
 
         def step():
             reorder()
             for l in range(NL):
-                kvd.kvd_decode_attn(q, c_self[l], out, ws, lens=lens_in, flags=self_flags,
+                kvd.kvd_decode_attn(q, c_self[l], out, ws, lens=lens_in,
+                                    flags=self_flags if l == 0 else flags,
                                     append=(kn, kn, lens))
                 kvd.kvd_decode_attn(q, c_cross[l], out, ws, fixed_len=F, rows_per_kv=beam,
                                     flags=flags)
@@ -1176,8 +1180,8 @@ def run_beam_step(torch, kvd, dev, stream, peak, flags, only_len=None, with_sele
                             flags=self_flags, **sel)
         kvd.kvd_beam_reorder_kv(c_self, R, beam, sel["parent"], lens=lens_in, flags=self_flags)
         for l in range(NL):
-            kvd.kvd_decode_attn(q, c_self[l], out, ws, lens=lens_in, flags=self_flags,
-                                append=(kn, kn, lens))
+            kvd.kvd_decode_attn(q, c_self[l], out, ws, lens=lens_in,
+                                flags=self_flags if l == 0 else flags, append=(kn, kn, lens))
             kvd.kvd_decode_attn(q, c_cross[l], out, ws, fixed_len=F, rows_per_kv=beam,
                                 flags=flags)
 

@@ -282,3 +282,56 @@ def test_binding_refuses_mistyped_and_strided_tensors():
                               n, nxt, ws)
     kvd.kvd_greedy_accept(logits, draft, n, nxt, ws)  # the same call, well formed
     torch.cuda.synchronize()
+
+
+def test_beam_step_chain_with_early_self_calls_matches_plain_launches():
+    # The beam step as bench.py times it: the reorder, then per layer a self decode with
+    # the new token appended and a cross decode shared per window. Launched with PDL,
+    # the first self call after the reorder waits before touching its cache; every
+    # later self call and every cross call stages its K/V before its dependency wait.
+    # The same chain with plain launches must give the same bits (outputs, caches,
+    # lengths), repeated over several replays of the launch sequence.
+    import kv_cached_decode_gb300 as kvd
+
+    W, beam, NL, H, cap, F, L = 4, 3, 6, 4, 256, 640, 150
+    R = W * beam
+    rng = make_rng(8801)
+    parent = gen_parents(rng, W, beam)
+    base_self = [gen_cache(rng, R, H, cap, D, "f16", 0.125) for _ in range(NL)]
+    base_cross = [gen_cache(rng, W, H, F, D, "f16", 0.125) for _ in range(NL)]
+    q = dev16(gen_new_kv(rng, R, H, 1, D, "f16", 0.125)[0], "f16")
+    kn, vn = (dev16(a, "f16") for a in gen_new_kv(rng, R, H, 1, D, "f16", 0.125))
+    pd = dev_i32(parent)
+    cross_t = [tuple(dev16(a, "f16") for a in kv) for kv in base_cross]
+    c_cross = [kvd.make_cache(*kv) for kv in cross_t]
+    P, E = kvd.KVD_FLAG_PDL, kvd.KVD_FLAG_PDL | kvd.KVD_FLAG_EARLY_KV
+
+    def run(pdl):
+        selfs = [tuple(dev16(a, "f16") for a in kv) for kv in base_self]
+        c_self = [kvd.make_cache(*kv) for kv in selfs]
+        outs = [torch.empty_like(q) for _ in range(2 * NL)]
+        ws = kvd.new_workspace(kvd.kvd_workspace_size(kvd.KVD_OP_DECODE_ATTN, R, H, H, beam, 1, F))
+        lens_in = dev_i32(np.full(R, L, np.int32))
+        lens = dev_i32(np.zeros(R, np.int32))
+        err = new_err()
+        kvd.kvd_beam_reorder_kv(c_self, R, beam, pd, lens=lens_in, flags=P if pdl else 0,
+                                dev_err=err)
+        for l in range(NL):
+            sf = (P if l == 0 else E) if pdl else 0
+            kvd.kvd_decode_attn(q, c_self[l], outs[2 * l], ws, lens=lens_in, flags=sf,
+                                append=(kn, vn, lens), dev_err=err)
+            kvd.kvd_decode_attn(q, c_cross[l], outs[2 * l + 1], ws, fixed_len=F,
+                                rows_per_kv=beam, flags=E if pdl else 0, dev_err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        return ([host16(o) for o in outs], [(host16(k), host16(v)) for k, v in selfs],
+                lens.cpu().numpy())
+
+    want = run(False)
+    for _ in range(3):
+        got = run(True)
+        for a, b in zip(got[0], want[0]):
+            assert np.array_equal(a, b)
+        for (ka, va), (kb, vb) in zip(got[1], want[1]):
+            assert np.array_equal(ka, kb) and np.array_equal(va, vb)
+        assert np.array_equal(got[2], want[2]) and np.all(got[2] == L + 1)
