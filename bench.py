@@ -923,7 +923,7 @@ def run_ours(args):
     # K/V before the dependency wait where that is legal (PDL + early K/V).
     del g_dec, g_ver
     torch.cuda.empty_cache()
-    long_pts, c4, c5 = None, None, None
+    long_pts, c4, c5, next_rows = None, None, None, None
     if not args.no_extra_sections:
         sweep_flags = kvd.KVD_FLAG_PDL | kvd.KVD_FLAG_EARLY_KV
         sampler2 = ClockSampler(local)
@@ -939,6 +939,19 @@ def run_ours(args):
         c5 = run_beam_step(torch, kvd, dev, stream, peak, sweep_flags, only_len=224,
                            with_selection=False, quiet=True)[0]
         windows.append((c5, t_a, time.time()))
+        torch.cuda.empty_cache()
+        # The rows beyond the decode path: causal prefill, beam selection and stochastic
+        # acceptance, each with its clocks.
+        next_rows = {}
+        t_a = time.time()
+        next_rows["prefill"] = run_prefill(torch, kvd, dev, stream, sweep_flags, quiet=True)
+        windows.append((next_rows["prefill"], t_a, time.time()))
+        for name, fn in (("beam_select", run_beam_select), ("sample_accept", run_sample_accept)):
+            t_a = time.time()
+            next_rows[name] = fn(torch, kvd, dev, stream, peak, sweep_flags, quiet=True)
+            t_b = time.time()
+            for rec in next_rows[name]:
+                windows.append((rec, t_a, t_b))
         for rec, a, b in windows:
             rec["clocks"] = sampler2.summary(a, b)
         for rec in long_pts:
@@ -1019,6 +1032,7 @@ def run_ours(args):
             "points": long_pts},
         "gqa_lm_step": c4,
         "beam_step": c5,
+        "next_rows": next_rows,
         "cpu_baseline": cpu,
         "e2e": {"value": round(value_e2e, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": step.in_bytes, "d2h_bytes_per_step": step.out_bytes},
@@ -1194,11 +1208,13 @@ def run_beam_step(torch, kvd, dev, stream, peak, flags, only_len=None, with_sele
     return records
 
 
-def run_beam_select(torch, kvd, dev, stream, peak, flags):
+def run_beam_select(torch, kvd, dev, stream, peak, flags, quiet=False):
     """Logit filters + beam-search selection over fp32 logits of 51865 ids: the beam
     workload (8 windows x beam 5 = 40 rows, 8.3 MB, suppression list of 88 ids) and
     greedy mode (beam 1, no walk) on 1 and 16 rows. The graph cycles through distinct
-    copies of the logits holding more than twice the L2, so every launch reads HBM."""
+    copies of the logits holding more than twice the L2, so every launch reads HBM.
+    Returns the records (also printed unless quiet)."""
+    records = []
     w = WORKLOADS["beam_select"]
     V, eot = w["vocab"], w["eot"]
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -1232,19 +1248,24 @@ def run_beam_select(torch, kvd, dev, stream, peak, flags):
         if kind == "beam":
             nbytes += rows * 20 + W * 4
         gbs = nbytes / (t * 1e-3) / 1e9
-        print(json.dumps({"sweep": "beam_select", "mode": kind, "rows": rows, "beam": beam,
-                          "vocab": V, "us": round(t * 1e3, 3), "bytes": nbytes,
-                          "gbs": round(gbs, 1), "pct_peak": round(100 * gbs / peak, 1),
-                          "distinct_buffers": n, "flags": flags}), flush=True)
+        rec = {"sweep": "beam_select", "mode": kind, "rows": rows, "beam": beam, "vocab": V,
+               "us": round(t * 1e3, 3), "bytes": nbytes, "gbs": round(gbs, 1),
+               "pct_peak": round(100 * gbs / peak, 1), "distinct_buffers": n, "flags": flags}
+        records.append(rec)
+        if not quiet:
+            print(json.dumps(rec), flush=True)
         del pool, g
         torch.cuda.empty_cache()
+    return records
 
 
-def run_sample_accept(torch, kvd, dev, stream, peak, flags):
+def run_sample_accept(torch, kvd, dev, stream, peak, flags, quiet=False):
     """Temperature sampling and stochastic speculative acceptance over fp32 logits of
     51865 ids: k = 5 drafts (6 main-model rows + 5 draft rows per batch row) and plain
     sampling (k = 0), at batch 1 and 16. Distinct copies of the inputs cycle through
-    more than twice the L2, so every launch reads HBM."""
+    more than twice the L2, so every launch reads HBM. Returns the records (also printed
+    unless quiet)."""
+    records = []
     V = 51865
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     i32 = dict(dtype=torch.int32, device=dev)
@@ -1273,12 +1294,15 @@ def run_sample_accept(torch, kvd, dev, stream, peak, flags):
         t = time_graph(torch, g, stream, max(3, int(4e-3 / (n * 5e-6)))) / n  # ms per launch
         nbytes = one + B * (2 * k * 4 + 4 + 8) + B * k * 4
         gbs = nbytes / (t * 1e-3) / 1e9
-        print(json.dumps({"sweep": "sample_accept", "k": k, "batch": B, "vocab": V,
-                          "us": round(t * 1e3, 3), "bytes": nbytes, "gbs": round(gbs, 1),
-                          "pct_peak": round(100 * gbs / peak, 1), "distinct_buffers": n,
-                          "flags": flags}), flush=True)
+        rec = {"sweep": "sample_accept", "k": k, "batch": B, "vocab": V,
+               "us": round(t * 1e3, 3), "bytes": nbytes, "gbs": round(gbs, 1),
+               "pct_peak": round(100 * gbs / peak, 1), "distinct_buffers": n, "flags": flags}
+        records.append(rec)
+        if not quiet:
+            print(json.dumps(rec), flush=True)
         del tpool, dpool, g
         torch.cuda.empty_cache()
+    return records
 
 
 def run_gqa_lm_step(torch, kvd, dev, stream, peak, flags, quiet=False):
@@ -1350,11 +1374,12 @@ def run_gqa_lm_step(torch, kvd, dev, stream, peak, flags, quiet=False):
     return rec
 
 
-def run_prefill(torch, kvd, dev, stream, flags):
+def run_prefill(torch, kvd, dev, stream, flags, quiet=False):
     """Prefill of the GQA decoder-LM prompts: 16 rows, 9 query heads on 3 KV heads, bf16,
     prompt lengths uniform in [256, 2048] (the decode step's cache lengths), one layer per
     call; 30 layers' caches in a graph. Reports tensor TFLOP/s of the causal attention
-    (Q.K^T and P.V over each prompt token's visible keys)."""
+    (Q.K^T and P.V over each prompt token's visible keys). Returns the record (also
+    printed unless quiet)."""
     w = WORKLOADS["gqa_lm_step"]
     NL, B, Hq, Hkv, cap = w["n_layers"], w["batch"], w["n_q_heads"], w["n_kv_heads"], w["capacity"]
     gen = torch.Generator(device=dev)
@@ -1391,12 +1416,16 @@ def run_prefill(torch, kvd, dev, stream, flags):
             peak = float(json.load(f)["bf16_tflops"])
     except Exception:
         pass
-    print(json.dumps({"sweep": "prefill", "layers": NL, "batch": B, "heads": f"{Hq}/{Hkv}",
-                      "mean_prompt": round(float(plens_np.mean()), 1), "us_per_layer":
-                      round(t * 1e3, 2), "tflops": round(tflops, 1),
-                      "frac_of_bf16_peak": None if peak is None else round(tflops / peak, 4),
-                      "tokens_per_s": round(float(plens_np.sum()) / (t * 1e-3), 1)}),
-          flush=True)
+    rec = {"sweep": "prefill", "layers": NL, "batch": B, "heads": f"{Hq}/{Hkv}",
+           "mean_prompt": round(float(plens_np.mean()), 1), "us_per_layer": round(t * 1e3, 2),
+           "tflops": round(tflops, 1),
+           "frac_of_bf16_peak": None if peak is None else round(tflops / peak, 4),
+           "tokens_per_s": round(float(plens_np.sum()) / (t * 1e-3), 1)}
+    del kv_tensors, caches, q, kn, out
+    torch.cuda.empty_cache()
+    if not quiet:
+        print(json.dumps(rec), flush=True)
+    return rec
 
 
 def run_tiny_layer(torch, kvd, dev, stream, flags):
