@@ -45,12 +45,14 @@ constexpr int kPfPBufs = 2;    // P buffers in tensor memory
 // The hand-offs, per tile j (one producer iteration per tile):
 //  * the rows wait for S_j, write P_j into P buffer j % 2 and signal P_j;
 //  * the producer waits for that signal, issues P_j . V_j and then S_{j+2} into S buffer
-//    j % 2 (the rows have read S_j), and refills the slot of tile j - 1 with tile
-//    j - 1 + kPfSlots once P_{j-1} . V_{j-1} has completed.
+//    j % 2 (the rows have read S_j), and refills the slot of tile j - 2 with tile
+//    j - 2 + kPfSlots.
 // A commit tracks every MMA its thread issued before it, and P_{j-2} . V_{j-2} is issued
-// before S_j, so a row that sees S_j complete may overwrite P buffer j % 2 without a wait
-// of its own. The refilled pair is needed kPfSlots - 3 iterations later.
-static_assert(kPfSBufs == 2 && kPfPBufs == 2 && kPfSlots >= 4, "the hand-offs above");
+// before S_j. So a row that sees S_j complete may overwrite P buffer j % 2 without a wait
+// of its own, and the signal of P_j, sent after the rows saw S_j, tells the producer that
+// the slot of tile j - 2 is free (no wait on P_{j-2} . V_{j-2}). The refilled pair is
+// needed by S_{j-2+kPfSlots}, issued kPfSlots - 4 iterations later.
+static_assert(kPfSBufs == 2 && kPfPBufs == 2 && kPfSlots >= 5, "the hand-offs above");
 constexpr int kPfMinBlocks = 2;  // blocks per SM the sizes below are chosen for
 // tensor memory: S buffers (64 fp32 columns each), O (64), then P buffers (32 columns
 // each: a row's 64 weights, two 16-bit values per column)
@@ -272,14 +274,13 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
             __syncwarp();
             // S_{j+2} into the S buffer the rows have read S_j from
             if (j + kPfSBufs < n_tiles && !(ok = issue_s(j + kPfSBufs))) break;
-            // the slot of tile j - 1 takes tile j - 1 + kPfSlots once P_{j-1} . V_{j-1}
-            // (the last reader of that slot) has completed
-            if (j >= 1 && j - 1 + kPfSlots < n_tiles) {
-                if (!(ok = wait_all(kBarO + (j - 1) % kPfPBufs, ((j - 1) / kPfPBufs) & 1)))
-                    break;
-                if (elect_one()) load_kv(j - 1 + kPfSlots);
+            // the rows saw S_j complete before they signalled P_j, and P_{j-2} . V_{j-2}
+            // (the last reader of the slot of tile j - 2) was issued before S_j: that
+            // slot takes tile j - 2 + kPfSlots
+            if (j >= 2 && j - 2 + kPfSlots < n_tiles) {
+                if (elect_one()) load_kv(j - 2 + kPfSlots);
                 __syncwarp();
-                kv_issued = j + kPfSlots;
+                kv_issued = j - 1 + kPfSlots;
             }
         }
         if (!ok && elect_one()) {
