@@ -111,11 +111,26 @@ AttnPlan plan_attention(int batch, int n_q_heads, int n_kv_heads, int rows_per_k
     P.tiles_per_split = 2 * std::max(1, (P.rounds + s - 1) / s);
     P.splits = P.tiles_total > 0 ? (P.tiles_total + P.tiles_per_split - 1) / P.tiles_per_split : 1;
     P.cluster = P.splits > 1 && P.splits <= max_cluster;
+    P.cgroups = 1;
     P.stages = P.tiles_per_split >= 4 ? 4 : 2;
     P.part_offset = KVD_WS_COUNTER_BYTES;
     const size_t slots = (size_t)P.units * P.splits * P.msub;
     P.ml_offset = align_up(P.part_offset + slots * 64 * sizeof(float), 256);
     P.ws_bytes = (P.splits > 1 && !P.cluster) ? P.ml_offset + slots * 2 * sizeof(float) : 0;
+    return P;
+}
+
+AttnPlan plan_grouped(int batch, int n_q_heads, int n_kv_heads, int rows_per_kv, int qlen,
+                      int len_bound, int mmax, int groups, int csize) {
+    AttnPlan P = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, qlen, len_bound, mmax,
+                                groups * csize, 1);
+    const int cs = (P.splits + groups - 1) / groups;
+    P.cgroups = groups;
+    P.splits = cs * groups;
+    P.cluster = true;
+    const size_t slots = (size_t)P.units * groups * P.msub;
+    P.ml_offset = align_up(P.part_offset + slots * 64 * sizeof(float), 256);
+    P.ws_bytes = P.ml_offset + slots * 2 * sizeof(float);
     return P;
 }
 
@@ -148,7 +163,8 @@ extern "C" size_t kvd_workspace_size(kvd_op op, int32_t batch, int32_t n_q_heads
         const AttnPlan P1 = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, q, max_len,
                                            mmax, 1, 1);
         if (!workspace_merge_pays(P1.units, P1.rounds)) return KVD_WS_COUNTER_BYTES;
-        // The most splits a launch can use bounds every workspace plan.
+        // The most splits a launch can use bounds every workspace plan (a grouped plan
+        // keeps kMaxGroups <= kMaxSplits partials per unit).
         const AttnPlan P = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, q, max_len,
                                           mmax, kMaxSplits, 1);
         return std::max<size_t>(P.ws_bytes, KVD_WS_COUNTER_BYTES);

@@ -79,7 +79,9 @@ struct AttnParams {
     int32_t stages;
     int32_t box_rows;
     int32_t early;
-    int32_t cluster;   // 1: the splits of a unit form one thread-block cluster
+    int32_t cluster;   // 1: the splits of a unit form thread-block clusters
+    int32_t cgroups;   // clusters per unit; > 1: their first CTAs merge through the workspace
+    int32_t csize;     // CTAs per cluster (splits / cgroups)
     int32_t test_stall;  // test only: the last split of every unit never sees its first stage
     unsigned long long merge_wait_ns;  // the first CTA's bound on its wait for the partials
     int32_t append;    // 1: k_new/v_new are written at positions lens[b] .. lens[b]+qlen-1
@@ -143,7 +145,8 @@ __device__ __forceinline__ const float2* rope_table(const AttnParams& p, const u
 }
 
 struct CtaCtx {
-    int bk, h, sub, s, m0, mcount, len, new0, t_begin, t_end, n_tiles, unit;
+    // s: split of the unit; rank / grp: place in its cluster / the cluster's index
+    int bk, h, sub, s, rank, grp, m0, mcount, len, new0, t_begin, t_end, n_tiles, unit;
     bool bad;
 };
 
@@ -173,6 +176,8 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 
 __device__ __forceinline__ void setup_ctx(const AttnParams& p, CtaCtx& c) {
     c.s = blockIdx.x;
+    c.grp = p.cgroups > 1 ? c.s / p.csize : 0;
+    c.rank = c.s - c.grp * p.csize;
     c.h = blockIdx.y / p.nsub;
     c.sub = blockIdx.y % p.nsub;
     c.bk = blockIdx.z;
@@ -243,11 +248,11 @@ __device__ __forceinline__ bool prologue(const AttnParams& p, CtaCtx& c, uint8_t
     }
     if (tid == 0) {
         for (int j = 0; j < p.stages; ++j) mbar_init(smem_u32(&bars[j]), 1);
-        if (p.cluster && c.s == 0) mbar_init(smem_u32(&bars[p.stages]), 1);
+        if (p.cluster && c.rank == 0) mbar_init(smem_u32(&bars[p.stages]), 1);
         fence_barrier_init();
-        if (p.cluster && c.s == 0)  // the one arrival; the others' bytes complete the phase
+        if (p.cluster && c.rank == 0)  // the one arrival; the others' bytes complete the phase
             mbar_expect_tx(smem_u32(&bars[p.stages]),
-                           (p.splits - 1) * merge_bytes_per_cta(c.mcount));
+                           (p.csize - 1) * merge_bytes_per_cta(c.mcount));
         prefetch_tensormap(tmk);
         prefetch_tensormap(tmv);
         const uint32_t tx = 2u * p.box_rows * kRowBytes;
@@ -397,7 +402,7 @@ __device__ void abort_after_timeout(const AttnParams& p, const CtaCtx& c, uint64
     __syncthreads();
     if (p.cluster) {
         cluster_wait();
-        if (c.s == 0 && tid == 0)
+        if (c.rank == 0 && tid == 0)
             mbar_wait_bounded_cluster(smem_u32(&bars[p.stages]), 0, p.merge_wait_ns);
     }
 }
@@ -461,149 +466,15 @@ __device__ __forceinline__ bool run_tiles(const AttnParams& p, const CtaCtx& c, 
     return true;
 }
 
-// Combine the eight warps' partial states, then
-//  * one split: write the output;
-//  * splits forming a cluster: store the block's (max, sum, o) into the first CTA's merge
-//    slots (one float4 per thread, then one arrive per thread on its barrier); the first
-//    CTA waits for all of them and merges locally;
-//  * more splits than a cluster holds: publish to the workspace; the last block to
-//    arrive (atomic ticket) merges all splits, loading them in parallel.
-// Merges run over the splits in index order, so results do not depend on timing.
-// red: o [8][RMAX][red_stride], m [8][RMAX], l [8][RMAX]; mrg: [splits][msub][kSlot].
-template <typename T, int RMAX>
-__device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, float* mrg,
-                           uint64_t* merge_bar, int* misc, const int64_t* qoff,
-                           uint8_t* scratch4k) {
-    constexpr int RS = red_stride(RMAX);
-    const float* red_o = red;
-    const float* red_m = red + kWarps * RMAX * RS;
-    const float* red_l = red_m + kWarps * RMAX;
+// The partials of a unit in the workspace (n of them, slots unit * n * msub + i * msub +
+// m): the block that arrives last (atomic ticket) merges them in slot order, loading them
+// in parallel, and writes the output.
+template <typename T>
+__device__ void ws_merge_last(const AttnParams& p, const CtaCtx& c, float* red, int* misc,
+                              const int64_t* qoff, uint8_t* scratch4k, int n) {
     const int tid = threadIdx.x;
-    const int S = p.splits;
+    const int S = n;
     const size_t base = (size_t)c.unit * S * p.msub;
-
-    if (S > 1 && p.cluster) {
-        cluster_wait();  // the first CTA's merge barrier is initialised
-        const bool leader = c.s == 0;
-        const uint32_t dst = leader ? 0u : map_shared(smem_u32(mrg), 0);
-        const uint32_t rbar = leader ? 0u : map_shared(smem_u32(merge_bar), 0);
-        // One thread per float4 of a slot: 16 of o, then (max, sum). Loads are
-        // unconditional (the (max, sum) thread reads an o quad it ignores) and go in
-        // batches of four warps.
-        for (int it = tid; it < kSlotQuads * c.mcount; it += blockDim.x) {
-            const int m = it / kSlotQuads, k = it % kSlotQuads;
-            const int kk = min(k, kHeadDim / 4 - 1);
-            float mx = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * RMAX + m]);
-            const float ref = mx == -INFINITY ? 0.f : mx;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            float l = 0.f;
-#pragma unroll
-            for (int w0 = 0; w0 < kWarps; w0 += 4) {
-                float4 o[4];
-                float mw[4], lw[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int w = w0 + j;
-                    o[j] = *reinterpret_cast<const float4*>(red_o + (w * RMAX + m) * RS + 4 * kk);
-                    mw[j] = red_m[w * RMAX + m];
-                    lw[j] = red_l[w * RMAX + m];
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float a = exp2f(mw[j] - ref);
-                    l = fmaf(lw[j], a, l);
-                    v.x = fmaf(o[j].x, a, v.x);
-                    v.y = fmaf(o[j].y, a, v.y);
-                    v.z = fmaf(o[j].z, a, v.z);
-                    v.w = fmaf(o[j].w, a, v.w);
-                }
-            }
-            if (k == kHeadDim / 4) v = make_float4(mx, l, 0.f, 0.f);
-            const int slot = (c.s * p.msub + m) * kSlot + 4 * k;
-            if (leader)
-                *reinterpret_cast<float4*>(mrg + slot) = v;
-            else
-                st_async_v4(dst + slot * 4, v, rbar);
-        }
-        if (!leader) return;
-        // One warp waits for the other CTAs' bytes (merge_wait_ns: longer than any peer
-        // can take to send); the block barrier then orders those bytes, and the slots
-        // this CTA's own threads wrote, before every thread's reads.
-        const bool ok =
-            tid >= 32 || mbar_wait_bounded_cluster(smem_u32(merge_bar), 0, p.merge_wait_ns);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) flag_error(p.dev_err, KVD_ERR_TIMEOUT);
-            return;
-        }
-        // One thread per (query vector, 4 dims). Loads are unconditional (a split past S
-        // re-reads the last slot and gets weight 0) and go in batches of four, so they
-        // overlap; the sums run in split order.
-        for (int it = tid; it < c.mcount * (kHeadDim / 4); it += blockDim.x) {
-            const int m = it >> 4, q4 = it & 15;
-            const float* sl0 = mrg + m * kSlot;
-            const int stride = p.msub * kSlot;
-            float mx = -INFINITY;
-#pragma unroll
-            for (int r = 0; r < kMaxClusterSplits; ++r)
-                mx = fmaxf(mx, sl0[min(r, S - 1) * stride + kHeadDim]);
-            const float ref = mx == -INFINITY ? 0.f : mx;
-            float l = 0.f;
-            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-            for (int r0 = 0; r0 < S; r0 += 4) {
-                float4 v[4];
-                float mv[4], lv[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float* sl = sl0 + min(r0 + j, S - 1) * stride;
-                    v[j] = *reinterpret_cast<const float4*>(sl + 4 * q4);
-                    mv[j] = sl[kHeadDim];
-                    lv[j] = sl[kHeadDim + 1];
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float a = r0 + j < S ? exp2f(mv[j] - ref) : 0.f;
-                    l = fmaf(lv[j], a, l);
-                    o.x = fmaf(v[j].x, a, o.x);
-                    o.y = fmaf(v[j].y, a, o.y);
-                    o.z = fmaf(v[j].z, a, o.z);
-                    o.w = fmaf(v[j].w, a, o.w);
-                }
-            }
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint2 packed;
-            packed.x = Half16<T>::from_f2(o.x * inv, o.y * inv);
-            packed.y = Half16<T>::from_f2(o.z * inv, o.w * inv);
-            *reinterpret_cast<uint2*>(static_cast<T*>(p.out) + qoff[m] + 4 * q4) = packed;
-        }
-        return;
-    }
-
-    const size_t slot0 = base + (size_t)c.s * p.msub;
-    for (int idx = tid; idx < c.mcount * kHeadDim; idx += blockDim.x) {
-        const int m = idx >> 6, d = idx & 63;
-        float mx = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * RMAX + m]);
-        const float ref = mx == -INFINITY ? 0.f : mx;
-        float l = 0.f, o = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float a = exp2f(red_m[w * RMAX + m] - ref);
-            l = fmaf(red_l[w * RMAX + m], a, l);
-            o = fmaf(red_o[(w * RMAX + m) * RS + d], a, o);
-        }
-        if (S == 1) {
-            store_out<T>(p, qoff, m, d, l > 0.f ? o / l : 0.f);
-        } else {
-            p.ws_part[(slot0 + m) * kHeadDim + d] = o;
-            if (d == 0) p.ws_ml[slot0 + m] = make_float2(mx, l);
-        }
-    }
-    if (S == 1) return;
-
     __threadfence();
     __syncthreads();
     if (tid == 0) misc[0] = (atomicAdd(&p.ws_cnt[c.unit], 1) == S - 1) ? 1 : 0;
@@ -671,15 +542,188 @@ __device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, flo
     if (tid == 0) p.ws_cnt[c.unit] = 0;
 }
 
+// A cluster's merge of one float4 of query vector m's output: the slots of its CS splits
+// (at sl0 + r * stride: o[64], max, sum) combined in split order into (max, sum, o), o
+// unnormalised. Loads are unconditional (a split past CS re-reads the last slot and gets
+// weight 0) and go in batches of four, so they overlap.
+__device__ __forceinline__ void merge_cluster_quad(const float* sl0, int stride, int CS, int q4,
+                                                   float& mx, float& l, float4& o) {
+    mx = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kMaxClusterSplits; ++r)
+        mx = fmaxf(mx, sl0[min(r, CS - 1) * stride + kHeadDim]);
+    const float ref = mx == -INFINITY ? 0.f : mx;
+    l = 0.f;
+    o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+    for (int r0 = 0; r0 < CS; r0 += 4) {
+        float4 v[4];
+        float mv[4], lv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float* sl = sl0 + min(r0 + j, CS - 1) * stride;
+            v[j] = *reinterpret_cast<const float4*>(sl + 4 * q4);
+            mv[j] = sl[kHeadDim];
+            lv[j] = sl[kHeadDim + 1];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float a = r0 + j < CS ? exp2f(mv[j] - ref) : 0.f;
+            l = fmaf(lv[j], a, l);
+            o.x = fmaf(v[j].x, a, o.x);
+            o.y = fmaf(v[j].y, a, o.y);
+            o.z = fmaf(v[j].z, a, o.z);
+            o.w = fmaf(v[j].w, a, o.w);
+        }
+    }
+}
+
+// Combine the eight warps' partial states, then
+//  * one split: write the output;
+//  * splits forming clusters: store the block's (max, sum, o) into the merge slots of its
+//    cluster's first CTA (one float4 per thread, asynchronous stores counted on that
+//    CTA's barrier); the first CTA waits for all of them and merges locally. With one
+//    cluster per unit it writes the output; with several, each first CTA publishes its
+//    cluster's (max, sum, o) to the workspace and the last to arrive merges those;
+//  * more splits than a cluster holds, without clusters: publish to the workspace; the
+//    last block to arrive (atomic ticket) merges all splits, loading them in parallel.
+// Merges run over the splits in index order, so results do not depend on timing. The
+// merge across clusters is compiled only into the GROUPED builds, which run the launches
+// whose plan has several clusters per unit: kept out of the other builds, the code after
+// the cluster merge stays as short as the chain of every single-cluster launch needs.
+// red: o [8][RMAX][red_stride], m [8][RMAX], l [8][RMAX]; mrg: [splits][msub][kSlot].
+template <typename T, int RMAX, bool GROUPED>
+__device__ void finish_cta(const AttnParams& p, const CtaCtx& c, float* red, float* mrg,
+                           uint64_t* merge_bar, int* misc, const int64_t* qoff,
+                           uint8_t* scratch4k) {
+    constexpr int RS = red_stride(RMAX);
+    const float* red_o = red;
+    const float* red_m = red + kWarps * RMAX * RS;
+    const float* red_l = red_m + kWarps * RMAX;
+    const int tid = threadIdx.x;
+    const int S = p.splits;
+    const size_t base = (size_t)c.unit * S * p.msub;
+
+    if (S > 1 && p.cluster) {
+        const int CS = p.csize;  // splits of this cluster
+        cluster_wait();  // the first CTA's merge barrier is initialised
+        const bool leader = c.rank == 0;
+        const uint32_t dst = leader ? 0u : map_shared(smem_u32(mrg), 0);
+        const uint32_t rbar = leader ? 0u : map_shared(smem_u32(merge_bar), 0);
+        // One thread per float4 of a slot: 16 of o, then (max, sum). Loads are
+        // unconditional (the (max, sum) thread reads an o quad it ignores) and go in
+        // batches of four warps.
+        for (int it = tid; it < kSlotQuads * c.mcount; it += blockDim.x) {
+            const int m = it / kSlotQuads, k = it % kSlotQuads;
+            const int kk = min(k, kHeadDim / 4 - 1);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * RMAX + m]);
+            const float ref = mx == -INFINITY ? 0.f : mx;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            float l = 0.f;
+#pragma unroll
+            for (int w0 = 0; w0 < kWarps; w0 += 4) {
+                float4 o[4];
+                float mw[4], lw[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int w = w0 + j;
+                    o[j] = *reinterpret_cast<const float4*>(red_o + (w * RMAX + m) * RS + 4 * kk);
+                    mw[j] = red_m[w * RMAX + m];
+                    lw[j] = red_l[w * RMAX + m];
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float a = exp2f(mw[j] - ref);
+                    l = fmaf(lw[j], a, l);
+                    v.x = fmaf(o[j].x, a, v.x);
+                    v.y = fmaf(o[j].y, a, v.y);
+                    v.z = fmaf(o[j].z, a, v.z);
+                    v.w = fmaf(o[j].w, a, v.w);
+                }
+            }
+            if (k == kHeadDim / 4) v = make_float4(mx, l, 0.f, 0.f);
+            const int slot = (c.rank * p.msub + m) * kSlot + 4 * k;
+            if (leader)
+                *reinterpret_cast<float4*>(mrg + slot) = v;
+            else
+                st_async_v4(dst + slot * 4, v, rbar);
+        }
+        if (!leader) return;
+        // One warp waits for the other CTAs' bytes (merge_wait_ns: longer than any peer
+        // can take to send); the block barrier then orders those bytes, and the slots
+        // this CTA's own threads wrote, before every thread's reads.
+        const bool ok =
+            tid >= 32 || mbar_wait_bounded_cluster(smem_u32(merge_bar), 0, p.merge_wait_ns);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) flag_error(p.dev_err, KVD_ERR_TIMEOUT);
+            return;
+        }
+        if (GROUPED && p.cgroups > 1) {
+            // this cluster's (max, sum, o), unnormalised, for the merge across clusters
+            for (int it = tid; it < c.mcount * (kHeadDim / 4); it += blockDim.x) {
+                const int m = it >> 4, q4 = it & 15;
+                float mx, l;
+                float4 o;
+                merge_cluster_quad(mrg + m * kSlot, p.msub * kSlot, CS, q4, mx, l, o);
+                const size_t slot = ((size_t)c.unit * p.cgroups + c.grp) * p.msub + m;
+                *reinterpret_cast<float4*>(p.ws_part + slot * kHeadDim + 4 * q4) = o;
+                if (q4 == 0) p.ws_ml[slot] = make_float2(mx, l);
+            }
+            ws_merge_last<T>(p, c, red, misc, qoff, scratch4k, p.cgroups);
+            return;
+        }
+        // One thread per (query vector, 4 dims).
+        for (int it = tid; it < c.mcount * (kHeadDim / 4); it += blockDim.x) {
+            const int m = it >> 4, q4 = it & 15;
+            float mx, l;
+            float4 o;
+            merge_cluster_quad(mrg + m * kSlot, p.msub * kSlot, CS, q4, mx, l, o);
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint2 packed;
+            packed.x = Half16<T>::from_f2(o.x * inv, o.y * inv);
+            packed.y = Half16<T>::from_f2(o.z * inv, o.w * inv);
+            *reinterpret_cast<uint2*>(static_cast<T*>(p.out) + qoff[m] + 4 * q4) = packed;
+        }
+        return;
+    }
+
+    const size_t slot0 = base + (size_t)c.s * p.msub;
+    for (int idx = tid; idx < c.mcount * kHeadDim; idx += blockDim.x) {
+        const int m = idx >> 6, d = idx & 63;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * RMAX + m]);
+        const float ref = mx == -INFINITY ? 0.f : mx;
+        float l = 0.f, o = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float a = exp2f(red_m[w * RMAX + m] - ref);
+            l = fmaf(red_l[w * RMAX + m], a, l);
+            o = fmaf(red_o[(w * RMAX + m) * RS + d], a, o);
+        }
+        if (S == 1) {
+            store_out<T>(p, qoff, m, d, l > 0.f ? o / l : 0.f);
+        } else {
+            p.ws_part[(slot0 + m) * kHeadDim + d] = o;
+            if (d == 0) p.ws_ml[slot0 + m] = make_float2(mx, l);
+        }
+    }
+    if (S == 1) return;
+    ws_merge_last<T>(p, c, red, misc, qoff, scratch4k, S);
+}
+
 // ------------------------------------------------- one query vector per KV head (SIMT) --
-template <typename T, bool ROPE>
+template <typename T, bool ROPE, bool GROUPED = false>
 __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: 4 blocks per SM
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
     constexpr int RM = 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
-    const SmemLayout L = smem_layout(p.stages, RM, merge_slots(p.cluster, p.splits, p.msub),
+    const SmemLayout L = smem_layout(p.stages, RM,
+                                     merge_slots(p.cluster, p.csize, p.msub),
                                      app_units(p));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
     float* red = reinterpret_cast<float*>(smem + L.red_off);
@@ -792,7 +836,8 @@ __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: 4 blocks per
         }
     }
     __syncthreads();
-    finish_cta<T, RM>(p, c, red, mrg, &bars[p.stages], misc, qoff, smem + L.bar_off - 4096);
+    finish_cta<T, RM, GROUPED>(p, c, red, mrg, &bars[p.stages], misc, qoff,
+                               smem + L.bar_off - 4096);
 }
 
 // ------------------------------------ 2..16 query vectors per KV head (tensor cores) ----
@@ -805,7 +850,7 @@ __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: 4 blocks per
 // constant 0, their S and O accumulators are not kept, and the block needs about 30
 // fewer registers -- three blocks per SM without spilling, so that more of the next
 // launch's blocks (and its thread-block clusters) fit beside a running launch.
-template <typename T, int MINB, bool ROPE, int RM = 16>
+template <typename T, int MINB, bool ROPE, int RM = 16, bool GROUPED = false>
 __global__ void __launch_bounds__(kThreads, MINB)
     block_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
@@ -813,7 +858,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
     constexpr bool kFull = RM == 16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
-    const SmemLayout L = smem_layout(p.stages, RM, merge_slots(p.cluster, p.splits, p.msub),
+    const SmemLayout L = smem_layout(p.stages, RM,
+                                     merge_slots(p.cluster, p.csize, p.msub),
                                      app_units(p));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
     float* red = reinterpret_cast<float*>(smem + L.red_off);
@@ -1017,7 +1063,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
         }
     }
     __syncthreads();
-    finish_cta<T, RM>(p, c, red, mrg, &bars[p.stages], misc, qoff, smem + L.bar_off - 4096);
+    finish_cta<T, RM, GROUPED>(p, c, red, mrg, &bars[p.stages], misc, qoff,
+                               smem + L.bar_off - 4096);
 }
 
 // ---------------------------------------------------------------- no-allocation scratch
@@ -1077,12 +1124,15 @@ int prepare_kernel(size_t smem_bytes) {
 // resident blocks per SM; its build for blocks of at most 8 query vectors (3 per SM);
 // the first two also with the rotary encoding compiled in (the rotation code is kept out
 // of the other builds, whose register budgets it would raise).
-enum Variant { kSimt = 1, kMma = 2, kMma3 = 3, kSimtRope = 4, kMmaRope = 5, kMma8 = 6 };
+enum Variant {
+    kSimt = 1, kMma = 2, kMma3 = 3, kSimtRope = 4, kMmaRope = 5, kMma8 = 6,
+    kSimtG = 7, kMmaG = 8  // kSimt / kMma with the merge across clusters of a unit
+};
 
 // Rows of the warp partials (the red area) of a variant: 16 for the tensor-core builds,
 // 8 for the 8-vector build, 1 for the CUDA-core kernel.
 constexpr int variant_rmax(int var) {
-    return (var == kSimt || var == kSimtRope) ? 1 : var == kMma8 ? 8 : 16;
+    return (var == kSimt || var == kSimtRope || var == kSimtG) ? 1 : var == kMma8 ? 8 : 16;
 }
 
 template <typename T>
@@ -1096,6 +1146,8 @@ int prepare(int var) {
     case kMmaRope: return prepare_kernel<block_attn_kernel<T, 2, true>>(smem);
     case kMma8: return prepare_kernel<block_attn_kernel<T, 3, false, 8>>(smem);
     case kSimtRope: return prepare_kernel<decode_attn_kernel<T, true>>(smem);
+    case kMmaG: return prepare_kernel<block_attn_kernel<T, 2, false, 16, true>>(smem);
+    case kSimtG: return prepare_kernel<decode_attn_kernel<T, false, true>>(smem);
     default: return prepare_kernel<decode_attn_kernel<T, false>>(smem);
     }
 }
@@ -1108,6 +1160,8 @@ const void* kernel_of(int var) {
     case kMmaRope: return reinterpret_cast<const void*>(block_attn_kernel<T, 2, true>);
     case kMma8: return reinterpret_cast<const void*>(block_attn_kernel<T, 3, false, 8>);
     case kSimtRope: return reinterpret_cast<const void*>(decode_attn_kernel<T, true>);
+    case kMmaG: return reinterpret_cast<const void*>(block_attn_kernel<T, 2, false, 16, true>);
+    case kSimtG: return reinterpret_cast<const void*>(decode_attn_kernel<T, false, true>);
     default: return reinterpret_cast<const void*>(decode_attn_kernel<T, false>);
     }
 }
@@ -1115,7 +1169,7 @@ const void* kernel_of(int var) {
 template <typename T>
 kvd_status launch_attn(int var, dim3 grid, cudaStream_t st, bool pdl, unsigned cl,
                        const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p) {
-    const int slots = merge_slots(p.cluster, p.splits, p.msub);
+    const int slots = merge_slots(p.cluster, p.csize, p.msub);
     const int app_rows = app_units(p);
     const uint32_t mma_smem = smem_layout(p.stages, 16, slots, app_rows).total;
     const uint32_t simt_smem = smem_layout(p.stages, 1, slots, app_rows).total;
@@ -1135,6 +1189,12 @@ kvd_status launch_attn(int var, dim3 grid, cudaStream_t st, bool pdl, unsigned c
     case kSimtRope:
         return launch_ex(decode_attn_kernel<T, true>, grid, dim3(kThreads), simt_smem, st, pdl,
                          cl, mk, mv, p);
+    case kMmaG:
+        return launch_ex(block_attn_kernel<T, 2, false, 16, true>, grid, dim3(kThreads), mma_smem,
+                         st, pdl, cl, mk, mv, p);
+    case kSimtG:
+        return launch_ex(decode_attn_kernel<T, false, true>, grid, dim3(kThreads), simt_smem, st,
+                         pdl, cl, mk, mv, p);
     default:
         return launch_ex(decode_attn_kernel<T, false>, grid, dim3(kThreads), simt_smem, st, pdl,
                          cl, mk, mv, p);
@@ -1142,8 +1202,8 @@ kvd_status launch_attn(int var, dim3 grid, cudaStream_t st, bool pdl, unsigned c
 }
 
 size_t plan_smem(const AttnPlan& P, int var, int app_rows) {
-    return smem_layout(P.stages, variant_rmax(var), merge_slots(P.cluster, P.splits, P.msub),
-                       app_rows)
+    return smem_layout(P.stages, variant_rmax(var),
+                       merge_slots(P.cluster, P.splits / P.cgroups, P.msub), app_rows)
         .total;
 }
 
@@ -1190,12 +1250,16 @@ int resident(const void* kern, int kid, size_t smem, int cluster, int nsm) {
 // Split choice. Blocks of one launch should all be resident at once: a second, partial
 // wave costs as much as the first. So, for few long units, take the most splits whose
 // clusters (one per unit) are all resident together; fall back to one block per unit
-// when none fits (many units fill the GPU by themselves). Only for a handful of units
-// over a long range, where even 16-block clusters leave each block streaming many
-// tiles, split further and merge through the workspace.
+// when none fits (many units fill the GPU by themselves). For a handful of units over a
+// range longer than one cluster takes in a round per block, give each unit several
+// clusters, merged through the workspace after each has merged on chip, as long as all
+// of them are resident at once and each block's tiles at least halve. Failing that, and
+// only where even 16-block clusters leave each block streaming many tiles, split
+// further without clusters and merge through the workspace.
+// kern_g / kid_g: the variant's build with the merge across clusters (null: none).
 AttnPlan choose_plan(const void* kern, int kid, int var, int nsm, int batch, int n_q_heads,
                      int n_kv_heads, int rows_per_kv, int qlen, int len_bound, int max_cluster,
-                     int app_rows) {
+                     int app_rows, const void* kern_g, int kid_g) {
     const int mmax = variant_rmax(var) > 1 ? kMmaQueryBlock : 1;
     const AttnPlan P1 = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, qlen, len_bound,
                                        mmax, 1, max_cluster);
@@ -1204,8 +1268,26 @@ AttnPlan choose_plan(const void* kern, int kid, int var, int nsm, int batch, int
         AttnPlan W = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, qlen, len_bound,
                                     mmax, kMaxSplits, 1);
         const int blocks = resident(kern, kid, plan_smem(W, var, app_rows), 1, nsm);
-        return plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, qlen, len_bound, mmax,
-                              std::max(1, blocks / P1.units), max_cluster);
+        W = plan_attention(batch, n_q_heads, n_kv_heads, rows_per_kv, qlen, len_bound, mmax,
+                           std::max(1, blocks / P1.units), max_cluster);
+        // Several clusters per unit, each merging on chip, leave the workspace only their
+        // first CTAs' partials. Where the plain merge would gather many partials that pays
+        // even with more tiles per block (measured: 1 row x 4 KV heads over 32768
+        // positions, 64 plain splits 17.1 us, 3 clusters of 16 per head 14.1 us; with 37
+        // plain splits, 2 clusters per head lost, 18.9 -> 20.1 us): taken with the most
+        // clusters per unit that are all resident at once.
+        if (kern_g && W.splits >= kGroupedMinSplits && max_cluster >= 2) {
+            const int most = std::min(kMaxGroups, (P1.rounds + max_cluster - 1) / max_cluster);
+            for (int g = most; g >= 2; --g) {
+                const AttnPlan G = plan_grouped(batch, n_q_heads, n_kv_heads, rows_per_kv,
+                                                qlen, len_bound, mmax, g, max_cluster);
+                const int cs = G.splits / G.cgroups;
+                if (cs >= 2 &&
+                    resident(kern_g, kid_g, plan_smem(G, var, app_rows), cs, nsm) >= G.units * g)
+                    return G;
+            }
+        }
+        return W;
     }
     int last = 0;
     for (int s = std::min(P1.rounds, max_cluster); s >= 2; --s) {
@@ -1258,9 +1340,14 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
         const int mc = bf ? prepare<__nv_bfloat16>(var) : prepare<__half>(var);
         if (mc <= 0) return false;
         const void* kern = bf ? kernel_of<__nv_bfloat16>(var) : kernel_of<__half>(var);
-        out = choose_plan(kern, var * 2 + (bf ? 1 : 0), var, nsm,
-                          batch, n_q_heads,
-                          kv->n_kv_heads, rows_per_kv, qlen, len_bound, mc, app_rows);
+        // the build with the merge across clusters, for the variants that have one
+        const int gvar = var == kSimt ? kSimtG : var == kMma ? kMmaG : 0;
+        const void* kern_g = nullptr;
+        if (gvar && (bf ? prepare<__nv_bfloat16>(gvar) : prepare<__half>(gvar)) == mc)
+            kern_g = bf ? kernel_of<__nv_bfloat16>(gvar) : kernel_of<__half>(gvar);
+        out = choose_plan(kern, var * 2 + (bf ? 1 : 0), var, nsm, batch, n_q_heads,
+                          kv->n_kv_heads, rows_per_kv, qlen, len_bound, mc, app_rows, kern_g,
+                          gvar * 2 + (bf ? 1 : 0));
         return true;
     };
     // Whether a tensor-core plan keeps all its blocks resident at once.
@@ -1308,8 +1395,12 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
             P = P3;
         }
     }
+    // several clusters per unit run on the build with the merge across clusters (only
+    // kSimt and kMma plans have them)
+    if (P.cgroups > 1) var = var == kSimt ? kSimtG : kMmaG;
     if ((int64_t)kv->n_kv_heads * P.nsub > 65535) return KVD_ERR_UNSUPPORTED;
-    if (P.splits > 1 && !P.cluster) {
+    const bool ws_merge = (P.splits > 1 && !P.cluster) || P.cgroups > 1;
+    if (ws_merge) {
         if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < P.ws_bytes)
             return KVD_ERR_WORKSPACE;
         if ((size_t)P.units * sizeof(int32_t) > KVD_WS_COUNTER_BYTES) return KVD_ERR_UNSUPPORTED;
@@ -1338,6 +1429,8 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
     p.box_rows = std::min(64, kv->capacity);
     p.early = (flags & KVD_FLAG_EARLY_KV) ? 1 : 0;
     p.cluster = P.cluster ? 1 : 0;
+    p.cgroups = P.cgroups;
+    p.csize = P.splits / P.cgroups;
     p.test_stall = (flags & KVD_FLAG_TEST_STALL) ? 1 : 0;
     p.merge_wait_ns = merge_wait_budget(P.tiles_per_split, p.stages);
     p.append = app ? 1 : 0;
@@ -1362,12 +1455,12 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
     // The built-in scratch keeps whatever the previous call left; a plan that merges
     // through it needs its units' arrival counters at zero (a call that stopped early
     // could have left them non-zero). Cleared here, after every check has passed.
-    if (noalloc && P.splits > 1 && !P.cluster &&
+    if (noalloc && ws_merge &&
         cudaMemsetAsync(ws, 0, (size_t)P.units * sizeof(int32_t), stream) != cudaSuccess)
         return KVD_ERR_CUDA;
     const bool pdl = (flags & (KVD_FLAG_PDL | KVD_FLAG_EARLY_KV)) != 0;
     const dim3 grid(P.splits, kv->n_kv_heads * P.nsub, P.bkv);
-    const unsigned cl = P.cluster ? (unsigned)P.splits : 1u;
+    const unsigned cl = P.cluster ? (unsigned)(P.splits / P.cgroups) : 1u;
     return bf ? launch_attn<__nv_bfloat16>(var, grid, stream, pdl, cl, mk, mv, p)
               : launch_attn<__half>(var, grid, stream, pdl, cl, mk, mv, p);
 }

@@ -72,9 +72,12 @@ kvd_status launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 // block) triple is a "unit". The attended range of a unit is cut into `splits` chunks
 // of `tiles_per_split` 64-position tiles, one thread block each. Splits of one unit
 // that fit in one thread-block cluster merge through distributed shared memory (no
-// workspace); more splits merge through the workspace.
+// workspace). A unit may also span `cgroups` clusters: each merges on chip, then their
+// first CTAs merge through the workspace. Without clusters, more splits than one cluster
+// holds merge through the workspace.
 struct AttnPlan {
     int bkv, group, M, msub, nsub, units, tiles_total, rounds, splits, tiles_per_split, stages;
+    int cgroups;  // clusters per unit (1: one cluster, or no cluster)
     bool cluster;
     size_t part_offset, ml_offset, ws_bytes;
 };
@@ -86,6 +89,10 @@ constexpr int kMaxClusterSplits = 16;  // largest cluster used for a merge
 // A workspace merge (more splits than a cluster holds) is only considered for at most
 // this many units: more units already fill the GPU with cluster-sized splits.
 constexpr int kWsMaxUnits = 8;
+// Most clusters per unit (kMaxGroups * kMaxClusterSplits <= kMaxSplits).
+constexpr int kMaxGroups = 8;
+// Least plain splits per unit for which several clusters per unit replace them.
+constexpr int kGroupedMinSplits = 48;
 // What the workspace merge costs (a global ticket, partials written and read back by
 // the last block), in 64-position tiles of per-block streaming time.
 constexpr int kWsMergeTiles = 12;
@@ -100,6 +107,14 @@ AttnPlan plan_attention(int batch, int n_q_heads, int n_kv_heads, int rows_per_k
 // off: the tiles a block streams must drop by more than the merge costs. Depends only
 // on the shape, so workspace sizing and the launcher agree.
 bool workspace_merge_pays(int units, int rounds);
+
+// The plan with `groups` clusters of at most `csize` splits per unit (the splits of the
+// plan for groups * csize blocks, padded to a multiple of `groups`: padding blocks have no
+// tiles). Their first CTAs merge through the workspace. It is considered only where
+// workspace_merge_pays, and needs no more workspace than the plain workspace merge.
+AttnPlan plan_grouped(int batch, int n_q_heads, int n_kv_heads, int rows_per_kv, int qlen,
+                      int len_bound, int mmax, int groups, int csize);
+
 
 // Workspace bytes of greedy_accept for a given target block count (greedy_accept.cu);
 // sized with kWsTargetBound, an upper bound of the block count any launch targets.

@@ -273,12 +273,24 @@ def test_verify_single_token_equals_decode():
     assert_attn_close(b, want, "f16", "decode")
 
 
-# Few (row, head) units over a long range: 16-block clusters would leave each block
-# 16 rounds of tiles, so the range is cut into 128 splits whose partials are merged
-# through the workspace by the last block to arrive.
+# Few (row, head) units over a long range: one 16-block cluster per unit would leave each
+# block 16 rounds of tiles, so the range is cut into 128 splits. With 2 units all 16
+# clusters (8 per unit, 16 blocks each) are resident at once: each cluster merges on chip,
+# and the last of a unit's 8 first CTAs to arrive merges their partials through the
+# workspace.
 def test_decode_workspace_merge_long_cache():
     got, want = run_attention("f16", 1, 2, 2, 32768, lens=np.array([32000], np.int32), seed=130)
-    assert_attn_close(got, want, "f16", "decode 2 units x 125 splits")
+    assert_attn_close(got, want, "f16", "decode 2 units x 8 clusters of 16 splits")
+
+
+# 8 units over a long range: only about 2 clusters of 16 per unit can be resident at
+# once, which would leave each block more tiles than plain splits do, so every block
+# publishes its partial to the workspace and the last to arrive merges them (ragged rows:
+# the second row's blocks past its length have no tiles).
+def test_decode_workspace_merge_without_clusters():
+    got, want = run_attention("f16", 2, 20, 4, 32768, lens=np.array([32768, 17001], np.int32),
+                              seed=132)
+    assert_attn_close(got, want, "f16", "decode 8 units, workspace merge of plain splits")
 
 
 def test_verify_workspace_merge_sixteen_queries():

@@ -30,7 +30,8 @@ def _gpu():
 
 # (dtype, batch, q heads, kv heads, capacity, lengths or None, fixed length)
 CASES = [
-    # two (row, head) units over 32768 positions: 125 splits merged in the scratch buffer
+    # two (row, head) units over 32768 positions: 8 clusters of 16 splits per unit, the
+    # clusters' partials merged in the scratch buffer
     ("f16", 1, 2, 2, 32768, [32000], 0),
     # ragged GQA rows: merged inside thread-block clusters, scratch counters unused
     ("bf16", 4, 9, 3, 700, [700, 1, 333, 64], 0),
@@ -82,10 +83,11 @@ def test_noalloc_matches_workspace_entry_point_twice(case):
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     import kv_cached_decode_gb300 as kvd
 
-    # 2 KV heads x 16 query heads each over 32768 positions merge through 128 splits of
-    # 16 query vectors: about 1 MiB of partials, more than the built-in 512 KiB.
-    K = torch.zeros(1, 2, 32768, D, dtype=torch.float16, device="cuda")
-    q = torch.zeros(1, 32, 1, D, dtype=torch.float16, device="cuda")
+    # 8 KV heads x 16 query heads each over 32768 positions: plain splits merged through
+    # the scratch (at most about 2 clusters per unit fit at once), 8 units x 30 or more
+    # splits x 16 query vectors: over 1 MiB of partials, more than the built-in 512 KiB.
+    K = torch.zeros(1, 8, 32768, D, dtype=torch.float16, device="cuda")
+    q = torch.zeros(1, 128, 1, D, dtype=torch.float16, device="cuda")
     out = torch.full_like(q, 5.0)
     with pytest.raises(kvd.KvdError) as ei:
         kvd.kvd_decode_attn_noalloc(q, kvd.make_cache(K, K), out, fixed_len=32768)
