@@ -34,9 +34,10 @@
 //    on its mbarrier; that CTA merges them locally while the others exit. The split
 //    count is the largest whose clusters are all resident at once (occupancy
 //    calculator), so a launch never runs a second, partial wave. Only a handful of
-//    units over a long range split further: those partials go through the workspace
-//    and the last block to arrive (atomic ticket) merges them. Merges run in fixed
-//    split order, so results are repeatable.
+//    units over a long range split further: each unit then spans several clusters,
+//    whose first CTAs' merged partials go through the workspace (or, with few enough
+//    splits, every block's partial does), and the last block to arrive (atomic
+//    ticket) merges them. Merges run in fixed split order, so results are repeatable.
 //  * Programmatic dependent launch: every block lets the next kernel on the stream
 //    start as soon as its own copies are issued; with KVD_FLAG_EARLY_KV it also issues
 //    those copies before waiting for the previous kernel.
