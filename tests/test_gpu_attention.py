@@ -293,6 +293,16 @@ def test_decode_workspace_merge_without_clusters():
     assert_attn_close(got, want, "f16", "decode 8 units, workspace merge of plain splits")
 
 
+# Two rows over 32768 positions, the second only 3000 long: that row's clusters past the
+# first hold no tiles at all, and their first CTAs publish empty partials (max -inf, sum
+# 0) that the merge across clusters must weigh 0. bf16, one query vector per KV head (the
+# CUDA-core build with the merge across clusters).
+def test_decode_grouped_merge_empty_clusters():
+    got, want = run_attention("bf16", 2, 1, 1, 32768, lens=np.array([32768, 3000], np.int32),
+                              seed=133)
+    assert_attn_close(got, want, "bf16", "decode, clusters past the length empty")
+
+
 def test_verify_workspace_merge_sixteen_queries():
     # 16 query heads on one KV head, qlen 1: 16 query vectors per block, 128 splits
     got, want = run_attention("bf16", 1, 16, 1, 32768, lens=np.array([32768], np.int32), qlen=1,
@@ -331,6 +341,19 @@ def run_fused(dtype, B, Hq, Hkv, cap, lens_in, qlen, *, verify, seed, flags=0):
     torch.cuda.synchronize()
     return host16(out), want, host16(Kd), host16(Vd), Kw, Vw, lens_out.cpu().numpy(), \
         lens_out_w, e.item(), err
+
+
+# The new token appended inside a launch whose units span several clusters (2 units over
+# 32768 positions): the block whose slab holds position 30000 writes it to the cache and
+# attends to it, and its cluster's partial reaches the merge across clusters.
+@pytest.mark.parametrize("flags", [0, 3])  # plain, and PDL + early K/V
+def test_decode_fused_append_several_clusters_per_unit(flags):
+    got, want, Kg, Vg, Kw, Vw, lo, low, e, err = run_fused(
+        "f16", 1, 2, 2, 32768, [30000], 1, verify=False, seed=134, flags=flags)
+    assert e == 0 and not err
+    assert np.array_equal(Kg, Kw) and np.array_equal(Vg, Vw)
+    assert np.array_equal(lo, low)
+    assert_attn_close(got, want, "f16", "fused decode, several clusters per unit")
 
 
 @pytest.mark.parametrize("flags", [0, 3])  # plain, and PDL + early K/V
