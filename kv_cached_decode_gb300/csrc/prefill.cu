@@ -167,13 +167,11 @@ __global__ void __launch_bounds__(kPfThreads, kPfMinBlocks)
         }
     };
     if (rows_live == 0) {
-        if (!producer) {
-            if (tid == 0) tslot[1] = 0;
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(sQ + swz(tid, c)) = make_uint4(0u, 0u, 0u, 0u);
-            store_rows();
-        }
+        // no live row: the tile's rows below max_len get zeros, by plain stores
+        const int nrows = min(kPfRows, p.max_len - q0);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + head_off +
+                                              (int64_t)q0 * kHeadDim);
+        for (int x = tid; x < nrows * 8; x += kPfThreads) dst[x] = make_uint4(0u, 0u, 0u, 0u);
         pdl_trigger();
         return;
     }
