@@ -7,9 +7,11 @@ unwritten, and leave the context and stream usable: the next normal call on the 
 stream matches the fp64 oracle. Every
 merge path is covered: one split per unit, the cluster merge (the split that gives up
 is a non-first CTA, which sends nothing, so the first CTA's bounded wait for the
-partials runs out and it writes no output), and the workspace merge (the unit's arrival
-counter is left non-zero and the workspace is re-zeroed, as the header says). Each stall
-costs a few seconds of waiting.
+partials runs out and it writes no output), several clusters per unit merged through the
+workspace (the stalled cluster's first CTA gives up, so the unit's last arrival never
+comes), and plain splits merged through the workspace. After a workspace merge the
+unit's arrival counter is left non-zero and the workspace is re-zeroed, as the header
+says. Each stall costs a few seconds of waiting.
 """
 
 import numpy as np
@@ -37,7 +39,10 @@ CASES = [
     ("cluster-tensor-cores", "f16", 1, 20, 20, 1500, 1),
     ("cluster-cuda-cores", "bf16", 1, 4, 4, 4096, 1),
     ("cluster-verify-block", "f16", 1, 20, 20, 1500, 5),
-    ("workspace-merge", "f16", 1, 1, 1, 32768, 1),
+    # 1 unit over 32768 positions: 8 clusters of 16 splits, merged through the workspace
+    ("clusters-per-unit", "f16", 1, 1, 1, 32768, 1),
+    # 8 GQA units over 32768 positions: plain splits merged through the workspace
+    ("workspace-merge-plain", "f16", 2, 20, 4, 32768, 1),
 ]
 
 
