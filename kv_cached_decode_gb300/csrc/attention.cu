@@ -543,9 +543,9 @@ __device__ void ws_merge_last(const AttnParams& p, const CtaCtx& c, float* red, 
     if (tid == 0) p.ws_cnt[c.unit] = 0;
 }
 
-// A cluster's merge of one float4 of query vector m's output: the slots of its CS splits
-// (at sl0 + r * stride: o[64], max, sum) combined in split order into (max, sum, o), o
-// unnormalised. Loads are unconditional (a split past CS re-reads the last slot and gets
+// A cluster's merge of float4 q4 of one query vector's output: the vector's slots in
+// the cluster's CS splits (at sl0 + r * stride: o[64], max, sum) combined in split order
+// into (max, sum, o), o unnormalised. Loads are unconditional (a split past CS re-reads the last slot and gets
 // weight 0) and go in batches of four, so they overlap.
 __device__ __forceinline__ void merge_cluster_quad(const float* sl0, int stride, int CS, int q4,
                                                    float& mx, float& l, float4& o) {
@@ -1399,6 +1399,18 @@ kvd_status attention(bool verify, kvd_dtype dtype, int32_t batch, int32_t n_q_he
     // several clusters per unit run on the build with the merge across clusters (only
     // kSimt and kMma plans have them)
     if (P.cgroups > 1) var = var == kSimt ? kSimtG : kMmaG;
+    // Few blocks, each streaming more tiles than the ring holds: when every block can
+    // have an SM of its own, a ring as deep as the block's tiles stages all of them
+    // before the dependency wait (kept only if the clusters all stay resident).
+    if (P.cluster && P.cgroups == 1 && P.tiles_per_split > P.stages &&
+        P.tiles_per_split <= kMaxStages && (int64_t)P.units * P.splits <= nsm) {
+        AttnPlan D = P;
+        D.stages = P.tiles_per_split;
+        const void* kern = bf ? kernel_of<__nv_bfloat16>(var) : kernel_of<__half>(var);
+        if (resident(kern, var * 2 + (bf ? 1 : 0), plan_smem(D, var, app_rows), D.splits, nsm) >=
+            D.units)
+            P = D;
+    }
     if ((int64_t)kv->n_kv_heads * P.nsub > 65535) return KVD_ERR_UNSUPPORTED;
     const bool ws_merge = (P.splits > 1 && !P.cluster) || P.cgroups > 1;
     if (ws_merge) {

@@ -82,7 +82,7 @@ struct AttnPlan {
     size_t part_offset, ml_offset, ws_bytes;
 };
 
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 8;  // deepest K/V ring of an attention block
 constexpr int kMmaQueryBlock = 16;     // query vectors per block on the tensor-core path
 constexpr int kMaxSplits = 128;        // splits per unit (merge scratch is sized for this)
 constexpr int kMaxClusterSplits = 16;  // largest cluster used for a merge
