@@ -76,6 +76,34 @@ def test_workspace_sizes_cover_the_counter_region(lib):
     assert kvd_workspace_size(KVD_OP_GREEDY_ACCEPT, 1, qlen=0, vocab=10) == 0
 
 
+@pytest.mark.parametrize("shape", [
+    # (batch, q heads, kv heads, rows per kv, qlen, length): few (row, KV head) units over
+    # long ranges, the shapes whose launches may span several clusters per unit
+    (1, 1, 1, 1, 1, 32768), (1, 2, 2, 1, 1, 32768), (1, 20, 4, 1, 1, 16384),
+    (1, 20, 4, 1, 1, 32768), (2, 20, 4, 1, 1, 32768), (1, 8, 1, 1, 1, 16384),
+    (1, 16, 1, 1, 1, 32768), (1, 16, 1, 1, 6, 65536), (5, 5, 5, 5, 1, 65536),
+])
+def test_workspace_size_covers_several_clusters_per_unit(lib, shape):
+    """A launch over few long units may give each unit up to 8 clusters whose first CTAs
+    merge through the workspace: the size the library reports must hold those 8 partials
+    per (unit, query vector), 64 fp32 values and a (max, sum) pair each, after the
+    counters."""
+    from kv_cached_decode_gb300 import (KVD_OP_DECODE_ATTN, KVD_OP_VERIFY_ATTN,
+                                        KVD_WS_COUNTER_BYTES, kvd_workspace_size)
+
+    B, Hq, Hkv, rpk, qlen, L = shape
+    op = KVD_OP_DECODE_ATTN if qlen == 1 else KVD_OP_VERIFY_ATTN
+    got = kvd_workspace_size(op, B, Hq, Hkv, rpk, qlen, L)
+    M = rpk * (Hq // Hkv) * qlen                  # query vectors per (row, KV head)
+    mmax = 16 if M >= 2 else 1
+    nsub = -(-M // mmax)
+    msub = -(-M // nsub)
+    units = (B // rpk) * Hkv * nsub
+    slots = units * 8 * msub
+    need = KVD_WS_COUNTER_BYTES + -(-(slots * 64 * 4) // 256) * 256 + slots * 2 * 4
+    assert got >= need, (shape, got, need)
+
+
 def _fake_cache(**kw):
     from kv_cached_decode_gb300 import Cache
 
